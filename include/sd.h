@@ -1,0 +1,231 @@
+/* sd.h -- C ABI of the GB300 verification-step library (libsdverify.so).
+ *
+ * One verification step of speculative decoding with adaptive verification,
+ * in two stages that run entirely on one GPU:
+ *
+ *   sd_plan    planning stage: per-slot survival, global top-B, budget
+ *              argmax against a step-cost table, varlen compaction.
+ *   sd_verify  sampling stage: vocab-wide speculative rejection sampling on
+ *              the compacted target/draft logits (sd_verify_rows followed by
+ *              sd_verify_finalize).
+ *
+ * Sources (page title, section):
+ *   [AV-blog]  fosworld blog "추측 디코딩과 vLLM 적응형 검증"
+ *   [AV-page]  agentlenshq "vLLM DSpark을 활용한 적응형 검증(Adaptive Verification)"
+ *   [DSD-page] discuss.pytorch.kr "DSD: Cohere의 하드웨어 인식 동적 추측 디코딩"
+ *
+ * Conventions shared by every entry point
+ *   - Every pointer argument is a DEVICE pointer unless stated otherwise; the
+ *     caller allocates and frees every buffer.  The library keeps no global
+ *     state and never allocates.
+ *   - Calls enqueue work on `stream` (a cudaStream_t; NULL = the legacy
+ *     default stream) and return without synchronising.  The return value
+ *     reports host-side argument validation and launch errors only.
+ *   - Problems found on the device (bad lengths, non-finite data, ...) are
+ *     OR-ed into the caller's `err_flag` word (SD_DEV_ERR_* bits).  The word
+ *     is sticky: the library never clears it; the caller zeroes it and reads
+ *     it after any synchronisation.  A call that finds a device error still
+ *     writes well-formed outputs (see each entry point), so later calls in
+ *     the same stream never read out of bounds.
+ *   - The planner's choice of B stays on the device; the host only ever
+ *     knows the upper bound bs*(k_max+1) of target rows ([AV-blog] "켜는
+ *     방법과 제약": the CPU knows only an upper bound of the lengths decided
+ *     on the GPU), so every launch is sized from that bound.
+ */
+#ifndef SD_VERIFY_H_
+#define SD_VERIFY_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  SD_OK = 0,
+  SD_ERR_INVALID_ARG = -1,  /* NULL pointer, negative size, unknown enum value */
+  SD_ERR_SHAPE = -2,        /* sizes inconsistent with each other (e.g. T >= cost_len) */
+  SD_ERR_UNSUPPORTED = -3,  /* valid but beyond this build's limits (SD_MAX_*) */
+  SD_ERR_CUDA = -4,         /* a CUDA runtime call or launch failed */
+  SD_ERR_DEVICE_CHECK = -5  /* reserved for callers mapping err_flag to a status */
+} sd_status;
+
+typedef enum { SD_F32 = 0, SD_BF16 = 1 } sd_dtype;
+
+typedef enum {
+  SD_MODE_ADAPTIVE = 0,  /* budget chosen by the cost model ([AV-page] Budget Calculation) */
+  SD_MODE_ALL_SLOTS = 1  /* every drafted slot verified (fixed-K speculative decoding) */
+} sd_mode;
+
+/* Device error bits (OR-ed into *err_flag). */
+#define SD_DEV_ERR_DRAFT_LENS 0x001      /* draft_lens[i] outside [0, k_max] */
+#define SD_DEV_ERR_CONF 0x002            /* a confidence logit is NaN/inf */
+#define SD_DEV_ERR_COST 0x004            /* a used cost entry is not finite and > 0 */
+#define SD_DEV_ERR_CU_SEQLENS 0x008      /* cu_seqlens not a valid compaction */
+#define SD_DEV_ERR_DRAFT_ID 0x010        /* a verified draft id outside [0, V) */
+#define SD_DEV_ERR_TEMP 0x020            /* a temperature < 0 or not finite */
+#define SD_DEV_ERR_UNIFORM 0x040         /* a uniform outside [0, 1) */
+#define SD_DEV_ERR_LOGITS 0x080          /* a logit row holds NaN/+inf or no finite value */
+#define SD_DEV_ERR_TIMEOUT 0x100         /* a bounded wait inside a kernel gave up */
+
+/* Limits of this build. */
+#define SD_MAX_K 15            /* k_max <= 15: at most 16 query rows per request */
+#define SD_MAX_PLAN_SLOTS 8192 /* pow2ceil(bs) * pow2ceil(k_max) <= 8192 for sd_plan */
+#define SD_MAX_VERIFY_BS 4096  /* bs <= 4096 for sd_verify_rows */
+#define SD_MAX_V (1 << 22)     /* V <= 4,194,304 */
+
+/* ------------------------------------------------------------------------
+ * sd_plan -- planning stage of adaptive verification.
+ *
+ * Passages: [AV-blog] "동작" steps 1-3 (survival = product of per-position
+ * acceptance estimates front to back; slots of all requests compete for the
+ * budget and the chosen slots are always a contiguous prefix of each draft;
+ * the number of slots maximises expected accepted tokens / expected step time
+ * from a table profiled at start-up); [AV-page] "DSpark 신뢰도 스케줄링
+ * 메커니즘" (Global Top-B Selection; Budget Calculation: one bonus token per
+ * sampling request plus the survival of the B best slots, against the cost
+ * of T non-draft plus B draft tokens; Execution Pipeline: the budget is sized
+ * from the previous step's double-buffered confidences, the assignment runs
+ * on the GPU without a host round trip) and "기술적 구현 및 CUDA Graphs"
+ * (Cost Modeling: the cost curve is forced monotone; CUDA Graph Padding: the
+ * table carries the graph-size staircase).
+ *
+ * Computes, with a_{i,j} = 1/(1+exp(-conf_{i,j})) and
+ * s_{i,j} = prod_{m<=j} a_{i,m} (fp32):
+ *   order all N = sum(draft_lens) slots by (s desc, packed index asc);
+ *   cost'[n] = max(cost_table[1..n]);
+ *   B* = smallest argmax over B in [0, min(N, cost_len-1-T)] of
+ *        (bs + sum of the B largest s) / cost'[T+B];
+ *   a slot is selected iff its rank < B*.
+ *
+ * Arguments
+ *   conf_logits      [N] fp32, packed by request: slot (i,j) at
+ *                    offset_i + j, offset = exclusive scan of draft_lens.
+ *                    Unused (may be NULL) in SD_MODE_ALL_SLOTS.
+ *   budget_conf      [N'] fp32 previous-step confidences packed by
+ *                    budget_draft_lens [bs_budget], or NULL to size the budget
+ *                    from conf_logits.  When given, B* is computed from them
+ *                    (same T, R = bs) and clipped to min(N, cost_len-1-T);
+ *                    the slots are still assigned by the current conf_logits.
+ *   draft_lens       [bs] int32, 0 <= draft_lens[i] <= k_max.
+ *   cost_table       [cost_len] fp32, cost of a step of n tokens at index n.
+ *                    Unused (may be NULL) in SD_MODE_ALL_SLOTS.
+ *   T                non-draft tokens of the step (>= 1 in adaptive mode).
+ * Outputs
+ *   B_out            [1] int32: B*.
+ *   slot_mask        [bs*k_max] uint8: slot (i,j) at i*k_max+j, 1 = verified.
+ *   num_verified     [bs] int32: n_i (a prefix of request i's draft).
+ *   cu_seqlens       [bs+1] int32: cu[0] = 0, cu[i+1] = cu[i] + n_i + 1
+ *                    (n_i verified drafts plus one target/bonus row).
+ *   err_flag         [1] int32, sticky SD_DEV_ERR_* bits.  On a device error
+ *                    the outputs describe B = 0 (n_i = 0, cu[i] = i).
+ *   workspace        unused by this build (ws_bytes may be 0).
+ * Limits: 1 <= bs, 0 <= k_max <= SD_MAX_K, pow2ceil(bs)*pow2ceil(k_max)
+ * <= SD_MAX_PLAN_SLOTS (SD_ERR_UNSUPPORTED otherwise).  One CTA, one launch.
+ * ---------------------------------------------------------------------- */
+size_t sd_plan_workspace_bytes(int bs, int k_max);
+sd_status sd_plan(const float* conf_logits, const float* budget_conf,
+                  const int* budget_draft_lens, int bs_budget, const int* draft_lens,
+                  int bs, int k_max, const float* cost_table, int cost_len, int T,
+                  sd_mode mode, int* B_out, uint8_t* slot_mask, int* num_verified,
+                  int* cu_seqlens, int* err_flag, void* workspace, size_t ws_bytes,
+                  void* stream);
+
+/* ------------------------------------------------------------------------
+ * sd_verify -- sampling stage: speculative rejection sampling over the
+ * vocabulary, = sd_verify_rows followed by sd_verify_finalize.
+ *
+ * Passages: [AV-blog] "추측 디코딩이란" (the target scores all drafted
+ * positions in one pass; drafts are accepted front to back up to the first
+ * mismatch, where the target's own token is inserted, so every step emits at
+ * least one token), "속도, 메모리, 정확도에 주는 영향" row 정확도 (with the
+ * original papers' rejection-sampling rule the output distribution equals the
+ * target model's) and "참고 링크 / 논문" (Leviathan et al. 2023; Chen et al.
+ * 2023); [AV-page] "현재 제한 사항" (logits are compacted after the forward).
+ *
+ * For request i with n_i = cu[i+1]-cu[i]-1 verified drafts, temperature
+ * tau_i, target rows t_j (j = 0..n_i) and draft rows d_j (j < n_i):
+ *   tau_i > 0: p_j = softmax(t_j/tau_i), q_j = softmax(d_j/tau_i);
+ *              slot j accepted iff uniforms[i][j] * q_j(x_j) <= p_j(x_j).
+ *   tau_i = 0: slot j accepted iff x_j == argmax t_j (lowest index on ties);
+ *              draft rows are not read.
+ *   a_i = first rejected slot, else n_i.
+ *   final token y_i: tau_i = 0: argmax t_{a_i}; tau_i > 0: inverse CDF with
+ *   u = uniforms[i][k_max] (smallest k with sum_{l<=k} w_l > u * sum w) over
+ *   w = max(p_{a_i} - q_{a_i}, 0) after a rejection, or w = p_{n_i} (bonus)
+ *   when every slot was accepted; if that residual has no positive mass in
+ *   fp32, w = p_{a_i}.
+ *   out_tokens[i] = (x_0 .. x_{a_i-1}, y_i, -1 ...), accepted_len[i] = a_i.
+ *
+ * Arguments
+ *   target_logits  [rows_cap, V] fp32 or bf16, row-major, compacted: the row of
+ *                  (i,j) is cu_seqlens[i]+j.  rows_cap >= bs*(k_max+1) is the
+ *                  caller's allocation; only rows < cu_seqlens[bs] are read.
+ *   draft_logits   [bs*k_max, V] same dtype, compacted: row of (i,j) is
+ *                  cu_seqlens[i]-i+j.  Only rows of requests with tau > 0 are
+ *                  read.  May be NULL if every temperature is 0.
+ *   dt, V          element type and vocabulary size.
+ *   draft_ids      [bs*k_max] int32, compacted like the draft rows.
+ *   uniforms       [bs, k_max+1] fp32 in [0,1): slot tests then the final draw.
+ *   temps          [bs] fp32 >= 0.
+ *   cu_seqlens     [bs+1] int32 from sd_plan (or the caller).
+ * Outputs
+ *   accepted_len   [bs] int32; out_tokens [bs, k_max+1] int32, -1 padded.
+ *   probs_out      [bs*k_max, 2] fp32 or NULL: (p_j(x_j), q_j(x_j)) of every
+ *                  verified slot of a tau > 0 request, at the draft-row index
+ *                  (diagnostics; other entries untouched).
+ *   err_flag       [1] int32, sticky SD_DEV_ERR_* bits.  On SD_DEV_ERR_CU_SEQLENS
+ *                  no row is read and outputs are accepted_len = 0,
+ *                  out_tokens = -1.
+ *   workspace      device scratch of sd_verify_workspace_bytes(bs, k_max)
+ *                  bytes, 16-byte aligned: per-row accept flags and candidate
+ *                  tokens passed from the rows kernel to the finalize kernel.
+ *                  Needs no initialisation.
+ * Layout requirements for the fast path: V*elem and the logits base pointers
+ * 16-byte aligned (bulk-copy staging); otherwise a slower staged path runs.
+ * ---------------------------------------------------------------------- */
+size_t sd_verify_workspace_bytes(int bs, int k_max);
+
+/* Launch tuning of the rows kernel; 0 in any field = automatic.  The result
+ * does not depend on it. */
+typedef struct {
+  int cluster;   /* CTAs sharing one row pair: 1, 2, 4, 8 or 16 */
+  int stages;    /* row slices in flight per CTA (1..4) */
+  int clusters;  /* persistent clusters launched (<= what fits at once) */
+} sd_launch_cfg;
+
+sd_status sd_verify(const void* target_logits, const void* draft_logits, sd_dtype dt, int V,
+                    const int* draft_ids, const float* uniforms, const float* temps,
+                    const int* cu_seqlens, int bs, int k_max, int* accepted_len,
+                    int* out_tokens, float* probs_out, int* err_flag, void* workspace,
+                    size_t ws_bytes, void* stream);
+
+/* First half of sd_verify: one pass over every compacted row; writes the
+ * per-row accept flag and the candidate final token of every row that could
+ * end its request's accepted prefix into the workspace.  cfg may be NULL. */
+sd_status sd_verify_rows(const void* target_logits, const void* draft_logits, sd_dtype dt,
+                         int V, const int* draft_ids, const float* uniforms,
+                         const float* temps, const int* cu_seqlens, int bs, int k_max,
+                         float* probs_out, int* err_flag, void* workspace, size_t ws_bytes,
+                         const sd_launch_cfg* cfg, void* stream);
+
+/* Second half of sd_verify: per request, a_i and out_tokens from the
+ * workspace written by sd_verify_rows on the same stream. */
+sd_status sd_verify_finalize(const int* draft_ids, const int* cu_seqlens, int bs, int k_max,
+                             int* accepted_len, int* out_tokens, int* err_flag,
+                             const void* workspace, size_t ws_bytes, void* stream);
+
+/* Launch shape the rows kernel would use for (V, dt) and the requested
+ * tuning (NULL = automatic), on the current device.  Host-only query. */
+sd_status sd_verify_launch_info(int V, sd_dtype dt, const sd_launch_cfg* req,
+                                sd_launch_cfg* chosen, int* threads, size_t* smem_bytes);
+
+const char* sd_status_string(sd_status s);
+int sd_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SD_VERIFY_H_ */
