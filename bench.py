@@ -1,0 +1,526 @@
+#!/usr/bin/env python3
+"""Benchmark of one verification step (plan + verify) on synthetic data.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+Workload (default ``adaptive_hc``): BS=256 requests, K=7 drafted slots each,
+V=129280, bf16 logits, temperatures over {0, 0.7, 1.0}, T=256 non-draft tokens,
+cost(n) = 1 + 0.004*ceil16(n) -- the adaptive high-concurrency setup, the
+configuration that exercises every stage of the path (the planner chooses B,
+greedy and sampled requests mix).
+
+One step = sd_plan + sd_verify_rows + sd_verify_finalize on device-resident
+inputs.  Two input sets, each larger than the 129 MB L2, alternate between
+steps, so no step reads data the previous one left in L2.  Metric: verified
+draft tokens/s (sum of n_i over requests, per second).  Also reported:
+achieved HBM bandwidth of the rows kernel against the measured copy peak,
+planner latency, acceptance statistics, an end-to-end figure through the C
+ABI from pinned host buffers, and the CPU oracle as a reported baseline.
+
+Under torchrun (N > 1) every rank runs its own independent batch (different
+seed): the step shards by request with no data-path collective (weak scaling).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+from pathlib import Path
+
+import numpy as np
+
+ROOT = Path(__file__).resolve().parent
+sys.path.insert(0, str(ROOT))
+
+import sdsynth as S  # noqa: E402
+
+NOMINAL_HBM_GBS = 8000.0
+PEAKS = ROOT / "MEASURED_PEAKS.json"
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="adaptive_hc", choices=sorted(S.WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--seed", type=int, default=2026)
+    ap.add_argument("--cluster", type=int, default=0)
+    ap.add_argument("--stages", type=int, default=0)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    return ap.parse_args()
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def hbm_peak():
+    try:
+        d = json.loads(PEAKS.read_text())
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+class ClockSampler:
+    """Samples SM clocks and throttle reasons with nvidia-smi while running."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except (FileNotFoundError, OSError):
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        time.sleep(0.25)
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx = float(parts[1])
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[3:7]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle arms
+
+
+def oracle_step(w, seed, pi, vi_fn, budget_s, cu=None):
+    """Times the oracle (single thread) on a bounded sample of one step:
+    the full plan plus the sampling stage for as many requests as fit in
+    ``budget_s`` seconds.  Returns (verified draft tokens/s, sample text)."""
+    import oracle
+    t0 = time.perf_counter()
+    pl = oracle.plan(pi["conf"], pi["draft_lens"], w.k_max, pi["cost"], pi["T"], pi["mode"],
+                     budget_conf=pi["budget_conf"], budget_draft_lens=pi["budget_draft_lens"])
+    t_plan = time.perf_counter() - t0
+    cu = pl["cu_seqlens"]
+    n = np.diff(cu) - 1
+    vi = vi_fn(cu)
+    done, tokens, t_ver = 0, 0, 0.0
+    for i in range(w.bs):
+        t1 = time.perf_counter()
+        oracle.verify(vi["target"], vi["draft"] if len(vi["draft"]) else None, w.dtype, w.V,
+                      vi["draft_ids"], vi["uniforms"], vi["temps"], cu, w.k_max, requests=[i])
+        t_ver += time.perf_counter() - t1
+        done += 1
+        tokens += int(n[i])
+        if t_ver + t_plan >= budget_s:
+            break
+    # per-request rate scaled to the whole step: plan once + all requests
+    per_req = t_ver / done
+    step_time = t_plan + per_req * w.bs
+    value = float(n.sum()) / step_time
+    sample = (f"oracle plan of all {w.bs} requests ({t_plan*1e3:.1f} ms) + sampling stage of "
+              f"{done} of {w.bs} requests ({t_ver:.2f} s), scaled to one full step "
+              f"({step_time:.2f} s)")
+    return value, sample, step_time
+
+
+def run_reference(args, w, rank, world):
+    if rank != 0:
+        return
+    pi = S.plan_inputs(w, args.seed, 0)
+
+    def vi_fn(cu):
+        return S.verify_inputs(w, args.seed, 0, cu, pi["draft_lens"])
+
+    vals, times = [], []
+    per_step = max(2.0, min(args.cpu_seconds, 60.0 / max(1, args.steps + args.warmup)))
+    for k in range(args.warmup + args.steps):
+        v, sample, st = oracle_step(w, args.seed, pi, vi_fn, per_step)
+        if k >= args.warmup:
+            vals.append(v)
+            times.append(st)
+    value = statistics.median(vals)
+    line = {
+        "impl": "reference", "metric": "verified draft tokens/s", "value": value,
+        "unit": "verified draft tokens/s", "n_gpus": args.gpus, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": 1e3 * statistics.median(times),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": config_of(w),
+        "cpu_baseline": {"value": value, "unit": "verified draft tokens/s", "cores": 1,
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "verified draft tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def config_of(w):
+    return {"workload": w.name, "bs": w.bs, "k_max": w.k_max, "V": w.V,
+            "logits": "fp32" if w.dtype == S.F32 else "bf16", "T": w.T,
+            "mode": "adaptive" if w.mode == S.MODE_ADAPTIVE else "all_slots",
+            "parallelism": "replicas (independent batch per GPU)",
+            "l2": "two alternating input sets, each larger than L2"}
+
+
+# ---------------------------------------------------------------------------
+# GPU arm
+
+
+def run_ours(args, w, rank, world, local):
+    import torch
+    import speculative_decoding_verification_sd_gb300 as sd
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    seed = args.seed + 1000 * rank
+    stream = torch.cuda.current_stream()
+    bs, k = w.bs, w.k_max
+    dtype = sd.SD_F32 if w.dtype == S.F32 else sd.SD_BF16
+    tdt = torch.float32 if w.dtype == S.F32 else torch.int16
+    rows_cap = bs * (k + 1)
+    elem = w.elem
+
+    def host(a, t):
+        return None if a is None else torch.from_numpy(np.ascontiguousarray(a, t))
+
+    pi = S.plan_inputs(w, seed, 0)
+    d_lens = host(pi["draft_lens"], np.int32).to(dev)
+    d_conf = host(pi["conf"], np.float32).to(dev) if pi["conf"] is not None else None
+    d_cost = host(pi["cost"], np.float32).to(dev) if pi["cost"] is not None else None
+    cost_len = 0 if pi["cost"] is None else len(pi["cost"])
+    d_B = torch.zeros(1, dtype=torch.int32, device=dev)
+    d_mask = torch.zeros((bs, max(k, 1)), dtype=torch.uint8, device=dev)
+    d_nv = torch.zeros(bs, dtype=torch.int32, device=dev)
+    d_cu = torch.zeros(bs + 1, dtype=torch.int32, device=dev)
+    d_err = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    def plan_call():
+        sd.sd_plan(d_conf, None, None, 0, d_lens, bs, k, d_cost, cost_len, w.T, w.mode, d_B, d_mask,
+                   d_nv, d_cu, d_err, None, 0, stream)
+
+    # The plan of this batch fixes the compacted layout the "target forward"
+    # would have produced; build the logits rows in that layout.
+    plan_call()
+    torch.cuda.synchronize()
+    cu = d_cu.cpu().numpy()
+    n = np.diff(cu) - 1
+    t0 = time.perf_counter()
+    vi = S.verify_inputs(w, seed, 0, cu, pi["draft_lens"])
+    gen_s = time.perf_counter() - t0
+    temps = vi["temps"]
+    B = int(cu[-1]) - bs
+    rows_t = int(cu[-1])
+    sets = []
+    for _ in range(2):
+        tgt = torch.empty((rows_cap, w.V), dtype=tdt, device=dev)
+        dft = torch.empty((max(bs * k, 1), w.V), dtype=tdt, device=dev)
+        th = torch.from_numpy(vi["target"].view(np.int16) if w.dtype == S.BF16 else vi["target"])
+        dh = torch.from_numpy(vi["draft"].view(np.int16) if w.dtype == S.BF16 else vi["draft"])
+        tgt[:rows_t].copy_(th)
+        if B > 0:
+            dft[:B].copy_(dh)
+        sets.append((tgt, dft))
+    d_ids = torch.zeros(max(bs * k, 1), dtype=torch.int32, device=dev)
+    if B > 0:
+        d_ids[:B] = torch.from_numpy(vi["draft_ids"]).to(dev)
+    d_u = torch.from_numpy(vi["uniforms"]).to(dev)
+    d_t = torch.from_numpy(temps).to(dev)
+    d_acc = torch.zeros(bs, dtype=torch.int32, device=dev)
+    d_out = torch.zeros((bs, k + 1), dtype=torch.int32, device=dev)
+    ws_bytes = sd.sd_verify_workspace_bytes(bs, k)
+    d_ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    cfg = {"cluster": args.cluster, "stages": args.stages}
+
+    def step(s, ev=None):
+        tgt, dft = sets[s & 1]
+        if ev:
+            ev[0].record(stream)
+        plan_call()
+        if ev:
+            ev[1].record(stream)
+        sd.sd_verify_rows(tgt, dft, dtype, w.V, d_ids, d_u, d_t, d_cu, bs, k, None, d_err, d_ws,
+                          ws_bytes, cfg=cfg, stream=stream)
+        if ev:
+            ev[2].record(stream)
+        sd.sd_verify_finalize(d_ids, d_cu, bs, k, d_acc, d_out, d_err, d_ws, ws_bytes, stream)
+        if ev:
+            ev[3].record(stream)
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    for s in range(args.warmup):
+        step(s)
+    barrier()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        barrier()
+        t_start.record(stream)
+        for s in range(args.steps):
+            step(s, evs[s])
+        t_end.record(stream)
+        barrier()
+    elapsed_ms = t_start.elapsed_time(t_end)
+    plan_ms = [e[0].elapsed_time(e[1]) for e in evs]
+    rows_ms = [e[1].elapsed_time(e[2]) for e in evs]
+    fin_ms = [e[2].elapsed_time(e[3]) for e in evs]
+    err = int(d_err.item())
+    acc = d_acc.cpu().numpy()
+
+    # Work units and algorithmic bytes of one step.
+    verified = int(n.sum())
+    sampled = temps > 0
+    rows_read = int((n + 1).sum() + n[sampled].sum())
+    bytes_rows = rows_read * w.V * elem
+    bytes_small = (bs + 1) * 4 + bs * 4 + B * 4 + bs * (k + 1) * 4 + rows_t * 5
+    bytes_alg = bytes_rows + bytes_small
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([elapsed_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed_ms = float(t.item())
+        u = torch.tensor([verified], device=dev, dtype=torch.float64)
+        dist.all_reduce(u)
+        total_verified = float(u.item())
+    else:
+        total_verified = float(verified)
+    value = total_verified * args.steps / (elapsed_ms / 1e3)
+    rows_avg_ms = sum(rows_ms) / len(rows_ms)
+    achieved = bytes_alg / (rows_avg_ms / 1e3) / 1e9
+    peak, peak_kind = hbm_peak()
+
+    # Planner alone: one launch (events) and 1000 launches in a CUDA graph.
+    plan_graph_us = None
+    try:
+        g = torch.cuda.CUDAGraph()
+        side = torch.cuda.Stream()
+        side.wait_stream(stream)
+        with torch.cuda.stream(side):
+            plan_call_s = lambda: sd.sd_plan(d_conf, None, None, 0, d_lens, bs, k, d_cost, cost_len,
+                                             w.T, w.mode, d_B, d_mask, d_nv, d_cu, d_err, None, 0, side)
+            plan_call_s()
+            torch.cuda.synchronize()
+            with torch.cuda.graph(g, stream=side):
+                for _ in range(1000):
+                    plan_call_s()
+        torch.cuda.synchronize()
+        a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        g.replay()
+        torch.cuda.synchronize()
+        a0.record(stream)
+        g.replay()
+        a1.record(stream)
+        torch.cuda.synchronize()
+        plan_graph_us = 1e3 * a0.elapsed_time(a1) / 1000.0
+    except Exception as ex:  # graph capture unsupported -> report the event time only
+        print(f"# planner graph timing skipped: {ex}", file=sys.stderr)
+
+    # End to end through the C ABI from pinned host buffers.
+    e2e = None
+    if not args.no_e2e:
+        e2e = run_e2e(args, w, sd, dev, stream, pi, vi, cu, ws_bytes, cfg, rows_cap)
+        if world > 1 and e2e is not None:
+            import torch.distributed as dist
+            t = torch.tensor([e2e["_ms"]], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e2e["value"] = total_verified * args.steps / (float(t.item()) / 1e3)
+        if e2e is not None:
+            e2e.pop("_ms", None)
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        v, sample, _ = oracle_step(w, seed, pi, lambda c: vi, args.cpu_seconds)
+        cpu = {"value": v, "unit": "verified draft tokens/s", "cores": 1, "kind": "oracle",
+               "sample": sample}
+
+    accepted = int(acc.sum())
+    pos = np.zeros(k)
+    for j in range(k):
+        pos[j] = float((acc > j).mean())
+    line = {
+        "metric": "verified draft tokens/s", "value": value, "unit": "verified draft tokens/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": elapsed_ms / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16" if w.dtype == S.BF16 else "f32",
+        "data": "synthetic", "config": config_of(w),
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": None,
+                     "kernel": "rows_kernel (sd_verify_rows)", "peak_kind": peak_kind,
+                     "frac_of_nominal_8tbs": achieved / NOMINAL_HBM_GBS,
+                     "bytes_per_launch": bytes_alg, "avg_launch_ms": rows_avg_ms},
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": 3 * args.steps,
+        "clocks": clk.summary(),
+        "detail": {
+            "B": B, "verified_draft_tokens_per_step": verified, "target_rows": rows_t,
+            "draft_rows_read": int(n[sampled].sum()), "bytes_alg_per_step": bytes_alg,
+            "bytes_per_verified_token": bytes_alg / max(verified, 1),
+            "plan_us_event": 1e3 * statistics.median(plan_ms),
+            "plan_us_graph": plan_graph_us,
+            "rows_us_median": 1e3 * statistics.median(rows_ms),
+            "finalize_us_median": 1e3 * statistics.median(fin_ms),
+            "accepted_draft_tokens_per_step": accepted,
+            "emitted_tokens_per_s": (accepted + bs) * args.steps / (elapsed_ms / 1e3),
+            "mean_acceptance_length": 1.0 + accepted / bs,
+            "per_position_cumulative_acceptance": [round(x, 4) for x in pos],
+            "device_err_flag": err, "input_generation_s": gen_s,
+            "launch": sd.sd_verify_launch_info(w.V, dtype, args.cluster, args.stages),
+        },
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def run_e2e(args, w, sd, dev, stream, pi, vi, cu, ws_bytes, cfg, rows_cap):
+    """Same step from pinned host buffers: H2D of every input, plan, verify,
+    D2H of accepted lengths and tokens, all inside the timed region."""
+    import torch
+    bs, k = w.bs, w.k_max
+    dtype = sd.SD_F32 if w.dtype == S.F32 else sd.SD_BF16
+    tdt = torch.float32 if w.dtype == S.F32 else torch.int16
+    rows_t = int(cu[-1])
+    B = rows_t - bs
+
+    def pin(a, t=None):
+        x = torch.from_numpy(np.ascontiguousarray(a if t is None else a.astype(t)))
+        return x.pin_memory()
+
+    h_conf = pin(pi["conf"], np.float32) if pi["conf"] is not None else None
+    h_lens = pin(pi["draft_lens"], np.int32)
+    h_cost = pin(pi["cost"], np.float32) if pi["cost"] is not None else None
+    h_tgt = pin(vi["target"].view(np.int16) if w.dtype == S.BF16 else vi["target"])
+    h_dft = pin(vi["draft"].view(np.int16) if w.dtype == S.BF16 else vi["draft"])
+    h_ids = pin(vi["draft_ids"], np.int32)
+    h_u = pin(vi["uniforms"], np.float32)
+    h_t = pin(vi["temps"], np.float32)
+    h_acc = torch.empty(bs, dtype=torch.int32).pin_memory()
+    h_out = torch.empty((bs, k + 1), dtype=torch.int32).pin_memory()
+    d_conf = torch.empty_like(h_conf, device=dev) if h_conf is not None else None
+    d_lens = torch.empty_like(h_lens, device=dev)
+    d_cost = torch.empty_like(h_cost, device=dev) if h_cost is not None else None
+    d_tgt = torch.empty((rows_cap, w.V), dtype=tdt, device=dev)
+    d_dft = torch.empty((max(bs * k, 1), w.V), dtype=tdt, device=dev)
+    d_ids = torch.zeros(max(bs * k, 1), dtype=torch.int32, device=dev)
+    d_u = torch.empty_like(h_u, device=dev)
+    d_t = torch.empty_like(h_t, device=dev)
+    d_B = torch.zeros(1, dtype=torch.int32, device=dev)
+    d_mask = torch.zeros((bs, max(k, 1)), dtype=torch.uint8, device=dev)
+    d_nv = torch.zeros(bs, dtype=torch.int32, device=dev)
+    d_cu = torch.zeros(bs + 1, dtype=torch.int32, device=dev)
+    d_err = torch.zeros(1, dtype=torch.int32, device=dev)
+    d_acc = torch.zeros(bs, dtype=torch.int32, device=dev)
+    d_out = torch.zeros((bs, k + 1), dtype=torch.int32, device=dev)
+    d_ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    h2d = 0
+    for h in (h_conf, h_lens, h_cost, h_tgt, h_dft, h_ids, h_u, h_t):
+        if h is not None:
+            h2d += h.numel() * h.element_size()
+    d2h = h_acc.numel() * 4 + h_out.numel() * 4
+
+    def step():
+        if h_conf is not None:
+            d_conf.copy_(h_conf, non_blocking=True)
+        d_lens.copy_(h_lens, non_blocking=True)
+        if h_cost is not None:
+            d_cost.copy_(h_cost, non_blocking=True)
+        d_tgt[:rows_t].copy_(h_tgt, non_blocking=True)
+        if B > 0:
+            d_dft[:B].copy_(h_dft, non_blocking=True)
+            d_ids[:B].copy_(h_ids, non_blocking=True)
+        d_u.copy_(h_u, non_blocking=True)
+        d_t.copy_(h_t, non_blocking=True)
+        sd.sd_plan(d_conf, None, None, 0, d_lens, bs, k, d_cost,
+                   0 if h_cost is None else h_cost.numel(), w.T, w.mode, d_B, d_mask, d_nv, d_cu,
+                   d_err, None, 0, stream)
+        sd.sd_verify_rows(d_tgt, d_dft, dtype, w.V, d_ids, d_u, d_t, d_cu, bs, k, None, d_err, d_ws,
+                          ws_bytes, cfg=cfg, stream=stream)
+        sd.sd_verify_finalize(d_ids, d_cu, bs, k, d_acc, d_out, d_err, d_ws, ws_bytes, stream)
+        h_acc.copy_(d_acc, non_blocking=True)
+        h_out.copy_(d_out, non_blocking=True)
+
+    for _ in range(min(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1)
+    n = np.diff(cu) - 1
+    return {"value": float(n.sum()) * args.steps / (ms / 1e3), "unit": "verified draft tokens/s",
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+            "ms_per_step": ms / args.steps, "_ms": ms}
+
+
+def main():
+    args = parse()
+    rank, world, local = dist_env()
+    w = S.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        run_reference(args, w, rank, world)
+        return
+    run_ours(args, w, rank, world, local)
+
+
+if __name__ == "__main__":
+    main()

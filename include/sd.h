@@ -222,6 +222,12 @@ sd_status sd_verify_launch_info(int V, sd_dtype dt, const sd_launch_cfg* req,
                                 sd_launch_cfg* chosen, int* threads, size_t* smem_bytes);
 
 const char* sd_status_string(sd_status s);
+
+/* Name and text of the last CUDA error an entry point returned SD_ERR_CUDA
+ * for, on the calling host thread ("no error" if none).  The pointer stays
+ * valid until the thread's next failing call. */
+const char* sd_last_error_string(void);
+
 int sd_abi_version(void);
 
 #ifdef __cplusplus

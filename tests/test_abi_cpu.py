@@ -1,0 +1,122 @@
+"""CPU-side checks of the C-ABI library: it loads without a GPU, exports every
+symbol include/sd.h declares, and rejects invalid arguments on the host
+before touching CUDA."""
+import ctypes
+import re
+from pathlib import Path
+
+import pytest
+
+ROOT = Path(__file__).resolve().parent.parent
+
+
+@pytest.fixture(scope="module")
+def lib():
+    import torch  # noqa: F401  (shares its CUDA runtime with the library)
+    import speculative_decoding_verification_sd_gb300 as sd
+    sd.build()
+    return sd._lib.load()
+
+
+def declared_symbols():
+    text = (ROOT / "include" / "sd.h").read_text()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"\b(sd_[a-z_]+)\s*\(", text)
+    return sorted(set(names))
+
+
+def test_header_declarations_are_exported(lib):
+    names = declared_symbols()
+    assert "sd_plan" in names and "sd_verify" in names
+    for n in names:
+        assert hasattr(lib, n), f"{n} declared in include/sd.h but not exported"
+    import speculative_decoding_verification_sd_gb300 as sd
+    assert sorted(sd._lib.EXPORTS) == names
+
+
+def test_abi_version_and_status_strings(lib):
+    import speculative_decoding_verification_sd_gb300 as sd
+    assert lib.sd_abi_version() == 1
+    for st in (0, -1, -2, -3, -4, -5):
+        assert sd._lib.status_string(st)
+
+
+def test_workspace_sizes(lib):
+    import speculative_decoding_verification_sd_gb300 as sd
+    assert sd.sd_plan_workspace_bytes(256, 7) == 0
+    rows = 256 * 8
+    assert sd.sd_verify_workspace_bytes(256, 7) >= rows * 5
+    assert sd.sd_verify_workspace_bytes(0, 7) == 0
+
+
+FAKE = 1 << 20  # a non-null address that is never dereferenced on these paths
+
+
+def test_plan_rejects_bad_arguments_on_host(lib):
+    import speculative_decoding_verification_sd_gb300 as sd
+    P = FAKE
+
+    def call(**kw):
+        a = dict(conf_logits=P, budget_conf=None, budget_draft_lens=None, bs_budget=0,
+                 draft_lens=P, bs=4, k_max=3, cost_table=P, cost_len=65, T=4, mode=0, B_out=P,
+                 slot_mask=P, num_verified=P, cu_seqlens=P, err_flag=P, workspace=None,
+                 ws_bytes=0, stream=0)
+        a.update(kw)
+        return lib.sd_plan(a["conf_logits"], a["budget_conf"], a["budget_draft_lens"],
+                           a["bs_budget"], a["draft_lens"], a["bs"], a["k_max"], a["cost_table"],
+                           a["cost_len"], a["T"], a["mode"], a["B_out"], a["slot_mask"],
+                           a["num_verified"], a["cu_seqlens"], a["err_flag"], a["workspace"],
+                           a["ws_bytes"], a["stream"])
+
+    assert call(bs=0) == sd.SD_ERR_INVALID_ARG
+    assert call(k_max=-1) == sd.SD_ERR_INVALID_ARG
+    assert call(k_max=16) == sd.SD_ERR_UNSUPPORTED
+    assert call(mode=7) == sd.SD_ERR_INVALID_ARG
+    assert call(draft_lens=None) == sd.SD_ERR_INVALID_ARG
+    assert call(err_flag=None) == sd.SD_ERR_INVALID_ARG
+    assert call(conf_logits=None) == sd.SD_ERR_INVALID_ARG
+    assert call(T=0) == sd.SD_ERR_INVALID_ARG
+    assert call(T=65) == sd.SD_ERR_SHAPE
+    assert call(bs=2048, k_max=7) == sd.SD_ERR_UNSUPPORTED
+    assert call(budget_conf=P, budget_draft_lens=None) == sd.SD_ERR_INVALID_ARG
+
+
+def test_verify_rejects_bad_arguments_on_host(lib):
+    import speculative_decoding_verification_sd_gb300 as sd
+    P = FAKE
+    nb = sd.sd_verify_workspace_bytes(4, 3)
+
+    def call(**kw):
+        a = dict(t=P, d=P, dt=1, V=1024, ids=P, u=P, temps=P, cu=P, bs=4, k_max=3, acc=P, out=P,
+                 probs=None, err=P, ws=P, nb=nb, stream=0)
+        a.update(kw)
+        return lib.sd_verify(a["t"], a["d"], a["dt"], a["V"], a["ids"], a["u"], a["temps"],
+                             a["cu"], a["bs"], a["k_max"], a["acc"], a["out"], a["probs"],
+                             a["err"], a["ws"], a["nb"], a["stream"])
+
+    assert call(bs=0) == sd.SD_ERR_INVALID_ARG
+    assert call(k_max=20) == sd.SD_ERR_UNSUPPORTED
+    assert call(bs=5000) == sd.SD_ERR_UNSUPPORTED
+    assert call(dt=9) == sd.SD_ERR_INVALID_ARG
+    assert call(V=0) == sd.SD_ERR_INVALID_ARG
+    assert call(V=(1 << 22) + 1) == sd.SD_ERR_UNSUPPORTED
+    assert call(t=None) == sd.SD_ERR_INVALID_ARG
+    assert call(acc=None) == sd.SD_ERR_INVALID_ARG
+    assert call(ws=None) == sd.SD_ERR_INVALID_ARG
+    assert call(ws=P + 4) == sd.SD_ERR_INVALID_ARG  # workspace not 16-byte aligned
+    assert call(nb=nb - 1) == sd.SD_ERR_SHAPE
+
+
+def test_binding_refuses_host_tensors(lib):
+    import torch
+    import speculative_decoding_verification_sd_gb300 as sd
+    with pytest.raises(ValueError):
+        sd.sd_verify_workspace_bytes(1, 1) and sd._ptr(torch.zeros(3))
+
+
+def test_product_path_does_not_import_the_oracle():
+    pkg = ROOT / "speculative_decoding_verification_sd_gb300"
+    for f in list(pkg.rglob("*.py")) + list(pkg.rglob("*.cu")) + list(pkg.rglob("*.cuh")) + list(pkg.rglob("*.h")):
+        text = f.read_text()
+        assert "import oracle" not in text and "from oracle" not in text, f
+        assert "sd_oracle" not in text, f

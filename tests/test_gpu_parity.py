@@ -1,0 +1,194 @@
+"""GPU parity: the C-ABI path against the CPU oracle on identical seeded bytes.
+
+Small cases compare every output; full-size workloads compare the plan
+exactly, the sampled requests one by one against the oracle, and every
+request through invariants (and greedy requests against the target argmax).
+"""
+import numpy as np
+import pytest
+
+import sdsynth as S
+from harness import (TALLY, check_properties, compare_plan, compare_verify, gpu_plan,
+                     gpu_verify, oracle_plan, oracle_verify)
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+if not torch.cuda.is_available():
+    pytest.skip("needs a CUDA GPU", allow_module_level=True)
+
+import speculative_decoding_verification_sd_gb300 as sd  # noqa: E402
+
+
+def _step(w, seed, step=0, cfg=None, requests=None, split=False):
+    pi = S.plan_inputs(w, seed, step)
+    o_plan = oracle_plan(pi, w.k_max)
+    g_plan = gpu_plan(pi, w.k_max)
+    assert g_plan["err"] == 0
+    compare_plan(g_plan, o_plan, f"{w.name} seed={seed} step={step}")
+    cu = o_plan["cu_seqlens"]
+    vi = S.verify_inputs(w, seed, step, cu, pi["draft_lens"])
+    g = gpu_verify(w, vi, cu, w.k_max, cfg=cfg, split=split)
+    assert g["err"] == 0
+    o = oracle_verify(w, vi, cu, w.k_max, requests=requests)
+    compare_verify(g, o, cu, w.k_max, requests=requests, what=f"{w.name} seed={seed}")
+    check_properties(g, cu, w.k_max, w.V, vi["draft_ids"])
+    return pi, o_plan, vi, g, o
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_tiny_all_outputs(seed):
+    _step(S.WORKLOADS["tiny"], seed)
+
+
+SMALL = S.WORKLOADS["adaptive_hc"].with_(bs=12, k_max=5, T=12, name="small")
+
+
+@pytest.mark.parametrize("dtype", [S.F32, S.BF16])
+@pytest.mark.parametrize("V", [20000, 1003])
+@pytest.mark.parametrize("cluster", [1, 2, 4, 8, 16])
+def test_small_every_cluster_shape(dtype, V, cluster):
+    """Several slices per row, ragged last slice, both the bulk-copy path
+    (V*elem % 16 == 0) and the staged path (V = 1003)."""
+    w = SMALL.with_(V=V, dtype=dtype)
+    _step(w, 100 + cluster, cfg={"cluster": cluster})
+
+
+@pytest.mark.parametrize("stages", [1, 2, 3, 4])
+def test_small_stage_counts(stages):
+    w = SMALL.with_(V=20000, dtype=S.BF16, bs=32, T=32)
+    _step(w, 7, cfg={"cluster": 2, "stages": stages, "clusters": 3})
+
+
+def test_varlen_draft_lengths_and_zero_drafts():
+    w = S.WORKLOADS["varlen_mixed"].with_(bs=24, V=5000)
+    for step in range(3):
+        _step(w, 11, step)
+    # A plan that verifies nothing: every request has only its bonus row.
+    w0 = SMALL.with_(V=3000, cost=np.arange(2049, dtype=np.float32))
+    pi = S.plan_inputs(w0, 3, 0)
+    assert oracle_plan(pi, w0.k_max)["B"] == 0
+    _step(w0, 3)
+
+
+def _full(name, seed, n_sample, step=0):
+    w = S.WORKLOADS[name]
+    rng = np.random.default_rng(seed)
+    req = sorted(rng.choice(w.bs, size=min(n_sample, w.bs), replace=False).tolist())
+    pi, o_plan, vi, g, o = _step(w, seed, step, requests=req)
+    # Greedy requests emit the target argmax along the accepted path.
+    cu = o_plan["cu_seqlens"]
+    amax = g["target_dev"][: int(cu[-1])]
+    if w.dtype == S.BF16:
+        amax = amax.view(torch.bfloat16)
+    amax = amax.float().argmax(dim=1).cpu().numpy()
+    for i in np.nonzero(vi["temps"] == 0)[0]:
+        a = g["accepted_len"][i]
+        assert list(g["out_tokens"][i, : a + 1]) == [int(amax[cu[i] + j]) for j in range(a + 1)]
+    return g
+
+
+def test_full_adaptive_hc():
+    g = _full("adaptive_hc", 2024, 24)
+    # the planner verifies a strict subset of the 7 drafted slots
+    assert 0 < (g["accepted_len"] >= 0).sum()
+
+
+def test_full_dense_fixed_k():
+    _full("dense_fixed_k", 5, 12)
+
+
+def test_full_varlen_mixed_steps():
+    w = S.WORKLOADS["varlen_mixed"]
+    for step in range(w.steps):  # budget from the previous step's confidences
+        pi = S.plan_inputs(w, 77, step)
+        compare_plan(gpu_plan(pi, w.k_max), oracle_plan(pi, w.k_max), f"varlen step {step}")
+    for step in (0, 1, w.steps - 1):
+        _full("varlen_mixed", 77, 8, step)
+
+
+def test_full_stress():
+    _full("stress", 31337, 16)
+
+
+# ---------------------------------------------------------------------------
+# device-side checks: bad data raises a flag and yields well-formed outputs
+
+
+def test_bad_cu_seqlens_flags_and_reads_nothing():
+    w = SMALL.with_(V=2000)
+    pi = S.plan_inputs(w, 1, 0)
+    o_plan = oracle_plan(pi, w.k_max)
+    cu = o_plan["cu_seqlens"].copy()
+    vi = S.verify_inputs(w, 1, 0, cu, pi["draft_lens"])
+    bad = cu.copy()
+    bad[3] = bad[2] + w.k_max + 5  # a request longer than k_max + 1 rows
+    g = gpu_verify(w, vi, bad, w.k_max)
+    assert g["err"] & sd.SD_DEV_ERR_CU_SEQLENS
+    assert np.all(g["accepted_len"] == 0)
+    assert np.all(g["out_tokens"] == -1)
+
+
+def test_bad_draft_id_and_nan_logits_flag():
+    w = SMALL.with_(V=2000)
+    pi = S.plan_inputs(w, 2, 0)
+    cu = oracle_plan(pi, w.k_max)["cu_seqlens"]
+    vi = S.verify_inputs(w, 2, 0, cu, pi["draft_lens"])
+    if len(vi["draft_ids"]) == 0:
+        pytest.skip("no verified slot")
+    vi["draft_ids"] = vi["draft_ids"].copy()
+    vi["draft_ids"][0] = w.V + 3
+    g = gpu_verify(w, vi, cu, w.k_max)
+    assert g["err"] & sd.SD_DEV_ERR_DRAFT_ID
+    check_properties(g, cu, w.k_max, w.V, vi["draft_ids"])
+    vi2 = S.verify_inputs(w, 2, 0, cu, pi["draft_lens"])
+    vi2["target"] = vi2["target"].copy()
+    vi2["target"][0, 5] = np.float32(np.nan)
+    g2 = gpu_verify(w, vi2, cu, w.k_max)
+    assert g2["err"] & sd.SD_DEV_ERR_LOGITS
+
+
+def test_plan_device_checks():
+    w = SMALL.with_(V=2000)
+    pi = S.plan_inputs(w, 4, 0)
+    pi_bad = dict(pi, draft_lens=pi["draft_lens"].copy())
+    pi_bad["draft_lens"][2] = w.k_max + 1
+    g = gpu_plan(pi_bad, w.k_max)
+    assert g["err"] & sd.SD_DEV_ERR_DRAFT_LENS
+    assert g["B"] == 0 and list(g["cu_seqlens"]) == list(range(w.bs + 1))
+    pi_nan = dict(pi, conf=pi["conf"].copy())
+    pi_nan["conf"][1] = np.nan
+    assert gpu_plan(pi_nan, w.k_max)["err"] & sd.SD_DEV_ERR_CONF
+    pi_cost = dict(pi, cost=pi["cost"].copy())
+    pi_cost["cost"][w.T + 1] = -1.0
+    assert gpu_plan(pi_cost, w.k_max)["err"] & sd.SD_DEV_ERR_COST
+
+
+def test_random_small_plans_match_oracle():
+    rng = np.random.default_rng(99)
+    for trial in range(60):
+        bs = int(rng.integers(1, 40))
+        k_max = int(rng.integers(0, 9))
+        dl = rng.integers(0, k_max + 1, bs).astype(np.int32)
+        T = int(rng.integers(1, 50))
+        L = T + int(rng.integers(0, dl.sum() + 3))
+        n = np.arange(L + 1)
+        cost = (1.0 + rng.uniform(0, 0.05) * n + (trial % 2) * rng.uniform(0, 0.3, n.size)).astype(np.float32)
+        pi = {"draft_lens": dl, "conf": rng.normal(1, 2, dl.sum()).astype(np.float32), "cost": cost,
+              "T": T, "mode": S.MODE_ADAPTIVE, "budget_conf": None, "budget_draft_lens": None}
+        if trial % 3 == 0 and k_max > 0:
+            bdl = rng.integers(0, k_max + 1, int(rng.integers(1, 40))).astype(np.int32)
+            pi["budget_conf"] = rng.normal(1, 2, bdl.sum()).astype(np.float32)
+            pi["budget_draft_lens"] = bdl
+        g = gpu_plan(pi, k_max)
+        assert g["err"] == 0
+        compare_plan(g, oracle_plan(pi, k_max), f"trial {trial}")
+        if trial % 5 == 0:
+            pa = dict(pi, mode=S.MODE_ALL_SLOTS)
+            compare_plan(gpu_plan(pa, k_max), oracle_plan(pa, k_max), f"all-slots {trial}")
+
+
+def test_zz_near_boundary_budget():
+    """Mismatches at near-boundary decisions stay within 0.01 % of decisions."""
+    TALLY.dump()
+    assert TALLY.near_mismatches <= max(1, 1e-4 * TALLY.decisions), TALLY.__dict__
