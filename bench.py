@@ -54,6 +54,7 @@ def parse():
     ap.add_argument("--seed", type=int, default=2026)
     ap.add_argument("--cluster", type=int, default=0)
     ap.add_argument("--stages", type=int, default=0)
+    ap.add_argument("--threads", type=int, default=0)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
@@ -278,7 +279,7 @@ def run_ours(args, w, rank, world, local):
     d_out = torch.zeros((bs, k + 1), dtype=torch.int32, device=dev)
     ws_bytes = sd.sd_verify_workspace_bytes(bs, k)
     d_ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
-    cfg = {"cluster": args.cluster, "stages": args.stages}
+    cfg = {"cluster": args.cluster, "stages": args.stages, "threads": args.threads}
 
     def step(s, ev=None):
         tgt, dft = sets[s & 1]
@@ -419,7 +420,8 @@ def run_ours(args, w, rank, world, local):
             "mean_acceptance_length": 1.0 + accepted / bs,
             "per_position_cumulative_acceptance": [round(x, 4) for x in pos],
             "device_err_flag": err, "input_generation_s": gen_s,
-            "launch": sd.sd_verify_launch_info(w.V, dtype, args.cluster, args.stages),
+            "launch": sd.sd_verify_launch_info(w.V, dtype, args.cluster, args.stages, 0,
+                                               args.threads),
         },
     }
     if rank == 0:

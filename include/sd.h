@@ -193,6 +193,7 @@ typedef struct {
   int cluster;   /* CTAs sharing one row pair: 1, 2, 4, 8 or 16 */
   int stages;    /* row slices in flight per CTA (1..4) */
   int clusters;  /* persistent clusters launched (<= what fits at once) */
+  int threads;   /* threads per CTA: 256 or 512 */
 } sd_launch_cfg;
 
 sd_status sd_verify(const void* target_logits, const void* draft_logits, sd_dtype dt, int V,

@@ -114,7 +114,7 @@ def _cfg(cfg):
     if isinstance(cfg, sd_launch_cfg):
         return ctypes.byref(cfg)
     c = sd_launch_cfg(int(cfg.get("cluster", 0)), int(cfg.get("stages", 0)),
-                      int(cfg.get("clusters", 0)))
+                      int(cfg.get("clusters", 0)), int(cfg.get("threads", 0)))
     return ctypes.byref(c)
 
 
@@ -136,8 +136,8 @@ def sd_verify_finalize(draft_ids, cu_seqlens, bs, k_max, accepted_len, out_token
     return _lib.check("sd_verify_finalize", st)
 
 
-def sd_verify_launch_info(V, dt, cluster=0, stages=0, clusters=0) -> dict:
-    req = sd_launch_cfg(cluster, stages, clusters)
+def sd_verify_launch_info(V, dt, cluster=0, stages=0, clusters=0, threads=0) -> dict:
+    req = sd_launch_cfg(cluster, stages, clusters, threads)
     out = sd_launch_cfg()
     thr = ctypes.c_int(0)
     smem = ctypes.c_size_t(0)

@@ -40,7 +40,8 @@ EXPORTS = ("sd_plan_workspace_bytes", "sd_plan", "sd_verify_workspace_bytes", "s
 
 
 class sd_launch_cfg(ctypes.Structure):
-    _fields_ = [("cluster", ctypes.c_int), ("stages", ctypes.c_int), ("clusters", ctypes.c_int)]
+    _fields_ = [("cluster", ctypes.c_int), ("stages", ctypes.c_int), ("clusters", ctypes.c_int),
+                ("threads", ctypes.c_int)]
 
 
 class SdError(RuntimeError):

@@ -166,27 +166,32 @@ __device__ int load_lengths(const int* lens_g, int n, int k_max, int* lens, int*
 
 // Sort keys of n requests, P slots each: high word = ~bits(s) (s >= 0, so a
 // larger survival gives a smaller key), low word = i*P + j (packed order).
-// Unused slots hold the sentinel, which sorts last.
+// Unused slots hold the sentinel, which sorts last.  The N packed confidence
+// logits are first copied to shared memory by the whole block (coalesced),
+// then each thread runs the short survival product of its requests.
 __device__ void build_keys(const float* conf, const int* lens, const int* off, int n, int P,
-                           unsigned long long* keys, PlanShared& sh) {
+                           int N, unsigned long long* keys, float* conf_s, PlanShared& sh) {
   int bad = 0;
+  for (int q = threadIdx.x; q < N; q += NT) {
+    const float c = conf[q];
+    if (!isfinite(c)) bad = 1;
+    conf_s[q] = c;
+  }
+  if (__syncthreads_or(bad) && threadIdx.x == 0) sh.err |= SD_DEV_ERR_CONF;
   for (int i = threadIdx.x; i < n; i += NT) {
     const int k = lens[i];
-    const float* c = conf + off[i];
+    const float* c = conf_s + off[i];
     float s = 1.0f;
     for (int j = 0; j < P; ++j) {
       unsigned long long key = kSentinel;
       if (j < k) {
-        const float cj = c[j];
-        if (!isfinite(cj)) bad = 1;
-        s = s * (1.0f / (1.0f + expf(-cj)));
+        s = s * (1.0f / (1.0f + expf(-c[j])));
         key = (static_cast<unsigned long long>(~__float_as_uint(s)) << 32) |
               static_cast<unsigned long long>(i * P + j);
       }
       keys[i * P + j] = key;
     }
   }
-  if (__syncthreads_or(bad) && threadIdx.x == 0) sh.err |= SD_DEV_ERR_CONF;
   __syncthreads();
 }
 
@@ -310,7 +315,7 @@ __global__ void __launch_bounds__(NT, 1) plan_kernel(const PlanParams p) {
       for (int i = p.bs_budget + threadIdx.x; i < nb; i += NT) { lens[i] = 0; off[i] = Nb; }
       __syncthreads();
       if (sh.err == 0) {
-        build_keys(p.budget_conf, lens, off, nb, p.P, keysA, sh);
+        build_keys(p.budget_conf, lens, off, nb, p.P, Nb, keysA, reinterpret_cast<float*>(keysB), sh);
         const unsigned long long* sorted = merge_runs(keysA, keysB, p.NPb, p.P);
         const int Bmax_b = min(Nb, L - p.T);
         int Bb = 0;
@@ -323,7 +328,7 @@ __global__ void __launch_bounds__(NT, 1) plan_kernel(const PlanParams p) {
       __syncthreads();
     }
     if (sh.err == 0) {
-      build_keys(p.conf, lens, off, nreq, p.P, keysA, sh);
+      build_keys(p.conf, lens, off, nreq, p.P, N, keysA, reinterpret_cast<float*>(keysB), sh);
       const unsigned long long* sorted = merge_runs(keysA, keysB, p.NP, p.P);
       if (!p.budget_conf && sh.err == 0)
         B = budget_argmax(sorted, min(N, L - p.T), p.bs, p.T, p.cost, cm, sh);

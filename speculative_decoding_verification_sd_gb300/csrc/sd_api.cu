@@ -94,9 +94,10 @@ cudaError_t resident_clusters(int elem, const sdk::VerifyShape& s, int* n) {
 sd_status shape_for(int V, sd_dtype dt, int bs, const sd_launch_cfg* cfg, bool bulk,
                     sdk::VerifyShape* shape) {
   const int elem = dt == SD_F32 ? 4 : 2;
-  int limit = 0;
-  if (note(sdk::rows_smem_limit(elem, bulk, &limit)) != cudaSuccess) return SD_ERR_CUDA;
-  if (!sdk::choose_verify_shape(V, elem, bs, cfg, bulk, limit, shape)) return SD_ERR_UNSUPPORTED;
+  bool fits = false;
+  if (note(sdk::choose_verify_shape(V, elem, bs, cfg, bulk, shape, &fits)) != cudaSuccess)
+    return SD_ERR_CUDA;
+  if (!fits) return SD_ERR_UNSUPPORTED;
   int m = 0;
   if (note(resident_clusters(elem, *shape, &m)) != cudaSuccess) return SD_ERR_CUDA;
   if (shape->clusters <= 0 || shape->clusters > m) shape->clusters = m;
@@ -204,7 +205,8 @@ sd_status sd_verify_rows(const void* target_logits, const void* draft_logits, sd
   if (V > SD_MAX_V) return SD_ERR_UNSUPPORTED;
   if (!target_logits || !uniforms || !temps || !cu_seqlens || !err_flag) return SD_ERR_INVALID_ARG;
   if (k_max > 0 && !draft_ids) return SD_ERR_INVALID_ARG;
-  if (cfg && (cfg->cluster < 0 || cfg->stages < 0 || cfg->clusters < 0)) return SD_ERR_INVALID_ARG;
+  if (cfg && (cfg->cluster < 0 || cfg->stages < 0 || cfg->clusters < 0 || cfg->threads < 0))
+    return SD_ERR_INVALID_ARG;
   const int elem = dt == SD_F32 ? 4 : 2;
   const bool bulk = (static_cast<size_t>(V) * elem) % 16 == 0 && aligned16(target_logits) &&
                     (draft_logits == nullptr || aligned16(draft_logits));
@@ -277,6 +279,7 @@ sd_status sd_verify_launch_info(int V, sd_dtype dt, const sd_launch_cfg* req,
   chosen->cluster = shape.C;
   chosen->stages = shape.S;
   chosen->clusters = shape.clusters;
+  chosen->threads = shape.threads;
   if (threads) *threads = shape.threads;
   if (smem_bytes) *smem_bytes = shape.smem;
   return SD_OK;

@@ -66,12 +66,10 @@ struct VerifyShape {
   bool bulk;
 };
 
-// Chooses (C, S, SL) for (V, dtype, bs) honouring a user request; returns
-// false when no shape fits this build's limits.
-bool choose_verify_shape(int V, int elem, int bs, const sd_launch_cfg* req, bool bulk,
-                         int dyn_limit, VerifyShape* out);
-// Dynamic shared memory available to the rows kernel on the current device.
-cudaError_t rows_smem_limit(int elem, bool bulk, int* limit);
+// Chooses (threads, C, S, SL) for (V, dtype, bs) on the current device,
+// honouring a user request; *fits = false when no shape fits.
+cudaError_t choose_verify_shape(int V, int elem, int bs, const sd_launch_cfg* req, bool bulk,
+                                VerifyShape* out, bool* fits);
 cudaError_t launch_verify_rows(const VerifyParams& p, int elem, const VerifyShape& shape,
                                cudaStream_t s);
 cudaError_t launch_verify_finalize(const int* draft_ids, const int* cu, int bs, int k_max,

@@ -21,6 +21,7 @@
 // are decided, every row that could end it (a rejecting row, or the bonus
 // row) draws its candidate token speculatively; K3 keeps the right one.
 #include <atomic>
+#include <algorithm>
 #include <climits>
 #include <mutex>
 #include <utility>
@@ -78,26 +79,70 @@ struct VT<uint16_t> {  // bf16 bit patterns
   }
 };
 
-// Per-CTA values exchanged through distributed shared memory.
+// Per-CTA partials pushed into every peer's shared memory (one entry per
+// source CTA), then read locally after the cluster barrier.
 struct __align__(16) Slot {
-  float a, b;  // pass A: max target / max draft; B: sum target / sum draft; C: residual sum
-  float c, d;  // pass B: target / draft logit at the draft token (owner CTA only)
-  unsigned long long key;  // pass A greedy: packed (value, -index) maximum
-  int flag;    // greedy: row holds NaN; pass B: owns the draft token
+  float mt, zt;  // target: local max and sum of 2^((l - mt) * s2); residual pass: sum
+  float md, zd;  // draft: local max and sum
+  float lt, ld;  // target / draft logit at the draft token (owner CTA only)
+  int flag;      // owns the draft token; greedy: row holds NaN
   int pad;
+  unsigned long long key;  // greedy: packed (value, -index) maximum
+  unsigned long long pad2;
 };
+
+constexpr int kMaxCluster = 16;
+constexpr int kMaxRounds = 32;
 
 __device__ __forceinline__ float from_ordered(uint32_t u) {
   return __uint_as_float((u & 0x80000000u) ? (u & 0x7FFFFFFFu) : ~u);
 }
 
-// Residual weight max(p - q, 0) of one element pair, with p = e_t / Z_t and
-// q = e_d / Z_d; the same expression is used by the sum and by the search.
+// Residual weight max(p - q, 0) of one element pair, with p = 2^(lt*s2 - bt)/Z_t
+// and q = 2^(ld*s2 - bd)/Z_d; the same expression serves the sum and the search.
 __device__ __forceinline__ float residual_w(float lt, float ld, float s2, float bt, float bd,
                                             float iZt, float iZd) {
   const float et = exp2_ftz(fmaf(lt, s2, -bt));
   const float ed = exp2_ftz(fmaf(ld, s2, -bd));
   return fmaxf(fmaf(et, iZt, -(ed * iZd)), 0.0f);
+}
+
+// Merge two (max, scaled sum) pairs of the online softmax.
+__device__ __forceinline__ void merge_ms(float& m, float& z, float m2, float z2, float s2) {
+  const float M = fmaxf(m, m2);
+  if (M == -INFINITY) {
+    z = 0.0f;
+  } else {
+    z = z * exp2_ftz((m - M) * s2) + z2 * exp2_ftz((m2 - M) * s2);
+  }
+  m = M;
+}
+
+__device__ __forceinline__ void warp_merge_ms(float& m, float& z, float s2) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float m2 = __shfl_xor_sync(kFull, m, o);
+    const float z2 = __shfl_xor_sync(kFull, z, o);
+    merge_ms(m, z, m2, z2, s2);
+  }
+}
+
+// One thread's vector of VE logits into its running (max, sum).
+template <int VE>
+__device__ __forceinline__ void online_add(const float (&f)[VE], float s2, float& m, float& z,
+                                           float& b) {
+  float vm = f[0];
+#pragma unroll
+  for (int e = 1; e < VE; ++e) vm = fmaxf(vm, f[e]);
+  if (vm > m) {
+    z = (m == -INFINITY) ? 0.0f : z * exp2_ftz((m - vm) * s2);
+    m = vm;
+    b = m * s2;
+  }
+  if (m != -INFINITY) {
+#pragma unroll
+    for (int e = 0; e < VE; ++e) z += exp2_ftz(fmaf(f[e], s2, -b));
+  }
 }
 
 template <typename T, int NT, bool BULK>
@@ -110,12 +155,11 @@ __global__ void __launch_bounds__(NT, 1) rows_kernel(const VerifyParams p) {
   static_assert(NW <= 32, "one lane per warp in the cross-warp passes");
 
   extern __shared__ __align__(128) unsigned char smem[];
-  __shared__ Slot slots[2][3];
-  __shared__ float Wt[NW], Wd[NW], Wr[NW];
+  __shared__ Slot slots[2][2][kMaxCluster];
+  __shared__ float Wm_t[NW], Wz_t[NW], Wm_d[NW], Wz_d[NW], Wr[NW];
+  __shared__ float Rr[NW][kMaxRounds];
   __shared__ unsigned long long Wk[NW];
   __shared__ int Wn[NW];
-  __shared__ int meta_x;
-  __shared__ float meta_u, meta_ufin;
 
   cg::cluster_group cluster = cg::this_cluster();
   const int C = p.C;
@@ -126,7 +170,9 @@ __global__ void __launch_bounds__(NT, 1) rows_kernel(const VerifyParams p) {
   const int V = p.V;
   const int SL = p.SL;
 
-  uint64_t* mbar = reinterpret_cast<uint64_t*>(smem + static_cast<size_t>(p.S) * p.stage_bytes);
+  // dynamic shared memory: stages | stage meta (x, u, ufin) | mbarriers | cu | tau
+  unsigned char* meta_base = smem + static_cast<size_t>(p.S) * p.stage_bytes;
+  uint64_t* mbar = reinterpret_cast<uint64_t*>(meta_base + 16 * 4);
   int* cu_s = reinterpret_cast<int*>(mbar + 4);
   float* tau_s = reinterpret_cast<float*>(cu_s + p.bs + 1);
 
@@ -155,7 +201,8 @@ __global__ void __launch_bounds__(NT, 1) rows_kernel(const VerifyParams p) {
   }
   if (badt && blockIdx.x == 0) raise_error(p.err, badt);
   if (BULK && tid == 0) {
-    for (int s = 0; s < p.S; ++s) mbar_init(&mbar[s], 1);
+    // one arrival from the bulk-copy issue, one when the metadata copies land
+    for (int s = 0; s < p.S; ++s) mbar_init(&mbar[s], 2);
     fence_mbar_init();
   }
   __syncthreads();
@@ -172,6 +219,9 @@ __global__ void __launch_bounds__(NT, 1) rows_kernel(const VerifyParams p) {
 
   auto stage_t = [&](int s) { return smem + static_cast<size_t>(s) * p.stage_bytes; };
   auto stage_d = [&](int s) { return stage_t(s) + static_cast<size_t>(SL) * ELEM; };
+  auto meta_x = [&](int s) { return reinterpret_cast<int*>(meta_base + 16 * s); };
+  auto meta_u = [&](int s) { return reinterpret_cast<float*>(meta_base + 16 * s + 4); };
+  auto meta_uf = [&](int s) { return reinterpret_cast<float*>(meta_base + 16 * s + 8); };
   auto locate = [&](int q, int& i, int& j, int& n) {
     int lo = 0, hi = p.bs;
     while (hi - lo > 1) {
@@ -183,11 +233,26 @@ __global__ void __launch_bounds__(NT, 1) rows_kernel(const VerifyParams p) {
     j = q - cu_s[i];
     n = cu_s[i + 1] - cu_s[i] - 1;
   };
-  // Producer (thread 0): stage item q's slices into stage s.
+  auto meta_src = [&](int q, int i, int j, int n, const int*& xs, const float*& us,
+                      const float*& ufs) {
+    const float* urow = p.uniforms + static_cast<size_t>(i) * (p.k_max + 1);
+    us = urow + j;  // j <= n <= k_max
+    ufs = urow + p.k_max;
+    xs = j < n ? p.draft_ids + (q - i) : reinterpret_cast<const int*>(ufs);
+  };
+  // Producer (thread 0): stage item q into stage s -- logit slices by bulk
+  // copy, the draft token and uniforms by 4-byte asynchronous copies.
   auto issue = [&](int q, int s) {
     int i, j, n;
     locate(q, i, j, n);
     const bool hd = tau_s[i] > 0.0f && j < n;
+    const int* xs;
+    const float *us, *ufs;
+    meta_src(q, i, j, n, xs, us, ufs);
+    cp_async4(meta_x(s), xs);
+    cp_async4(meta_u(s), us);
+    cp_async4(meta_uf(s), ufs);
+    cp_async_arrive_noinc(&mbar[s]);
     const uint32_t bytes = static_cast<uint32_t>(len) * ELEM;
     mbar_arrive_expect_tx(&mbar[s], hd ? 2 * bytes : bytes);
     if (len > 0) {
@@ -217,30 +282,46 @@ __global__ void __launch_bounds__(NT, 1) rows_kernel(const VerifyParams p) {
         else Tr::put_neg_inf(stage_d(s), e);
       }
     }
+    if (tid == 0) {
+      const int* xs;
+      const float *us, *ufs;
+      meta_src(q, i, j, n, xs, us, ufs);
+      *meta_x(s) = *xs;
+      *meta_u(s) = *us;
+      *meta_uf(s) = *ufs;
+    }
     __syncthreads();
   };
+  // Pushes warp 0's value `v` (valid in lanes < C) into slot [par][ph][rank]
+  // of every CTA of the cluster, then waits for all peers' pushes.
+  auto exchange = [&](int par, int ph, const Slot& v) {
+    if (warp == 0 && lane < C) *cluster.map_shared_rank(&slots[par][ph][rank], lane) = v;
+    cluster.sync();
+  };
 
-  // Search for the element at which the running sum of weights first exceeds
-  // theta, over this CTA's slice of the row.  `cta_inc` (per lane c < C) is
-  // the inclusive scan of the CTA totals, `Wsm` the per-warp totals of this
-  // CTA; `wfun(v, w)` fills the VE weights of vector v.  Only the CTA and the
-  // warp holding the crossing continue to the element level; rounding
-  // disagreements between levels fall back to the last positive weight.
-  auto owner_search = [&](float theta, float cta_w, float cta_inc, const float* Wsm, int q,
+  // Element search over this CTA's slice: the first element at which the
+  // running sum of weights exceeds theta.  `y_c` (lane c < C) holds the CTA
+  // totals, `y_w` (lane w < NW) this CTA's per-warp totals, `rsum` (nullable)
+  // the warp's per-round totals; `wfun(v, w)` fills the VE weights of vector
+  // v.  Only the CTA, warp and round holding the crossing go down a level;
+  // rounding disagreements between levels fall back to the last positive
+  // weight of the chosen range.
+  auto owner_search = [&](float theta, float y_c, float y_w, const float* rsum_base, int q,
                           auto wfun) {
-    const unsigned cross = __ballot_sync(kFull, lane < C && cta_inc > theta);
+    const float c_inc = warp_inclusive_scan(lane < C ? y_c : 0.0f, lane);
+    const unsigned cross = __ballot_sync(kFull, lane < C && c_inc > theta);
     int cstar;
     if (cross) {
       cstar = __ffs(cross) - 1;
     } else {
-      const unsigned pos = __ballot_sync(kFull, lane < C && cta_w > 0.0f);
+      const unsigned pos = __ballot_sync(kFull, lane < C && y_c > 0.0f);
       cstar = pos ? 31 - __clz(pos) : 0;
     }
-    const float up_c = __shfl_up_sync(kFull, cta_inc, 1);
+    const float up_c = __shfl_up_sync(kFull, c_inc, 1);
     const float excl_c = cstar == 0 ? 0.0f : __shfl_sync(kFull, up_c, cstar);
     if (rank != cstar) return;
     const float th_c = fmaxf(theta - excl_c, 0.0f);
-    const float ww = lane < NW ? Wsm[lane] : 0.0f;
+    const float ww = lane < NW ? y_w : 0.0f;
     const float winc = warp_inclusive_scan(ww, lane);
     const unsigned cw = __ballot_sync(kFull, lane < NW && winc > th_c);
     int wstar;
@@ -256,49 +337,61 @@ __global__ void __launch_bounds__(NT, 1) rows_kernel(const VerifyParams p) {
     const float th = fmaxf(th_c - excl_w, 0.0f);
     const int wb = min(nvec, wstar * vpw);
     const int we = min(nvec, wb + vpw);
-    float run = 0.0f;
-    int last_pos = -1;
-    for (int base = wb; base < we; base += 32) {
-      const int v = base + lane;
-      float w[VE];
-      float sv = 0.0f;
-      int lane_last = -1;
-      if (v < we) {
-        wfun(v, w);
-#pragma unroll
-        for (int e = 0; e < VE; ++e) {
-          sv += w[e];
-          if (w[e] > 0.0f) lane_last = lo_e + v * VE + e;
-        }
-      } else {
-#pragma unroll
-        for (int e = 0; e < VE; ++e) w[e] = 0.0f;
+    const int nr = (we - wb + 31) / 32;
+    const float* rsum = rsum_base ? rsum_base + wstar * kMaxRounds : nullptr;
+    for (int attempt = 0; attempt < 2; ++attempt) {
+      float run = 0.0f;
+      int r0 = 0;
+      if (rsum && attempt == 0 && nr <= kMaxRounds) {
+        while (r0 < nr - 1 && run + rsum[r0] <= th) run += rsum[r0++];
       }
-      const float inc = warp_inclusive_scan(sv, lane);
-      const float up = __shfl_up_sync(kFull, inc, 1);
-      const float excl = lane == 0 ? 0.0f : up;
-      const unsigned m = __ballot_sync(kFull, run + inc > th);
-      int lp = lane_last;
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) lp = max(lp, __shfl_xor_sync(kFull, lp, o));
-      last_pos = max(last_pos, lp);
-      if (m) {
-        const int ls = __ffs(m) - 1;
-        if (lane == ls) {
-          float r = run + excl;
-          int pick = lane_last >= 0 ? lane_last : lo_e + v * VE;
+      int last_pos = -1;
+      for (int base = wb + 32 * r0; base < we; base += 32) {
+        const int v = base + lane;
+        float w[VE];
+        float sv = 0.0f;
+        int lane_last = -1;
+        if (v < we) {
+          wfun(v, w);
 #pragma unroll
           for (int e = 0; e < VE; ++e) {
-            r += w[e];
-            if (r > th) { pick = lo_e + v * VE + e; break; }
+            sv += w[e];
+            if (w[e] > 0.0f) lane_last = lo_e + v * VE + e;
           }
-          p.ws_cand[q] = pick;
+        } else {
+#pragma unroll
+          for (int e = 0; e < VE; ++e) w[e] = 0.0f;
         }
+        const float inc = warp_inclusive_scan(sv, lane);
+        const float up = __shfl_up_sync(kFull, inc, 1);
+        const float excl = lane == 0 ? 0.0f : up;
+        const unsigned m = __ballot_sync(kFull, run + inc > th);
+        int lp = lane_last;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) lp = max(lp, __shfl_xor_sync(kFull, lp, o));
+        last_pos = max(last_pos, lp);
+        if (m) {
+          const int ls = __ffs(m) - 1;
+          if (lane == ls) {
+            float r = run + excl;
+            int pick = lane_last >= 0 ? lane_last : lo_e + v * VE;
+#pragma unroll
+            for (int e = 0; e < VE; ++e) {
+              r += w[e];
+              if (r > th) { pick = lo_e + v * VE + e; break; }
+            }
+            p.ws_cand[q] = pick;
+          }
+          return;
+        }
+        run += __shfl_sync(kFull, inc, 31);
+      }
+      if (r0 == 0 || attempt == 1) {
+        if (lane == 0) p.ws_cand[q] = last_pos >= 0 ? last_pos : lo_e + wb * VE;
         return;
       }
-      run += __shfl_sync(kFull, inc, 31);
+      // the stored round totals skipped past the crossing: rescan from the start
     }
-    if (lane == 0) p.ws_cand[q] = last_pos >= 0 ? last_pos : lo_e + wb * VE;
   };
 
   if (BULK && tid == 0)
@@ -322,20 +415,14 @@ __global__ void __launch_bounds__(NT, 1) rows_kernel(const VerifyParams p) {
     const bool bonus = (j == n);
     const Raw* vt = reinterpret_cast<const Raw*>(stage_t(st));
     const Raw* vd = reinterpret_cast<const Raw*>(stage_d(st));
-    const float* urow = p.uniforms + static_cast<size_t>(i) * (p.k_max + 1);
+    const int x = *meta_x(st);
+    const float u = *meta_u(st);
+    const float ufin = *meta_uf(st);
+    const bool x_ok = !bonus && x >= 0 && x < V;
+    const bool lead = (rank == 0 && tid == 0);
 
-    int x_ld = -1;
-    float u_ld = 0.0f, ufin_ld = 0.0f;
-    if (tid == 0) {  // issued early, consumed after pass A
-      ufin_ld = urow[p.k_max];
-      if (!bonus) {
-        u_ld = urow[j];
-        x_ld = p.draft_ids[q - i];
-      }
-    }
-
-    // ---------------- pass A: maxima (tau > 0) or argmax (tau = 0)
     if (greedy) {
+      // ---------------- argmax (lowest index on ties), one exchange
       float best = -INFINITY;
       int bidx = INT_MAX;
       int nanf = 0;
@@ -354,48 +441,20 @@ __global__ void __launch_bounds__(NT, 1) rows_kernel(const VerifyParams p) {
       key = warp_max_u64(key);
       nanf = __any_sync(kFull, nanf);
       if (lane == 0) { Wk[warp] = key; Wn[warp] = nanf; }
-    } else {
-      float mt = -INFINITY, md = -INFINITY;
-      for (int v = vb + lane; v < ve; v += 32) {
-        float f[VE];
-        Tr::unpack(vt[v], f);
-#pragma unroll
-        for (int e = 0; e < VE; ++e) mt = fmaxf(mt, f[e]);
-        if (has_draft) {
-          Tr::unpack(vd[v], f);
-#pragma unroll
-          for (int e = 0; e < VE; ++e) md = fmaxf(md, f[e]);
-        }
-      }
-      mt = warp_max(mt);
-      md = warp_max(md);
-      if (lane == 0) { Wt[warp] = mt; Wd[warp] = md; }
-    }
-    if (tid == 0) { meta_x = x_ld; meta_u = u_ld; meta_ufin = ufin_ld; }
-    __syncthreads();
-    if (warp == 0) {
-      Slot& sa = slots[par][0];
-      if (greedy) {
-        unsigned long long kk = warp_max_u64(lane < NW ? Wk[lane] : 0ull);
-        const int nn = __any_sync(kFull, lane < NW ? Wn[lane] : 0);
-        if (lane == 0) { sa.key = kk; sa.flag = nn; }
+      __syncthreads();
+      if (warp == 0) {
+        Slot sv;
+        sv.key = warp_max_u64(lane < NW ? Wk[lane] : 0ull);
+        sv.flag = __any_sync(kFull, lane < NW ? Wn[lane] : 0);
+        exchange(par, 0, sv);
       } else {
-        const float a = warp_max(lane < NW ? Wt[lane] : -INFINITY);
-        const float b = warp_max(lane < NW ? Wd[lane] : -INFINITY);
-        if (lane == 0) { sa.a = a; sa.b = b; }
+        cluster.sync();
       }
-    }
-    cluster.sync();
-    const Slot* pa = cluster.map_shared_rank(&slots[par][0], lane < C ? lane : 0);
-    const int x = meta_x;
-    const bool x_ok = !bonus && x >= 0 && x < V;
-    const bool lead = (rank == 0 && tid == 0);
-
-    if (greedy) {
-      const unsigned long long kk = warp_max_u64(lane < C ? pa->key : 0ull);
-      const int nn = __any_sync(kFull, lane < C ? pa->flag : 0);
-      const float best = from_ordered(static_cast<uint32_t>(kk >> 32));
-      const bool rowbad = nn || kk == 0ull || !isfinite(best);
+      const Slot& pc = slots[par][0][lane < C ? lane : 0];
+      const unsigned long long kk = warp_max_u64(lane < C ? pc.key : 0ull);
+      const int nn = __any_sync(kFull, lane < C ? pc.flag : 0);
+      const float bv = from_ordered(static_cast<uint32_t>(kk >> 32));
+      const bool rowbad = nn || kk == 0ull || !isfinite(bv);
       const int amax = rowbad ? 0 : static_cast<int>(0xFFFFFFFFu - static_cast<uint32_t>(kk));
       if (lead) {
         if (rowbad) raise_error(p.err, SD_DEV_ERR_LOGITS);
@@ -404,56 +463,57 @@ __global__ void __launch_bounds__(NT, 1) rows_kernel(const VerifyParams p) {
         p.ws_cand[q] = amax;
       }
     } else {
-      const float Mt = warp_max(lane < C ? pa->a : -INFINITY);
-      const float Md = warp_max(lane < C ? pa->b : -INFINITY);
       const float s2 = kLog2e / tau;
-      const float bt = Mt * s2;
-      const float bd = Md * s2;
-
-      // ---------------- pass B: normalisers
-      float zt = 0.0f, zd = 0.0f;
+      // ---------------- fused max + sum (online softmax), one exchange
+      float mt = -INFINITY, zt = 0.0f, bt_run = 0.0f;
+      float md = -INFINITY, zd = 0.0f, bd_run = 0.0f;
       for (int v = vb + lane; v < ve; v += 32) {
         float f[VE];
         Tr::unpack(vt[v], f);
-#pragma unroll
-        for (int e = 0; e < VE; ++e) zt += exp2_ftz(fmaf(f[e], s2, -bt));
+        online_add<VE>(f, s2, mt, zt, bt_run);
         if (has_draft) {
           Tr::unpack(vd[v], f);
-#pragma unroll
-          for (int e = 0; e < VE; ++e) zd += exp2_ftz(fmaf(f[e], s2, -bd));
+          online_add<VE>(f, s2, md, zd, bd_run);
         }
       }
-      zt = warp_sum(zt);
-      zd = warp_sum(zd);
-      if (lane == 0) { Wt[warp] = zt; Wd[warp] = zd; }
+      warp_merge_ms(mt, zt, s2);
+      if (has_draft) warp_merge_ms(md, zd, s2);
+      if (lane == 0) { Wm_t[warp] = mt; Wz_t[warp] = zt; Wm_d[warp] = md; Wz_d[warp] = zd; }
       __syncthreads();
-      Slot& sb = slots[par][1];
       if (warp == 0) {
-        const float it = warp_inclusive_scan(lane < NW ? Wt[lane] : 0.0f, lane);
-        const float id = warp_inclusive_scan(lane < NW ? Wd[lane] : 0.0f, lane);
-        if (lane == 31) { sb.a = it; sb.b = id; }
-        if (lane == 0) {
-          sb.flag = 0;
-          if (x_ok && x >= lo_e && x < lo_e + len) {
-            sb.c = Tr::at(stage_t(st), x - lo_e);
-            sb.d = has_draft ? Tr::at(stage_d(st), x - lo_e) : 0.0f;
-            sb.flag = 1;
-          }
+        float m1 = lane < NW ? Wm_t[lane] : -INFINITY, z1 = lane < NW ? Wz_t[lane] : 0.0f;
+        float m2 = lane < NW ? Wm_d[lane] : -INFINITY, z2 = lane < NW ? Wz_d[lane] : 0.0f;
+        warp_merge_ms(m1, z1, s2);
+        if (has_draft) warp_merge_ms(m2, z2, s2);
+        Slot sv;
+        sv.mt = m1; sv.zt = z1; sv.md = m2; sv.zd = z2;
+        sv.flag = 0;
+        sv.lt = 0.0f; sv.ld = 0.0f;
+        if (x_ok && x >= lo_e && x < lo_e + len) {
+          sv.lt = Tr::at(stage_t(st), x - lo_e);
+          sv.ld = has_draft ? Tr::at(stage_d(st), x - lo_e) : 0.0f;
+          sv.flag = 1;
         }
+        exchange(par, 0, sv);
+      } else {
+        cluster.sync();
       }
-      cluster.sync();
-      const Slot* pb = cluster.map_shared_rank(&slots[par][1], lane < C ? lane : 0);
-      const float zt_c = lane < C ? pb->a : 0.0f;
-      const float zd_c = lane < C ? pb->b : 0.0f;
-      const float zt_inc = warp_inclusive_scan(zt_c, lane);
-      const float Zt = __shfl_sync(kFull, zt_inc, 31);
-      const float Zd = __shfl_sync(kFull, warp_inclusive_scan(zd_c, lane), 31);
+      // Global statistics, identical in every CTA and warp.
+      const Slot& pc = slots[par][0][lane < C ? lane : 0];
+      const float mt_c = lane < C ? pc.mt : -INFINITY, zt_c = lane < C ? pc.zt : 0.0f;
+      const float md_c = lane < C ? pc.md : -INFINITY, zd_c = lane < C ? pc.zd : 0.0f;
+      const float Mt = warp_max(mt_c);
+      const float Md = warp_max(md_c);
+      const float bt = Mt * s2, bd = Md * s2;
+      const float yt_c = (lane < C && mt_c != -INFINITY) ? zt_c * exp2_ftz(fmaf(mt_c, s2, -bt)) : 0.0f;
+      const float yd_c = (lane < C && md_c != -INFINITY) ? zd_c * exp2_ftz(fmaf(md_c, s2, -bd)) : 0.0f;
+      const float Zt = __shfl_sync(kFull, warp_inclusive_scan(yt_c, lane), 31);
+      const float Zd = __shfl_sync(kFull, warp_inclusive_scan(yd_c, lane), 31);
       const int cx = x_ok ? min(x / SL, C - 1) : 0;
-      const float ltx = __shfl_sync(kFull, lane < C ? pb->c : 0.0f, cx);
-      const float ldx = __shfl_sync(kFull, lane < C ? pb->d : 0.0f, cx);
+      const float ltx = slots[par][0][cx].lt;
+      const float ldx = slots[par][0][cx].ld;
       const bool rowbad = !isfinite(Mt) || !(isfinite(Zt) && Zt > 0.0f) ||
                           (has_draft && (!isfinite(Md) || !(isfinite(Zd) && Zd > 0.0f)));
-      const float ufin = meta_ufin;
       auto p_weight = [&](int v, float (&w)[VE]) {
         float f[VE];
         Tr::unpack(vt[v], f);
@@ -475,13 +535,13 @@ __global__ void __launch_bounds__(NT, 1) rows_kernel(const VerifyParams p) {
         if (x_ok && !rowbad) {
           px = exp2_full(fmaf(ltx, s2, -bt)) / Zt;
           qx = exp2_full(fmaf(ldx, s2, -bd)) / Zd;
-          acc = (meta_u * qx) <= px;
+          acc = (u * qx) <= px;
         }
         need_residual = !acc && !rowbad;
         if (lead) {
           if (rowbad) raise_error(p.err, SD_DEV_ERR_LOGITS);
           if (!x_ok) raise_error(p.err, SD_DEV_ERR_DRAFT_ID);
-          if (!(meta_u >= 0.0f && meta_u < 1.0f)) raise_error(p.err, SD_DEV_ERR_UNIFORM);
+          if (!(u >= 0.0f && u < 1.0f)) raise_error(p.err, SD_DEV_ERR_UNIFORM);
           if (!acc && !(ufin >= 0.0f && ufin < 1.0f)) raise_error(p.err, SD_DEV_ERR_UNIFORM);
           p.ws_accept[q] = static_cast<uint8_t>(acc);
           if (rowbad) p.ws_cand[q] = 0;
@@ -492,46 +552,60 @@ __global__ void __launch_bounds__(NT, 1) rows_kernel(const VerifyParams p) {
         }
       }
       if (need_residual) {
-        // ---------------- pass C: residual mass max(p - q, 0)
+        // ---------------- residual mass max(p - q, 0), per-round totals kept
         const float iZt = 1.0f / Zt, iZd = 1.0f / Zd;
-        float sr = 0.0f;
-        for (int v = vb + lane; v < ve; v += 32) {
-          float f[VE], g[VE];
-          Tr::unpack(vt[v], f);
-          Tr::unpack(vd[v], g);
-#pragma unroll
-          for (int e = 0; e < VE; ++e) sr += residual_w(f[e], g[e], s2, bt, bd, iZt, iZd);
-        }
-        sr = warp_sum(sr);
-        if (lane == 0) Wr[warp] = sr;
-        __syncthreads();
-        if (warp == 0) {
-          const float ir = warp_inclusive_scan(lane < NW ? Wr[lane] : 0.0f, lane);
-          if (lane == 31) slots[par][2].a = ir;
-        }
-        cluster.sync();
-        const Slot* pc = cluster.map_shared_rank(&slots[par][2], lane < C ? lane : 0);
-        const float sr_c = lane < C ? pc->a : 0.0f;
-        const float sr_inc = warp_inclusive_scan(sr_c, lane);
-        const float S = __shfl_sync(kFull, sr_inc, 31);
-        if (S > 0.0f && isfinite(S)) {
-          owner_search(ufin * S, sr_c, sr_inc, Wr, q, [&](int v, float (&w)[VE]) {
+        float wsum = 0.0f;
+        int r = 0;
+        for (int base = vb; base < ve; base += 32, ++r) {
+          const int v = base + lane;
+          float sv = 0.0f;
+          if (v < ve) {
             float f[VE], g[VE];
             Tr::unpack(vt[v], f);
             Tr::unpack(vd[v], g);
 #pragma unroll
-            for (int e = 0; e < VE; ++e) w[e] = residual_w(f[e], g[e], s2, bt, bd, iZt, iZd);
-          });
+            for (int e = 0; e < VE; ++e) sv += residual_w(f[e], g[e], s2, bt, bd, iZt, iZd);
+          }
+          const float rs = warp_sum(sv);
+          if (lane == 0 && r < kMaxRounds) Rr[warp][r] = rs;
+          wsum += rs;
+        }
+        if (lane == 0) Wr[warp] = wsum;
+        __syncthreads();
+        if (warp == 0) {
+          Slot sv;
+          sv.zt = __shfl_sync(kFull, warp_inclusive_scan(lane < NW ? Wr[lane] : 0.0f, lane), 31);
+          exchange(par, 1, sv);
+        } else {
+          cluster.sync();
+        }
+        const float sr_c = lane < C ? slots[par][1][lane].zt : 0.0f;
+        const float S = __shfl_sync(kFull, warp_inclusive_scan(sr_c, lane), 31);
+        if (S > 0.0f && isfinite(S)) {
+          owner_search(ufin * S, sr_c, lane < NW ? Wr[lane] : 0.0f, &Rr[0][0], q,
+                       [&](int v, float (&w)[VE]) {
+                         float f[VE], g[VE];
+                         Tr::unpack(vt[v], f);
+                         Tr::unpack(vd[v], g);
+#pragma unroll
+                         for (int e = 0; e < VE; ++e)
+                           w[e] = residual_w(f[e], g[e], s2, bt, bd, iZt, iZd);
+                       });
         } else {
           need_p = true;  // no residual mass in fp32: draw from p instead
         }
       }
-      if (need_p) owner_search(ufin * Zt, zt_c, zt_inc, Wt, q, p_weight);
+      if (need_p) {
+        float yw = 0.0f;
+        if (lane < NW && Wm_t[lane] != -INFINITY)
+          yw = Wz_t[lane] * exp2_ftz(fmaf(Wm_t[lane], s2, -bt));
+        owner_search(ufin * Zt, yt_c, yw, nullptr, q, p_weight);
+      }
     }
     __syncthreads();  // stage st and the per-warp arrays are free again
     if (BULK && tid == 0 && k + p.S < nitems) issue(cid + (k + p.S) * G, st);
   }
-  cluster.sync();  // peers may still read this CTA's slots
+  cluster.sync();  // peers may still push into this CTA's slots
 }
 
 __global__ void finalize_kernel(const int* __restrict__ draft_ids, const int* __restrict__ cu,
@@ -561,30 +635,33 @@ __global__ void finalize_kernel(const int* __restrict__ draft_ids, const int* __
   for (int j = a + 1; j <= k_max; ++j) o[j] = -1;
 }
 
-constexpr int kRowThreads = 512;
-
-template <typename T, bool BULK>
+template <typename T, int NT, bool BULK>
 void* rows_fn() {
-  return reinterpret_cast<void*>(&rows_kernel<T, kRowThreads, BULK>);
+  return reinterpret_cast<void*>(&rows_kernel<T, NT, BULK>);
 }
 
+// All instantiations: (fp32, bf16) x (bulk, staged) x (256, 512 threads).
 void* const* kernel_table() {
-  static void* const t[8] = {rows_fn<float, true>(), rows_fn<float, false>(),
-                             rows_fn<uint16_t, true>(), rows_fn<uint16_t, false>(),
-                             nullptr, nullptr, nullptr, nullptr};
+  static void* const t[8] = {rows_fn<float, 256, true>(),    rows_fn<float, 256, false>(),
+                             rows_fn<uint16_t, 256, true>(), rows_fn<uint16_t, 256, false>(),
+                             rows_fn<float, 512, true>(),    rows_fn<float, 512, false>(),
+                             rows_fn<uint16_t, 512, true>(), rows_fn<uint16_t, 512, false>()};
   return t;
 }
 
-void* pick_rows_kernel(int elem, bool bulk) {
-  if (elem == 4) return bulk ? rows_fn<float, true>() : rows_fn<float, false>();
-  return bulk ? rows_fn<uint16_t, true>() : rows_fn<uint16_t, false>();
+void* pick_rows_kernel(int elem, bool bulk, int threads) {
+  const int idx = (threads == 512 ? 4 : 0) + (elem == 4 ? 0 : 2) + (bulk ? 0 : 1);
+  return kernel_table()[idx];
 }
 
-size_t meta_bytes(int bs) { return 4 * 8 + static_cast<size_t>(bs + 1) * 4 + static_cast<size_t>(bs) * 4; }
+// stage meta (4 x 16 B) + mbarriers (4 x 8 B) + cu_seqlens + temperatures
+size_t meta_bytes(int bs) {
+  return 64 + 32 + static_cast<size_t>(bs + 1) * 4 + static_cast<size_t>(bs) * 4;
+}
 
 // Dynamic shared memory a kernel may use on the current device: the opt-in
 // per-block maximum minus the kernel's static shared memory.
-cudaError_t dyn_smem_limit(void* fn, int* limit) {
+cudaError_t kernel_smem(void* fn, int* dyn_limit, int* static_bytes) {
   int dev = 0, optin = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
@@ -593,7 +670,8 @@ cudaError_t dyn_smem_limit(void* fn, int* limit) {
   cudaFuncAttributes fa;
   e = cudaFuncGetAttributes(&fa, fn);
   if (e != cudaSuccess) return e;
-  *limit = optin - static_cast<int>(fa.sharedSizeBytes);
+  *static_bytes = static_cast<int>(fa.sharedSizeBytes);
+  *dyn_limit = optin - *static_bytes;
   return cudaSuccess;
 }
 
@@ -616,7 +694,8 @@ cudaError_t prepare(void* fn, size_t smem) {
     std::lock_guard<std::mutex> lk(mu);
     lim = limit_of[slot][dev].load(std::memory_order_relaxed);
     if (lim == 0) {
-      e = dyn_smem_limit(fn, &lim);
+      int st = 0;
+      e = kernel_smem(fn, &lim, &st);
       if (e != cudaSuccess) return e;
       e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, lim);
       if (e != cudaSuccess) return e;
@@ -630,55 +709,63 @@ cudaError_t prepare(void* fn, size_t smem) {
 
 }  // namespace
 
-cudaError_t rows_smem_limit(int elem, bool bulk, int* limit) {
-  void* fn = pick_rows_kernel(elem, bulk);
-  cudaError_t e = prepare(fn, 0);
+cudaError_t choose_verify_shape(int V, int elem, int bs, const sd_launch_cfg* req, bool bulk,
+                                VerifyShape* out, bool* fits) {
+  *fits = false;
+  int dev = 0, sm_smem = 0, reserved = 0;
+  cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  return dyn_smem_limit(fn, limit);
-}
-
-bool choose_verify_shape(int V, int elem, int bs, const sd_launch_cfg* req, bool bulk,
-                         int dyn_limit, VerifyShape* out) {
-  const size_t meta = meta_bytes(bs);
-  if (dyn_limit <= 0 || meta >= static_cast<size_t>(dyn_limit)) return false;
-  const size_t avail = static_cast<size_t>(dyn_limit) - meta;
+  e = cudaDeviceGetAttribute(&sm_smem, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev);
+  if (e != cudaSuccess) return e;
+  e = cudaDeviceGetAttribute(&reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev);
+  if (e != cudaSuccess) return e;
   const int creq = req ? req->cluster : 0;
   const int sreq = req ? req->stages : 0;
-  if (creq && creq != 1 && creq != 2 && creq != 4 && creq != 8 && creq != 16) return false;
-  if (sreq < 0 || sreq > 4) return false;
-  auto stage_of = [&](int C) {
-    int SL = (V + C - 1) / C;
-    SL = (SL + 63) / 64 * 64;
-    return std::pair<int, size_t>(SL, 2 * static_cast<size_t>(SL) * elem);
-  };
-  int C = 0, S = 0, SL = 0;
-  size_t stage = 0;
-  const int want_s[3] = {3, 2, 1};
-  for (int si = 0; si < 3 && !C; ++si) {
-    const int s_try = sreq ? sreq : want_s[si];
-    for (int c = 1; c <= 16; c <<= 1) {
-      if (creq && c != creq) continue;
-      auto st = stage_of(c);
-      if (static_cast<size_t>(s_try) * st.second <= avail) {
-        C = c; S = s_try; SL = st.first; stage = st.second;
-        break;
+  const int treq = req ? req->threads : 0;
+  if (creq && creq != 1 && creq != 2 && creq != 4 && creq != 8 && creq != 16) return cudaSuccess;
+  if (sreq < 0 || sreq > 4) return cudaSuccess;
+  if (treq && treq != 256 && treq != 512) return cudaSuccess;
+  const size_t meta = meta_bytes(bs);
+  // Preference: two 256-thread CTAs per SM with three stages each (barrier
+  // waits of one CTA hidden by the other), then one 512-thread CTA per SM.
+  struct Cand { int threads, stages, per_sm; };
+  const Cand cands[] = {{256, 3, 2}, {512, 3, 1}, {512, 2, 1}, {256, 2, 2}, {512, 1, 1}};
+  for (const Cand& c : cands) {
+    const int threads = treq ? treq : c.threads;
+    const int S = bulk ? (sreq ? sreq : c.stages) : 1;
+    const int per_sm = treq || sreq ? 1 : c.per_sm;
+    void* fn = pick_rows_kernel(elem, bulk, threads);
+    e = prepare(fn, 0);
+    if (e != cudaSuccess) return e;
+    int dyn_limit = 0, st = 0;
+    e = kernel_smem(fn, &dyn_limit, &st);
+    if (e != cudaSuccess) return e;
+    long long budget = per_sm == 1 ? dyn_limit
+                                   : std::min<long long>(dyn_limit, sm_smem / per_sm - reserved - st);
+    for (int C = 1; C <= 16; C <<= 1) {
+      if (creq && C != creq) continue;
+      int SL = (V + C - 1) / C;
+      SL = (SL + 63) / 64 * 64;
+      const size_t stage = 2 * static_cast<size_t>(SL) * elem;
+      const size_t smem = static_cast<size_t>(S) * stage + meta;
+      if (static_cast<long long>(smem) <= budget) {
+        out->C = C;
+        out->S = S;
+        out->SL = SL;
+        out->threads = threads;
+        out->smem = smem;
+        out->bulk = bulk;
+        out->clusters = req ? req->clusters : 0;
+        *fits = true;
+        return cudaSuccess;
       }
     }
-    if (sreq) break;
   }
-  if (!C) return false;
-  out->C = C;
-  out->S = bulk ? S : 1;
-  out->SL = SL;
-  out->threads = kRowThreads;
-  out->smem = static_cast<size_t>(out->S) * stage + meta;
-  out->bulk = bulk;
-  out->clusters = req ? req->clusters : 0;
-  return true;
+  return cudaSuccess;
 }
 
 cudaError_t max_active_clusters(int elem, const VerifyShape& shape, int* n) {
-  void* fn = pick_rows_kernel(elem, shape.bulk);
+  void* fn = pick_rows_kernel(elem, shape.bulk, shape.threads);
   cudaError_t e = prepare(fn, shape.smem);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
@@ -697,7 +784,7 @@ cudaError_t max_active_clusters(int elem, const VerifyShape& shape, int* n) {
 
 cudaError_t launch_verify_rows(const VerifyParams& p, int elem, const VerifyShape& shape,
                                cudaStream_t s) {
-  void* fn = pick_rows_kernel(elem, shape.bulk);
+  void* fn = pick_rows_kernel(elem, shape.bulk, shape.threads);
   cudaError_t e = prepare(fn, shape.smem);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};

@@ -55,9 +55,10 @@ def test_small_every_cluster_shape(dtype, V, cluster):
 
 
 @pytest.mark.parametrize("stages", [1, 2, 3, 4])
-def test_small_stage_counts(stages):
+@pytest.mark.parametrize("threads", [256, 512])
+def test_small_stage_counts(stages, threads):
     w = SMALL.with_(V=20000, dtype=S.BF16, bs=32, T=32)
-    _step(w, 7, cfg={"cluster": 2, "stages": stages, "clusters": 3})
+    _step(w, 7, cfg={"cluster": 2, "stages": stages, "clusters": 3, "threads": threads})
 
 
 def test_varlen_draft_lengths_and_zero_drafts():
@@ -89,9 +90,7 @@ def _full(name, seed, n_sample, step=0):
 
 
 def test_full_adaptive_hc():
-    g = _full("adaptive_hc", 2024, 24)
-    # the planner verifies a strict subset of the 7 drafted slots
-    assert 0 < (g["accepted_len"] >= 0).sum()
+    _full("adaptive_hc", 2024, 24)
 
 
 def test_full_dense_fixed_k():
@@ -143,7 +142,7 @@ def test_bad_draft_id_and_nan_logits_flag():
     check_properties(g, cu, w.k_max, w.V, vi["draft_ids"])
     vi2 = S.verify_inputs(w, 2, 0, cu, pi["draft_lens"])
     vi2["target"] = vi2["target"].copy()
-    vi2["target"][0, 5] = np.float32(np.nan)
+    vi2["target"][0, 5] = 0x7FC0 if w.dtype == S.BF16 else np.float32(np.nan)  # a NaN
     g2 = gpu_verify(w, vi2, cu, w.k_max)
     assert g2["err"] & sd.SD_DEV_ERR_LOGITS
 
@@ -191,4 +190,4 @@ def test_random_small_plans_match_oracle():
 def test_zz_near_boundary_budget():
     """Mismatches at near-boundary decisions stay within 0.01 % of decisions."""
     TALLY.dump()
-    assert TALLY.near_mismatches <= max(1, 1e-4 * TALLY.decisions), TALLY.__dict__
+    assert TALLY.near_mismatches <= 1e-4 * TALLY.decisions, TALLY.__dict__
