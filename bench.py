@@ -9,11 +9,10 @@ cost(n) = 1 + 0.004*ceil16(n) -- the adaptive high-concurrency setup, the
 configuration that exercises every stage of the path (the planner chooses B,
 greedy and sampled requests mix).
 
-One step = sd_plan + sd_verify_rows + sd_verify_finalize on device-resident
-inputs.  Two input sets, each larger than the 129 MB L2, alternate between
+One step = sd_plan + sd_verify on device-resident inputs.  Two input sets, each larger than the 129 MB L2, alternate between
 steps, so no step reads data the previous one left in L2.  Metric: verified
 draft tokens/s (sum of n_i over requests, per second).  Also reported:
-achieved HBM bandwidth of the rows kernel against the measured copy peak,
+achieved HBM bandwidth of the sampling kernel against the measured copy peak,
 planner latency, acceptance statistics, an end-to-end figure through the C
 ABI from pinned host buffers, and the CPU oracle as a reported baseline.
 
@@ -52,9 +51,9 @@ def parse():
     ap.add_argument("--workload", default="adaptive_hc", choices=sorted(S.WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--seed", type=int, default=2026)
-    ap.add_argument("--cluster", type=int, default=0)
-    ap.add_argument("--stages", type=int, default=0)
     ap.add_argument("--threads", type=int, default=0)
+    ap.add_argument("--blocks", type=int, default=0)
+    ap.add_argument("--blocks-per-sm", type=int, default=0)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
@@ -278,8 +277,8 @@ def run_ours(args, w, rank, world, local):
     d_acc = torch.zeros(bs, dtype=torch.int32, device=dev)
     d_out = torch.zeros((bs, k + 1), dtype=torch.int32, device=dev)
     ws_bytes = sd.sd_verify_workspace_bytes(bs, k)
-    d_ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
-    cfg = {"cluster": args.cluster, "stages": args.stages, "threads": args.threads}
+    d_ws = sd.verify_workspace(bs, k, dev)
+    cfg = {"threads": args.threads, "blocks": args.blocks, "blocks_per_sm": args.blocks_per_sm}
 
     def step(s, ev=None):
         tgt, dft = sets[s & 1]
@@ -288,13 +287,10 @@ def run_ours(args, w, rank, world, local):
         plan_call()
         if ev:
             ev[1].record(stream)
-        sd.sd_verify_rows(tgt, dft, dtype, w.V, d_ids, d_u, d_t, d_cu, bs, k, None, d_err, d_ws,
-                          ws_bytes, cfg=cfg, stream=stream)
+        sd.sd_verify_ex(tgt, dft, dtype, w.V, d_ids, d_u, d_t, d_cu, bs, k, d_acc, d_out, None,
+                        d_err, d_ws, ws_bytes, cfg=cfg, stream=stream)
         if ev:
             ev[2].record(stream)
-        sd.sd_verify_finalize(d_ids, d_cu, bs, k, d_acc, d_out, d_err, d_ws, ws_bytes, stream)
-        if ev:
-            ev[3].record(stream)
 
     def barrier():
         if world > 1:
@@ -305,7 +301,7 @@ def run_ours(args, w, rank, world, local):
     for s in range(args.warmup):
         step(s)
     barrier()
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
     with ClockSampler(local) as clk:
@@ -318,7 +314,6 @@ def run_ours(args, w, rank, world, local):
     elapsed_ms = t_start.elapsed_time(t_end)
     plan_ms = [e[0].elapsed_time(e[1]) for e in evs]
     rows_ms = [e[1].elapsed_time(e[2]) for e in evs]
-    fin_ms = [e[2].elapsed_time(e[3]) for e in evs]
     err = int(d_err.item())
     acc = d_acc.cpu().numpy()
 
@@ -327,7 +322,10 @@ def run_ours(args, w, rank, world, local):
     sampled = temps > 0
     rows_read = int((n + 1).sum() + n[sampled].sum())
     bytes_rows = rows_read * w.V * elem
-    bytes_small = (bs + 1) * 4 + bs * 4 + B * 4 + bs * (k + 1) * 4 + rows_t * 5
+    # small inputs and outputs: cu_seqlens, temps, draft ids, uniforms, accepted
+    # lengths and tokens, and the per-row statistics written and read back
+    bytes_small = ((bs + 1) * 4 + bs * 4 + B * 4 + bs * (k + 1) * 4 + bs * 4 + bs * (k + 1) * 4
+                   + 2 * 16 * rows_read)
     bytes_alg = bytes_rows + bytes_small
     if world > 1:
         import torch.distributed as dist
@@ -400,12 +398,12 @@ def run_ours(args, w, rank, world, local):
         "data": "synthetic", "config": config_of(w),
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": None,
-                     "kernel": "rows_kernel (sd_verify_rows)", "peak_kind": peak_kind,
+                     "kernel": "verify_kernel (sd_verify)", "peak_kind": peak_kind,
                      "frac_of_nominal_8tbs": achieved / NOMINAL_HBM_GBS,
                      "bytes_per_launch": bytes_alg, "avg_launch_ms": rows_avg_ms},
         "cpu_baseline": cpu,
         "e2e": e2e,
-        "gpu_launches": 3 * args.steps,
+        "gpu_launches": 2 * args.steps,
         "clocks": clk.summary(),
         "detail": {
             "B": B, "verified_draft_tokens_per_step": verified, "target_rows": rows_t,
@@ -413,15 +411,14 @@ def run_ours(args, w, rank, world, local):
             "bytes_per_verified_token": bytes_alg / max(verified, 1),
             "plan_us_event": 1e3 * statistics.median(plan_ms),
             "plan_us_graph": plan_graph_us,
-            "rows_us_median": 1e3 * statistics.median(rows_ms),
-            "finalize_us_median": 1e3 * statistics.median(fin_ms),
+            "verify_us_median": 1e3 * statistics.median(rows_ms),
             "accepted_draft_tokens_per_step": accepted,
             "emitted_tokens_per_s": (accepted + bs) * args.steps / (elapsed_ms / 1e3),
             "mean_acceptance_length": 1.0 + accepted / bs,
             "per_position_cumulative_acceptance": [round(x, 4) for x in pos],
             "device_err_flag": err, "input_generation_s": gen_s,
-            "launch": sd.sd_verify_launch_info(w.V, dtype, args.cluster, args.stages, 0,
-                                               args.threads),
+            "launch": sd.sd_verify_launch_info(w.V, dtype, bs, args.threads, args.blocks,
+                                               args.blocks_per_sm),
         },
     }
     if rank == 0:
@@ -470,7 +467,7 @@ def run_e2e(args, w, sd, dev, stream, pi, vi, cu, ws_bytes, cfg, rows_cap):
     d_err = torch.zeros(1, dtype=torch.int32, device=dev)
     d_acc = torch.zeros(bs, dtype=torch.int32, device=dev)
     d_out = torch.zeros((bs, k + 1), dtype=torch.int32, device=dev)
-    d_ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    d_ws = sd.verify_workspace(bs, k, dev)
     h2d = 0
     for h in (h_conf, h_lens, h_cost, h_tgt, h_dft, h_ids, h_u, h_t):
         if h is not None:
@@ -492,9 +489,8 @@ def run_e2e(args, w, sd, dev, stream, pi, vi, cu, ws_bytes, cfg, rows_cap):
         sd.sd_plan(d_conf, None, None, 0, d_lens, bs, k, d_cost,
                    0 if h_cost is None else h_cost.numel(), w.T, w.mode, d_B, d_mask, d_nv, d_cu,
                    d_err, None, 0, stream)
-        sd.sd_verify_rows(d_tgt, d_dft, dtype, w.V, d_ids, d_u, d_t, d_cu, bs, k, None, d_err, d_ws,
-                          ws_bytes, cfg=cfg, stream=stream)
-        sd.sd_verify_finalize(d_ids, d_cu, bs, k, d_acc, d_out, d_err, d_ws, ws_bytes, stream)
+        sd.sd_verify_ex(d_tgt, d_dft, dtype, w.V, d_ids, d_u, d_t, d_cu, bs, k, d_acc, d_out, None,
+                        d_err, d_ws, ws_bytes, cfg=cfg, stream=stream)
         h_acc.copy_(d_acc, non_blocking=True)
         h_out.copy_(d_out, non_blocking=True)
 

@@ -6,8 +6,7 @@
  *   sd_plan    planning stage: per-slot survival, global top-B, budget
  *              argmax against a step-cost table, varlen compaction.
  *   sd_verify  sampling stage: vocab-wide speculative rejection sampling on
- *              the compacted target/draft logits (sd_verify_rows followed by
- *              sd_verify_finalize).
+ *              the compacted target/draft logits, one kernel.
  *
  * Sources (page title, section):
  *   [AV-blog]  fosworld blog "추측 디코딩과 vLLM 적응형 검증"
@@ -16,8 +15,9 @@
  *
  * Conventions shared by every entry point
  *   - Every pointer argument is a DEVICE pointer unless stated otherwise; the
- *     caller allocates and frees every buffer.  The library keeps no global
- *     state and never allocates.
+ *     caller allocates and frees every buffer; the library never allocates.
+ *     Host-side state is limited to per-device launch settings applied once
+ *     (shared-memory limits) and the per-thread last-error text.
  *   - Calls enqueue work on `stream` (a cudaStream_t; NULL = the legacy
  *     default stream) and return without synchronising.  The return value
  *     reports host-side argument validation and launch errors only.
@@ -67,12 +67,11 @@ typedef enum {
 #define SD_DEV_ERR_TEMP 0x020            /* a temperature < 0 or not finite */
 #define SD_DEV_ERR_UNIFORM 0x040         /* a uniform outside [0, 1) */
 #define SD_DEV_ERR_LOGITS 0x080          /* a logit row holds NaN/+inf or no finite value */
-#define SD_DEV_ERR_TIMEOUT 0x100         /* a bounded wait inside a kernel gave up */
 
 /* Limits of this build. */
 #define SD_MAX_K 15            /* k_max <= 15: at most 16 query rows per request */
 #define SD_MAX_PLAN_SLOTS 8192 /* pow2ceil(bs) * pow2ceil(k_max) <= 8192 for sd_plan */
-#define SD_MAX_VERIFY_BS 4096  /* bs <= 4096 for sd_verify_rows */
+#define SD_MAX_VERIFY_BS 4096  /* bs <= 4096 for sd_verify */
 #define SD_MAX_V (1 << 22)     /* V <= 4,194,304 */
 
 /* ------------------------------------------------------------------------
@@ -134,7 +133,7 @@ sd_status sd_plan(const float* conf_logits, const float* budget_conf,
 
 /* ------------------------------------------------------------------------
  * sd_verify -- sampling stage: speculative rejection sampling over the
- * vocabulary, = sd_verify_rows followed by sd_verify_finalize.
+ * vocabulary, one persistent kernel.
  *
  * Passages: [AV-blog] "추측 디코딩이란" (the target scores all drafted
  * positions in one pass; drafts are accepted front to back up to the first
@@ -172,29 +171,24 @@ sd_status sd_plan(const float* conf_logits, const float* budget_conf,
  *   cu_seqlens     [bs+1] int32 from sd_plan (or the caller).
  * Outputs
  *   accepted_len   [bs] int32; out_tokens [bs, k_max+1] int32, -1 padded.
- *   probs_out      [bs*k_max, 2] fp32 or NULL: (p_j(x_j), q_j(x_j)) of every
- *                  verified slot of a tau > 0 request, at the draft-row index
- *                  (diagnostics; other entries untouched).
+ *   probs_out      [bs*k_max, 2] fp32 or NULL: (p_j(x_j), q_j(x_j)) of the
+ *                  verified slots of a tau > 0 request up to its first
+ *                  rejection, at the draft-row index (diagnostics; other
+ *                  entries untouched).
  *   err_flag       [1] int32, sticky SD_DEV_ERR_* bits.  On SD_DEV_ERR_CU_SEQLENS
- *                  no row is read and outputs are accepted_len = 0,
+ *                  no logit is read and outputs are accepted_len = 0,
  *                  out_tokens = -1.
  *   workspace      device scratch of sd_verify_workspace_bytes(bs, k_max)
- *                  bytes, 16-byte aligned: per-row accept flags and candidate
- *                  tokens passed from the rows kernel to the finalize kernel.
- *                  Needs no initialisation.
- * Layout requirements for the fast path: V*elem and the logits base pointers
- * 16-byte aligned (bulk-copy staging); otherwise a slower staged path runs.
+ *                  bytes, 16-byte aligned: per-row statistics, per-request
+ *                  arrival counts and a work counter.  It must be zero-filled
+ *                  once before its first use (e.g. cudaMemsetAsync); every
+ *                  call leaves the counters at zero again.  One call at a time
+ *                  per workspace.
+ * Layout: rows are read with 16-byte vector loads when V*elem is a multiple
+ * of 16 and both logits base pointers are 16-byte aligned, element by
+ * element otherwise (same results, slower).
  * ---------------------------------------------------------------------- */
 size_t sd_verify_workspace_bytes(int bs, int k_max);
-
-/* Launch tuning of the rows kernel; 0 in any field = automatic.  The result
- * does not depend on it. */
-typedef struct {
-  int cluster;   /* CTAs sharing one row pair: 1, 2, 4, 8 or 16 */
-  int stages;    /* row slices in flight per CTA (1..4) */
-  int clusters;  /* persistent clusters launched (<= what fits at once) */
-  int threads;   /* threads per CTA: 256 or 512 */
-} sd_launch_cfg;
 
 sd_status sd_verify(const void* target_logits, const void* draft_logits, sd_dtype dt, int V,
                     const int* draft_ids, const float* uniforms, const float* temps,
@@ -202,25 +196,26 @@ sd_status sd_verify(const void* target_logits, const void* draft_logits, sd_dtyp
                     int* out_tokens, float* probs_out, int* err_flag, void* workspace,
                     size_t ws_bytes, void* stream);
 
-/* First half of sd_verify: one pass over every compacted row; writes the
- * per-row accept flag and the candidate final token of every row that could
- * end its request's accepted prefix into the workspace.  cfg may be NULL. */
-sd_status sd_verify_rows(const void* target_logits, const void* draft_logits, sd_dtype dt,
-                         int V, const int* draft_ids, const float* uniforms,
-                         const float* temps, const int* cu_seqlens, int bs, int k_max,
-                         float* probs_out, int* err_flag, void* workspace, size_t ws_bytes,
-                         const sd_launch_cfg* cfg, void* stream);
+/* Launch tuning of the sampling kernel; 0 in any field = automatic.  Results
+ * do not depend on it. */
+typedef struct {
+  int threads;        /* threads per CTA: 256 or 512 */
+  int blocks;         /* persistent CTAs launched (capped at what fits at once) */
+  int blocks_per_sm;  /* CTAs per SM to aim for */
+  int reserved;       /* must be 0 */
+} sd_launch_cfg;
 
-/* Second half of sd_verify: per request, a_i and out_tokens from the
- * workspace written by sd_verify_rows on the same stream. */
-sd_status sd_verify_finalize(const int* draft_ids, const int* cu_seqlens, int bs, int k_max,
-                             int* accepted_len, int* out_tokens, int* err_flag,
-                             const void* workspace, size_t ws_bytes, void* stream);
+/* sd_verify with an explicit launch shape (cfg may be NULL). */
+sd_status sd_verify_ex(const void* target_logits, const void* draft_logits, sd_dtype dt, int V,
+                       const int* draft_ids, const float* uniforms, const float* temps,
+                       const int* cu_seqlens, int bs, int k_max, int* accepted_len,
+                       int* out_tokens, float* probs_out, int* err_flag, void* workspace,
+                       size_t ws_bytes, const sd_launch_cfg* cfg, void* stream);
 
-/* Launch shape the rows kernel would use for (V, dt) and the requested
- * tuning (NULL = automatic), on the current device.  Host-only query. */
-sd_status sd_verify_launch_info(int V, sd_dtype dt, const sd_launch_cfg* req,
-                                sd_launch_cfg* chosen, int* threads, size_t* smem_bytes);
+/* Launch shape sd_verify_ex would use for (V, dt, bs) and `req` (NULL =
+ * automatic) on the current device.  Host-only query. */
+sd_status sd_verify_launch_info(int V, sd_dtype dt, int bs, const sd_launch_cfg* req,
+                                sd_launch_cfg* chosen, size_t* smem_bytes);
 
 const char* sd_status_string(sd_status s);
 

@@ -23,15 +23,15 @@ import torch
 from . import _lib
 from ._lib import (SD_BF16, SD_DEV_ERR_CONF, SD_DEV_ERR_COST, SD_DEV_ERR_CU_SEQLENS,  # noqa: F401
                    SD_DEV_ERR_DRAFT_ID, SD_DEV_ERR_DRAFT_LENS, SD_DEV_ERR_LOGITS,
-                   SD_DEV_ERR_TEMP, SD_DEV_ERR_TIMEOUT, SD_DEV_ERR_UNIFORM, SD_ERR_CUDA,
+                   SD_DEV_ERR_TEMP, SD_DEV_ERR_UNIFORM, SD_ERR_CUDA,
                    SD_ERR_DEVICE_CHECK, SD_ERR_INVALID_ARG, SD_ERR_SHAPE, SD_ERR_UNSUPPORTED,
                    SD_F32, SD_MAX_K, SD_MAX_PLAN_SLOTS, SD_MAX_V, SD_MAX_VERIFY_BS,
                    SD_MODE_ADAPTIVE, SD_MODE_ALL_SLOTS, SD_OK, SdError, sd_launch_cfg)
 
 __all__ = [
-    "sd_plan", "sd_verify", "sd_verify_rows", "sd_verify_finalize", "sd_plan_workspace_bytes",
+    "sd_plan", "sd_verify", "sd_verify_ex", "sd_plan_workspace_bytes",
     "sd_verify_workspace_bytes", "sd_verify_launch_info", "plan", "verify", "PlanResult",
-    "VerifyResult", "SdError", "build", "library_path",
+    "VerifyResult", "SdError", "build", "library_path", "verify_workspace",
 ]
 
 
@@ -113,39 +113,36 @@ def _cfg(cfg):
         return None
     if isinstance(cfg, sd_launch_cfg):
         return ctypes.byref(cfg)
-    c = sd_launch_cfg(int(cfg.get("cluster", 0)), int(cfg.get("stages", 0)),
-                      int(cfg.get("clusters", 0)), int(cfg.get("threads", 0)))
+    c = sd_launch_cfg(int(cfg.get("threads", 0)), int(cfg.get("blocks", 0)),
+                      int(cfg.get("blocks_per_sm", 0)), 0)
     return ctypes.byref(c)
 
 
-def sd_verify_rows(target_logits, draft_logits, dt, V, draft_ids, uniforms, temps, cu_seqlens,
-                   bs, k_max, probs_out, err_flag, workspace, ws_bytes, cfg=None, stream=None):
-    st = _lib.load().sd_verify_rows(_ptr(target_logits), _ptr(draft_logits), _dt(dt), int(V),
-                                    _ptr(draft_ids), _ptr(uniforms), _ptr(temps),
-                                    _ptr(cu_seqlens), int(bs), int(k_max), _ptr(probs_out),
-                                    _ptr(err_flag), _ptr(workspace), int(ws_bytes), _cfg(cfg),
-                                    _stream(stream))
-    return _lib.check("sd_verify_rows", st)
+def sd_verify_ex(target_logits, draft_logits, dt, V, draft_ids, uniforms, temps, cu_seqlens, bs,
+                 k_max, accepted_len, out_tokens, probs_out, err_flag, workspace, ws_bytes,
+                 cfg=None, stream=None):
+    st = _lib.load().sd_verify_ex(_ptr(target_logits), _ptr(draft_logits), _dt(dt), int(V),
+                                  _ptr(draft_ids), _ptr(uniforms), _ptr(temps), _ptr(cu_seqlens),
+                                  int(bs), int(k_max), _ptr(accepted_len), _ptr(out_tokens),
+                                  _ptr(probs_out), _ptr(err_flag), _ptr(workspace), int(ws_bytes),
+                                  _cfg(cfg), _stream(stream))
+    return _lib.check("sd_verify_ex", st)
 
 
-def sd_verify_finalize(draft_ids, cu_seqlens, bs, k_max, accepted_len, out_tokens, err_flag,
-                       workspace, ws_bytes, stream=None):
-    st = _lib.load().sd_verify_finalize(_ptr(draft_ids), _ptr(cu_seqlens), int(bs), int(k_max),
-                                        _ptr(accepted_len), _ptr(out_tokens), _ptr(err_flag),
-                                        _ptr(workspace), int(ws_bytes), _stream(stream))
-    return _lib.check("sd_verify_finalize", st)
-
-
-def sd_verify_launch_info(V, dt, cluster=0, stages=0, clusters=0, threads=0) -> dict:
-    req = sd_launch_cfg(cluster, stages, clusters, threads)
+def sd_verify_launch_info(V, dt, bs, threads=0, blocks=0, blocks_per_sm=0) -> dict:
+    req = sd_launch_cfg(threads, blocks, blocks_per_sm, 0)
     out = sd_launch_cfg()
-    thr = ctypes.c_int(0)
     smem = ctypes.c_size_t(0)
-    st = _lib.load().sd_verify_launch_info(int(V), _dt(dt), ctypes.byref(req), ctypes.byref(out),
-                                           ctypes.byref(thr), ctypes.byref(smem))
+    st = _lib.load().sd_verify_launch_info(int(V), _dt(dt), int(bs), ctypes.byref(req),
+                                           ctypes.byref(out), ctypes.byref(smem))
     _lib.check("sd_verify_launch_info", st)
-    return {"cluster": out.cluster, "stages": out.stages, "clusters": out.clusters,
-            "threads": thr.value, "smem_bytes": smem.value}
+    return {"threads": out.threads, "blocks": out.blocks, "smem_bytes": smem.value}
+
+
+def verify_workspace(bs: int, k_max: int, device=None) -> torch.Tensor:
+    """A zero-filled workspace for sd_verify (zero-filled once; calls keep it so)."""
+    return torch.zeros(sd_verify_workspace_bytes(bs, k_max), dtype=torch.uint8,
+                       device=device or torch.device("cuda"))
 
 
 # ---------------------------------------------------------------------------
@@ -183,6 +180,11 @@ def plan(draft_lens: torch.Tensor, k_max: int, conf: Optional[torch.Tensor] = No
     if err is None:
         err = torch.zeros(1, dtype=torch.int32, device=dev)
     bsb = 0 if budget_draft_lens is None else budget_draft_lens.numel()
+    # an empty packed array is still a valid (unread) buffer for the C ABI
+    if conf is not None and conf.numel() == 0:
+        conf = torch.zeros(1, dtype=torch.float32, device=dev)
+    if budget_conf is not None and budget_conf.numel() == 0:
+        budget_conf = torch.zeros(1, dtype=torch.float32, device=dev)
     sd_plan(conf, budget_conf, budget_draft_lens, bsb, draft_lens, bs, k_max, cost,
             0 if cost is None else cost.numel(), T, mode, B, mask, nv, cu, err, None, 0, stream)
     return PlanResult(B, mask[:, :k_max], nv, cu, err)
@@ -200,9 +202,8 @@ def verify(target: torch.Tensor, draft: Optional[torch.Tensor], dt, V: int,
     pr = torch.full((max(bs * k_max, 1), 2), float("nan"), dtype=torch.float32, device=dev) if probs else None
     if err is None:
         err = torch.zeros(1, dtype=torch.int32, device=dev)
-    nbytes = sd_verify_workspace_bytes(bs, k_max)
     if workspace is None:
-        workspace = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+        workspace = verify_workspace(bs, k_max, dev)
     sd_verify(target, draft, dt, V, draft_ids, uniforms, temps, cu_seqlens, bs, k_max, acc, out,
               pr, err, workspace, workspace.numel(), stream)
     return VerifyResult(acc, out, pr, err)

@@ -26,7 +26,6 @@ SD_DEV_ERR_DRAFT_ID = 0x010
 SD_DEV_ERR_TEMP = 0x020
 SD_DEV_ERR_UNIFORM = 0x040
 SD_DEV_ERR_LOGITS = 0x080
-SD_DEV_ERR_TIMEOUT = 0x100
 
 SD_MAX_K = 15
 SD_MAX_PLAN_SLOTS = 8192
@@ -35,13 +34,13 @@ SD_MAX_V = 1 << 22
 
 # Every symbol include/sd.h declares.
 EXPORTS = ("sd_plan_workspace_bytes", "sd_plan", "sd_verify_workspace_bytes", "sd_verify",
-           "sd_verify_rows", "sd_verify_finalize", "sd_verify_launch_info", "sd_status_string",
-           "sd_last_error_string", "sd_abi_version")
+           "sd_verify_ex", "sd_verify_launch_info", "sd_status_string", "sd_last_error_string",
+           "sd_abi_version")
 
 
 class sd_launch_cfg(ctypes.Structure):
-    _fields_ = [("cluster", ctypes.c_int), ("stages", ctypes.c_int), ("clusters", ctypes.c_int),
-                ("threads", ctypes.c_int)]
+    _fields_ = [("threads", ctypes.c_int), ("blocks", ctypes.c_int),
+                ("blocks_per_sm", ctypes.c_int), ("reserved", ctypes.c_int)]
 
 
 class SdError(RuntimeError):
@@ -79,15 +78,12 @@ def load(path: Path | None = None) -> ctypes.CDLL:
     lib.sd_plan.argtypes = [P, P, P, i32, P, i32, i32, P, i32, i32, i32, P, P, P, P, P, P, sz, P]
     lib.sd_verify.restype = i32
     lib.sd_verify.argtypes = [P, P, i32, i32, P, P, P, P, i32, i32, P, P, P, P, P, sz, P]
-    lib.sd_verify_rows.restype = i32
-    lib.sd_verify_rows.argtypes = [P, P, i32, i32, P, P, P, P, i32, i32, P, P, P, sz,
-                                   ctypes.POINTER(sd_launch_cfg), P]
-    lib.sd_verify_finalize.restype = i32
-    lib.sd_verify_finalize.argtypes = [P, P, i32, i32, P, P, P, P, sz, P]
+    lib.sd_verify_ex.restype = i32
+    lib.sd_verify_ex.argtypes = [P, P, i32, i32, P, P, P, P, i32, i32, P, P, P, P, P, sz,
+                                 ctypes.POINTER(sd_launch_cfg), P]
     lib.sd_verify_launch_info.restype = i32
-    lib.sd_verify_launch_info.argtypes = [i32, i32, ctypes.POINTER(sd_launch_cfg),
-                                          ctypes.POINTER(sd_launch_cfg), ctypes.POINTER(i32),
-                                          ctypes.POINTER(sz)]
+    lib.sd_verify_launch_info.argtypes = [i32, i32, i32, ctypes.POINTER(sd_launch_cfg),
+                                          ctypes.POINTER(sd_launch_cfg), ctypes.POINTER(sz)]
     _lib = lib
     return lib
 

@@ -32,76 +32,38 @@ size_t align16(size_t v) { return (v + 15) & ~static_cast<size_t>(15); }
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 struct VerifyWs {
-  uint8_t* accept;
-  int* cand;
-  int* status;
+  sdk::RowStat* st_t;
+  sdk::RowStat* st_d;
+  int* req_cnt;
+  int* ctrl;
 };
 
 size_t verify_ws_bytes(int bs, int k_max) {
-  const size_t rows = static_cast<size_t>(bs) * (k_max + 1);
-  return align16(rows) + align16(rows * 4) + 16;
+  const size_t rows_t = static_cast<size_t>(bs) * (k_max + 1);
+  const size_t rows_d = static_cast<size_t>(bs) * k_max;
+  return 16 * rows_t + 16 * rows_d + align16(4 * static_cast<size_t>(bs)) + 16;
 }
 
 VerifyWs carve(void* ws, int bs, int k_max) {
-  const size_t rows = static_cast<size_t>(bs) * (k_max + 1);
+  const size_t rows_t = static_cast<size_t>(bs) * (k_max + 1);
+  const size_t rows_d = static_cast<size_t>(bs) * k_max;
   char* b = static_cast<char*>(ws);
   VerifyWs w;
-  w.accept = reinterpret_cast<uint8_t*>(b);
-  w.cand = reinterpret_cast<int*>(b + align16(rows));
-  w.status = reinterpret_cast<int*>(b + align16(rows) + align16(rows * 4));
+  w.st_t = reinterpret_cast<sdk::RowStat*>(b);
+  w.st_d = reinterpret_cast<sdk::RowStat*>(b + 16 * rows_t);
+  w.req_cnt = reinterpret_cast<int*>(b + 16 * rows_t + 16 * rows_d);
+  w.ctrl = reinterpret_cast<int*>(b + 16 * rows_t + 16 * rows_d +
+                                  align16(4 * static_cast<size_t>(bs)));
   return w;
 }
 
-// Per-device cache of the co-resident cluster count for a launch shape.
-struct ClusterCache {
-  std::mutex mu;
-  struct Entry {
-    int dev, elem, C, S, SL, threads, bulk;
-    size_t smem;
-    int n;
-  } e[64];
-  int used = 0;
-};
-ClusterCache g_clusters;
-
-cudaError_t resident_clusters(int elem, const sdk::VerifyShape& s, int* n) {
-  int dev = 0;
-  cudaError_t err = cudaGetDevice(&dev);
-  if (err != cudaSuccess) return err;
-  {
-    std::lock_guard<std::mutex> lk(g_clusters.mu);
-    for (int k = 0; k < g_clusters.used; ++k) {
-      const auto& c = g_clusters.e[k];
-      if (c.dev == dev && c.elem == elem && c.C == s.C && c.S == s.S && c.SL == s.SL &&
-          c.threads == s.threads && c.bulk == static_cast<int>(s.bulk) && c.smem == s.smem) {
-        *n = c.n;
-        return cudaSuccess;
-      }
-    }
-  }
-  int m = 0;
-  err = sdk::max_active_clusters(elem, s, &m);
-  if (err != cudaSuccess) return err;
-  if (m < 1) return cudaErrorInvalidConfiguration;
-  std::lock_guard<std::mutex> lk(g_clusters.mu);
-  if (g_clusters.used < 64)
-    g_clusters.e[g_clusters.used++] = {dev, elem, s.C, s.S, s.SL, s.threads,
-                                      static_cast<int>(s.bulk), s.smem, m};
-  *n = m;
-  return cudaSuccess;
-}
-
-sd_status shape_for(int V, sd_dtype dt, int bs, const sd_launch_cfg* cfg, bool bulk,
+sd_status shape_for(int V, sd_dtype dt, int bs, const sd_launch_cfg* cfg, bool vec,
                     sdk::VerifyShape* shape) {
   const int elem = dt == SD_F32 ? 4 : 2;
   bool fits = false;
-  if (note(sdk::choose_verify_shape(V, elem, bs, cfg, bulk, shape, &fits)) != cudaSuccess)
+  if (note(sdk::choose_verify_shape(V, elem, bs, cfg, vec, shape, &fits)) != cudaSuccess)
     return SD_ERR_CUDA;
-  if (!fits) return SD_ERR_UNSUPPORTED;
-  int m = 0;
-  if (note(resident_clusters(elem, *shape, &m)) != cudaSuccess) return SD_ERR_CUDA;
-  if (shape->clusters <= 0 || shape->clusters > m) shape->clusters = m;
-  return SD_OK;
+  return fits ? SD_OK : SD_ERR_UNSUPPORTED;
 }
 
 }  // namespace
@@ -185,33 +147,29 @@ size_t sd_verify_workspace_bytes(int bs, int k_max) {
   return verify_ws_bytes(bs, k_max);
 }
 
-static sd_status check_verify_common(int bs, int k_max, void* workspace, size_t ws_bytes) {
+sd_status sd_verify_ex(const void* target_logits, const void* draft_logits, sd_dtype dt, int V,
+                       const int* draft_ids, const float* uniforms, const float* temps,
+                       const int* cu_seqlens, int bs, int k_max, int* accepted_len,
+                       int* out_tokens, float* probs_out, int* err_flag, void* workspace,
+                       size_t ws_bytes, const sd_launch_cfg* cfg, void* stream) {
   if (bs < 1 || k_max < 0) return SD_ERR_INVALID_ARG;
   if (k_max > SD_MAX_K || bs > SD_MAX_VERIFY_BS) return SD_ERR_UNSUPPORTED;
   if (!workspace || !aligned16(workspace)) return SD_ERR_INVALID_ARG;
   if (ws_bytes < verify_ws_bytes(bs, k_max)) return SD_ERR_SHAPE;
-  return SD_OK;
-}
-
-sd_status sd_verify_rows(const void* target_logits, const void* draft_logits, sd_dtype dt, int V,
-                         const int* draft_ids, const float* uniforms, const float* temps,
-                         const int* cu_seqlens, int bs, int k_max, float* probs_out,
-                         int* err_flag, void* workspace, size_t ws_bytes,
-                         const sd_launch_cfg* cfg, void* stream) {
-  sd_status st = check_verify_common(bs, k_max, workspace, ws_bytes);
-  if (st != SD_OK) return st;
   if (dt != SD_F32 && dt != SD_BF16) return SD_ERR_INVALID_ARG;
   if (V < 1) return SD_ERR_INVALID_ARG;
   if (V > SD_MAX_V) return SD_ERR_UNSUPPORTED;
-  if (!target_logits || !uniforms || !temps || !cu_seqlens || !err_flag) return SD_ERR_INVALID_ARG;
+  if (!target_logits || !uniforms || !temps || !cu_seqlens || !err_flag || !accepted_len ||
+      !out_tokens)
+    return SD_ERR_INVALID_ARG;
   if (k_max > 0 && !draft_ids) return SD_ERR_INVALID_ARG;
-  if (cfg && (cfg->cluster < 0 || cfg->stages < 0 || cfg->clusters < 0 || cfg->threads < 0))
+  if (cfg && (cfg->threads < 0 || cfg->blocks < 0 || cfg->blocks_per_sm < 0))
     return SD_ERR_INVALID_ARG;
   const int elem = dt == SD_F32 ? 4 : 2;
-  const bool bulk = (static_cast<size_t>(V) * elem) % 16 == 0 && aligned16(target_logits) &&
-                    (draft_logits == nullptr || aligned16(draft_logits));
+  const bool vec = (static_cast<size_t>(V) * elem) % 16 == 0 && aligned16(target_logits) &&
+                   (draft_logits == nullptr || aligned16(draft_logits));
   sdk::VerifyShape shape;
-  st = shape_for(V, dt, bs, cfg, bulk, &shape);
+  sd_status st = shape_for(V, dt, bs, cfg, vec, &shape);
   if (st != SD_OK) return st;
   VerifyWs w = carve(workspace, bs, k_max);
   sdk::VerifyParams p;
@@ -224,32 +182,16 @@ sd_status sd_verify_rows(const void* target_logits, const void* draft_logits, sd
   p.cu = cu_seqlens;
   p.bs = bs;
   p.k_max = k_max;
+  p.accepted_len = accepted_len;
+  p.out_tokens = out_tokens;
   p.probs_out = probs_out;
   p.err = err_flag;
-  p.ws_accept = w.accept;
-  p.ws_cand = w.cand;
-  p.ws_status = w.status;
-  p.C = shape.C;
-  p.S = shape.S;
-  p.SL = shape.SL;
-  p.stage_bytes = static_cast<int>(2 * static_cast<size_t>(shape.SL) * elem);
-  return note(sdk::launch_verify_rows(p, elem, shape, static_cast<cudaStream_t>(stream))) ==
+  p.st_t = w.st_t;
+  p.st_d = w.st_d;
+  p.req_cnt = w.req_cnt;
+  p.ctrl = w.ctrl;
+  return note(sdk::launch_verify(p, elem, shape, static_cast<cudaStream_t>(stream))) ==
                  cudaSuccess
-             ? SD_OK
-             : SD_ERR_CUDA;
-}
-
-sd_status sd_verify_finalize(const int* draft_ids, const int* cu_seqlens, int bs, int k_max,
-                             int* accepted_len, int* out_tokens, int* err_flag,
-                             const void* workspace, size_t ws_bytes, void* stream) {
-  sd_status st = check_verify_common(bs, k_max, const_cast<void*>(workspace), ws_bytes);
-  if (st != SD_OK) return st;
-  if (!cu_seqlens || !accepted_len || !out_tokens || !err_flag) return SD_ERR_INVALID_ARG;
-  if (k_max > 0 && !draft_ids) return SD_ERR_INVALID_ARG;
-  VerifyWs w = carve(const_cast<void*>(workspace), bs, k_max);
-  return note(sdk::launch_verify_finalize(draft_ids, cu_seqlens, bs, k_max, accepted_len,
-                                          out_tokens, err_flag, w.accept, w.cand, w.status,
-                                          static_cast<cudaStream_t>(stream))) == cudaSuccess
              ? SD_OK
              : SD_ERR_CUDA;
 }
@@ -259,28 +201,24 @@ sd_status sd_verify(const void* target_logits, const void* draft_logits, sd_dtyp
                     const int* cu_seqlens, int bs, int k_max, int* accepted_len, int* out_tokens,
                     float* probs_out, int* err_flag, void* workspace, size_t ws_bytes,
                     void* stream) {
-  if (!accepted_len || !out_tokens) return SD_ERR_INVALID_ARG;
-  sd_status st = sd_verify_rows(target_logits, draft_logits, dt, V, draft_ids, uniforms, temps,
-                                cu_seqlens, bs, k_max, probs_out, err_flag, workspace, ws_bytes,
-                                nullptr, stream);
-  if (st != SD_OK) return st;
-  return sd_verify_finalize(draft_ids, cu_seqlens, bs, k_max, accepted_len, out_tokens, err_flag,
-                            workspace, ws_bytes, stream);
+  return sd_verify_ex(target_logits, draft_logits, dt, V, draft_ids, uniforms, temps, cu_seqlens,
+                      bs, k_max, accepted_len, out_tokens, probs_out, err_flag, workspace,
+                      ws_bytes, nullptr, stream);
 }
 
-sd_status sd_verify_launch_info(int V, sd_dtype dt, const sd_launch_cfg* req,
-                                sd_launch_cfg* chosen, int* threads, size_t* smem_bytes) {
-  if (V < 1 || (dt != SD_F32 && dt != SD_BF16) || !chosen) return SD_ERR_INVALID_ARG;
+sd_status sd_verify_launch_info(int V, sd_dtype dt, int bs, const sd_launch_cfg* req,
+                                sd_launch_cfg* chosen, size_t* smem_bytes) {
+  if (V < 1 || bs < 1 || (dt != SD_F32 && dt != SD_BF16) || !chosen) return SD_ERR_INVALID_ARG;
+  if (bs > SD_MAX_VERIFY_BS || V > SD_MAX_V) return SD_ERR_UNSUPPORTED;
   const int elem = dt == SD_F32 ? 4 : 2;
-  const bool bulk = (static_cast<size_t>(V) * elem) % 16 == 0;
+  const bool vec = (static_cast<size_t>(V) * elem) % 16 == 0;
   sdk::VerifyShape shape;
-  sd_status st = shape_for(V, dt, 1, req, bulk, &shape);
+  sd_status st = shape_for(V, dt, bs, req, vec, &shape);
   if (st != SD_OK) return st;
-  chosen->cluster = shape.C;
-  chosen->stages = shape.S;
-  chosen->clusters = shape.clusters;
   chosen->threads = shape.threads;
-  if (threads) *threads = shape.threads;
+  chosen->blocks = shape.blocks;
+  chosen->blocks_per_sm = 0;
+  chosen->reserved = 0;
   if (smem_bytes) *smem_bytes = shape.smem;
   return SD_OK;
 }

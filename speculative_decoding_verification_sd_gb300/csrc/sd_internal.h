@@ -38,6 +38,14 @@ size_t plan_smem_bytes(const PlanParams& p);
 cudaError_t launch_plan(const PlanParams& p, cudaStream_t s);
 
 // ---------------------------------------------------------------- sampler
+// Statistics of one logit row, 16 bytes: m = max logit, z = sum over the row
+// of 2^((l - m) * log2(e) / tau) (tau > 0), lx = logit at the slot's draft
+// token, amax = lowest index of the maximum (tau = 0; -1 if the row is bad).
+struct __align__(16) RowStat {
+  float m, z, lx;
+  int amax;
+};
+
 struct VerifyParams {
   const void* target;
   const void* draft;
@@ -48,34 +56,27 @@ struct VerifyParams {
   const int* cu;
   int bs;
   int k_max;
+  int* accepted_len;
+  int* out_tokens;
   float* probs_out;
   int* err;
-  uint8_t* ws_accept;  // [rows_cap]
-  int* ws_cand;        // [rows_cap]
-  int* ws_status;      // [1] 0 = rows pass ran on valid cu_seqlens
-  // launch shape
-  int C;            // cluster size
-  int S;            // stages
-  int SL;           // vocabulary slice per CTA (elements, multiple of 64)
-  int stage_bytes;  // 2 * SL * elem
+  RowStat* st_t;  // [bs*(k_max+1)]
+  RowStat* st_d;  // [bs*k_max]
+  int* req_cnt;   // [bs]   rows finished per request; zero between calls
+  int* ctrl;      // [4]    work counter, CTAs finished; zero between calls
 };
 
 struct VerifyShape {
-  int C, S, SL, threads, clusters;
+  int threads, blocks;
   size_t smem;
-  bool bulk;
+  bool vec;
 };
 
-// Chooses (threads, C, S, SL) for (V, dtype, bs) on the current device,
-// honouring a user request; *fits = false when no shape fits.
-cudaError_t choose_verify_shape(int V, int elem, int bs, const sd_launch_cfg* req, bool bulk,
+// Chooses the launch of the sampling kernel for (V, dtype, bs) on the current
+// device, honouring a user request; *fits = false when nothing fits.
+cudaError_t choose_verify_shape(int V, int elem, int bs, const sd_launch_cfg* req, bool vec,
                                 VerifyShape* out, bool* fits);
-cudaError_t launch_verify_rows(const VerifyParams& p, int elem, const VerifyShape& shape,
-                               cudaStream_t s);
-cudaError_t launch_verify_finalize(const int* draft_ids, const int* cu, int bs, int k_max,
-                                   int* accepted_len, int* out_tokens, int* err,
-                                   const uint8_t* ws_accept, const int* ws_cand,
-                                   const int* ws_status, cudaStream_t s);
-cudaError_t max_active_clusters(int elem, const VerifyShape& shape, int* n);
+cudaError_t launch_verify(const VerifyParams& p, int elem, const VerifyShape& shape,
+                          cudaStream_t s);
 
 }  // namespace sdk

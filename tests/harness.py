@@ -92,7 +92,7 @@ def compare_plan(g, o, what=""):
     return same
 
 
-def gpu_verify(w, vi, cu, k_max, cfg=None, rows_cap=None, split=False):
+def gpu_verify(w, vi, cu, k_max, cfg=None, rows_cap=None, workspace=None):
     """Runs the sampling stage through the C ABI with capacity-sized buffers."""
     import torch
     import speculative_decoding_verification_sd_gb300 as sd
@@ -107,22 +107,17 @@ def gpu_verify(w, vi, cu, k_max, cfg=None, rows_cap=None, split=False):
     tp = torch.from_numpy(vi["temps"]).to(torch_dev())
     cu_d = torch.from_numpy(np.asarray(cu, np.int32)).to(torch_dev())
     dt = sd.SD_F32 if w.dtype == S.F32 else sd.SD_BF16
-    if not split and cfg is None:
-        r = sd.verify(tgt, dft, dt, w.V, ids, u, tp, cu_d, k_max, probs=True)
-        acc, out, probs, err = r.accepted_len, r.out_tokens, r.probs, r.err
-    else:
-        acc = torch.empty(bs, dtype=torch.int32, device=torch_dev())
-        out = torch.empty((bs, k_max + 1), dtype=torch.int32, device=torch_dev())
-        probs = torch.full((max(bs * k_max, 1), 2), float("nan"), dtype=torch.float32, device=torch_dev())
-        err = torch.zeros(1, dtype=torch.int32, device=torch_dev())
-        nb = sd.sd_verify_workspace_bytes(bs, k_max)
-        ws = torch.empty(nb, dtype=torch.uint8, device=torch_dev())
-        sd.sd_verify_rows(tgt, dft, dt, w.V, ids, u, tp, cu_d, bs, k_max, probs, err, ws, nb, cfg=cfg)
-        sd.sd_verify_finalize(ids, cu_d, bs, k_max, acc, out, err, ws, nb)
+    acc = torch.empty(bs, dtype=torch.int32, device=torch_dev())
+    out = torch.empty((bs, k_max + 1), dtype=torch.int32, device=torch_dev())
+    probs = torch.full((max(bs * k_max, 1), 2), float("nan"), dtype=torch.float32, device=torch_dev())
+    err = torch.zeros(1, dtype=torch.int32, device=torch_dev())
+    ws = workspace if workspace is not None else sd.verify_workspace(bs, k_max, torch_dev())
+    sd.sd_verify_ex(tgt, dft, dt, w.V, ids, u, tp, cu_d, bs, k_max, acc, out, probs, err, ws,
+                    ws.numel(), cfg=cfg)
     torch.cuda.synchronize()
     return {"accepted_len": acc.cpu().numpy(), "out_tokens": out.cpu().numpy(),
-            "probs": probs.cpu().numpy() if probs is not None else None, "err": int(err.item()),
-            "target_dev": tgt, "draft_dev": dft}
+            "probs": probs.cpu().numpy(), "err": int(err.item()),
+            "target_dev": tgt, "draft_dev": dft, "workspace": ws}
 
 
 def oracle_verify(w, vi, cu, k_max, requests=None):

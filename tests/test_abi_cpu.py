@@ -102,9 +102,13 @@ def test_verify_rejects_bad_arguments_on_host(lib):
     assert call(V=(1 << 22) + 1) == sd.SD_ERR_UNSUPPORTED
     assert call(t=None) == sd.SD_ERR_INVALID_ARG
     assert call(acc=None) == sd.SD_ERR_INVALID_ARG
+    assert call(out=None) == sd.SD_ERR_INVALID_ARG
     assert call(ws=None) == sd.SD_ERR_INVALID_ARG
     assert call(ws=P + 4) == sd.SD_ERR_INVALID_ARG  # workspace not 16-byte aligned
     assert call(nb=nb - 1) == sd.SD_ERR_SHAPE
+    bad_cfg = sd.sd_launch_cfg(-1, 0, 0, 0)
+    assert lib.sd_verify_ex(P, P, 1, 1024, P, P, P, P, 4, 3, P, P, None, P, P, nb,
+                            ctypes.byref(bad_cfg), 0) == sd.SD_ERR_INVALID_ARG
 
 
 def test_binding_refuses_host_tensors(lib):
