@@ -67,6 +67,7 @@ typedef enum {
 #define SD_DEV_ERR_TEMP 0x020            /* a temperature < 0 or not finite */
 #define SD_DEV_ERR_UNIFORM 0x040         /* a uniform outside [0, 1) */
 #define SD_DEV_ERR_LOGITS 0x080          /* a logit row holds NaN/+inf or no finite value */
+#define SD_DEV_ERR_TIMEOUT 0x100         /* a bounded wait for a staged copy gave up */
 
 /* Limits of this build. */
 #define SD_MAX_K 15            /* k_max <= 15: at most 16 query rows per request */
@@ -171,10 +172,10 @@ sd_status sd_plan(const float* conf_logits, const float* budget_conf,
  *   cu_seqlens     [bs+1] int32 from sd_plan (or the caller).
  * Outputs
  *   accepted_len   [bs] int32; out_tokens [bs, k_max+1] int32, -1 padded.
- *   probs_out      [bs*k_max, 2] fp32 or NULL: (p_j(x_j), q_j(x_j)) of the
- *                  verified slots of a tau > 0 request up to its first
- *                  rejection, at the draft-row index (diagnostics; other
- *                  entries untouched).
+ *   probs_out      [bs*k_max, 2] fp32 or NULL: (p_j(x_j), q_j(x_j)) of every
+ *                  verified slot of a tau > 0 request, at the draft-row
+ *                  index (diagnostics; entries of greedy requests and of
+ *                  unverified slots untouched).
  *   err_flag       [1] int32, sticky SD_DEV_ERR_* bits.  On SD_DEV_ERR_CU_SEQLENS
  *                  no logit is read and outputs are accepted_len = 0,
  *                  out_tokens = -1.

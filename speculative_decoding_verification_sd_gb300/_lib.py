@@ -26,6 +26,7 @@ SD_DEV_ERR_DRAFT_ID = 0x010
 SD_DEV_ERR_TEMP = 0x020
 SD_DEV_ERR_UNIFORM = 0x040
 SD_DEV_ERR_LOGITS = 0x080
+SD_DEV_ERR_TIMEOUT = 0x100
 
 SD_MAX_K = 15
 SD_MAX_PLAN_SLOTS = 8192

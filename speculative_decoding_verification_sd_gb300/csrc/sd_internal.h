@@ -6,7 +6,7 @@
 #include <stddef.h>
 #include <stdint.h>
 
-#include "../../include/sd.h"
+#include "sd.h"
 
 namespace sdk {
 

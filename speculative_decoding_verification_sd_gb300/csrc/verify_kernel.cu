@@ -105,7 +105,8 @@ __device__ __forceinline__ float from_ordered(uint32_t u) {
 }
 
 // One thread's values into its running (max, scaled sum) at scale s2:
-// z = sum 2^((l - m) * s2) with m the running maximum.
+// z = sum 2^((l - m) * s2) with m the running maximum.  The exponent
+// arguments and the sum use packed fp32x2 arithmetic.
 template <int VE>
 __device__ __forceinline__ void online_add(const float (&f)[VE], float s2, float& m, float& z,
                                            float& b) {
@@ -118,12 +119,222 @@ __device__ __forceinline__ void online_add(const float (&f)[VE], float s2, float
     b = m * s2;
   }
   if (m != -INFINITY) {
+    if constexpr (VE % 2 == 0) {
+      const float2 s22 = make_float2(s2, s2);
+      const float2 nb2 = make_float2(-b, -b);
+      float2 acc = make_float2(0.0f, 0.0f);
 #pragma unroll
-    for (int e = 0; e < VE; ++e) z += exp2_ftz(fmaf(f[e], s2, -b));
+      for (int e = 0; e < VE; e += 2) {
+        const float2 t = __ffma2_rn(make_float2(f[e], f[e + 1]), s22, nb2);
+        acc = __fadd2_rn(acc, make_float2(exp2_ftz(t.x), exp2_ftz(t.y)));
+      }
+      z += acc.x + acc.y;
+    } else {
+#pragma unroll
+      for (int e = 0; e < VE; ++e) z += exp2_ftz(fmaf(f[e], s2, -b));
+    }
   }
 }
 
-constexpr int kUnroll = 8;
+
+// Packed bf16x2 maximum (NaN-ignoring / NaN-propagating), fp32 maximum that
+// propagates NaN.
+__device__ __forceinline__ uint32_t bmax2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("max.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+__device__ __forceinline__ uint32_t bmax2_nan(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("max.NaN.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+__device__ __forceinline__ float fmax_nan(float a, float b) {
+  float d;
+  asm("max.NaN.f32 %0, %1, %2;" : "=f"(d) : "f"(a), "f"(b));
+  return d;
+}
+__device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+// Counter increment that publishes this thread's earlier writes (release)
+// and sees everything published before earlier increments (acquire).
+__device__ __forceinline__ int atom_add_acq_rel(int* p, int v) {
+  int old;
+  asm volatile("atom.add.acq_rel.gpu.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
+}
+
+// Running softmax statistics of one lane over a chunk: (m, z2) with
+// z2.x + z2.y = sum 2^((l - m) * s2); the chunk's maximum is folded in once.
+template <typename T>
+struct ChunkOps;
+
+template <>
+struct ChunkOps<uint16_t> {  // 8 bf16 per 16-byte vector
+  static constexpr uint32_t kNegInf2 = 0xFF80FF80u;
+  __device__ __forceinline__ static uint4 neg_inf() {
+    return make_uint4(kNegInf2, kNegInf2, kNegInf2, kNegInf2);
+  }
+  template <int N>
+  __device__ __forceinline__ static void softmax(const uint4 (&r)[N], float s2, float& m,
+                                                 float2& z2, float& nb) {
+    uint32_t mx = kNegInf2;
+#pragma unroll
+    for (int q = 0; q < N; ++q) mx = bmax2(mx, bmax2(bmax2(r[q].x, r[q].y), bmax2(r[q].z, r[q].w)));
+    const float lm = fmaxf(bf_lo(mx), bf_hi(mx));
+    if (lm > m) {
+      if (m == -INFINITY) {
+        z2 = make_float2(0.0f, 0.0f);
+      } else {
+        const float sc = exp2_ftz((m - lm) * s2);
+        z2 = __fmul2_rn(z2, make_float2(sc, sc));
+      }
+      m = lm;
+      nb = -m * s2;
+    }
+    if (m != -INFINITY) {
+      const float2 s22 = make_float2(s2, s2), nb2 = make_float2(nb, nb);
+#pragma unroll
+      for (int q = 0; q < N; ++q) {
+        const uint32_t w4[4] = {r[q].x, r[q].y, r[q].z, r[q].w};
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
+          const float2 t = __ffma2_rn(make_float2(bf_lo(w4[h]), bf_hi(w4[h])), s22, nb2);
+          z2 = __fadd2_rn(z2, make_float2(exp2_ftz(t.x), exp2_ftz(t.y)));
+        }
+      }
+    }
+  }
+  // Running argmax of one lane: the first vector whose maximum strictly
+  // exceeds the best so far is kept whole in registers (bvec, at vector
+  // index bv); the element index is resolved once per row by first_of.
+  template <int N>
+  __device__ __forceinline__ static void argmax(const uint4 (&r)[N], int v0, float& best,
+                                                uint4& bvec, int& bv, int& nanf) {
+#pragma unroll
+    for (int q = 0; q < N; ++q) {
+      const uint32_t mx = bmax2_nan(bmax2_nan(r[q].x, r[q].y), bmax2_nan(r[q].z, r[q].w));
+      const float lo = bf_lo(mx), hi = bf_hi(mx);
+      nanf |= (lo != lo) | (hi != hi);
+      const float vm = fmaxf(lo, hi);
+      const bool up = vm > best;  // strictly larger: earlier vectors keep ties
+      best = up ? vm : best;
+      bvec = up ? r[q] : bvec;
+      bv = up ? v0 + 32 * q : bv;
+    }
+  }
+  // Lowest element index of `best` inside the kept vector.
+  __device__ __forceinline__ static int first_of(const uint4& r, int v, float best) {
+    const uint32_t w4[4] = {r.x, r.y, r.z, r.w};
+    int e = 7;
+#pragma unroll
+    for (int h = 3; h >= 0; --h) {
+      if (bf_hi(w4[h]) == best) e = 2 * h + 1;
+      if (bf_lo(w4[h]) == best) e = 2 * h;
+    }
+    return v * 8 + e;
+  }
+};
+
+template <>
+struct ChunkOps<float> {  // 4 fp32 per 16-byte vector
+  __device__ __forceinline__ static float4 neg_inf() {
+    return make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+  }
+  template <int N>
+  __device__ __forceinline__ static void softmax(const float4 (&r)[N], float s2, float& m,
+                                                 float2& z2, float& nb) {
+    float lm = -INFINITY;
+#pragma unroll
+    for (int q = 0; q < N; ++q) lm = fmaxf(fmaxf(lm, fmaxf(r[q].x, r[q].y)), fmaxf(r[q].z, r[q].w));
+    if (lm > m) {
+      if (m == -INFINITY) {
+        z2 = make_float2(0.0f, 0.0f);
+      } else {
+        const float sc = exp2_ftz((m - lm) * s2);
+        z2 = __fmul2_rn(z2, make_float2(sc, sc));
+      }
+      m = lm;
+      nb = -m * s2;
+    }
+    if (m != -INFINITY) {
+      const float2 s22 = make_float2(s2, s2), nb2 = make_float2(nb, nb);
+#pragma unroll
+      for (int q = 0; q < N; ++q) {
+        const float2 t0 = __ffma2_rn(make_float2(r[q].x, r[q].y), s22, nb2);
+        const float2 t1 = __ffma2_rn(make_float2(r[q].z, r[q].w), s22, nb2);
+        z2 = __fadd2_rn(z2, make_float2(exp2_ftz(t0.x), exp2_ftz(t0.y)));
+        z2 = __fadd2_rn(z2, make_float2(exp2_ftz(t1.x), exp2_ftz(t1.y)));
+      }
+    }
+  }
+  template <int N>
+  __device__ __forceinline__ static void argmax(const float4 (&r)[N], int v0, float& best,
+                                                float4& bvec, int& bv, int& nanf) {
+#pragma unroll
+    for (int q = 0; q < N; ++q) {
+      const float vm = fmax_nan(fmax_nan(r[q].x, r[q].y), fmax_nan(r[q].z, r[q].w));
+      nanf |= vm != vm;
+      const bool up = vm > best;
+      best = up ? vm : best;
+      bvec = up ? r[q] : bvec;
+      bv = up ? v0 + 32 * q : bv;
+    }
+  }
+  __device__ __forceinline__ static int first_of(const float4& r, int v, float best) {
+    int e = 3;
+    if (r.z == best) e = 2;
+    if (r.y == best) e = 1;
+    if (r.x == best) e = 0;
+    return v * 4 + e;
+  }
+};
+
+constexpr int kUnroll = 8;          // element path: loads in flight per thread
+constexpr int kChunkBytes = 4096;       // vector path: one bulk copy
+constexpr int kSlots = 3;               // ring slots per warp
+constexpr float kLn2 = 0.693147180559945309f;
+// log2(e) split into two floats (hi + lo) for a double-float exponent.
+constexpr float kLog2eHi = 1.44269502162933349609375f;
+constexpr float kLog2eLo = 1.925963033500011079e-08f;
+constexpr float kTwo40 = 1099511627776.0f;            // 2^40
+constexpr float kTwo56 = 72057594037927936.0f;        // 2^56
+constexpr float kTwo64 = 18446744073709551616.0f;     // 2^64
+
+__device__ __forceinline__ unsigned long long warp_sum_u64(unsigned long long v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(kFull, v, o);
+  return v;
+}
+
+__device__ __forceinline__ unsigned long long warp_scan_u64(unsigned long long v, int lane) {
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const unsigned long long t = __shfl_up_sync(kFull, v, o);
+    if (lane >= o) v += t;
+  }
+  return v;
+}
+
+// 2^(d * s2) with d = l - M given as (d_hi, d_lo) and s2 = s2_hi + s2_lo: the
+// exponent is formed in double-float so its rounding does not depend on |d|.
+// Written with explicitly rounded intrinsics so that every call site computes
+// bit-identical values (the final draw recomputes weights it summed before).
+__device__ __forceinline__ float exp2_df(float d_hi, float d_lo, float s2_hi, float s2_lo) {
+  const float t_hi = __fmul_rn(d_hi, s2_hi);
+  const float t_lo = __fadd_rn(__fmaf_rn(d_hi, s2_hi, -t_hi),
+                               __fmaf_rn(d_hi, s2_lo, __fmul_rn(d_lo, s2_hi)));
+  const float e = exp2_ftz(t_hi);
+  return __fmaf_rn(__fmul_rn(e, kLn2), t_lo, e);
+}
+
+// l - M split exactly into (hi, lo) (Knuth's two-sum).
+__device__ __forceinline__ void two_diff(float l, float M, float& hi, float& lo) {
+  hi = __fsub_rn(l, M);
+  const float bb = __fsub_rn(hi, l);
+  lo = __fadd_rn(__fsub_rn(l, __fsub_rn(hi, bb)), __fsub_rn(-M, bb));
+}
 
 template <typename T, int NT, bool VEC>
 __global__ void __launch_bounds__(NT, NT <= 256 ? 2 : 1) verify_kernel(const VerifyParams p) {
@@ -131,28 +342,42 @@ __global__ void __launch_bounds__(NT, NT <= 256 ? 2 : 1) verify_kernel(const Ver
   using Raw = typename Tr::Raw;
   constexpr int VE = Tr::VE;
   constexpr int NW = NT / 32;
+  constexpr int CB = kChunkBytes;  // bytes per ring slot (one chunk)
+  constexpr int VPC = CB / 16;     // 16-byte vectors per chunk
+  constexpr int VPL = VPC / 32;    // vectors per lane per chunk
+  constexpr int EPC = CB / static_cast<int>(sizeof(T));  // elements per chunk
+  constexpr int BW = NW - 1;       // the warp that keeps the per-row books
   static_assert(NW <= 32, "one lane per warp in the cross-warp reductions");
+  static_assert(VPL * 32 * 16 == CB, "chunk is a whole number of warp-wide vectors");
+  constexpr size_t kRing = VEC ? static_cast<size_t>(NW) * kSlots * CB : 0;
+  constexpr int kBars = VEC ? NW * kSlots : 0;
 
-  extern __shared__ __align__(16) unsigned char smem[];
-  int* cu_s = reinterpret_cast<int*>(smem);                  // [bs+1]
-  float* tau_s = reinterpret_cast<float*>(cu_s + p.bs + 1);  // [bs]
-  int* order = reinterpret_cast<int*>(tau_s + p.bs);         // [bs] request order
-  int* ustart = order + p.bs;                                // [bs+1] first unit of order[k]
-  float* R = reinterpret_cast<float*>(ustart + p.bs + 1);    // [rounds * NW] final-draw sums
+  extern __shared__ __align__(128) unsigned char smem[];
+  unsigned char* ring = smem;                                   // [NW][kSlots][CB]
+  uint64_t* mbar = reinterpret_cast<uint64_t*>(smem + kRing);   // [NW][kSlots]
+  int* cu_s = reinterpret_cast<int*>(mbar + kBars);             // [bs+1]
+  float* tau_s = reinterpret_cast<float*>(cu_s + p.bs + 1);     // [bs]
+  int* order = reinterpret_cast<int*>(tau_s + p.bs);            // [bs] request order
+  int* ustart = order + p.bs;                                   // [bs+1] first unit of order[k]
+  unsigned long long* R = reinterpret_cast<unsigned long long*>(
+      reinterpret_cast<uintptr_t>(ustart + p.bs + 1 + 1) & ~static_cast<uintptr_t>(7));
 
-  __shared__ float red_f[NW];
-  __shared__ float red_g[NW];
-  __shared__ unsigned long long red_k[NW];
+  // per-warp partial row statistics, double-buffered by unit parity
+  __shared__ float red_m[2][NW], red_z[2][NW];
+  __shared__ unsigned long long red_k[2][NW];
+  __shared__ int red_n[2][NW];
   __shared__ int red_i[NW];
-  __shared__ float s_lx;
-  __shared__ int s_unit[2];
-  __shared__ int s_last, s_a, s_pick, s_entry, s_count;
-  __shared__ float s_S, s_th;
+  __shared__ float s_lx[2];
+  __shared__ int s_q[4];        // unit queue of this CTA: the k-th unit at s_q[k & 3]
+  __shared__ int s_pending[2];  // request whose last row ended unit k-1 (or -1)
+  __shared__ int s_a, s_pick, s_count, s_found, s_ch, s_lastpos, s_hit;
+  __shared__ unsigned long long s_th;
+  __shared__ unsigned long long red_u[NW];
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int V = p.V;
   const int nvec = (V + VE - 1) / VE;  // VE divides V on the vector path
-  const int rounds = (nvec + NT - 1) / NT;
+  const size_t row_bytes = static_cast<size_t>(V) * sizeof(T);
 
   // ---- per-call checks of the compaction (identical verdict in every CTA)
   for (int i = tid; i <= p.bs; i += NT) cu_s[i] = p.cu[i];
@@ -242,111 +467,215 @@ __global__ void __launch_bounds__(NT, NT <= 256 ? 2 : 1) verify_kernel(const Ver
       run += (n + 1) + (tau_s[i] > 0.0f ? n : 0);
     }
     if (tid == 0) ustart[p.bs] = total;
-    __syncthreads();
   }
+  if (VEC && tid == 0) {
+    for (int b = 0; b < kBars; ++b) mbar_init(&mbar[b], 1);
+    fence_mbar_init();
+  }
+  if (tid == 0) {
+    s_q[0] = atomicAdd(&p.ctrl[0], 1);
+    s_q[1] = atomicAdd(&p.ctrl[0], 1);
+  }
+  __syncthreads();
   const int U_total = ustart[p.bs];
+
+  // Unit -> (request, row kind, slot, row index).
+  struct Unit {
+    int i, j, n, c0;
+    bool draft, greedy;
+    size_t row;
+  };
+  auto locate = [&](int u) {
+    int lo = 0, hi = p.bs;  // ustart[lo] <= u < ustart[hi]
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (ustart[mid] <= u) lo = mid;
+      else hi = mid;
+    }
+    Unit t;
+    t.i = order[lo];
+    const int r = u - ustart[lo];
+    t.c0 = cu_s[t.i];
+    t.n = cu_s[t.i + 1] - t.c0 - 1;
+    t.greedy = !(tau_s[t.i] > 0.0f);
+    t.draft = r > t.n;
+    t.j = t.draft ? r - (t.n + 1) : r;
+    t.row = t.draft ? static_cast<size_t>(t.c0 - t.i + t.j) : static_cast<size_t>(t.c0 + t.j);
+    return t;
+  };
+  auto row_base = [&](const Unit& t) {
+    return reinterpret_cast<const char*>(t.draft ? p.draft : p.target) + t.row * row_bytes;
+  };
+
+  // ---- per-warp bulk-copy ring (vector path): this warp's chunks of the
+  // k-th unit are w, w + NW, ...; the fetch cursor runs up to kSlots chunks
+  // ahead of consumption, across unit boundaries, but never past a unit of
+  // the queue that is not yet known.
+  uint32_t cseq = 0, iseq = 0;  // chunks consumed / issued by this warp
+  int fk = 0, fc = warp;        // fetch cursor: queue position, chunk index
+  int fk_cached = -1;           // queue position whose row base is cached
+  const char* f_base = nullptr;
+  const int nch_row = static_cast<int>((row_bytes + CB - 1) / CB);
+  auto refill = [&](int k_limit) {
+    while (iseq - cseq < static_cast<uint32_t>(kSlots) && fk <= k_limit) {
+      if (fc >= nch_row) {
+        ++fk;
+        fc = warp;
+        continue;
+      }
+      if (fk_cached != fk) {
+        const int u = s_q[fk & 3];
+        if (u >= U_total) break;
+        f_base = row_base(locate(u));
+        fk_cached = fk;
+      }
+      const int slot = static_cast<int>(iseq % kSlots);
+      const uint32_t bytes = static_cast<uint32_t>(
+          min(static_cast<size_t>(CB), row_bytes - static_cast<size_t>(fc) * CB));
+      if (lane == 0) {
+        uint64_t* bar = &mbar[warp * kSlots + slot];
+        mbar_arrive_expect_tx(bar, bytes);
+        bulk_load_nohint(ring + (warp * kSlots + slot) * CB, f_base + static_cast<size_t>(fc) * CB,
+                         bytes, bar);
+      }
+      ++iseq;
+      fc += NW;
+    }
+  };
+  if constexpr (VEC) refill(1);
 
   // ------------------------------------------------------------------------
   // Final draw over one row (pair): the first element whose running weight
-  // sum exceeds u * S.  Weights are summed per (round, warp) in vocabulary
-  // order; warp 0 finds the entry holding the crossing and recomputes its 32
-  // vectors to pick the element.  Rounding disagreements between levels fall
-  // back to the last positive weight of the chosen range.  Returns S.
-  auto draw = [&](auto weights, float ufin) -> float {
-    for (int r = 0; r < rounds; ++r) {
-      const int v = r * NT + tid;
-      float s = 0.0f;
-      if (v < nvec) {
-        float w[VE];
-        weights(v, w);
+  // sum exceeds u * S.  The row is cut into chunks of CU units (vectors, or
+  // elements on the element path); warp w sums chunks w, w + NW, ... in
+  // 64-bit fixed point (each unit's fp32 weight sum converted), so the chunk
+  // prefix is exact and the crossing chunk is found without rounding.  Warp 0
+  // then recomputes that chunk with the precise weight function and walks it
+  // element by element; should the recomputed chunk not reach the threshold
+  // (the two weight functions differ by rounding) the chunk's last positive
+  // weight stands in.  Returns false when the weights have no mass.
+  constexpr int CU = VEC ? 256 : (4096 / static_cast<int>(sizeof(T)));  // units per chunk
+  constexpr int UL = CU / 32;                                             // units per lane
+  constexpr int UPT = CU > NT ? CU / NT : 1;  // units per thread in the precise walk
+  static_assert(CU % NT == 0 || NT % CU == 0, "chunk and block sizes nest");
+  const int nch = (nvec + CU - 1) / CU;
+  // The fast weight pass: all of a lane's loads for a chunk are issued before
+  // any weight is computed (the rows come from L2, latency-bound otherwise).
+  auto draw = [&](bool resid, const Raw* rt, const Raw* rd, auto fast, auto precise, float scale,
+                  float ufin) -> bool {
+    if (tid == 0) s_hit = 0;
+    constexpr int QB = VEC ? 4 : 8;  // units loaded ahead per lane
+    for (int c = warp; c < nch; c += NW) {
+      unsigned long long ls = 0;
+      for (int q0 = 0; q0 < UL; q0 += QB) {
+        Raw a[QB], b[QB];
 #pragma unroll
-        for (int e = 0; e < VE; ++e) s += w[e];
+        for (int q = 0; q < QB; ++q) {
+          const int u = c * CU + (q0 + q) * 32 + lane;
+          if (u < nvec) {
+            a[q] = ld_stream(rt + u);
+            if (resid) b[q] = ld_stream(rd + u);
+          }
+        }
+#pragma unroll
+        for (int q = 0; q < QB; ++q) {
+          const int u = c * CU + (q0 + q) * 32 + lane;
+          if (u < nvec) ls += __float2ull_rn(__fmul_rn(fast(a[q], b[q]), scale));
+        }
       }
-      s = warp_sum(s);
-      if (lane == 0) R[r * NW + warp] = s;
+      ls = warp_sum_u64(ls);
+      if (lane == 0) R[c] = ls;
     }
     __syncthreads();
     if (warp == 0) {
-      const int E = rounds * NW;
-      const int epl = (E + 31) / 32;
-      const int eb = min(E, lane * epl), ee = min(E, eb + epl);
-      float ls = 0.0f;
-      for (int e = eb; e < ee; ++e) ls += R[e];
-      const float inc = warp_inclusive_scan(ls, lane);
-      const float S = __shfl_sync(kFull, inc, 31);
-      if (lane == 0) s_S = S;
-      if (S > 0.0f && isfinite(S)) {
-        const float theta = ufin * S;
-        const unsigned cm = __ballot_sync(kFull, inc > theta);
-        int ln;
-        if (cm) {
-          ln = __ffs(cm) - 1;
-        } else {
-          const unsigned pm = __ballot_sync(kFull, ls > 0.0f);
-          ln = pm ? 31 - __clz(pm) : 0;
-        }
-        const float up = __shfl_up_sync(kFull, inc, 1);
-        const float excl = ln == 0 ? 0.0f : __shfl_sync(kFull, up, ln);
+      const int epl = (nch + 31) / 32;
+      const int eb = min(nch, lane * epl), ee = min(nch, eb + epl);
+      unsigned long long lsum = 0;
+      for (int e = eb; e < ee; ++e) lsum += R[e];
+      const unsigned long long inc = warp_scan_u64(lsum, lane);
+      const unsigned long long S = __shfl_sync(kFull, inc, 31);
+      if (S > 0) {
+        // thr = floor(u * S) < S: the crossing is the first C_k > thr
+        const unsigned long long thr = __umul64hi(__float2ull_rn(ufin * kTwo64), S);
+        const unsigned cm = __ballot_sync(kFull, inc > thr);
+        const int ln = __ffs(cm) - 1;
+        const unsigned long long up = __shfl_up_sync(kFull, inc, 1);
+        const unsigned long long excl = ln == 0 ? 0ull : __shfl_sync(kFull, up, ln);
         if (lane == ln) {
-          float run = excl;
-          int ent = -1, lastpos = -1;
+          unsigned long long run = excl;
+          int ch = ee - 1;
           for (int e = eb; e < ee; ++e) {
-            if (R[e] > 0.0f) lastpos = e;
-            if (run + R[e] > theta) { ent = e; break; }
+            if (run + R[e] > thr) { ch = e; break; }
             run += R[e];
           }
-          if (ent < 0) {
-            ent = lastpos >= 0 ? lastpos : eb;
-            run = excl;
-            for (int e = eb; e < ent; ++e) run += R[e];
-          }
-          s_entry = ent;
-          s_th = fmaxf(theta - run, 0.0f);
+          s_ch = ch;
+          s_th = thr - run;
         }
-        __syncwarp();
-        const int ent = s_entry;
-        const float th = s_th;
-        const int v = (ent / NW) * NT + (ent % NW) * 32 + lane;
-        float w[VE];
-        float sv = 0.0f;
-        int lane_last = -1;
-        if (v < nvec) {
-          weights(v, w);
-#pragma unroll
-          for (int e = 0; e < VE; ++e) {
-            sv += w[e];
-            if (w[e] > 0.0f) lane_last = v * VE + e;
-          }
-        } else {
-#pragma unroll
-          for (int e = 0; e < VE; ++e) w[e] = 0.0f;
-        }
-        const float vinc = warp_inclusive_scan(sv, lane);
-        const float vup = __shfl_up_sync(kFull, vinc, 1);
-        const float vex = lane == 0 ? 0.0f : vup;
-        const unsigned m = __ballot_sync(kFull, vinc > th);
-        int lp = lane_last;
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) lp = max(lp, __shfl_xor_sync(kFull, lp, o));
-        if (m) {
-          const int lsel = __ffs(m) - 1;
-          if (lane == lsel) {
-            float rr = vex;
-            int pick = lane_last >= 0 ? lane_last : v * VE;
-#pragma unroll
-            for (int e = 0; e < VE; ++e) {
-              rr += w[e];
-              if (rr > th) { pick = v * VE + e; break; }
-            }
-            s_pick = pick;
-          }
-        } else if (lane == 0) {
-          s_pick = lp >= 0 ? lp : 0;
-        }
+      }
+      if (lane == 0) {
+        s_found = S > 0;
+        s_lastpos = -1;
       }
     }
     __syncthreads();
-    return s_S;
+    if (s_found) {
+      // the crossing chunk, recomputed with the precise weights: one unit per
+      // thread, exact 64-bit prefix across the block in vocabulary order
+      const int ch = s_ch;
+      const unsigned long long th = s_th;
+      const int ub = ch * CU + tid * UPT;  // this thread's first unit
+      unsigned long long wi[UPT][VE];
+      unsigned long long sv = 0;
+      int lastpos = -1;
+#pragma unroll
+      for (int k = 0; k < UPT; ++k)
+#pragma unroll
+        for (int e = 0; e < VE; ++e) wi[k][e] = 0;
+      if (tid * UPT < CU) {
+#pragma unroll
+        for (int k = 0; k < UPT; ++k) {
+          const int u = ub + k;
+          if (u < nvec) {
+            precise(u, wi[k]);
+#pragma unroll
+            for (int e = 0; e < VE; ++e) {
+              sv += wi[k][e];
+              if (wi[k][e] > 0) lastpos = u * VE + e;
+            }
+          }
+        }
+      }
+      const unsigned long long winc = warp_scan_u64(sv, lane);
+      if (lane == 31) red_u[warp] = winc;
+      if (lastpos >= 0) atomicMax(&s_lastpos, lastpos);
+      __syncthreads();
+      if (warp == 0) {
+        const unsigned long long wt = lane < NW ? red_u[lane] : 0ull;
+        const unsigned long long wti = warp_scan_u64(wt, lane);
+        if (lane < NW) red_u[lane] = wti - wt;  // exclusive warp offsets
+      }
+      __syncthreads();
+      const unsigned long long before = red_u[warp] + winc - sv;  // exclusive prefix
+      if (before <= th && th < before + sv) {
+        unsigned long long acc = before;
+        int pk = -1;
+#pragma unroll
+        for (int k = 0; k < UPT; ++k)
+#pragma unroll
+          for (int e = 0; e < VE; ++e) {
+            acc += wi[k][e];
+            if (pk < 0 && acc > th) pk = (ub + k) * VE + e;
+          }
+        s_pick = pk;
+        s_hit = 1;
+      }
+      __syncthreads();
+      // the two weight functions differ by rounding: a threshold past the
+      // recomputed chunk takes the chunk's last positive weight
+      if (tid == 0 && !s_hit) s_pick = s_lastpos >= 0 ? s_lastpos : ch * CU * VE;
+    }
+    __syncthreads();
+    return s_found != 0;
   };
 
   // ------------------------------------------------------------------------
@@ -357,42 +686,49 @@ __global__ void __launch_bounds__(NT, NT <= 256 ? 2 : 1) verify_kernel(const Ver
     const int d0 = c0 - i;
     const float tau = tau_s[i];
     const bool greedy = !(tau > 0.0f);
-    const float s2 = greedy ? 0.0f : kLog2e / tau;
+    // s2 = log2(e) / tau as a double-float
+    float s2h = 0.0f, s2l = 0.0f;
+    if (!greedy) {
+      s2h = kLog2eHi / tau;
+      s2l = (fmaf(-s2h, tau, kLog2eHi) + kLog2eLo) / tau;
+    }
     const float* urow = p.uniforms + static_cast<size_t>(i) * (p.k_max + 1);
-    if (tid == 0) {
-      int a = n;
-      for (int j = 0; j < n; ++j) {
-        const int x = p.draft_ids[d0 + j];
-        const bool x_ok = x >= 0 && x < V;
-        if (!x_ok) raise_error(p.err, SD_DEV_ERR_DRAFT_ID);
-        const float4 ts = __ldcg(reinterpret_cast<const float4*>(p.st_t + c0 + j));
-        bool acc;
-        if (greedy) {
-          const int amax = __float_as_int(ts.w);
-          if (amax < 0) raise_error(p.err, SD_DEV_ERR_LOGITS);
-          acc = x_ok && amax >= 0 && x == amax;
-        } else {
-          const float4 ds = __ldcg(reinterpret_cast<const float4*>(p.st_d + d0 + j));
-          const bool ok = isfinite(ts.x) && isfinite(ts.y) && ts.y > 0.0f && isfinite(ds.x) &&
-                          isfinite(ds.y) && ds.y > 0.0f;
-          float px = 0.0f, qx = 0.0f;
-          if (ok && x_ok) {
-            px = exp2_full(fmaf(ts.z, s2, -ts.x * s2)) / ts.y;
-            qx = exp2_full(fmaf(ds.z, s2, -ds.x * s2)) / ds.y;
-          }
-          if (!ok) raise_error(p.err, SD_DEV_ERR_LOGITS);
-          const float u = urow[j];
-          if (!(u >= 0.0f && u < 1.0f)) raise_error(p.err, SD_DEV_ERR_UNIFORM);
-          acc = ok && x_ok && (u * qx) <= px;
-          if (p.probs_out) {
-            p.probs_out[2 * static_cast<size_t>(d0 + j)] = px;
-            p.probs_out[2 * static_cast<size_t>(d0 + j) + 1] = qx;
-          }
+    // accept tests of all slots in parallel (thread j tests slot j)
+    if (tid == 0) { s_a = n; s_pick = 0; }
+    __syncthreads();
+    if (tid < n) {
+      const int j = tid;
+      const int x = p.draft_ids[d0 + j];
+      const bool x_ok = x >= 0 && x < V;
+      if (!x_ok) raise_error(p.err, SD_DEV_ERR_DRAFT_ID);
+      const float4 ts = __ldcg(reinterpret_cast<const float4*>(p.st_t + c0 + j));
+      bool acc;
+      if (greedy) {
+        const int amax = __float_as_int(ts.w);
+        if (amax < 0) raise_error(p.err, SD_DEV_ERR_LOGITS);
+        acc = x_ok && amax >= 0 && x == amax;
+      } else {
+        const float4 ds = __ldcg(reinterpret_cast<const float4*>(p.st_d + d0 + j));
+        const bool ok = isfinite(ts.x) && isfinite(ts.y) && ts.y > 0.0f && isfinite(ds.x) &&
+                        isfinite(ds.y) && ds.y > 0.0f;
+        float px = 0.0f, qx = 0.0f;
+        if (ok && x_ok) {
+          float h, l;
+          two_diff(ts.z, ts.x, h, l);
+          px = exp2_df(h, l, s2h, s2l) / ts.y;
+          two_diff(ds.z, ds.x, h, l);
+          qx = exp2_df(h, l, s2h, s2l) / ds.y;
         }
-        if (!acc) { a = j; break; }
+        if (!ok) raise_error(p.err, SD_DEV_ERR_LOGITS);
+        const float u = urow[j];
+        if (!(u >= 0.0f && u < 1.0f)) raise_error(p.err, SD_DEV_ERR_UNIFORM);
+        acc = ok && x_ok && (u * qx) <= px;
+        if (p.probs_out) {
+          p.probs_out[2 * static_cast<size_t>(d0 + j)] = px;
+          p.probs_out[2 * static_cast<size_t>(d0 + j) + 1] = qx;
+        }
       }
-      s_a = a;
-      s_pick = 0;
+      if (!acc) atomicMin(&s_a, j);
     }
     __syncthreads();
     const int a = s_a;
@@ -418,34 +754,69 @@ __global__ void __launch_bounds__(NT, NT <= 256 ? 2 : 1) verify_kernel(const Ver
                                                      static_cast<size_t>(c0 + a) * V);
         const Raw* rd = reinterpret_cast<const Raw*>(
             static_cast<const T*>(p.draft) + static_cast<size_t>(reject ? d0 + a : 0) * V);
-        const float bt = ts.x * s2, bd = ds.x * s2;
+        const float Mt = ts.x, Md = ds.x;
         const float iZt = 1.0f / ts.y, iZd = 1.0f / ds.y;
-        float S = 0.0f;
+        const float s2 = kLog2e / tau;
+        const float bt = Mt * s2, bd = Md * s2;
+        bool found = false;
         if (reject) {
-          S = draw(
-              [&](int v, float (&w)[VE]) {
+          // residual max(p - q, 0) <= 1, fixed point 2^56
+          found = draw(
+              true, rt, rd,
+              [&](const Raw& ra, const Raw& rb) {
                 float f[VE], g[VE];
-                Tr::unpack(rt[v], f);
-                Tr::unpack(rd[v], g);
+                Tr::unpack(ra, f);
+                Tr::unpack(rb, g);
+                float ws = 0.0f;
 #pragma unroll
                 for (int e = 0; e < VE; ++e) {
                   const float et = exp2_ftz(fmaf(f[e], s2, -bt));
                   const float ed = exp2_ftz(fmaf(g[e], s2, -bd));
-                  w[e] = fmaxf(fmaf(et, iZt, -(ed * iZd)), 0.0f);
+                  ws += fmaxf(fmaf(et, iZt, -(ed * iZd)), 0.0f);
+                }
+                return ws;
+              },
+              [&](int u, unsigned long long (&wi)[VE]) {
+                float f[VE], g[VE];
+                Tr::unpack(rt[u], f);
+                Tr::unpack(rd[u], g);
+#pragma unroll
+                for (int e = 0; e < VE; ++e) {
+                  float h, l;
+                  two_diff(f[e], Mt, h, l);
+                  const float et = exp2_df(h, l, s2h, s2l);
+                  two_diff(g[e], Md, h, l);
+                  const float ed = exp2_df(h, l, s2h, s2l);
+                  const float w = fmaxf(__fmaf_rn(et, iZt, -__fmul_rn(ed, iZd)), 0.0f);
+                  wi[e] = __float2ull_rn(__fmul_rn(w, kTwo56));
                 }
               },
-              ufin);
+              kTwo56, ufin);
         }
         // bonus token, or a residual with no mass in fp32: draw from p
-        if (!reject || !(S > 0.0f && isfinite(S))) {
+        // (unnormalised 2^((l - M) s2) <= 1 in fixed point 2^40)
+        if (!found) {
           draw(
-              [&](int v, float (&w)[VE]) {
+              false, rt, rt,
+              [&](const Raw& ra, const Raw&) {
                 float f[VE];
-                Tr::unpack(rt[v], f);
+                Tr::unpack(ra, f);
+                float ws = 0.0f;
 #pragma unroll
-                for (int e = 0; e < VE; ++e) w[e] = exp2_ftz(fmaf(f[e], s2, -bt));
+                for (int e = 0; e < VE; ++e) ws += exp2_ftz(fmaf(f[e], s2, -bt));
+                return ws;
               },
-              ufin);
+              [&](int u, unsigned long long (&wi)[VE]) {
+                float f[VE];
+                Tr::unpack(rt[u], f);
+#pragma unroll
+                for (int e = 0; e < VE; ++e) {
+                  float h, l;
+                  two_diff(f[e], Mt, h, l);
+                  wi[e] = __float2ull_rn(__fmul_rn(exp2_df(h, l, s2h, s2l), kTwo40));
+                }
+              },
+              kTwo40, ufin);
         }
       }
     }
@@ -462,40 +833,62 @@ __global__ void __launch_bounds__(NT, NT <= 256 ? 2 : 1) verify_kernel(const Ver
   };
 
   // ------------------------------------------------------------------------
-  // Work loop: one row per unit.
-  if (tid == 0) s_unit[0] = atomicAdd(&p.ctrl[0], 1);
-  __syncthreads();
-  int buf = 0;
-  int cur = s_unit[0];
-  while (cur < U_total) {
-    int nxt = 0;
-    if (tid == 0) nxt = atomicAdd(&p.ctrl[0], 1);  // next unit, consumed after this one
-    int lo = 0, hi = p.bs;  // ustart[lo] <= cur < ustart[hi]
-    while (hi - lo > 1) {
-      const int mid = (lo + hi) >> 1;
-      if (ustart[mid] <= cur) lo = mid;
-      else hi = mid;
-    }
-    const int i = order[lo];
-    const int r = cur - ustart[lo];
-    const int c0 = cu_s[i];
-    const int n = cu_s[i + 1] - c0 - 1;
-    const float tau = tau_s[i];
-    const bool greedy = !(tau > 0.0f);
-    const bool is_draft = r > n;
-    const int j = is_draft ? r - (n + 1) : r;
-    const size_t row = is_draft ? static_cast<size_t>(c0 - i + j) : static_cast<size_t>(c0 + j);
-    const Raw* rowp = reinterpret_cast<const Raw*>(
-        static_cast<const T*>(is_draft ? p.draft : p.target) + row * V);
-    const int x = j < n ? p.draft_ids[c0 - i + j] : -1;
-    const int vx = (x >= 0 && x < V) ? x / VE : -1;
-    if (tid == 0) s_lx = 0.0f;
-    __syncthreads();
+  // Work loop: one row per unit.  After the barrier that ends unit k, warp BW
+  // folds the warps' partials into the row statistics, stores them and counts
+  // the row for its request with an acquire-release increment whose result
+  // is only read at the end of unit k + 1: the CTA that saw the last row of a
+  // request then runs the request's tail.
+  int pend_i = -1, pend_old = 0, pend_rows = 0;  // warp BW lane 0: outstanding count
+  for (int k = 0;; ++k) {
+    const int cur = s_q[k & 3];
+    if (cur >= U_total) break;
+    const int par = k & 1;
+    int nxt2 = 0;
+    if (tid == 0) nxt2 = atomicAdd(&p.ctrl[0], 1);  // the unit after next
+    const Unit t = locate(cur);
+    const int x = t.j < t.n ? p.draft_ids[t.c0 - t.i + t.j] : -1;
+    const bool x_ok = x >= 0 && x < V;
+    const float tau = tau_s[t.i];
+    const float s2 = t.greedy ? 0.0f : kLog2e / tau;
 
-    float4 stat = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-    if (greedy) {
-      float best = -INFINITY;
-      int bidx = INT_MAX, nanf = 0;
+    float best = -INFINITY;  // greedy
+    int bidx = INT_MAX, nanf = 0, bv = -1;
+    Raw bvec;
+    float m = -INFINITY, nb = 0.0f;  // sampling
+    float2 z2 = make_float2(0.0f, 0.0f);
+    if constexpr (VEC) {
+      const int cx = x_ok ? x / EPC : -1;
+      refill(k + 1);
+      for (int c = warp; c < nch_row; c += NW) {
+        const int slot = static_cast<int>(cseq % kSlots);
+        uint64_t* bar = &mbar[warp * kSlots + slot];
+        if (!mbar_wait_bounded(bar, (cseq / kSlots) & 1, 1u << 24))
+          raise_error(p.err, SD_DEV_ERR_TIMEOUT);
+        const unsigned char* chunk = ring + (warp * kSlots + slot) * CB;
+        const int nv = min(VPC, nvec - c * VPC);
+        if (c == cx && lane == 0) {
+          float v;
+          if (sizeof(T) == 2)
+            v = __uint_as_float(static_cast<uint32_t>(reinterpret_cast<const uint16_t*>(chunk)[x - c * EPC]) << 16);
+          else
+            v = reinterpret_cast<const float*>(chunk)[x - c * EPC];
+          s_lx[par] = v;
+        }
+        Raw rv[VPL];
+#pragma unroll
+        for (int q = 0; q < VPL; ++q)
+          rv[q] = lane + 32 * q < nv ? reinterpret_cast<const Raw*>(chunk)[lane + 32 * q]
+                                     : ChunkOps<T>::neg_inf();
+        if (t.greedy) ChunkOps<T>::argmax(rv, c * VPC + lane, best, bvec, bv, nanf);
+        else ChunkOps<T>::softmax(rv, s2, m, z2, nb);
+        __syncwarp();
+        ++cseq;
+        refill(k + 1);
+      }
+      if (t.greedy && bv >= 0) bidx = ChunkOps<T>::first_of(bvec, bv, best);
+    } else {
+      const Raw* rowp = reinterpret_cast<const Raw*>(row_base(t));
+      float b = 0.0f, z = 0.0f;
       for (int v0 = tid; v0 < nvec; v0 += NT * kUnroll) {
         Raw rv[kUnroll];
 #pragma unroll
@@ -509,97 +902,80 @@ __global__ void __launch_bounds__(NT, NT <= 256 ? 2 : 1) verify_kernel(const Ver
           if (v < nvec) {
             float f[VE];
             Tr::unpack(rv[q], f);
-            if (v == vx) {
-#pragma unroll
-              for (int e = 0; e < VE; ++e)
-                if (v * VE + e == x) s_lx = f[e];
-            }
-#pragma unroll
-            for (int e = 0; e < VE; ++e) {
-              nanf |= (f[e] != f[e]);
-              if (f[e] > best) { best = f[e]; bidx = v * VE + e; }
+            if (v == x) s_lx[par] = f[0];
+            if (t.greedy) {
+              nanf |= (f[0] != f[0]);
+              if (f[0] > best) { best = f[0]; bidx = v; }
+            } else {
+              online_add<VE>(f, s2, m, z, b);
             }
           }
         }
       }
-      // Lowest index among the maxima: a thread meets its elements in
-      // increasing index order, so its first maximum is its lowest.
+      z2 = make_float2(z, 0.0f);
+    }
+
+    // warp partials
+    if (t.greedy) {
       unsigned long long key = bidx == INT_MAX ? 0ull
           : (static_cast<unsigned long long>(ordered_bits(best)) << 32) |
                 static_cast<unsigned long long>(0xFFFFFFFFu - static_cast<uint32_t>(bidx));
       key = warp_max_u64(key);
       nanf = __any_sync(kFull, nanf);
-      if (lane == 0) { red_k[warp] = key; red_i[warp] = nanf; }
-      __syncthreads();
-      if (tid == 0) {
-        unsigned long long kk = 0ull;
-        int nn = 0;
-        for (int w = 0; w < NW; ++w) {
-          kk = red_k[w] > kk ? red_k[w] : kk;
-          nn |= red_i[w];
-        }
+      if (lane == 0) { red_k[par][warp] = key; red_n[par][warp] = nanf; }
+    } else {
+      const float mw = warp_max(m);
+      const float zr = (m == -INFINITY || mw == -INFINITY) ? 0.0f
+                                                          : (z2.x + z2.y) * exp2_ftz((m - mw) * s2);
+      const float zw = warp_sum(zr);
+      if (lane == 0) { red_m[par][warp] = mw; red_z[par][warp] = zw; }
+    }
+    if (warp == BW && lane == 0) {
+      s_pending[par] = (pend_i >= 0 && pend_old == pend_rows - 1) ? pend_i : -1;
+      pend_i = -1;
+    }
+    if (tid == 0) s_q[(k + 2) & 3] = nxt2;
+    __syncthreads();
+    if (warp == BW) {
+      float4 stat;
+      if (t.greedy) {
+        const unsigned long long kk = warp_max_u64(lane < NW ? red_k[par][lane] : 0ull);
+        const int nn = __any_sync(kFull, lane < NW ? red_n[par][lane] : 0);
         const float bv = from_ordered(static_cast<uint32_t>(kk >> 32));
         const bool rowbad = nn || kk == 0ull || !isfinite(bv);
         const int amax = rowbad ? -1 : static_cast<int>(0xFFFFFFFFu - static_cast<uint32_t>(kk));
-        stat = make_float4(bv, 0.0f, s_lx, __int_as_float(amax));
+        stat = make_float4(bv, 0.0f, s_lx[par], __int_as_float(amax));
+      } else {
+        const float mw = lane < NW ? red_m[par][lane] : -INFINITY;
+        const float M = warp_max(mw);
+        const float zr = (lane < NW && mw != -INFINITY && M != -INFINITY)
+                             ? red_z[par][lane] * exp2_ftz((mw - M) * s2)
+                             : 0.0f;
+        stat = make_float4(M, warp_sum(zr), s_lx[par], __int_as_float(0));
       }
-    } else {
-      const float s2 = kLog2e / tau;
-      float m = -INFINITY, z = 0.0f, b = 0.0f;
-      for (int v0 = tid; v0 < nvec; v0 += NT * kUnroll) {
-        Raw rv[kUnroll];
-#pragma unroll
-        for (int q = 0; q < kUnroll; ++q) {
-          const int v = v0 + q * NT;
-          if (v < nvec) rv[q] = ld_stream(rowp + v);
-        }
-#pragma unroll
-        for (int q = 0; q < kUnroll; ++q) {
-          const int v = v0 + q * NT;
-          if (v < nvec) {
-            float f[VE];
-            Tr::unpack(rv[q], f);
-            if (v == vx) {
-#pragma unroll
-              for (int e = 0; e < VE; ++e)
-                if (v * VE + e == x) s_lx = f[e];
-            }
-            online_add<VE>(f, s2, m, z, b);
-          }
-        }
-      }
-      // block max, then every thread rescales its sum to the block max
-      const float mw = warp_max(m);
-      if (lane == 0) red_f[warp] = mw;
-      __syncthreads();
-      float M = -INFINITY;
-#pragma unroll
-      for (int w = 0; w < NW; ++w) M = fmaxf(M, red_f[w]);
-      const float zr = (m == -INFINITY || M == -INFINITY) ? 0.0f : z * exp2_ftz((m - M) * s2);
-      const float zw = warp_sum(zr);
-      if (lane == 0) red_g[warp] = zw;
-      __syncthreads();
-      if (tid == 0) {
-        float Z = 0.0f;
-        for (int w = 0; w < NW; ++w) Z += red_g[w];
-        stat = make_float4(M, Z, s_lx, __int_as_float(0));
+      if (lane == 0) {
+        RowStat* dst = t.draft ? p.st_d + t.row : p.st_t + t.row;
+        __stcg(reinterpret_cast<float4*>(dst), stat);
+        pend_rows = (t.n + 1) + (t.greedy ? 0 : t.n);
+        pend_i = t.i;
+        pend_old = atom_add_acq_rel(&p.req_cnt[t.i], 1);  // read one unit later
       }
     }
-    if (tid == 0) {
-      RowStat* dst = is_draft ? p.st_d + row : p.st_t + row;
-      __stcg(reinterpret_cast<float4*>(dst), stat);
+    if constexpr (VEC) refill(k + 2);  // the unit after next is known now
+    const int tail_i = s_pending[par];
+    if (tail_i >= 0) {
       __threadfence();
-      const int rows_i = (n + 1) + (greedy ? 0 : n);
-      s_last = atomicAdd(&p.req_cnt[i], 1) == rows_i - 1;
-      s_unit[buf ^ 1] = nxt;
+      tail(tail_i);
     }
-    __syncthreads();
-    if (s_last) {
-      __threadfence();
-      tail(i);
-    }
-    buf ^= 1;
-    cur = s_unit[buf];
+  }
+  // the count of the last unit
+  __syncthreads();
+  if (warp == BW && lane == 0)
+    s_pending[0] = (pend_i >= 0 && pend_old == pend_rows - 1) ? pend_i : -1;
+  __syncthreads();
+  if (s_pending[0] >= 0) {
+    __threadfence();
+    tail(s_pending[0]);
   }
   // The last CTA out resets the work counters for the next call.
   if (tid == 0) {
@@ -669,37 +1045,49 @@ cudaError_t prepare(void* fn, size_t smem) {
 size_t verify_smem_bytes(int bs, int V, int elem, bool vec, int threads) {
   const int VE = vec ? 16 / elem : 1;
   const int nvec = (V + VE - 1) / VE;
-  const int rounds = (nvec + threads - 1) / threads;
-  return static_cast<size_t>(4) * (4 * static_cast<size_t>(bs) + 2) +
-         static_cast<size_t>(rounds) * (threads / 32) * 4 + 16;
+  const int units_per_chunk = vec ? 256 : 4096 / elem;
+  const int nch = (nvec + units_per_chunk - 1) / units_per_chunk;
+  const int nw = threads / 32;
+  const size_t ring = vec ? static_cast<size_t>(nw) * kSlots * (kChunkBytes + 8) : 0;
+  return ring + static_cast<size_t>(4) * (4 * static_cast<size_t>(bs) + 2) + 16 +
+         static_cast<size_t>(nch) * 8;
 }
 
 cudaError_t choose_verify_shape(int V, int elem, int bs, const sd_launch_cfg* req, bool vec,
                                 VerifyShape* out, bool* fits) {
   *fits = false;
-  const int threads = (req && req->threads) ? req->threads : 512;
-  if (threads != 256 && threads != 512) return cudaSuccess;
-  void* fn = pick_kernel(elem, vec, threads);
-  const size_t smem = verify_smem_bytes(bs, V, elem, vec, threads);
-  cudaError_t e = prepare(fn, 0);
-  if (e != cudaSuccess) return e;
-  if (prepare(fn, smem) != cudaSuccess) return cudaSuccess;  // beyond this build's limits
-  int dev = 0, sms = 0, per_sm = 0;
-  e = cudaGetDevice(&dev);
+  const int treq = req ? req->threads : 0;
+  if (treq && treq != 256 && treq != 512) return cudaSuccess;
+  int dev = 0, sms = 0;
+  cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return e;
-  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, threads, smem);
-  if (e != cudaSuccess) return e;
-  if (per_sm < 1) return cudaSuccess;
-  const int want = (req && req->blocks_per_sm) ? req->blocks_per_sm : 2;
-  per_sm = std::min(per_sm, want);
-  out->threads = threads;
-  out->blocks = sms * per_sm;
-  if (req && req->blocks > 0) out->blocks = std::min(req->blocks, out->blocks);
-  out->smem = smem;
-  out->vec = vec;
-  *fits = true;
+  // 512 threads (16 warps, 192 KB ring) unless the shared memory does not
+  // fit (large batches), then 256 threads (96 KB ring).
+  const int cands[2] = {512, 256};
+  for (int ci = 0; ci < 2; ++ci) {
+    const int threads = treq ? treq : cands[ci];
+    if (treq && ci > 0) break;
+    void* fn = pick_kernel(elem, vec, threads);
+    const size_t smem = verify_smem_bytes(bs, V, elem, vec, threads);
+    e = prepare(fn, 0);
+    if (e != cudaSuccess) return e;
+    if (prepare(fn, smem) != cudaSuccess) continue;  // does not fit
+    int per_sm = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, threads, smem);
+    if (e != cudaSuccess) return e;
+    if (per_sm < 1) continue;
+    const int want = (req && req->blocks_per_sm) ? req->blocks_per_sm : 2;
+    per_sm = std::min(per_sm, want);
+    out->threads = threads;
+    out->blocks = sms * per_sm;
+    if (req && req->blocks > 0) out->blocks = std::min(req->blocks, out->blocks);
+    out->smem = smem;
+    out->vec = vec;
+    *fits = true;
+    return cudaSuccess;
+  }
   return cudaSuccess;
 }
 
