@@ -46,8 +46,8 @@ FALLBACK_HBM_GBS = 6800.0
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=3000)
+    ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--workload", default="adaptive_hc", choices=sorted(S.WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--seed", type=int, default=2026)
@@ -57,6 +57,8 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--no-plan-graph", action="store_true",
+                    help="skip the planner CUDA-graph timing (1000 launches)")
     return ap.parse_args()
 
 
@@ -75,6 +77,28 @@ def hbm_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+KERNEL_SOURCES = ("verify_kernel.cu", "sd_device.cuh", "sd_internal.h")
+
+
+def profiled_traffic(workload):
+    """DRAM bytes (read + write) per sampling launch from the committed ncu
+    summary of this workload, or None when the kernel sources have changed
+    since those counters were taken."""
+    import hashlib
+    import re
+    f = ROOT / "profiles" / f"verify_kernel_{workload}.md"
+    if not f.exists():
+        return None
+    text = f.read_text()
+    mh = re.search(r"kernel_sources_sha256_16:\s*([0-9a-f]{16})", text)
+    mt = re.search(r"traffic_bytes_per_launch:\s*(\d+)", text)
+    if not mh or not mt:
+        return None
+    src = ROOT / "speculative_decoding_verification_sd_gb300" / "csrc"
+    h = hashlib.sha256(b"".join((src / n).read_bytes() for n in KERNEL_SOURCES)).hexdigest()
+    return int(mt.group(1)) if h[:16] == mh.group(1) else None
+
+
 class ClockSampler:
     """Samples SM clocks and throttle reasons with nvidia-smi while running."""
 
@@ -86,12 +110,13 @@ class ClockSampler:
         self.index = index
         self.proc = None
         self.lines = []
+        self.win = None
 
     def __enter__(self):
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "100"],
+                 "--format=csv,noheader,nounits", "-lms", "50"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.t = threading.Thread(target=self._read, daemon=True)
             self.t.start()
@@ -102,7 +127,11 @@ class ClockSampler:
 
     def _read(self):
         for line in self.proc.stdout:
-            self.lines.append(line.strip())
+            self.lines.append((time.monotonic(), line.strip()))
+
+    def window(self, t0, t1):
+        """Restrict the summary to samples taken between t0 and t1 (monotonic)."""
+        self.win = (t0, t1)
 
     def __exit__(self, *a):
         time.sleep(0.25)
@@ -116,7 +145,12 @@ class ClockSampler:
     def summary(self):
         sm, mx, reasons = [], None, set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
+        lines = self.lines
+        win = self.win
+        if win is not None:
+            inside = [x for x in lines if win[0] <= x[0] <= win[1]]
+            lines = inside if inside else lines
+        for _, ln in lines:
             parts = [p.strip() for p in ln.split(",")]
             if len(parts) < 7:
                 continue
@@ -175,11 +209,20 @@ def run_reference(args, w, rank, world):
         return
     pi = S.plan_inputs(w, args.seed, 0)
 
+    cache = {}
+
     def vi_fn(cu):
-        return S.verify_inputs(w, args.seed, 0, cu, pi["draft_lens"])
+        # the plan is the same every step: build the logits once
+        key = cu.tobytes()
+        if key not in cache:
+            cache.clear()
+            cache[key] = S.verify_inputs(w, args.seed, 0, cu, pi["draft_lens"])
+        return cache[key]
 
     vals, times = [], []
-    per_step = max(2.0, min(args.cpu_seconds, 60.0 / max(1, args.steps + args.warmup)))
+    # each step samples whole requests until its share of about two minutes
+    # is used up (at least one request per step)
+    per_step = min(args.cpu_seconds, 120.0 / max(1, args.steps + args.warmup))
     for k in range(args.warmup + args.steps):
         v, sample, st = oracle_step(w, args.seed, pi, vi_fn, per_step)
         if k >= args.warmup:
@@ -306,11 +349,13 @@ def run_ours(args, w, rank, world, local):
     t_end = torch.cuda.Event(enable_timing=True)
     with ClockSampler(local) as clk:
         barrier()
+        w0 = time.monotonic()
         t_start.record(stream)
         for s in range(args.steps):
             step(s, evs[s])
         t_end.record(stream)
         barrier()
+        clk.window(w0, time.monotonic())
     elapsed_ms = t_start.elapsed_time(t_end)
     plan_ms = [e[0].elapsed_time(e[1]) for e in evs]
     rows_ms = [e[1].elapsed_time(e[2]) for e in evs]
@@ -345,6 +390,8 @@ def run_ours(args, w, rank, world, local):
     # Planner alone: one launch (events) and 1000 launches in a CUDA graph.
     plan_graph_us = None
     try:
+        if args.no_plan_graph:
+            raise RuntimeError("disabled by --no-plan-graph")
         g = torch.cuda.CUDAGraph()
         side = torch.cuda.Stream()
         side.wait_stream(stream)
@@ -397,7 +444,7 @@ def run_ours(args, w, rank, world, local):
         "vs_baseline": None, "dtype": "bf16" if w.dtype == S.BF16 else "f32",
         "data": "synthetic", "config": config_of(w),
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "traffic": None,
+                     "frac": achieved / peak, "traffic": profiled_traffic(w.name),
                      "kernel": "verify_kernel (sd_verify)", "peak_kind": peak_kind,
                      "frac_of_nominal_8tbs": achieved / NOMINAL_HBM_GBS,
                      "bytes_per_launch": bytes_alg, "avg_launch_ms": rows_avg_ms},
