@@ -34,26 +34,51 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 struct VerifyWs {
   sdk::RowStat* st_t;
   sdk::RowStat* st_d;
+  float2* st_r;
+  unsigned long long* rs;
   int* req_cnt;
+  int* res_list;
+  int* slice_cnt;
   int* ctrl;
 };
 
-size_t verify_ws_bytes(int bs, int k_max) {
+// Workspace layout (each part 16-byte aligned):
+// st_t | st_d | st_r | rs | req_cnt | res_list | slice_cnt | ctrl.
+struct WsLayout {
+  size_t st_t, st_d, st_r, rs, req_cnt, res_list, slice_cnt, ctrl, total;
+};
+
+WsLayout ws_layout(int bs, int k_max) {
   const size_t rows_t = static_cast<size_t>(bs) * (k_max + 1);
   const size_t rows_d = static_cast<size_t>(bs) * k_max;
-  return 16 * rows_t + 16 * rows_d + align16(4 * static_cast<size_t>(bs)) + 16;
+  const size_t ib = align16(4 * static_cast<size_t>(bs));
+  WsLayout L;
+  L.st_t = 0;
+  L.st_d = L.st_t + 16 * rows_t;
+  L.st_r = L.st_d + 16 * rows_d;
+  L.rs = L.st_r + 8 * sdk::kMaxRanges * rows_t;
+  L.req_cnt = L.rs + 8 * sdk::kMaxRanges * static_cast<size_t>(bs);
+  L.res_list = L.req_cnt + ib;
+  L.slice_cnt = L.res_list + ib;
+  L.ctrl = L.slice_cnt + ib;
+  L.total = L.ctrl + 32;
+  return L;
 }
 
+size_t verify_ws_bytes(int bs, int k_max) { return ws_layout(bs, k_max).total; }
+
 VerifyWs carve(void* ws, int bs, int k_max) {
-  const size_t rows_t = static_cast<size_t>(bs) * (k_max + 1);
-  const size_t rows_d = static_cast<size_t>(bs) * k_max;
+  const WsLayout L = ws_layout(bs, k_max);
   char* b = static_cast<char*>(ws);
   VerifyWs w;
-  w.st_t = reinterpret_cast<sdk::RowStat*>(b);
-  w.st_d = reinterpret_cast<sdk::RowStat*>(b + 16 * rows_t);
-  w.req_cnt = reinterpret_cast<int*>(b + 16 * rows_t + 16 * rows_d);
-  w.ctrl = reinterpret_cast<int*>(b + 16 * rows_t + 16 * rows_d +
-                                  align16(4 * static_cast<size_t>(bs)));
+  w.st_t = reinterpret_cast<sdk::RowStat*>(b + L.st_t);
+  w.st_d = reinterpret_cast<sdk::RowStat*>(b + L.st_d);
+  w.st_r = reinterpret_cast<float2*>(b + L.st_r);
+  w.rs = reinterpret_cast<unsigned long long*>(b + L.rs);
+  w.req_cnt = reinterpret_cast<int*>(b + L.req_cnt);
+  w.res_list = reinterpret_cast<int*>(b + L.res_list);
+  w.slice_cnt = reinterpret_cast<int*>(b + L.slice_cnt);
+  w.ctrl = reinterpret_cast<int*>(b + L.ctrl);
   return w;
 }
 
@@ -188,7 +213,11 @@ sd_status sd_verify_ex(const void* target_logits, const void* draft_logits, sd_d
   p.err = err_flag;
   p.st_t = w.st_t;
   p.st_d = w.st_d;
+  p.st_r = w.st_r;
+  p.rs = w.rs;
   p.req_cnt = w.req_cnt;
+  p.res_list = w.res_list;
+  p.slice_cnt = w.slice_cnt;
   p.ctrl = w.ctrl;
   return note(sdk::launch_verify(p, elem, shape, static_cast<cudaStream_t>(stream))) ==
                  cudaSuccess

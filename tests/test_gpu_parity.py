@@ -70,10 +70,19 @@ def test_workspace_reuse_across_calls():
                            cfg={"threads": 256 if rep % 2 else 512, "blocks": 2 + rep})
         assert np.array_equal(again["accepted_len"], first["accepted_len"])
         assert np.array_equal(again["out_tokens"], first["out_tokens"])
-    # the counters at the end of the workspace are back at zero
-    nb = sd.sd_verify_workspace_bytes(w.bs, w.k_max)
-    cnt = ws[16 * (w.bs * (w.k_max + 1) + w.bs * w.k_max):nb]
-    assert int(cnt.count_nonzero()) == 0
+    # the counters in the workspace are back at zero: residual range sums,
+    # per-request arrivals, the residual-draw list, slice counts and the
+    # work counters (layout st_t | st_d | st_r | rs | req_cnt | res_list |
+    # slice_cnt | ctrl, each part 16-byte aligned)
+    rows_t, rows_d = w.bs * (w.k_max + 1), w.bs * w.k_max
+    ib = (4 * w.bs + 15) // 16 * 16
+    rs = 16 * rows_t + 16 * rows_d + 8 * 16 * rows_t
+    req_cnt = rs + 8 * 16 * w.bs
+    ctrl = req_cnt + 3 * ib
+    assert ctrl + 32 == sd.sd_verify_workspace_bytes(w.bs, w.k_max)
+    for off, size in ((rs, 8 * 16 * w.bs), (req_cnt, 4 * w.bs), (req_cnt + ib, 4 * w.bs),
+                      (req_cnt + 2 * ib, 4 * w.bs), (ctrl, 32)):
+        assert int(ws[off:off + size].count_nonzero()) == 0
 
 
 def test_varlen_draft_lengths_and_zero_drafts():
