@@ -34,7 +34,7 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 struct VerifyWs {
   sdk::RowStat* st_t;
   sdk::RowStat* st_d;
-  float2* st_r;
+  float2* st_c;
   unsigned long long* rs;
   int* req_cnt;
   int* res_list;
@@ -43,9 +43,9 @@ struct VerifyWs {
 };
 
 // Workspace layout (each part 16-byte aligned):
-// st_t | st_d | st_r | rs | req_cnt | res_list | slice_cnt | ctrl.
+// st_t | st_d | st_c | rs | req_cnt | res_list | slice_cnt | ctrl.
 struct WsLayout {
-  size_t st_t, st_d, st_r, rs, req_cnt, res_list, slice_cnt, ctrl, total;
+  size_t st_t, st_d, st_c, rs, req_cnt, res_list, slice_cnt, ctrl, total;
 };
 
 WsLayout ws_layout(int bs, int k_max) {
@@ -55,9 +55,9 @@ WsLayout ws_layout(int bs, int k_max) {
   WsLayout L;
   L.st_t = 0;
   L.st_d = L.st_t + 16 * rows_t;
-  L.st_r = L.st_d + 16 * rows_d;
-  L.rs = L.st_r + 8 * sdk::kMaxRanges * rows_t;
-  L.req_cnt = L.rs + 8 * sdk::kMaxRanges * static_cast<size_t>(bs);
+  L.st_c = L.st_d + 16 * rows_d;
+  L.rs = L.st_c + 8 * sdk::kStatStride * rows_t;
+  L.req_cnt = L.rs + 8 * sdk::kStatStride * static_cast<size_t>(bs);
   L.res_list = L.req_cnt + ib;
   L.slice_cnt = L.res_list + ib;
   L.ctrl = L.slice_cnt + ib;
@@ -73,7 +73,7 @@ VerifyWs carve(void* ws, int bs, int k_max) {
   VerifyWs w;
   w.st_t = reinterpret_cast<sdk::RowStat*>(b + L.st_t);
   w.st_d = reinterpret_cast<sdk::RowStat*>(b + L.st_d);
-  w.st_r = reinterpret_cast<float2*>(b + L.st_r);
+  w.st_c = reinterpret_cast<float2*>(b + L.st_c);
   w.rs = reinterpret_cast<unsigned long long*>(b + L.rs);
   w.req_cnt = reinterpret_cast<int*>(b + L.req_cnt);
   w.res_list = reinterpret_cast<int*>(b + L.res_list);
@@ -213,7 +213,7 @@ sd_status sd_verify_ex(const void* target_logits, const void* draft_logits, sd_d
   p.err = err_flag;
   p.st_t = w.st_t;
   p.st_d = w.st_d;
-  p.st_r = w.st_r;
+  p.st_c = w.st_c;
   p.rs = w.rs;
   p.req_cnt = w.req_cnt;
   p.res_list = w.res_list;

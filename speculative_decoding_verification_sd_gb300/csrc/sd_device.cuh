@@ -79,6 +79,12 @@ __device__ __forceinline__ uint64_t policy_evict_first() {
   return pol;
 }
 
+// Orders this thread's earlier generic-proxy accesses of shared memory
+// before later bulk (async-proxy) copies into it.
+__device__ __forceinline__ void fence_proxy_async() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 // Global -> this CTA's shared memory, completion counted in bytes on `bar`.
 // dst, src and bytes must be multiples of 16.
 __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes,

@@ -62,9 +62,9 @@ struct VerifyParams {
   int* err;
   RowStat* st_t;  // [bs*(k_max+1)]
   RowStat* st_d;  // [bs*k_max]
-  float2* st_r;   // [bs*(k_max+1)][kMaxRanges] per-range (max, scaled sum) of target rows
-  unsigned long long* rs;  // [bs][kMaxRanges] residual range sums (2^56 fixed point) of
-                           //   the listed residual draws; zero between calls
+  float2* st_c;   // [bs*(k_max+1)][kStatStride] per-chunk (max, scaled sum) of target rows
+  unsigned long long* rs;  // [bs][kStatStride] per-chunk residual sums (2^56 fixed point)
+                           //   of the listed residual draws; zero between calls
   int* req_cnt;   // [bs]   rows finished per request; zero between calls
   int* res_list;  // [bs]   listed residual draws, 1 + (request << 4 | slot); zero between calls
   int* slice_cnt; // [bs]   slices finished per listed residual draw; zero between calls
@@ -73,10 +73,10 @@ struct VerifyParams {
                   //        zero between calls
 };
 
-// Softmax statistics are kept per warp range of a row (one range per warp of
-// the CTA); a final draw is cut into at most kMaxDrawChunks chunks.
-constexpr int kMaxRanges = 16;
-constexpr int kMaxDrawChunks = 256;
+// Statistics chunks: a row is cut into at most kStatStride chunks whose
+// softmax statistics (target rows) or residual sums (listed draws) are kept,
+// so a final draw reads back one chunk instead of its row.
+constexpr int kStatStride = 128;
 
 struct VerifyShape {
   int threads, blocks;

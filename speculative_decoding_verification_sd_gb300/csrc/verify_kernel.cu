@@ -9,19 +9,25 @@
 //            accepted prefix draw a bonus token from p of the next row.
 //   tau = 0: accept iff x_j == argmax p_j; the correction/bonus is the argmax.
 //
-// Design (GB300): the work is a list of rows -- every compacted target row,
-// and the draft row of every verified slot of a sampling request -- handed
-// out to persistent CTAs by an atomic counter.  A CTA streams one whole row
-// from HBM with 16-byte loads and reduces it to its statistics (running max
-// and scaled sum at the request's temperature, or the argmax when greedy,
-// plus the logit at the draft token), which it stores in the workspace.  The
-// CTA that completes the last row of a request (a per-request arrival count)
-// takes the request's accept decisions from those statistics and, for a
-// sampling request, re-reads the one row pair that ends the accepted prefix
-// -- from L2, where it was streamed moments before -- to draw the residual or
-// bonus token by inverse CDF; it writes the request's outputs directly.
-// Sampling requests' rows are scheduled before greedy ones so the final draws
-// overlap the remaining streaming.  No CTA ever waits on another.
+// Design (GB300): one persistent CTA per SM, warp-specialised.  The work is
+// a list of rows -- every compacted target row, and the draft row of every
+// verified slot of a sampling request -- plus the residual draws, which are
+// listed as requests are decided.  In each CTA, NT/32 - 1 streaming warps
+// each own a contiguous range of every row and stream it from HBM through a
+// private ring of bulk copies (mbarrier completion) into shared memory,
+// reducing it to softmax statistics at the request's temperature (kept per
+// chunk for target rows) or to the argmax, plus the logit at the draft
+// token.  They never wait for one another.  The control warp hands out the
+// queue (a row from a global counter, or a slice of a listed residual draw),
+// folds each unit once every streaming warp has arrived on the unit's
+// barrier, stores the row statistics and counts the row for its request;
+// the CTA that counts a request's last row takes its accept decisions and
+// draws its final token: the argmax, a bonus token from p (the chunk
+// statistics locate the crossing chunk, which alone is read again), or --
+// after a rejection -- lists a residual draw, whose row pair is streamed
+// again in slices by whichever CTAs claim them; the CTA that folds the last
+// slice finishes the inverse CDF.  Inverse-CDF sums are exact 64-bit fixed
+// point, so the crossing chunk does not depend on summation order.
 #include <algorithm>
 #include <atomic>
 #include <climits>
@@ -83,22 +89,9 @@ __device__ __forceinline__ Raw ld_stream(const Raw* p) {
   return __ldg(p);
 }
 
-template <>
-__device__ __forceinline__ uint4 ld_stream<uint4>(const uint4* p) {
-  uint4 r;
-  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
-               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
-               : "l"(p));
-  return r;
-}
-
-template <>
-__device__ __forceinline__ float4 ld_stream<float4>(const float4* p) {
-  float4 r;
-  asm volatile("ld.global.nc.L1::no_allocate.v4.f32 {%0, %1, %2, %3}, [%4];"
-               : "=f"(r.x), "=f"(r.y), "=f"(r.z), "=f"(r.w)
-               : "l"(p));
-  return r;
+template <typename Raw>
+__device__ __forceinline__ void prefetch_l1(const Raw* p) {
+  asm volatile("prefetch.global.L1 [%0];" ::"l"(p));
 }
 
 __device__ __forceinline__ float from_ordered(uint32_t u) {
@@ -157,14 +150,6 @@ __device__ __forceinline__ float fmax_nan(float a, float b) {
 }
 __device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
-
-// Counter increment that publishes this thread's earlier writes (release)
-// and sees everything published before earlier increments (acquire).
-__device__ __forceinline__ int atom_add_acq_rel(int* p, int v) {
-  int old;
-  asm volatile("atom.add.acq_rel.gpu.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
-  return old;
-}
 
 __device__ __forceinline__ void st_release(int* p, int v) {
   asm volatile("st.release.gpu.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
@@ -308,17 +293,9 @@ struct ChunkOps<float> {  // 4 fp32 per 16-byte vector
   }
 };
 
-constexpr int kUnroll = 8;          // element path: loads in flight per thread
-constexpr int kChunkBytes = 4096;       // vector path: one bulk copy
-constexpr int kSlots = 3;               // ring slots per warp
+constexpr int kUnroll = 8;                 // element path: loads in flight per lane
+constexpr int kSlots = 3;                  // ring slots per streaming warp
 constexpr uint32_t kSpinLimit = 1u << 22;  // polls (~100 ns apart) before a wait gives up
-// Queue entries past the rows: slice s of listed residual draw e, the draw
-// of request i at slot a, as kResBase | e << 18 | s << 16 | i << 4 | a
-// (e, i < 4096, s < 4, a < 16), and three tokens.
-constexpr int kResBase = 1 << 30;
-constexpr int kNoop = INT_MAX - 2;
-constexpr int kPoll = INT_MAX - 1;
-constexpr int kEnd = INT_MAX;
 constexpr float kLn2 = 0.693147180559945309f;
 // log2(e) split into two floats (hi + lo) for a double-float exponent.
 constexpr float kLog2eHi = 1.44269502162933349609375f;
@@ -361,48 +338,1134 @@ __device__ __forceinline__ void two_diff(float l, float M, float& hi, float& lo)
   lo = __fadd_rn(__fsub_rn(l, __fsub_rn(hi, bb)), __fsub_rn(-M, bb));
 }
 
-template <typename T, int NT, bool VEC>
-__global__ void __launch_bounds__(NT, NT <= 256 ? 2 : 1) verify_kernel(const VerifyParams p) {
+// ---------------------------------------------------------------------------
+// Layout of one row for a launch with NS streaming warps.  The row's units
+// (16-byte vectors, or elements on the element path) are cut into nch
+// chunks of CU units; streaming warp w owns chunks [w * cpw, (w + 1) * cpw).
+// On the vector path a chunk is one bulk copy of at most kSlotBytes.  The
+// statistics chunks group g consecutive chunks of one warp (spw per warp,
+// NS * spw <= kStatStride).  A residual draw is streamed in S_sl slices:
+// slice s takes chunks [s * m_sl, (s + 1) * m_sl) of every warp's range.
+struct Geom {
+  int nvec, cpw, CU, nch, g, spw, S_sl, m_sl;
+};
+
+constexpr int kSlotBytes = 4352;  // largest chunk of the vector path (272 vectors)
+
+__device__ __forceinline__ Geom make_geom(int nvec, bool vec, int ns) {
+  Geom G;
+  G.nvec = nvec;
+  if (vec) {
+    constexpr int kMaxVec = kSlotBytes / 16;
+    G.cpw = max(1, (nvec + ns * kMaxVec - 1) / (ns * kMaxVec));
+    G.CU = (nvec + ns * G.cpw - 1) / (ns * G.cpw);
+  } else {
+    G.cpw = 4;
+    G.CU = 32 * ((nvec + ns * G.cpw * 32 - 1) / (ns * G.cpw * 32));
+  }
+  G.nch = (nvec + G.CU - 1) / G.CU;
+  const int spw_max = kStatStride / ns;
+  G.g = (G.cpw + spw_max - 1) / spw_max;
+  G.spw = (G.cpw + G.g - 1) / G.g;
+  G.S_sl = min(4, G.cpw);
+  G.m_sl = (G.cpw + G.S_sl - 1) / G.S_sl;
+  return G;
+}
+
+// Units [ub, ue) of statistics chunk sc (empty when past the row's end).
+__device__ __forceinline__ void stat_units(const Geom& G, int sc, int& ub, int& ue) {
+  const int w = sc / G.spw, j = sc - w * G.spw;
+  const int c0 = min(G.nch, w * G.cpw + j * G.g);
+  const int c1 = min(G.nch, min(w * G.cpw + (j + 1) * G.g, (w + 1) * G.cpw));
+  ub = min(G.nvec, c0 * G.CU);
+  ue = min(G.nvec, c1 * G.CU);
+  if (c1 <= c0) ue = ub;
+}
+
+// Release / acquire on a shared-memory word between the warps of a CTA.
+__device__ __forceinline__ void st_release_cta(int* p, int v) {
+  asm volatile("st.release.cta.shared::cta.s32 [%0], %1;" ::"r"(smem_addr(p)), "r"(v) : "memory");
+}
+// Relaxed shared-memory read for polling; the poll ends with an acquire.
+__device__ __forceinline__ int ld_volatile_cta(const int* p) {
+  return *reinterpret_cast<const volatile int*>(p);
+}
+
+__device__ __forceinline__ int ld_acquire_cta(const int* p) {
+  int v;
+  asm volatile("ld.acquire.cta.shared::cta.s32 %0, [%1];" : "=r"(v) : "r"(smem_addr(p)) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
+// Per-CTA state shared by the warps: request tables in shared memory and
+// the unit queue.  Position k of the queue is published in q[k % kDepth]
+// once pub >= k; the control warp keeps at most kWindow positions published
+// ahead of the last one it has folded.
+constexpr int kDepth = 4;
+constexpr int kWindow = 3;
+
+struct Cta {
+  const int* cu;     // [bs+1] cu_seqlens
+  const float* tau;  // [bs] temperatures (invalid ones as 0)
+  const int* order;  // [bs] request order of the work list
+  const int* ustart; // [bs+1] first row unit of order[k]
+  int* q;            // [kDepth] queue
+  int* pub;          // last published position
+  int nsamp;         // sampling requests
+  int U_rows;        // row units
+};
+
+// Row unit u -> (request, slot, kind, row index).
+struct Unit {
+  int i, j, n, c0;
+  bool draft, greedy;
+  size_t row;
+};
+
+__device__ __forceinline__ Unit locate(const Cta& C, int bs, int u) {
+  int lo = 0, hi = bs;  // ustart[lo] <= u < ustart[hi]
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (C.ustart[mid] <= u) lo = mid;
+    else hi = mid;
+  }
+  Unit t;
+  t.i = C.order[lo];
+  const int r = u - C.ustart[lo];
+  t.c0 = C.cu[t.i];
+  t.n = C.cu[t.i + 1] - t.c0 - 1;
+  t.greedy = !(C.tau[t.i] > 0.0f);
+  t.draft = r > t.n;
+  t.j = t.draft ? r - (t.n + 1) : r;
+  t.row = t.draft ? static_cast<size_t>(t.c0 - t.i + t.j) : static_cast<size_t>(t.c0 + t.j);
+  return t;
+}
+
+// Queue entries past the rows: slice s of listed residual draw e, the draw
+// of request i at slot a, as kResBase | e << 18 | s << 16 | i << 4 | a
+// (e, i < 4096, s < 4, a < 16); kEnd closes the queue.
+constexpr int kResBase = 1 << 30;
+constexpr int kEnd = INT_MAX;
+constexpr int kWait = INT_MAX - 1;  // scheduler: nothing to hand out yet
+__device__ __forceinline__ bool is_slice(int u) { return u >= kResBase && u < kWait; }
+
+// ---------------------------------------------------------------------------
+// Weight functions of the final draws.  A draw from p (target row rt, max
+// Mt, scale s2 = log2(e)/tau, also as the double-float s2h + s2l) weighs an
+// element 2^((l - Mt) s2) <= 1 (2^40 fixed point); a residual draw adds the
+// draft row rd (max Md) and both 1/Z and weighs max(p - q, 0) <= 1 (2^56).
+// fast_*: the fp32 sum over one unit, for chunk sums; precise_*: each
+// element with a double-float exponent, for the walk of the crossing chunk.
+template <typename Raw>
+struct DrawRows {
+  const Raw* rt;  // unit u at rt[u - off] (off > 0: a staged copy in shared memory)
+  const Raw* rd;
+  float Mt, Md, iZt, iZd, s2, s2h, s2l;
+  int off;
+};
+
+template <typename T, bool VEC>
+__device__ __forceinline__ DrawRows<typename VT<T, VEC>::Raw> make_rows(
+    const VerifyParams& p, const int* cu, int i, int a, float tau, const float4& ts,
+    const float4& ds, bool resid) {
+  using Raw = typename VT<T, VEC>::Raw;
+  DrawRows<Raw> w;
+  const int c0 = cu[i];
+  w.rt = reinterpret_cast<const Raw*>(static_cast<const T*>(p.target) +
+                                      static_cast<size_t>(c0 + a) * p.V);
+  w.rd = resid ? reinterpret_cast<const Raw*>(static_cast<const T*>(p.draft) +
+                                              static_cast<size_t>(c0 - i + a) * p.V)
+               : w.rt;
+  w.Mt = ts.x;
+  w.Md = ds.x;
+  w.iZt = 1.0f / ts.y;
+  w.iZd = 1.0f / ds.y;
+  w.s2 = kLog2e / tau;
+  w.s2h = kLog2eHi / tau;
+  w.s2l = (fmaf(-w.s2h, tau, kLog2eHi) + kLog2eLo) / tau;
+  w.off = 0;
+  return w;
+}
+
+template <typename T, bool VEC>
+__device__ __forceinline__ float fast_res(const DrawRows<typename VT<T, VEC>::Raw>& w,
+                                          const typename VT<T, VEC>::Raw& ra,
+                                          const typename VT<T, VEC>::Raw& rb) {
+  using Tr = VT<T, VEC>;
+  float f[Tr::VE], g[Tr::VE];
+  Tr::unpack(ra, f);
+  Tr::unpack(rb, g);
+  const float bt = w.Mt * w.s2, bd = w.Md * w.s2;
+  float ws = 0.0f;
+#pragma unroll
+  for (int e = 0; e < Tr::VE; ++e) {
+    const float et = exp2_ftz(fmaf(f[e], w.s2, -bt));
+    const float ed = exp2_ftz(fmaf(g[e], w.s2, -bd));
+    ws += fmaxf(fmaf(et, w.iZt, -__fmul_rn(ed, w.iZd)), 0.0f);
+  }
+  return ws;
+}
+
+template <typename T, bool VEC>
+__device__ __forceinline__ void precise_p(const DrawRows<typename VT<T, VEC>::Raw>& w, int u,
+                                          unsigned long long (&wi)[VT<T, VEC>::VE]) {
+  using Tr = VT<T, VEC>;
+  float f[Tr::VE];
+  Tr::unpack(w.rt[u - w.off], f);
+#pragma unroll
+  for (int e = 0; e < Tr::VE; ++e) {
+    float h, l;
+    two_diff(f[e], w.Mt, h, l);
+    wi[e] = __float2ull_rn(__fmul_rn(exp2_df(h, l, w.s2h, w.s2l), kTwo40));
+  }
+}
+
+template <typename T, bool VEC>
+__device__ __forceinline__ void precise_res(const DrawRows<typename VT<T, VEC>::Raw>& w, int u,
+                                            unsigned long long (&wi)[VT<T, VEC>::VE]) {
+  using Tr = VT<T, VEC>;
+  float f[Tr::VE], g[Tr::VE];
+  Tr::unpack(w.rt[u - w.off], f);
+  Tr::unpack(w.rd[u - w.off], g);
+#pragma unroll
+  for (int e = 0; e < Tr::VE; ++e) {
+    float h, l;
+    two_diff(f[e], w.Mt, h, l);
+    const float et = exp2_df(h, l, w.s2h, w.s2l);
+    two_diff(g[e], w.Md, h, l);
+    const float ed = exp2_df(h, l, w.s2h, w.s2l);
+    const float x = fmaxf(__fmaf_rn(et, w.iZt, -__fmul_rn(ed, w.iZd)), 0.0f);
+    wi[e] = __float2ull_rn(__fmul_rn(x, kTwo56));
+  }
+}
+
+// ---------------------------------------------------------------------------
+// A streaming warp: walks the queue, streams its chunk range of every unit
+// (through its ring of bulk copies on the vector path), leaves the unit's
+// partial results in shared memory and arrives on the unit's barrier.
+// Streaming warps never wait for one another.
+template <typename T, bool VEC, int NS>
+struct Streamer {
   using Tr = VT<T, VEC>;
   using Raw = typename Tr::Raw;
-  constexpr int VE = Tr::VE;
+  static constexpr int VE = Tr::VE;
+
+  const VerifyParams& p;
+  const Cta& C;
+  const Geom& G;
+  const int w, lane;
+  unsigned char* ring;      // this warp's kSlots slots
+  uint64_t* bar;            // this warp's kSlots barriers
+  const int cb, ce;         // this warp's chunks
+  uint32_t cseq = 0, iseq = 0;   // ring entries consumed / issued
+  int fk = 0, fe = 0, f_n = 0, f_c0 = 0, fk_cached = -1;
+  bool f_two = false;
+  const char* f_base = nullptr;
+  const char* f_base2 = nullptr;
+
+  __device__ Streamer(const VerifyParams& p_, const Cta& C_, const Geom& G_, int w_, int lane_,
+                      unsigned char* ring_all, uint64_t* bar_all)
+      : p(p_), C(C_), G(G_), w(w_), lane(lane_),
+        ring(ring_all + static_cast<size_t>(w_) * kSlots * kSlotBytes),
+        bar(bar_all + w_ * kSlots),
+        cb(min(G_.nch, w_ * G_.cpw)), ce(min(G_.nch, w_ * G_.cpw + G_.cpw)) {}
+
+  __device__ size_t row_bytes() const { return static_cast<size_t>(G.nvec) * 16; }
+
+  // Issues ring entries up to kSlots ahead of consumption, across published
+  // positions.  A row position takes one entry per chunk of [cb, ce); a
+  // slice takes two (target chunk, then draft chunk) per chunk of its part.
+  __device__ void refill() {
+    while (iseq - cseq < static_cast<uint32_t>(kSlots)) {
+      if (fk_cached != fk) {
+        if (fk > ld_acquire_cta(C.pub)) break;
+        const int u = C.q[fk % kDepth];
+        if (u == kEnd) break;
+        f_two = false;
+        f_n = 0;
+        if (u < C.U_rows) {
+          const Unit t = locate(C, p.bs, u);
+          f_base = reinterpret_cast<const char*>(t.draft ? p.draft : p.target) + t.row * row_bytes();
+          f_c0 = cb;
+          f_n = ce - cb;
+        } else if (is_slice(u)) {
+          const int i = (u >> 4) & 0xFFF, a = u & 15, s = (u >> 16) & 3;
+          const int c0 = C.cu[i];
+          f_base = reinterpret_cast<const char*>(p.target) + static_cast<size_t>(c0 + a) * row_bytes();
+          f_base2 = reinterpret_cast<const char*>(p.draft) + static_cast<size_t>(c0 - i + a) * row_bytes();
+          f_c0 = min(ce, cb + s * G.m_sl);
+          f_n = 2 * (min(ce, f_c0 + G.m_sl) - f_c0);
+          f_two = true;
+        }
+        fk_cached = fk;
+        fe = 0;
+      }
+      if (fe >= f_n) {
+        ++fk;
+        continue;
+      }
+      const int c = f_c0 + (f_two ? fe >> 1 : fe);
+      const char* base = (f_two && (fe & 1)) ? f_base2 : f_base;
+      const int slot = static_cast<int>(iseq % kSlots);
+      const size_t off = static_cast<size_t>(c) * G.CU * 16;
+      const uint32_t bytes = static_cast<uint32_t>(min(static_cast<size_t>(G.CU) * 16, row_bytes() - off));
+      if (lane == 0) {
+        mbar_arrive_expect_tx(&bar[slot], bytes);
+        bulk_load_nohint(ring + slot * kSlotBytes, base + off, bytes, &bar[slot]);
+      }
+      ++iseq;
+      ++fe;
+    }
+  }
+
+  // Waits for ring entry `seq`; returns its data.
+  __device__ const Raw* entry(uint32_t seq, int* err) {
+    const int slot = static_cast<int>(seq % kSlots);
+    if (!mbar_wait_bounded(&bar[slot], (seq / kSlots) & 1, 1u << 24)) raise_error(err, SD_DEV_ERR_TIMEOUT);
+    return reinterpret_cast<const Raw*>(ring + slot * kSlotBytes);
+  }
+
+  // Statistics chunk of chunk c of this warp.
+  __device__ int stat_of(int c) const { return w * G.spw + (c - w * G.cpw) / G.g; }
+  __device__ bool stat_ends(int c) const {
+    return c + 1 == ce || (c + 1 - w * G.cpw) % G.g == 0;
+  }
+
+  // Running (max, scaled sum) at scale s2 with one more (mc, zc) folded in.
+  __device__ static void combine(float& M, float& Z, float mc, float zc, float s2) {
+    if (mc == -INFINITY) return;
+    if (M == -INFINITY) {
+      M = mc;
+      Z = zc;
+    } else if (mc > M) {
+      Z = fmaf(Z, exp2_ftz((M - mc) * s2), zc);
+      M = mc;
+    } else {
+      Z = fmaf(zc, exp2_ftz((mc - M) * s2), Z);
+    }
+  }
+
+  // The warp's (max, scaled sum) of one chunk from the lanes' values.
+  __device__ static void chunk_reduce(float m, float z, float s2, float& mc, float& zc) {
+    mc = warp_max(m);
+    zc = warp_sum((m == -INFINITY || mc == -INFINITY) ? 0.0f : z * exp2_ftz((m - mc) * s2));
+  }
+
+  __device__ static float element_of(const Raw* d, int idx) {
+    if constexpr (sizeof(T) == 2)
+      return __uint_as_float(static_cast<uint32_t>(reinterpret_cast<const uint16_t*>(d)[idx]) << 16);
+    else
+      return reinterpret_cast<const float*>(d)[idx];
+  }
+
+  // Row unit u at queue position k: softmax statistics at the request's
+  // temperature (per chunk, kept for target rows of sampling requests) or
+  // the argmax, and the logit at the slot's draft token.
+  __device__ void row(int k, int u, float (*red_m)[NS], float (*red_z)[NS],
+                      unsigned long long (*red_k)[NS], int (*red_n)[NS], float* s_lx,
+                      unsigned long long* sbuf) {
+    const Unit t = locate(C, p.bs, u);
+    const int x = t.j < t.n ? p.draft_ids[t.c0 - t.i + t.j] : -1;
+    const bool x_ok = x >= 0 && x < p.V;
+    const float tau = C.tau[t.i];
+    const float s2 = t.greedy ? 0.0f : kLog2e / tau;
+    const bool keep = !t.greedy && !t.draft;
+    const Raw* rowp = reinterpret_cast<const Raw*>(
+        reinterpret_cast<const char*>(t.draft ? p.draft : p.target) + t.row * (static_cast<size_t>(p.V) * sizeof(T)));
+    float best = -INFINITY;  // greedy
+    int bv = -1, nanf = 0, bidx = INT_MAX;
+    Raw bvec{};
+    float Mw = -INFINITY, Zw = 0.0f, Ms = -INFINITY, Zs = 0.0f;  // sampling: range, stat chunk
+    for (int c = cb; c < ce; ++c) {
+      const int u0 = c * G.CU, nv = min(G.CU, G.nvec - u0);
+      float mc = -INFINITY, zc = 0.0f;
+      if constexpr (VEC) {
+        const Raw* d = entry(cseq, p.err);
+        if (x_ok && lane == 0 && x / VE >= u0 && x / VE < u0 + nv) s_lx[k % kDepth] = element_of(d, x - u0 * VE);
+        constexpr int VPL = (kSlotBytes / 16 + 31) / 32;  // vectors per lane and chunk
+        Raw rv[VPL];
+#pragma unroll
+        for (int q = 0; q < VPL; ++q) rv[q] = lane + 32 * q < nv ? d[lane + 32 * q] : ChunkOps<T>::neg_inf();
+        if (t.greedy) {
+          ChunkOps<T>::argmax(rv, u0 + lane, best, bvec, bv, nanf);
+        } else {
+          float m = -INFINITY, nb = 0.0f;
+          float2 z2 = make_float2(0.0f, 0.0f);
+          ChunkOps<T>::softmax(rv, s2, m, z2, nb);
+          chunk_reduce(m, z2.x + z2.y, s2, mc, zc);
+        }
+        __syncwarp();
+        ++cseq;
+        refill();
+      } else {
+        float m = -INFINITY, z = 0.0f, b = 0.0f;
+        for (int v0 = u0 + lane; v0 < u0 + nv; v0 += 32 * kUnroll) {
+          Raw rv[kUnroll];
+#pragma unroll
+          for (int q = 0; q < kUnroll; ++q)
+            if (v0 + 32 * q < u0 + nv) rv[q] = ld_stream(rowp + v0 + 32 * q);
+#pragma unroll
+          for (int q = 0; q < kUnroll; ++q) {
+            const int v = v0 + 32 * q;
+            if (v < u0 + nv) {
+              float f[VE];
+              Tr::unpack(rv[q], f);
+              if (v == x) s_lx[k % kDepth] = f[0];
+              if (t.greedy) {
+                nanf |= (f[0] != f[0]);
+                if (f[0] > best) { best = f[0]; bidx = v; }
+              } else {
+                online_add<VE>(f, s2, m, z, b);
+              }
+            }
+          }
+        }
+        if (!t.greedy) chunk_reduce(m, z, s2, mc, zc);
+      }
+      if (!t.greedy) {
+        combine(Ms, Zs, mc, zc, s2);
+        combine(Mw, Zw, mc, zc, s2);
+        if (stat_ends(c)) {
+          if (keep && lane == 0)
+            sbuf[stat_of(c)] = static_cast<unsigned long long>(__float_as_uint(Ms)) |
+                               (static_cast<unsigned long long>(__float_as_uint(Zs)) << 32);
+          Ms = -INFINITY;
+          Zs = 0.0f;
+        }
+      }
+    }
+    if (t.greedy) {
+      if constexpr (VEC) bidx = bv >= 0 ? ChunkOps<T>::first_of(bvec, bv, best) : INT_MAX;
+      unsigned long long key = bidx == INT_MAX ? 0ull
+          : (static_cast<unsigned long long>(ordered_bits(best)) << 32) |
+                static_cast<unsigned long long>(0xFFFFFFFFu - static_cast<uint32_t>(bidx));
+      key = warp_max_u64(key);
+      nanf = __any_sync(kFull, nanf);
+      if (lane == 0) {
+        red_k[k % kDepth][w] = key;
+        red_n[k % kDepth][w] = nanf;
+      }
+    } else if (lane == 0) {
+      red_m[k % kDepth][w] = Mw;
+      red_z[k % kDepth][w] = Zw;
+    }
+  }
+
+  // Slice unit u: this warp's part of a listed residual draw, summed per
+  // statistics chunk in 2^56 fixed point into the draw's chunk sums.
+  __device__ void slice(int u, unsigned long long* sbuf) {
+    const int e = (u >> 18) & 0xFFF, s = (u >> 16) & 3, i = (u >> 4) & 0xFFF, a = u & 15;
+    const int c0 = C.cu[i];
+    const float4 ts = __ldcg(reinterpret_cast<const float4*>(p.st_t + c0 + a));
+    const float4 ds = __ldcg(reinterpret_cast<const float4*>(p.st_d + c0 - i + a));
+    const DrawRows<Raw> wr = make_rows<T, VEC>(p, C.cu, i, a, C.tau[i], ts, ds, true);
+    if (lane == 0)
+      for (int j = 0; j < G.spw; ++j) sbuf[w * G.spw + j] = 0;  // chunks this slice misses
+    const int c_lo = min(ce, cb + s * G.m_sl), c_hi = min(ce, c_lo + G.m_sl);
+    unsigned long long acc = 0;
+    for (int c = c_lo; c < c_hi; ++c) {
+      const int u0 = c * G.CU, nv = min(G.CU, G.nvec - u0);
+      if constexpr (VEC) {
+        const Raw* dt = entry(cseq, p.err);
+        const Raw* dd = entry(cseq + 1, p.err);
+        constexpr int VPL = (kSlotBytes / 16 + 31) / 32;
+#pragma unroll 2
+        for (int q = 0; q < VPL; ++q) {
+          const int v = lane + 32 * q;
+          if (v < nv) acc += __float2ull_rn(__fmul_rn(fast_res<T, VEC>(wr, dt[v], dd[v]), kTwo56));
+        }
+        __syncwarp();
+        cseq += 2;
+        refill();
+      } else {
+        for (int v0 = u0 + lane; v0 < u0 + nv; v0 += 32 * kUnroll) {
+          Raw at[kUnroll], ad[kUnroll];
+#pragma unroll
+          for (int q = 0; q < kUnroll; ++q)
+            if (v0 + 32 * q < u0 + nv) {
+              at[q] = ld_stream(wr.rt + v0 + 32 * q);
+              ad[q] = ld_stream(wr.rd + v0 + 32 * q);
+            }
+#pragma unroll
+          for (int q = 0; q < kUnroll; ++q)
+            if (v0 + 32 * q < u0 + nv)
+              acc += __float2ull_rn(__fmul_rn(fast_res<T, VEC>(wr, at[q], ad[q]), kTwo56));
+        }
+      }
+      if (stat_ends(c) || c + 1 == c_hi) {
+        const unsigned long long sum = warp_sum_u64(acc);
+        if (lane == 0) sbuf[stat_of(c)] = sum;
+        acc = 0;
+      }
+    }
+  }
+
+  __device__ void run(uint64_t* pbar, float (*red_m)[NS], float (*red_z)[NS],
+                      unsigned long long (*red_k)[NS], int (*red_n)[NS], float* s_lx,
+                      unsigned long long (*s_stat)[kStatStride]) {
+    for (int k = 0;; ++k) {
+      bool ok = false;
+      for (uint32_t it = 0; it < kSpinLimit; ++it) {
+        if (ld_volatile_cta(C.pub) >= k) {
+          ok = ld_acquire_cta(C.pub) >= k;
+          break;
+        }
+        __nanosleep(64);
+      }
+      ok = __all_sync(kFull, ok);  // the same verdict in every lane
+      if (!ok) {
+        if (lane == 0) raise_error(p.err, SD_DEV_ERR_TIMEOUT);
+        break;
+      }
+      const int u = C.q[k % kDepth];
+      if (u == kEnd) break;
+      if constexpr (VEC) refill();
+      if (u < C.U_rows) row(k, u, red_m, red_z, red_k, red_n, s_lx, s_stat[k % kDepth]);
+      else if (is_slice(u)) slice(u, s_stat[k % kDepth]);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&pbar[k % kDepth]);
+    }
+    // entries issued but never consumed exist only after a time-out
+    if constexpr (VEC) {
+      while (cseq != iseq) {
+        entry(cseq, p.err);
+        ++cseq;
+      }
+    }
+  }
+};
+
+// ---------------------------------------------------------------------------
+// The control warp: hands out the queue, folds each finished unit, runs the
+// tail of every request whose last row it folds, and finishes every
+// residual draw whose last slice it folds.  Scheduling is lane 0's; folds,
+// tails and draws use the whole warp.
+template <typename T, bool VEC, int NS>
+struct Control {
+  using Tr = VT<T, VEC>;
+  using Raw = typename Tr::Raw;
+  static constexpr int VE = Tr::VE;
+  static constexpr int kCpl = (kStatStride + 31) / 32;  // statistics chunks per lane
+  static constexpr int kWalk = 12;                       // units per lane in one walk round
+  static constexpr int kJobs = 64;                       // job ring capacity
+
+  const VerifyParams& p;
+  const Cta& C;
+  const Geom& G;
+  const int lane;
+  uint64_t* pbar;
+  float (*red_m)[NS];
+  float (*red_z)[NS];
+  unsigned long long (*red_k)[NS];
+  int (*red_n)[NS];
+  float* s_lx;
+  unsigned long long* s_walk;  // [32][kWalk] unit sums of the walk in hand (per draw warp)
+  int* jobs;                   // [kJobs] job ring
+  int* jtail;                  // jobs appended
+  int* jhead;                  // jobs taken
+  int* jdone;                  // jobs read
+  unsigned long long (*s_stat)[kStatStride];  // per-chunk results of the units in flight
+  unsigned char* cbuf;         // [2][kSlotBytes] staged chunk of the walk in hand (draw warps)
+  uint64_t* cbar;              // its barrier
+  mutable uint32_t cphase = 0;
+  // lane 0's scheduler state: rows ran out; the next row id, fetched one
+  // schedule ahead; a slice slot taken before its draw was listed
+  bool rows_done = false;
+  int stash = 0, held = -1;
+
+  __device__ Control(const VerifyParams& p_, const Cta& C_, const Geom& G_, int lane_,
+                     uint64_t* pbar_, float (*rm)[NS], float (*rz)[NS],
+                     unsigned long long (*rk)[NS], int (*rn)[NS], float* lx,
+                     unsigned long long* walk_buf, int* jobs_, int* jtail_, int* jhead_,
+                     int* jdone_, unsigned long long (*stat_)[kStatStride], unsigned char* cbuf_,
+                     uint64_t* cbar_)
+      : p(p_), C(C_), G(G_), lane(lane_), pbar(pbar_), red_m(rm), red_z(rz), red_k(rk),
+        red_n(rn), s_lx(lx), s_walk(walk_buf), jobs(jobs_), jtail(jtail_), jhead(jhead_),
+        jdone(jdone_), s_stat(stat_), cbuf(cbuf_), cbar(cbar_) {}
+
+  // Copies units [ub, ue) of the draw's row (and draft row) into this warp's
+  // buffer with bulk copies (vector path, one chunk at most) and points w at
+  // the copy; false when the range does not qualify.
+  __device__ bool stage(DrawRows<Raw>& w, bool two, int ub, int ue) const {
+    if constexpr (!VEC) {
+      return false;
+    } else {
+      const uint32_t bytes = static_cast<uint32_t>(ue - ub) * 16u;
+      if (ue <= ub || bytes > static_cast<uint32_t>(kSlotBytes)) return false;
+      if (lane == 0) {
+        fence_proxy_async();  // earlier reads of the buffer before the copies
+        mbar_arrive_expect_tx(cbar, two ? 2 * bytes : bytes);
+        bulk_load_nohint(cbuf, w.rt + ub, bytes, cbar);
+        if (two) bulk_load_nohint(cbuf + kSlotBytes, w.rd + ub, bytes, cbar);
+      }
+      if (!mbar_wait_bounded(cbar, cphase & 1, 1u << 24) && lane == 0)
+        raise_error(p.err, SD_DEV_ERR_TIMEOUT);
+      ++cphase;
+      w.rt = reinterpret_cast<const Raw*>(cbuf);
+      w.rd = two ? reinterpret_cast<const Raw*>(cbuf + kSlotBytes) : w.rt;
+      w.off = ub;
+      return true;
+    }
+  }
+
+  // ---- scheduling (lane 0) ------------------------------------------------
+  // ctrl[0] rows handed out, ctrl[2] draws listed, ctrl[3] slice slots
+  // taken, ctrl[4] sampling requests decided.  Slot h is slice h % S_sl of
+  // the (h / S_sl)-th listed draw.
+  __device__ unsigned long long load_lc() const {
+    return ld_relaxed_u64(reinterpret_cast<const unsigned long long*>(p.ctrl + 2));
+  }
+  __device__ bool decided() const { return ld_acquire(&p.ctrl[4]) >= C.nsamp; }
+  __device__ int slot_unit(int h) const {
+    const int e = h / G.S_sl, s = h - e * G.S_sl;
+    int v = 0;  // the draw is listed; its publisher may still be storing the entry
+    for (uint32_t it = 0; it < kSpinLimit; ++it) {
+      v = *reinterpret_cast<const volatile int*>(&p.res_list[e]);
+      if (v != 0) {
+        v = ld_acquire(&p.res_list[e]);
+        break;
+      }
+      __nanosleep(32);
+    }
+    if (v == 0) {
+      raise_error(p.err, SD_DEV_ERR_TIMEOUT);
+      return kWait;
+    }
+    return kResBase | (e << 18) | (s << 16) | (v - 1);
+  }
+  // Next unit for this CTA: a listed slice first, else a row; kEnd once
+  // nothing is left anywhere; kWait when a draw may still be listed.
+  __device__ int schedule() {
+    const unsigned long long lc = load_lc();
+    const int avail = static_cast<int>(lc & 0xFFFFFFFFull) * G.S_sl;
+    if (held < 0 && static_cast<int>(lc >> 32) < avail) held = atomicAdd(&p.ctrl[3], 1);
+    if (held >= 0 && held < avail) {
+      const int h = held;
+      held = -1;
+      return slot_unit(h);
+    }
+    if (!rows_done) {
+      const int u = stash;
+      if (u < C.U_rows) {
+        stash = atomicAdd(&p.ctrl[0], 1);  // used by the next schedule
+        return u;
+      }
+      rows_done = true;
+    }
+    if (!decided()) return kWait;
+    const unsigned long long f = load_lc();  // the final list
+    const int fin = static_cast<int>(f & 0xFFFFFFFFull) * G.S_sl;
+    if (held < 0) {
+      if (static_cast<int>(f >> 32) >= fin) return kEnd;
+      held = atomicAdd(&p.ctrl[3], 1);
+    }
+    const int h = held;
+    held = -1;
+    return h < fin ? slot_unit(h) : kEnd;  // a slot past the final list is void
+  }
+
+  // ---- warp-wide draw helpers ---------------------------------------------
+  // The first of n weights (vocabulary order) whose running sum exceeds the
+  // threshold: floor(u * S) when use_u, else th_in clamped below S.  Each
+  // lane sums a contiguous block exactly in 64 bits.  Returns false when
+  // S = 0; else sets c (the index) and th (the threshold within it).
+  // Lane l holds the weights of entries [l * cpl, (l + 1) * cpl) in wv.
+  __device__ bool crossing(int n, const unsigned long long (&wv)[kCpl], bool use_u, float ufin,
+                           unsigned long long th_in, int& c_out, unsigned long long& th_out) const {
+    const int cpl = (n + 31) / 32;
+    const int b0 = min(n, lane * cpl), b1 = min(n, b0 + cpl);
+    unsigned long long ls = 0;
+#pragma unroll
+    for (int q = 0; q < kCpl; ++q) ls += wv[q];
+    const unsigned long long inc = warp_scan_u64(ls, lane);
+    const unsigned long long S = __shfl_sync(kFull, inc, 31);
+    if (S == 0) return false;
+    const unsigned long long thr =
+        use_u ? __umul64hi(__float2ull_rn(ufin * kTwo64), S) : (th_in < S ? th_in : S - 1);
+    const unsigned cm = __ballot_sync(kFull, inc > thr);
+    const int ln = __ffs(cm) - 1;
+    int c = -1;
+    unsigned long long th = 0;
+    if (lane == ln) {
+      unsigned long long run = inc - ls;
+      c = b1 - 1;
+      for (int q = 0; q < kCpl; ++q) {
+        if (q < cpl && b0 + q < b1) {
+          if (run + wv[q] > thr) { c = b0 + q; break; }
+          run += wv[q];
+        }
+      }
+      th = thr - run;
+    }
+    c_out = __shfl_sync(kFull, c, ln);
+    th_out = __shfl_sync(kFull, th, ln);
+    return true;
+  }
+
+  // The element of units [ub, ue) where the precise running weight passes
+  // th; the last positive weight when the threshold lies past them (the
+  // fast and precise weights differ by rounding).  Each lane takes a block
+  // of at most kWalk units: it first prefetches the block into L1, then sums
+  // each unit, keeping the sums in shared memory, so the lane holding the
+  // crossing recomputes one unit only.  Longer ranges go in rounds.
+  template <typename PF, typename FF>
+  __device__ int walk(PF pfn, FF pref, int ub, int ue, unsigned long long th) const {
+    unsigned long long* us = s_walk + lane * kWalk;
+    int lastpos = -1;
+    for (int rb = ub; rb < ue; rb += 32 * kWalk) {
+      const int re = min(ue, rb + 32 * kWalk);
+      const int upl = (re - rb + 31) / 32;
+      const int b0 = min(re, rb + lane * upl), b1 = min(re, b0 + upl);
+      for (int u = b0; u < b1; ++u) pref(u);
+      unsigned long long sv = 0;
+#pragma unroll 1
+      for (int u = b0; u < b1; ++u) {
+        unsigned long long wi[VE];
+        pfn(u, wi);
+        unsigned long long su = 0;
+#pragma unroll
+        for (int e = 0; e < VE; ++e) {
+          su += wi[e];
+          if (wi[e] > 0) lastpos = u * VE + e;
+        }
+        us[u - b0] = su;
+        sv += su;
+      }
+      const unsigned long long inc = warp_scan_u64(sv, lane);
+      const unsigned long long tot = __shfl_sync(kFull, inc, 31);
+      if (th < tot) {
+        int pk = -1;
+        if (sv > 0 && inc - sv <= th && th < inc) {
+          unsigned long long acc = inc - sv;
+          int u = b1 - 1;
+          for (int v = b0; v < b1; ++v) {
+            if (acc + us[v - b0] > th) {
+              u = v;
+              break;
+            }
+            acc += us[v - b0];
+          }
+          unsigned long long wi[VE];
+          pfn(u, wi);
+          pk = u * VE + VE - 1;
+          bool hit_e = false;
+#pragma unroll
+          for (int e = 0; e < VE; ++e) {
+            acc += wi[e];
+            if (!hit_e && acc > th) {
+              pk = u * VE + e;
+              hit_e = true;
+            }
+          }
+        }
+        const unsigned hit = __ballot_sync(kFull, pk >= 0);
+        return __shfl_sync(kFull, pk, __ffs(hit) - 1);
+      }
+      th -= tot;
+    }
+    const int lp = static_cast<int>(warp_max_u64(static_cast<unsigned long long>(lastpos + 1))) - 1;
+    return lp >= 0 ? lp : ub * VE;
+  }
+
+  // Draw from p of target row c0 + a (its per-chunk statistics give the
+  // chunk weights; only the crossing chunk is read again).
+  __device__ int bonus(size_t trow, const DrawRows<Raw>& w, float ufin) const {
+    const float2* stc = p.st_c + trow * kStatStride;
+    const int nst = NS * G.spw;
+    // all of a lane's chunk statistics are requested before any is used
+    const int cpl = (nst + 31) / 32, b0 = min(nst, lane * cpl), b1 = min(nst, b0 + cpl);
+    float2 st[kCpl];
+#pragma unroll
+    for (int q = 0; q < kCpl; ++q) {
+      int ub = 0, ue = 0;
+      if (q < cpl && b0 + q < b1) stat_units(G, b0 + q, ub, ue);
+      st[q] = ub < ue ? __ldcg(stc + b0 + q) : make_float2(-INFINITY, 0.0f);
+    }
+    unsigned long long wv[kCpl];
+#pragma unroll
+    for (int q = 0; q < kCpl; ++q)
+      wv[q] = (st[q].x != -INFINITY && st[q].y > 0.0f)
+                  ? __float2ull_rn(__fmul_rn(st[q].y * exp2_ftz((st[q].x - w.Mt) * w.s2), kTwo40))
+                  : 0ull;
+    int c;
+    unsigned long long th;
+    if (!crossing(nst, wv, true, ufin, 0ull, c, th)) {
+      if (lane == 0) raise_error(p.err, SD_DEV_ERR_LOGITS);
+      return 0;
+    }
+    int ub, ue;
+    stat_units(G, c, ub, ue);
+    DrawRows<Raw> ws = w;
+    const bool staged = stage(ws, false, ub, ue);
+    return walk([&](int u, unsigned long long (&wi)[VE]) { precise_p<T, VEC>(ws, u, wi); },
+                [&](int u) {
+                  if (!staged) prefetch_l1(ws.rt + u);
+                },
+                ub, ue, th);
+  }
+
+  // ---- per-request work (warp) --------------------------------------------
+  // Accept tests of request i (lane j tests slot j), then its final token:
+  // the argmax (greedy), a bonus draw from p (whole prefix accepted), or --
+  // at a rejection -- a residual draw, listed for the slices.
+  __device__ void tail(int i) const {
+    const int c0 = C.cu[i];
+    const int n = C.cu[i + 1] - c0 - 1;
+    const int d0 = c0 - i;
+    const float tau = C.tau[i];
+    const bool greedy = !(tau > 0.0f);
+    float s2h = 0.0f, s2l = 0.0f;
+    if (!greedy) {
+      s2h = kLog2eHi / tau;
+      s2l = (fmaf(-s2h, tau, kLog2eHi) + kLog2eLo) / tau;
+    }
+    const float* urow = p.uniforms + static_cast<size_t>(i) * (p.k_max + 1);
+    // lane j holds the statistics of slot j's rows (lane n: the bonus row)
+    float4 ts_l = make_float4(0.0f, 1.0f, 0.0f, 0.0f), ds_l = make_float4(0.0f, 1.0f, 0.0f, 0.0f);
+    if (lane <= n) ts_l = __ldcg(reinterpret_cast<const float4*>(p.st_t + c0 + lane));
+    if (lane < n && !greedy) ds_l = __ldcg(reinterpret_cast<const float4*>(p.st_d + d0 + lane));
+    bool acc = true;
+    if (lane < n) {
+      const int j = lane;
+      const int x = p.draft_ids[d0 + j];
+      const bool x_ok = x >= 0 && x < p.V;
+      if (!x_ok) raise_error(p.err, SD_DEV_ERR_DRAFT_ID);
+      const float4 ts = ts_l;
+      if (greedy) {
+        const int amax = __float_as_int(ts.w);
+        if (amax < 0) raise_error(p.err, SD_DEV_ERR_LOGITS);
+        acc = x_ok && amax >= 0 && x == amax;
+      } else {
+        const float4 ds = ds_l;
+        const bool ok = isfinite(ts.x) && isfinite(ts.y) && ts.y > 0.0f && isfinite(ds.x) &&
+                        isfinite(ds.y) && ds.y > 0.0f;
+        float px = 0.0f, qx = 0.0f;
+        if (ok && x_ok) {
+          float h, l;
+          two_diff(ts.z, ts.x, h, l);
+          px = exp2_df(h, l, s2h, s2l) / ts.y;
+          two_diff(ds.z, ds.x, h, l);
+          qx = exp2_df(h, l, s2h, s2l) / ds.y;
+        }
+        if (!ok) raise_error(p.err, SD_DEV_ERR_LOGITS);
+        const float u = urow[j];
+        if (!(u >= 0.0f && u < 1.0f)) raise_error(p.err, SD_DEV_ERR_UNIFORM);
+        acc = ok && x_ok && (u * qx) <= px;
+        if (p.probs_out) {
+          p.probs_out[2 * static_cast<size_t>(d0 + j)] = px;
+          p.probs_out[2 * static_cast<size_t>(d0 + j) + 1] = qx;
+        }
+      }
+    }
+    const unsigned rej = __ballot_sync(kFull, !acc);
+    const int a = rej ? __ffs(rej) - 1 : n;
+    float4 ts;
+    ts.x = __shfl_sync(kFull, ts_l.x, a);
+    ts.y = __shfl_sync(kFull, ts_l.y, a);
+    ts.z = __shfl_sync(kFull, ts_l.z, a);
+    ts.w = __shfl_sync(kFull, ts_l.w, a);
+    int pick = 0;
+    bool residual = false;
+    if (greedy) {
+      const int amax = __float_as_int(ts.w);
+      if (amax < 0 && lane == 0) raise_error(p.err, SD_DEV_ERR_LOGITS);
+      pick = amax >= 0 ? amax : 0;
+    } else {
+      const bool reject = a < n;
+      float4 ds;
+      ds.x = __shfl_sync(kFull, ds_l.x, a);
+      ds.y = __shfl_sync(kFull, ds_l.y, a);
+      ds.z = __shfl_sync(kFull, ds_l.z, a);
+      ds.w = __shfl_sync(kFull, ds_l.w, a);
+      const bool ok = isfinite(ts.x) && isfinite(ts.y) && ts.y > 0.0f &&
+                      (!reject || (isfinite(ds.x) && isfinite(ds.y) && ds.y > 0.0f));
+      const float ufin = urow[p.k_max];
+      if (lane == 0 && !(ufin >= 0.0f && ufin < 1.0f)) raise_error(p.err, SD_DEV_ERR_UNIFORM);
+      if (!ok) {
+        if (lane == 0) raise_error(p.err, SD_DEV_ERR_LOGITS);
+      } else if (reject) {
+        residual = true;
+      } else {
+        pick = bonus(static_cast<size_t>(c0 + a), make_rows<T, VEC>(p, C.cu, i, a, tau, ts, ds, false),
+                     ufin);
+      }
+    }
+    // outputs: the accepted draft tokens, the final token (a residual one is
+    // written by its draw's last slice), -1 after it
+    int* o = p.out_tokens + static_cast<size_t>(i) * (p.k_max + 1);
+    if (lane <= p.k_max)
+      o[lane] = lane < a ? p.draft_ids[d0 + lane] : (lane == a ? (residual ? -1 : pick) : -1);
+    __syncwarp();
+    if (lane == 0) {
+      p.accepted_len[i] = a;
+      p.req_cnt[i] = 0;  // leave the workspace ready for the next call
+      if (!greedy) {
+        if (residual) {
+          const int pos = atomicAdd(&p.ctrl[2], 1);
+          st_release(&p.res_list[pos], 1 + ((i << 4) | a));  // publishes the outputs too
+        }
+        __threadfence();
+        atomicAdd(&p.ctrl[4], 1);  // one more sampling request decided
+      }
+    }
+    __syncwarp();
+  }
+
+  // Last slice of listed draw e folded: the residual's chunk sums are
+  // complete; find the crossing chunk and walk it.
+  __device__ void finish(int e, int i, int a, const float4& ts, const float4& ds, float ufin) const {
+    const int c0 = C.cu[i];
+    const DrawRows<Raw> w = make_rows<T, VEC>(p, C.cu, i, a, C.tau[i], ts, ds, true);
+    unsigned long long* rs = p.rs + static_cast<size_t>(e) * kStatStride;
+    const int nst = NS * G.spw;
+    const int cpl = (nst + 31) / 32, b0 = min(nst, lane * cpl), b1 = min(nst, b0 + cpl);
+    unsigned long long wv[kCpl];
+#pragma unroll
+    for (int q = 0; q < kCpl; ++q) {
+      int ub = 0, ue = 0;
+      if (q < cpl && b0 + q < b1) stat_units(G, b0 + q, ub, ue);
+      wv[q] = ub < ue ? __ldcg(rs + b0 + q) : 0ull;
+    }
+    int c;
+    unsigned long long th;
+    int pick;
+    if (crossing(nst, wv, true, ufin, 0ull, c, th)) {
+      int ub, ue;
+      stat_units(G, c, ub, ue);
+      DrawRows<Raw> ws = w;
+      const bool staged = stage(ws, true, ub, ue);
+      pick = walk([&](int u, unsigned long long (&wi)[VE]) { precise_res<T, VEC>(ws, u, wi); },
+                  [&](int u) {
+                    if (!staged) {
+                      prefetch_l1(ws.rt + u);
+                      prefetch_l1(ws.rd + u);
+                    }
+                  },
+                  ub, ue, th);
+    } else {
+      pick = bonus(static_cast<size_t>(c0 + a), w, ufin);  // no residual mass in fp32: draw from p
+    }
+    for (int q = lane; q < nst; q += 32) rs[q] = 0;  // zero for the next call
+    __syncwarp();
+    if (lane == 0) {
+      p.out_tokens[static_cast<size_t>(i) * (p.k_max + 1) + a] = pick;
+      p.slice_cnt[e] = 0;
+      p.res_list[e] = 0;
+    }
+    __syncwarp();
+  }
+
+  // Unit u at position k is done in every streaming warp: fold it.
+  __device__ void fold(int k, int u) const {
+    const int sl = k % kDepth;
+    if (u < C.U_rows) {
+      const Unit t = locate(C, p.bs, u);
+      float4 stat;
+      if (t.greedy) {
+        const unsigned long long kk = warp_max_u64(lane < NS ? red_k[sl][lane] : 0ull);
+        const int nn = __any_sync(kFull, lane < NS ? red_n[sl][lane] : 0);
+        const float bv = from_ordered(static_cast<uint32_t>(kk >> 32));
+        const bool rowbad = nn || kk == 0ull || !isfinite(bv);
+        const int amax = rowbad ? -1 : static_cast<int>(0xFFFFFFFFu - static_cast<uint32_t>(kk));
+        stat = make_float4(bv, 0.0f, s_lx[sl], __int_as_float(amax));
+      } else {
+        const float s2 = kLog2e / C.tau[t.i];
+        const float mw = lane < NS ? red_m[sl][lane] : -INFINITY;
+        const float M = warp_max(mw);
+        const float zr = (lane < NS && mw != -INFINITY && M != -INFINITY)
+                             ? red_z[sl][lane] * exp2_ftz((mw - M) * s2)
+                             : 0.0f;
+        stat = make_float4(M, warp_sum(zr), s_lx[sl], __int_as_float(0));
+      }
+      if (!t.greedy && !t.draft) {  // the chunk statistics of a sampling request's target row
+        float2* stc = p.st_c + t.row * kStatStride;
+        for (int c = lane; c < NS * G.spw; c += 32) {
+          int ub, ue;
+          stat_units(G, c, ub, ue);
+          const unsigned long long v = s_stat[sl][c];
+          if (ub < ue)
+            __stcg(stc + c, make_float2(__uint_as_float(static_cast<uint32_t>(v)),
+                                        __uint_as_float(static_cast<uint32_t>(v >> 32))));
+        }
+      }
+      __threadfence();  // every lane's writes of the row before the count
+      __syncwarp();
+      int old = 0;
+      if (lane == 0) {
+        __stcg(reinterpret_cast<float4*>(t.draft ? p.st_d + t.row : p.st_t + t.row), stat);
+        __threadfence();  // the row's statistics before the count
+        old = atomicAdd(&p.req_cnt[t.i], 1);
+      }
+      old = __shfl_sync(kFull, old, 0);
+      if (old == (t.n + 1) + (t.greedy ? 0 : t.n) - 1) {  // the request's last row: its tail
+        __threadfence();  // the other rows' statistics, counted before this one
+        push_job(t.i);
+      }
+    } else if (is_slice(u)) {
+      const int e = (u >> 18) & 0xFFF;
+      unsigned long long* rs = p.rs + static_cast<size_t>(e) * kStatStride;
+      for (int c = lane; c < NS * G.spw; c += 32) {
+        const unsigned long long v = s_stat[sl][c];
+        if (v != 0) atomicAdd(rs + c, v);
+      }
+      __threadfence();  // every lane's sums before the count
+      __syncwarp();
+      int old = 0;
+      if (lane == 0) old = atomicAdd(&p.slice_cnt[e], 1);
+      old = __shfl_sync(kFull, old, 0);
+      if (old == G.S_sl - 1) {  // the draw's last slice: its finish
+        __threadfence();  // the other slices' sums, counted before this one
+        push_job(kFinishJob | (u & 0x3FFFFFFF));
+      }
+    }
+  }
+
+  // ---- jobs: tails and draw finishes, run by the draw warps ---------------
+  // The scheduling warp appends; each draw warp takes the next job.
+  static constexpr int kFinishJob = 1 << 30;
+  static constexpr int kStopJob = -1;
+  __device__ void push_job(int code) const {
+    if (lane == 0) {
+      const int t = *jtail;
+      uint32_t it = 0;
+      for (; it < kSpinLimit && t - ld_volatile_cta(jdone) >= kJobs; ++it) __nanosleep(64);
+      if (it >= kSpinLimit) raise_error(p.err, SD_DEV_ERR_TIMEOUT);  // the ring is full
+      jobs[t % kJobs] = code;
+      st_release_cta(jtail, t + 1);
+    }
+    __syncwarp();
+  }
+  __device__ void run_draw() {
+    for (;;) {
+      int code = kStopJob;
+      if (lane == 0) {
+        const int j = atomicAdd(jhead, 1);
+        bool ok = false;
+        for (uint32_t it = 0; it < kSpinLimit; ++it) {
+          if (ld_volatile_cta(jtail) > j) {
+            ok = ld_acquire_cta(jtail) > j;
+            break;
+          }
+          __nanosleep(64);
+        }
+        if (ok) {
+          code = jobs[j % kJobs];
+          atomicAdd(jdone, 1);
+        } else {
+          raise_error(p.err, SD_DEV_ERR_TIMEOUT);
+        }
+      }
+      code = __shfl_sync(kFull, code, 0);
+      if (code == kStopJob) break;
+      __threadfence();  // the unit's statistics and sums, counted by the scheduling warp
+      if (code & kFinishJob) {
+        const int e = (code >> 18) & 0xFFF, i = (code >> 4) & 0xFFF, a = code & 15;
+        const int c0 = C.cu[i];
+        const float4 ts = __ldcg(reinterpret_cast<const float4*>(p.st_t + c0 + a));
+        const float4 ds = __ldcg(reinterpret_cast<const float4*>(p.st_d + c0 - i + a));
+        const float ufin = p.uniforms[static_cast<size_t>(i) * (p.k_max + 1) + p.k_max];
+        finish(e, i, a, ts, ds, ufin);
+      } else {
+        tail(code);
+      }
+    }
+  }
+
+  __device__ void run_sched(int k_pub) {
+    int k_done = 0;
+    bool end_pub = false;
+    uint32_t idle = 0;
+    for (;;) {
+      bool progress = false;
+      if (!end_pub && k_pub < k_done + kWindow - 1) {
+        int e = kWait;
+        if (lane == 0) e = schedule();
+        e = __shfl_sync(kFull, e, 0);
+        if (e != kWait) {
+          if (lane == 0) {
+            C.q[(k_pub + 1) % kDepth] = e;
+            st_release_cta(C.pub, k_pub + 1);
+          }
+          ++k_pub;
+          end_pub = e == kEnd;
+          progress = true;
+        }
+      }
+      if (k_done <= k_pub) {
+        const int u = C.q[k_done % kDepth];
+        if (u == kEnd) break;
+        // one lane tests the barrier and the warp follows its verdict, so
+        // every lane takes the same path through the fold's shuffles
+        bool done = lane == 0 && mbar_try_wait(&pbar[k_done % kDepth], (k_done / kDepth) & 1);
+        done = __shfl_sync(kFull, done, 0);
+        if (done) {
+          __syncwarp();  // lane 0's acquire covers the whole warp
+          fold(k_done, u);
+          ++k_done;
+          progress = true;
+        }
+      }
+      if (progress) {
+        idle = 0;
+      } else if (++idle > kSpinLimit) {
+        if (lane == 0) raise_error(p.err, SD_DEV_ERR_TIMEOUT);
+        if (lane == 0 && !end_pub) {  // let the streaming warps finish
+          C.q[(k_pub + 1) % kDepth] = kEnd;
+          st_release_cta(C.pub, k_pub + 1);
+        }
+        break;
+      } else {
+        __nanosleep(64);
+      }
+    }
+    push_job(kStopJob);  // one per draw warp, after every job of the call
+    push_job(kStopJob);
+  }
+};
+
+// ---------------------------------------------------------------------------
+// The kernel: NT / 32 - 3 streaming warps, a scheduling warp and two draw
+// warps per CTA, one CTA per SM, persistent over the whole work list.
+template <typename T, int NT, bool VEC>
+__global__ void __launch_bounds__(NT, 1) verify_kernel(const __grid_constant__ VerifyParams p) {
+  using Raw = typename VT<T, VEC>::Raw;
+  constexpr int VE = VT<T, VEC>::VE;
   constexpr int NW = NT / 32;
-  constexpr int CB = kChunkBytes;  // bytes per ring slot (one chunk)
-  constexpr int VPC = CB / 16;     // 16-byte vectors per chunk
-  constexpr int VPL = VPC / 32;    // vectors per lane per chunk
-  constexpr int EPC = CB / static_cast<int>(sizeof(T));  // elements per chunk
-  constexpr int BW = NW - 1;       // the warp that keeps the per-row books
-  static_assert(NW <= 32, "one lane per warp in the cross-warp reductions");
-  static_assert(VPL * 32 * 16 == CB, "chunk is a whole number of warp-wide vectors");
-  constexpr size_t kRing = VEC ? static_cast<size_t>(NW) * kSlots * CB : 0;
-  constexpr int kBars = VEC ? NW * kSlots : 0;
+  constexpr int NS = NW - 3;  // streaming warps; warp NS schedules, NS + 1 and NS + 2 draw
+  static_assert(NS <= 32, "one lane of the control warp per streaming warp");
+  constexpr size_t kRing = VEC ? static_cast<size_t>(NS) * kSlots * kSlotBytes : 0;
+  constexpr int kBars = VEC ? NS * kSlots : 0;
 
   extern __shared__ __align__(128) unsigned char smem[];
-  unsigned char* ring = smem;                                   // [NW][kSlots][CB]
-  uint64_t* mbar = reinterpret_cast<uint64_t*>(smem + kRing);   // [NW][kSlots]
+  unsigned char* ring = smem;                                   // [NS][kSlots][kSlotBytes]
+  uint64_t* mbar = reinterpret_cast<uint64_t*>(smem + kRing);   // [NS][kSlots]
   int* cu_s = reinterpret_cast<int*>(mbar + kBars);             // [bs+1]
   float* tau_s = reinterpret_cast<float*>(cu_s + p.bs + 1);     // [bs]
   int* order = reinterpret_cast<int*>(tau_s + p.bs);            // [bs] request order
   int* ustart = order + p.bs;                                   // [bs+1] first unit of order[k]
 
-  // per-warp partial row statistics, double-buffered by unit parity
-  __shared__ float red_m[2][NW], red_z[2][NW];
-  __shared__ unsigned long long red_k[2][NW];
-  __shared__ int red_n[2][NW];
+  __shared__ uint64_t pbar[kDepth];  // position k done by every streaming warp
+  __shared__ int s_q[kDepth];        // the unit of position k at s_q[k % kDepth]
+  __shared__ int s_pub;              // positions 0..s_pub are published
+  __shared__ float red_m[kDepth][NS], red_z[kDepth][NS];
+  __shared__ unsigned long long red_k[kDepth][NS];
+  __shared__ int red_n[kDepth][NS];
+  __shared__ float s_lx[kDepth];
+  __shared__ unsigned long long s_stat[kDepth][kStatStride];
   __shared__ int red_i[NW];
-  __shared__ float s_lx[2];
-  __shared__ int s_q[4];        // unit queue of this CTA: the k-th unit at s_q[k & 3]
-  __shared__ int s_pending[2];  // request whose last row ended unit k-1 (or -1)
-  __shared__ int s_a, s_pick, s_count, s_found, s_ch, s_lastpos, s_hit, s_nsamp, s_last;
-  __shared__ unsigned long long s_th;
-  __shared__ unsigned long long red_u[NW];
-  __shared__ unsigned long long s_R[kMaxDrawChunks];  // chunk sums of the draw in hand
-  __shared__ unsigned long long s_Rr[kMaxRanges];     // range sums of a bonus draw
+  __shared__ int s_count, s_nsamp;
+  __shared__ unsigned long long s_walk[2][32 * Control<T, VEC, NS>::kWalk];
+  __shared__ int s_jobs[Control<T, VEC, NS>::kJobs];
+  __shared__ int s_jtail, s_jhead, s_jdone;
+  __shared__ __align__(128) unsigned char s_chunk[2][2 * kSlotBytes];  // draw warps' staging
+  __shared__ uint64_t s_cbar[2];
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int V = p.V;
-  const int nvec = (V + VE - 1) / VE;  // VE divides V on the vector path
-  const size_t row_bytes = static_cast<size_t>(V) * sizeof(T);
+  const int nvec = (p.V + VE - 1) / VE;  // VE divides V on the vector path
 
   // ---- per-call checks of the compaction (identical verdict in every CTA)
   for (int i = tid; i <= p.bs; i += NT) cu_s[i] = p.cu[i];
@@ -461,9 +1524,9 @@ __global__ void __launch_bounds__(NT, NT <= 256 ? 2 : 1) verify_kernel(const Ver
     return r;
   };
 
-  // ---- request order (sampling requests first, each group in index order)
-  // and each request's first unit: its n_i + 1 target rows, then its n_i
-  // draft rows when tau > 0.
+  // ---- work list: every request's n_i + 1 target rows, then its n_i draft
+  // rows when tau > 0; sampling requests first (their final draws then
+  // overlap the greedy requests' rows), each group in index order.
   {
     const int chunk = (p.bs + NT - 1) / NT;
     const int beg = min(p.bs, tid * chunk), end = min(p.bs, beg + chunk);
@@ -494,855 +1557,54 @@ __global__ void __launch_bounds__(NT, NT <= 256 ? 2 : 1) verify_kernel(const Ver
     }
     if (tid == 0) ustart[p.bs] = total;
   }
-  if (VEC && tid == 0) {
+  if (tid == 0) {
+    s_jtail = 0;
+    s_jhead = 0;
+    s_jdone = 0;
     for (int b = 0; b < kBars; ++b) mbar_init(&mbar[b], 1);
+    for (int b = 0; b < kDepth; ++b) mbar_init(&pbar[b], NS);
+    mbar_init(&s_cbar[0], 1);
+    mbar_init(&s_cbar[1], 1);
     fence_mbar_init();
   }
   __syncthreads();
-  // Geometry of the final draws: chunks of CUd = 32 * Ld units (Ld units per
-  // lane, at most kMaxDrawChunks chunks per row).
-  const int Ld = 4 * ((((nvec + 32 * kMaxDrawChunks - 1) / (32 * kMaxDrawChunks)) + 3) / 4);
-  const int CUd = 32 * Ld;
-  // Warp ranges of a row: warp w streams units [w * RU, (w + 1) * RU).
-  const int nch_row = static_cast<int>((row_bytes + CB - 1) / CB);
-  const int cpw = (nch_row + NW - 1) / NW;  // vector path: ring chunks per warp
-  const int RU = VEC ? cpw * VPC : 32 * ((nvec + 32 * NW - 1) / (32 * NW));
-  // The work list's rows; residual draws are added as requests are decided,
-  // each as S_sl slices: slice s takes the s-th part of every warp's range
-  // (m_sl ring chunks, or mu_sl elements, per warp).
-  const int U_stream = ustart[p.bs];
-  const int S_sl = VEC ? min(4, max(1, cpw)) : (RU >= 128 ? 4 : 1);
-  const int m_sl = (cpw + S_sl - 1) / S_sl;
-  const int mu_sl = 32 * ((RU + 32 * S_sl - 1) / (32 * S_sl));
 
-  // Unit -> (request, row kind, slot, row index).
-  struct Unit {
-    int i, j, n, c0;
-    bool draft, greedy;
-    size_t row;
-  };
-  auto locate = [&](int u) {
-    int lo = 0, hi = p.bs;  // ustart[lo] <= u < ustart[hi]
-    while (hi - lo > 1) {
-      const int mid = (lo + hi) >> 1;
-      if (ustart[mid] <= u) lo = mid;
-      else hi = mid;
+  const Geom G = make_geom(nvec, VEC, NS);
+  const Cta C{cu_s, tau_s, order, ustart, s_q, &s_pub, s_nsamp, ustart[p.bs]};
+  // The first kWindow positions: rows (no draw is listed yet); the row
+  // after them is the control warp's first stash.
+  int k_pub = -1;
+  int stash = 0;
+  if (warp == NS && lane == 0) {
+    const int u0 = atomicAdd(&p.ctrl[0], kWindow + 1);
+    for (int q = 0; q < kWindow && u0 + q < C.U_rows; ++q) {
+      s_q[q] = u0 + q;
+      k_pub = q;
     }
-    Unit t;
-    t.i = order[lo];
-    const int r = u - ustart[lo];
-    t.c0 = cu_s[t.i];
-    t.n = cu_s[t.i + 1] - t.c0 - 1;
-    t.greedy = !(tau_s[t.i] > 0.0f);
-    t.draft = r > t.n;
-    t.j = t.draft ? r - (t.n + 1) : r;
-    t.row = t.draft ? static_cast<size_t>(t.c0 - t.i + t.j) : static_cast<size_t>(t.c0 + t.j);
-    return t;
-  };
-  auto row_base = [&](const Unit& t) {
-    return reinterpret_cast<const char*>(t.draft ? p.draft : p.target) + t.row * row_bytes;
-  };
+    stash = u0 + kWindow;
+    s_pub = k_pub;
+  }
+  __syncthreads();
 
-  // ---- per-warp bulk-copy ring (vector path): this warp's chunks of every
-  // row are the contiguous range [cb_w, ce_w).  A row position takes one
-  // ring entry per chunk; a residual draw takes two (target chunk c, then
-  // draft chunk c).  The fetch cursor runs up to kSlots entries ahead of
-  // consumption, across positions, but stops at a position whose entry is
-  // not yet a unit.
-  const int cb_w = min(nch_row, warp * cpw), ce_w = min(nch_row, cb_w + cpw);
-  uint32_t cseq = 0, iseq = 0;  // entries consumed / issued by this warp
-  int fk = 0, fe = 0;           // fetch cursor: queue position, entry within it
-  int fk_cached = -1, f_n = 0;  // position whose bases are cached, its entries
-  int f_c0 = 0;                 // first chunk of the cached position
-  bool f_two = false;           // two entries (target, draft) per chunk
-  const char* f_base = nullptr;
-  const char* f_base2 = nullptr;
-  auto refill = [&](int k_limit) {
-    while (iseq - cseq < static_cast<uint32_t>(kSlots) && fk <= k_limit) {
-      if (fk_cached != fk) {
-        const int u = s_q[fk & 3];
-        if (u == kPoll || u == kEnd) break;  // not known yet / nothing follows
-        f_n = 0;
-        f_two = false;
-        if (u < U_stream) {
-          f_base = row_base(locate(u));
-          f_c0 = cb_w;
-          f_n = ce_w - cb_w;
-        } else if (u >= kResBase && u < kNoop) {
-          const int i = (u >> 4) & 0xFFF, a = u & 15, sl = (u >> 16) & 3;
-          f_base = reinterpret_cast<const char*>(p.target) +
-                   static_cast<size_t>(cu_s[i] + a) * row_bytes;
-          f_base2 = reinterpret_cast<const char*>(p.draft) +
-                    static_cast<size_t>(cu_s[i] - i + a) * row_bytes;
-          f_c0 = min(ce_w, cb_w + sl * m_sl);
-          f_n = 2 * (min(ce_w, f_c0 + m_sl) - f_c0);
-          f_two = true;
-        }
-        fk_cached = fk;
-        fe = 0;
-      }
-      if (fe >= f_n) {
-        ++fk;
-        continue;
-      }
-      const int c = f_c0 + (f_two ? fe >> 1 : fe);
-      const char* base = (f_two && (fe & 1)) ? f_base2 : f_base;
-      const int slot = static_cast<int>(iseq % kSlots);
-      const uint32_t bytes = static_cast<uint32_t>(
-          min(static_cast<size_t>(CB), row_bytes - static_cast<size_t>(c) * CB));
-      if (lane == 0) {
-        uint64_t* bar = &mbar[warp * kSlots + slot];
-        mbar_arrive_expect_tx(bar, bytes);
-        bulk_load_nohint(ring + (warp * kSlots + slot) * CB, base + static_cast<size_t>(c) * CB,
-                         bytes, bar);
-      }
-      ++iseq;
-      ++fe;
-    }
-  };
-
-  // ------------------------------------------------------------------------
-  // Final draws by inverse CDF: the first element (vocabulary order) whose
-  // running weight sum exceeds a threshold.  Weights are summed in 64-bit
-  // fixed point (residual max(p - q, 0) <= 1 at 2^56, unnormalised
-  // 2^((l - M) s2) <= 1 at 2^40), so every prefix over chunks is exact and
-  // the chunk holding the crossing is found without rounding.  That chunk is
-  // then recomputed with the precise weight function (double-float exponent)
-  // and walked block-wide; where the two weight functions disagree by
-  // rounding and the threshold passes the recomputed chunk, the chunk's last
-  // positive weight stands in.
-  //
-  // chunk_sums: fast fixed-point sums of the chunks c0 <= c < c1 of CUd
-  // units starting at unit ub (clipped at ue) -> out[c]; warp w sums chunks
-  // c0 + w, c0 + w + NW, ...; each lane issues QB loads per row before using
-  // any (the rows come from L2 or HBM, latency-bound otherwise).
-  auto chunk_sums = [&](auto resid_tag, const Raw* rt, const Raw* rd, auto fast, float scale,
-                        int ub, int ue, int c0, int c1, unsigned long long* out) {
-    constexpr bool resid = decltype(resid_tag)::value;
-    constexpr int QB = 2;  // loads ahead per lane and row (register budget)
-    for (int c = c0 + warp; c < c1; c += NW) {
-      const int cb = ub + c * CUd;
-      const int ce = min(cb + CUd, ue);
-      unsigned long long ls = 0;
-      for (int q0 = 0; q0 < Ld; q0 += QB) {
-        Raw a[QB], b[QB];
-#pragma unroll
-        for (int q = 0; q < QB; ++q) {
-          const int u = cb + (q0 + q) * 32 + lane;
-          if (u < ce) {
-            a[q] = ld_stream(rt + u);
-            if constexpr (resid) b[q] = ld_stream(rd + u);
-          }
-        }
-#pragma unroll
-        for (int q = 0; q < QB; ++q) {
-          const int u = cb + (q0 + q) * 32 + lane;
-          if (u < ce) ls += __float2ull_rn(__fmul_rn(fast(a[q], b[q]), scale));
-        }
-      }
-      ls = warp_sum_u64(ls);
-      if (lane == 0) out[c] = ls;
-    }
-  };
-
-  // crossing: over the n sums R[0..n) (shared memory), with threshold
-  // floor(u * S) when use_u, else th_in clamped below the total.  Sets
-  // s_found (total > 0), s_ch (the chunk) and s_th (threshold within it).
-  auto crossing = [&](const unsigned long long* R, int n, bool use_u, float ufin,
-                      unsigned long long th_in) {
-    __syncthreads();
-    if (warp == 0) {
-      const int epl = (n + 31) / 32;
-      const int eb = min(n, lane * epl), ee = min(n, eb + epl);
-      unsigned long long lsum = 0;
-      for (int e = eb; e < ee; ++e) lsum += R[e];
-      const unsigned long long inc = warp_scan_u64(lsum, lane);
-      const unsigned long long S = __shfl_sync(kFull, inc, 31);
-      if (S > 0) {
-        // thr < S, so some prefix exceeds it
-        const unsigned long long thr =
-            use_u ? __umul64hi(__float2ull_rn(ufin * kTwo64), S) : (th_in < S ? th_in : S - 1);
-        const unsigned cm = __ballot_sync(kFull, inc > thr);
-        const int ln = __ffs(cm) - 1;
-        const unsigned long long up = __shfl_up_sync(kFull, inc, 1);
-        const unsigned long long excl = ln == 0 ? 0ull : __shfl_sync(kFull, up, ln);
-        if (lane == ln) {
-          unsigned long long run = excl;
-          int ch = ee - 1;
-          for (int e = eb; e < ee; ++e) {
-            if (run + R[e] > thr) { ch = e; break; }
-            run += R[e];
-          }
-          s_ch = ch;
-          s_th = thr - run;
-        }
-      }
-      if (lane == 0) s_found = S > 0;
-    }
-    __syncthreads();
-  };
-
-  // pick_in: the precise walk over units [cb, ce) for threshold th (relative
-  // to cb): each thread takes a contiguous run of units, an exact 64-bit
-  // block prefix finds the run that holds the crossing, and that thread
-  // recomputes its run to find the element.  Sets s_pick.
-  auto pick_in = [&](auto precise, int cb, int ce, unsigned long long th) {
-    if (tid == 0) { s_hit = 0; s_lastpos = -1; }
-    __syncthreads();
-    const int upt = (ce - cb + NT - 1) / NT;
-    const int tb = min(ce, cb + tid * upt), te = min(ce, tb + upt);
-    unsigned long long sv = 0;
-    int lastpos = -1;
-    for (int u = tb; u < te; ++u) {
-      unsigned long long wi[VE];
-      precise(u, wi);
-#pragma unroll
-      for (int e = 0; e < VE; ++e) {
-        sv += wi[e];
-        if (wi[e] > 0) lastpos = u * VE + e;
-      }
-    }
-    const unsigned long long winc = warp_scan_u64(sv, lane);
-    if (lane == 31) red_u[warp] = winc;
-    if (lastpos >= 0) atomicMax(&s_lastpos, lastpos);
-    __syncthreads();
-    if (warp == 0) {
-      const unsigned long long wt = lane < NW ? red_u[lane] : 0ull;
-      const unsigned long long wti = warp_scan_u64(wt, lane);
-      if (lane < NW) red_u[lane] = wti - wt;  // exclusive warp offsets
-    }
-    __syncthreads();
-    const unsigned long long before = red_u[warp] + winc - sv;  // exclusive prefix
-    if (sv > 0 && before <= th && th < before + sv) {
-      unsigned long long acc = before;
-      int pk = -1;
-      for (int u = tb; u < te && pk < 0; ++u) {
-        unsigned long long wi[VE];
-        precise(u, wi);
-#pragma unroll
-        for (int e = 0; e < VE; ++e) {
-          acc += wi[e];
-          if (pk < 0 && acc > th) pk = u * VE + e;
-        }
-      }
-      s_pick = pk;
-      s_hit = 1;
-    }
-    __syncthreads();
-    if (tid == 0 && !s_hit) s_pick = s_lastpos >= 0 ? s_lastpos : cb * VE;
-    __syncthreads();
-  };
-
-  // Weight functions of a draw from p (target row rt, max Mt, temperature
-  // scale s2 = log2(e)/tau, also as the double-float s2h + s2l) and of a
-  // residual max(p - q, 0) (adds the draft row rd, max Md, and 1/Z of both).
-  struct DrawRows {
-    const Raw* rt;
-    const Raw* rd;
-    float Mt, Md, iZt, iZd, s2, s2h, s2l;
-  };
-  __shared__ DrawRows s_dr;  // the residual draw in hand
-  auto fast_p = [](const DrawRows& w) {
-    const float bt = w.Mt * w.s2, s2 = w.s2;
-    return [=](const Raw& ra, const Raw&) {
-      float f[VE];
-      Tr::unpack(ra, f);
-      float ws = 0.0f;
-#pragma unroll
-      for (int e = 0; e < VE; ++e) ws += exp2_ftz(fmaf(f[e], s2, -bt));
-      return ws;
-    };
-  };
-  auto precise_p = [](const DrawRows& w) {
-    return [=](int u, unsigned long long (&wi)[VE]) {
-      float f[VE];
-      Tr::unpack(w.rt[u], f);
-#pragma unroll
-      for (int e = 0; e < VE; ++e) {
-        float h, l;
-        two_diff(f[e], w.Mt, h, l);
-        wi[e] = __float2ull_rn(__fmul_rn(exp2_df(h, l, w.s2h, w.s2l), kTwo40));
-      }
-    };
-  };
-  auto fast_res = [](const DrawRows& w) {
-    const float bt = w.Mt * w.s2, bd = w.Md * w.s2, s2 = w.s2, iZt = w.iZt, iZd = w.iZd;
-    return [=](const Raw& ra, const Raw& rb) {
-      float f[VE], g[VE];
-      Tr::unpack(ra, f);
-      Tr::unpack(rb, g);
-      float ws = 0.0f;
-#pragma unroll
-      for (int e = 0; e < VE; ++e) {
-        const float et = exp2_ftz(fmaf(f[e], s2, -bt));
-        const float ed = exp2_ftz(fmaf(g[e], s2, -bd));
-        ws += fmaxf(fmaf(et, iZt, -(ed * iZd)), 0.0f);
-      }
-      return ws;
-    };
-  };
-  auto precise_res = [](const DrawRows& w) {
-    return [=](int u, unsigned long long (&wi)[VE]) {
-      float f[VE], g[VE];
-      Tr::unpack(w.rt[u], f);
-      Tr::unpack(w.rd[u], g);
-#pragma unroll
-      for (int e = 0; e < VE; ++e) {
-        float h, l;
-        two_diff(f[e], w.Mt, h, l);
-        const float et = exp2_df(h, l, w.s2h, w.s2l);
-        two_diff(g[e], w.Md, h, l);
-        const float ed = exp2_df(h, l, w.s2h, w.s2l);
-        const float x = fmaxf(__fmaf_rn(et, w.iZt, -__fmul_rn(ed, w.iZd)), 0.0f);
-        wi[e] = __float2ull_rn(__fmul_rn(x, kTwo56));
-      }
-    };
-  };
-
-  auto make_rows = [&](int i, int a, const float4& ts, const float4& ds, bool resid) {
-    const float tau = tau_s[i];
-    DrawRows w;
-    const int c0 = cu_s[i];
-    w.rt = reinterpret_cast<const Raw*>(static_cast<const T*>(p.target) +
-                                        static_cast<size_t>(c0 + a) * V);
-    w.rd = resid ? reinterpret_cast<const Raw*>(static_cast<const T*>(p.draft) +
-                                                static_cast<size_t>(c0 - i + a) * V)
-                 : w.rt;
-    w.Mt = ts.x;
-    w.Md = ds.x;
-    w.iZt = 1.0f / ts.y;
-    w.iZd = 1.0f / ds.y;
-    w.s2 = kLog2e / tau;
-    // s2 = log2(e) / tau as a double-float
-    w.s2h = kLog2eHi / tau;
-    w.s2l = (fmaf(-w.s2h, tau, kLog2eHi) + kLog2eLo) / tau;
-    return w;
-  };
-
-  // Draw from p of target row trow: the row's per-range statistics give the
-  // range sums, so only the crossing range is read again.
-  auto bonus_draw = [&](size_t trow, const DrawRows& w, float ufin) {
-    if (tid < kMaxRanges) {
-      unsigned long long r = 0;
-      if (tid < NW) {
-        const float2 st = __ldcg(p.st_r + trow * kMaxRanges + tid);
-        if (st.x != -INFINITY && st.y > 0.0f)
-          r = __float2ull_rn(__fmul_rn(st.y * exp2_ftz((st.x - w.Mt) * w.s2), kTwo40));
-      }
-      s_Rr[tid] = r;
-    }
-    crossing(s_Rr, NW, true, ufin, 0ull);
-    if (!s_found) {  // no mass: only a row that failed its checks gets here
-      if (tid == 0) {
-        raise_error(p.err, SD_DEV_ERR_LOGITS);
-        s_pick = 0;
-      }
-      __syncthreads();
-      return;
-    }
-    const int ub = min(nvec, s_ch * RU), ue = min(nvec, ub + RU);
-    const unsigned long long th_r = s_th;
-    const int nc = (ue - ub + CUd - 1) / CUd;
-    chunk_sums(std::false_type{}, w.rt, w.rt, fast_p(w), kTwo40, ub, ue, 0, nc, s_R);
-    crossing(s_R, nc, false, 0.0f, th_r);
-    if (!s_found) {
-      pick_in(precise_p(w), ub, ue, 0ull);
-      return;
-    }
-    const int cb = ub + s_ch * CUd;
-    pick_in(precise_p(w), cb, min(cb + CUd, ue), s_th);
-  };
-
-
-  // ------------------------------------------------------------------------
-  // Tail of request i: decisions from the row statistics, then the final
-  // token: the argmax (greedy), a bonus draw from p (whole prefix accepted),
-  // or -- at a rejection -- a residual draw, which is listed for the slice
-  // phase at the end of the work list.
-  auto tail = [&](int i) {
-    const int c0 = cu_s[i];
-    const int n = cu_s[i + 1] - c0 - 1;
-    const int d0 = c0 - i;
-    const float tau = tau_s[i];
-    const bool greedy = !(tau > 0.0f);
-    // s2 = log2(e) / tau as a double-float
-    float s2h = 0.0f, s2l = 0.0f;
-    if (!greedy) {
-      s2h = kLog2eHi / tau;
-      s2l = (fmaf(-s2h, tau, kLog2eHi) + kLog2eLo) / tau;
-    }
-    const float* urow = p.uniforms + static_cast<size_t>(i) * (p.k_max + 1);
-    // accept tests of all slots in parallel (thread j tests slot j)
-    if (tid == 0) { s_a = n; s_pick = 0; }
-    __syncthreads();
-    if (tid < n) {
-      const int j = tid;
-      const int x = p.draft_ids[d0 + j];
-      const bool x_ok = x >= 0 && x < V;
-      if (!x_ok) raise_error(p.err, SD_DEV_ERR_DRAFT_ID);
-      const float4 ts = __ldcg(reinterpret_cast<const float4*>(p.st_t + c0 + j));
-      bool acc;
-      if (greedy) {
-        const int amax = __float_as_int(ts.w);
-        if (amax < 0) raise_error(p.err, SD_DEV_ERR_LOGITS);
-        acc = x_ok && amax >= 0 && x == amax;
-      } else {
-        const float4 ds = __ldcg(reinterpret_cast<const float4*>(p.st_d + d0 + j));
-        const bool ok = isfinite(ts.x) && isfinite(ts.y) && ts.y > 0.0f && isfinite(ds.x) &&
-                        isfinite(ds.y) && ds.y > 0.0f;
-        float px = 0.0f, qx = 0.0f;
-        if (ok && x_ok) {
-          float h, l;
-          two_diff(ts.z, ts.x, h, l);
-          px = exp2_df(h, l, s2h, s2l) / ts.y;
-          two_diff(ds.z, ds.x, h, l);
-          qx = exp2_df(h, l, s2h, s2l) / ds.y;
-        }
-        if (!ok) raise_error(p.err, SD_DEV_ERR_LOGITS);
-        const float u = urow[j];
-        if (!(u >= 0.0f && u < 1.0f)) raise_error(p.err, SD_DEV_ERR_UNIFORM);
-        acc = ok && x_ok && (u * qx) <= px;
-        if (p.probs_out) {
-          p.probs_out[2 * static_cast<size_t>(d0 + j)] = px;
-          p.probs_out[2 * static_cast<size_t>(d0 + j) + 1] = qx;
-        }
-      }
-      if (!acc) atomicMin(&s_a, j);
-    }
-    __syncthreads();
-    const int a = s_a;
-    const float4 ts = __ldcg(reinterpret_cast<const float4*>(p.st_t + c0 + a));
-    bool residual = false;
-    if (greedy) {
-      const int amax = __float_as_int(ts.w);
-      if (tid == 0) {
-        if (amax < 0) raise_error(p.err, SD_DEV_ERR_LOGITS);
-        s_pick = amax >= 0 ? amax : 0;
-      }
+  if (warp < NS) {
+    Streamer<T, VEC, NS> S(p, C, G, warp, lane, ring, mbar);
+    S.run(pbar, red_m, red_z, red_k, red_n, s_lx, s_stat);
+  } else {
+    Control<T, VEC, NS> K(p, C, G, lane, pbar, red_m, red_z, red_k, red_n, s_lx,
+                          s_walk[warp == NS ? 0 : warp - NS - 1], s_jobs, &s_jtail, &s_jhead,
+                          &s_jdone, s_stat, s_chunk[warp == NS ? 0 : warp - NS - 1],
+                          &s_cbar[warp == NS ? 0 : warp - NS - 1]);
+    if (warp == NS) {
+      K.stash = stash;
+      K.run_sched(__shfl_sync(kFull, k_pub, 0));
     } else {
-      const bool reject = a < n;
-      float4 ds = make_float4(0.0f, 1.0f, 0.0f, 0.0f);
-      if (reject) ds = __ldcg(reinterpret_cast<const float4*>(p.st_d + d0 + a));
-      const bool ok = isfinite(ts.x) && isfinite(ts.y) && ts.y > 0.0f &&
-                      (!reject || (isfinite(ds.x) && isfinite(ds.y) && ds.y > 0.0f));
-      const float ufin = urow[p.k_max];
-      if (tid == 0 && !(ufin >= 0.0f && ufin < 1.0f)) raise_error(p.err, SD_DEV_ERR_UNIFORM);
-      if (!ok) {
-        if (tid == 0) raise_error(p.err, SD_DEV_ERR_LOGITS);
-      } else if (reject) {
-        residual = true;
-      } else {
-        bonus_draw(static_cast<size_t>(c0 + a), make_rows(i, a, ts, ds, false), ufin);
-      }
+      K.run_draw();
     }
-    __syncthreads();
-    if (tid == 0) {
-      int* o = p.out_tokens + static_cast<size_t>(i) * (p.k_max + 1);
-      p.accepted_len[i] = a;
-      for (int j = 0; j < a; ++j) o[j] = p.draft_ids[d0 + j];
-      o[a] = residual ? -1 : s_pick;  // a residual token is written by its last slice
-      for (int j = a + 1; j <= p.k_max; ++j) o[j] = -1;
-      p.req_cnt[i] = 0;  // leave the workspace ready for the next call
-      if (!greedy) {
-        if (residual) {
-          const int pos = atomicAdd(&p.ctrl[2], 1);
-          st_release(&p.res_list[pos], 1 + ((i << 4) | a));  // publishes the outputs too
-        }
-        atom_add_acq_rel(&p.ctrl[4], 1);  // one more sampling request decided
-      }
-    }
-    __syncthreads();
-  };
-
-  // ------------------------------------------------------------------------
-  // Work loop.  Position k of this CTA's queue (s_q[k & 3]) holds a row
-  // unit, a residual draw, or a token (kPoll, kNoop, kEnd).  Warp BW lane 0
-  // schedules position k + 3 right after the barrier that ends position k:
-  // a listed residual draw is claimed first, else the next row of the work
-  // list; once the rows are exhausted it yields kPoll (a draw may still be
-  // listed) or, when every sampling request is decided and every listed
-  // draw claimed, kEnd.  After that barrier warp BW also folds the warps'
-  // partials into the row statistics and counts the row for its request
-  // with an acquire-release increment whose result is read at the end of
-  // the next position: the CTA that saw the last row of a request runs the
-  // request's tail.
-  // Scheduler (warp BW lane 0).  Slices are handed out in order by an
-  // atomic counter (ctrl[3]); slot h is slice h % S_sl of the (h / S_sl)-th
-  // listed draw.  A slot taken before its draw is listed is held and
-  // scheduled once listed, or dropped once every sampling request is decided
-  // without it being listed.  The next row id is fetched one schedule ahead
-  // so that its atomic's latency is hidden.
-  bool rows_done = false;
-  int stash = 0;   // next row id
-  int held = -1;   // a slot taken but not yet listed
-  // (listed draws, slots taken): ctrl[2] and ctrl[3] in one 8-byte read
-  auto load_lc = [&]() {
-    return ld_relaxed_u64(reinterpret_cast<const unsigned long long*>(p.ctrl + 2));
-  };
-  // The queue entry of listed slot h.
-  auto slot_entry = [&](int h) -> int {
-    const int e = h / S_sl, sl = h - e * S_sl;
-    int v = 0;  // the draw is listed; its publisher may be finishing the store
-    for (uint32_t it = 0; it < kSpinLimit; ++it) {
-      v = ld_acquire(&p.res_list[e]);
-      if (v != 0) break;
-      __nanosleep(32);
-    }
-    if (v == 0) {
-      raise_error(p.err, SD_DEV_ERR_TIMEOUT);
-      return kNoop;
-    }
-    return kResBase | (e << 18) | (sl << 16) | (v - 1);
-  };
-  // A listed slice for this CTA (held, or newly taken when lc shows one
-  // untaken), else -1.
-  auto claim_residual = [&](unsigned long long lc) -> int {
-    const int avail = static_cast<int>(lc & 0xFFFFFFFFull) * S_sl;
-    if (held < 0 && static_cast<int>(lc >> 32) < avail) held = atomicAdd(&p.ctrl[3], 1);
-    if (held >= 0 && held < avail) {
-      const int h = held;
-      held = -1;
-      return slot_entry(h);
-    }
-    return -1;
-  };
-  auto decided = [&]() { return ld_acquire(&p.ctrl[4]) >= s_nsamp; };
-  auto schedule = [&](unsigned long long lc) -> int {
-    const int r = claim_residual(lc);
-    if (r != -1) return r;
-    if (!rows_done) {
-      const int u = stash;
-      if (u < U_stream) {
-        stash = atomicAdd(&p.ctrl[0], 1);  // used by the next schedule
-        return u;
-      }
-      rows_done = true;
-    }
-    if (held < 0 && decided()) {
-      const unsigned long long f = load_lc();  // final list
-      if (static_cast<int>(f >> 32) >= static_cast<int>(f & 0xFFFFFFFFull) * S_sl) return kEnd;
-      held = atomicAdd(&p.ctrl[3], 1);
-      if (held < static_cast<int>(f & 0xFFFFFFFFull) * S_sl) {
-        const int h = held;
-        held = -1;
-        return slot_entry(h);
-      }
-      held = -1;  // past the final list
-      return kEnd;
-    }
-    return kPoll;
-  };
-  // kPoll: settle the held slot if its draw is listed (or never will be).
-  auto poll = [&]() -> int {
-    const unsigned long long f = load_lc();
-    const int r = claim_residual(f);
-    if (r != -1) return r;
-    if (held >= 0 && decided()) {
-      const int avail = static_cast<int>(load_lc() & 0xFFFFFFFFull) * S_sl;
-      if (held < avail) {
-        const int h = held;
-        held = -1;
-        return slot_entry(h);
-      }
-      held = -1;  // past the final list
-    }
-    return kNoop;
-  };
-  if (warp == BW && lane == 0) {  // the first three positions: rows (no draw is listed yet)
-    const int u0 = atomicAdd(&p.ctrl[0], 4);
-    for (int q = 0; q < 3; ++q) {
-      if (u0 + q < U_stream) {
-        s_q[q] = u0 + q;
-      } else {
-        rows_done = true;
-        s_q[q] = decided() ? kEnd : kPoll;
-      }
-    }
-    stash = u0 + 3;
   }
-  __syncthreads();
-  if constexpr (VEC) refill(1);
-
-  int pend_i = -1, pend_old = 0, pend_rows = 0;  // warp BW lane 0: outstanding count
-  uint32_t polls = 0;                            // warp BW lane 0: fruitless polls
-  for (int k = 0;; ++k) {
-    int cur = s_q[k & 3];
-    if (cur == kEnd) break;
-    const int par = k & 1;
-    unsigned long long lc = 0;
-    if (warp == BW && lane == 0) lc = load_lc();  // consumed by this position's schedule
-    if (cur == kPoll) {
-      // Settle this CTA's own outstanding row count first: a tail it owes
-      // may be what the others wait for.
-      if (warp == BW && lane == 0) {
-        s_pending[par] = (pend_i >= 0 && pend_old == pend_rows - 1) ? pend_i : -1;
-        pend_i = -1;
-      }
-      __syncthreads();
-      if (s_pending[par] >= 0) {
-        __threadfence();
-        tail(s_pending[par]);
-      }
-      // One attempt: later positions may already hold this CTA's slices, so
-      // a poll never blocks; the scheduler keeps adding kPoll until the call
-      // is over (kEnd), bounded by kSpinLimit polls.
-      if (warp == BW && lane == 0) {
-        int r = poll();
-        if (r == kNoop) {
-          if (++polls > kSpinLimit) {
-            raise_error(p.err, SD_DEV_ERR_TIMEOUT);
-            r = kEnd;
-          } else {
-            __nanosleep(200);
-          }
-        }
-        s_q[k & 3] = r;
-      }
-      __syncthreads();
-      cur = s_q[k & 3];
-      if (cur == kEnd) break;
-    }
-    const bool is_row = cur < U_stream;
-    const bool is_res = cur >= kResBase && cur < kNoop;
-    Unit t{};
-    float s2 = 0.0f;
-    int ri = 0, ra = 0, re = 0;
-    if (is_row) {
-      t = locate(cur);
-      const int x = t.j < t.n ? p.draft_ids[t.c0 - t.i + t.j] : -1;
-      const bool x_ok = x >= 0 && x < V;
-      const float tau = tau_s[t.i];
-      s2 = t.greedy ? 0.0f : kLog2e / tau;
-
-      float best = -INFINITY;  // greedy
-      int bidx = INT_MAX, nanf = 0, bv = -1;
-      Raw bvec;
-      float m = -INFINITY, nb = 0.0f;  // sampling
-      float2 z2 = make_float2(0.0f, 0.0f);
-      if constexpr (VEC) {
-        const int cx = x_ok ? x / EPC : -1;
-        refill(k + 1);
-        for (int c = cb_w; c < ce_w; ++c) {
-          const int slot = static_cast<int>(cseq % kSlots);
-          uint64_t* bar = &mbar[warp * kSlots + slot];
-          if (!mbar_wait_bounded(bar, (cseq / kSlots) & 1, 1u << 24))
-            raise_error(p.err, SD_DEV_ERR_TIMEOUT);
-          const unsigned char* chunk = ring + (warp * kSlots + slot) * CB;
-          const int nv = min(VPC, nvec - c * VPC);
-          if (c == cx && lane == 0) {
-            float v;
-            if (sizeof(T) == 2)
-              v = __uint_as_float(static_cast<uint32_t>(reinterpret_cast<const uint16_t*>(chunk)[x - c * EPC]) << 16);
-            else
-              v = reinterpret_cast<const float*>(chunk)[x - c * EPC];
-            s_lx[par] = v;
-          }
-          Raw rv[VPL];
-  #pragma unroll
-          for (int q = 0; q < VPL; ++q)
-            rv[q] = lane + 32 * q < nv ? reinterpret_cast<const Raw*>(chunk)[lane + 32 * q]
-                                       : ChunkOps<T>::neg_inf();
-          if (t.greedy) ChunkOps<T>::argmax(rv, c * VPC + lane, best, bvec, bv, nanf);
-          else ChunkOps<T>::softmax(rv, s2, m, z2, nb);
-          __syncwarp();
-          ++cseq;
-          refill(k + 1);
-        }
-        if (t.greedy && bv >= 0) bidx = ChunkOps<T>::first_of(bvec, bv, best);
-      } else {
-        const Raw* rowp = reinterpret_cast<const Raw*>(row_base(t));
-        float b = 0.0f, z = 0.0f;
-        const int eb = min(nvec, warp * RU), ee = min(nvec, eb + RU);  // this warp's range
-        for (int v0 = eb + lane; v0 < ee; v0 += 32 * kUnroll) {
-          Raw rv[kUnroll];
-  #pragma unroll
-          for (int q = 0; q < kUnroll; ++q) {
-            const int v = v0 + q * 32;
-            if (v < ee) rv[q] = ld_stream(rowp + v);
-          }
-  #pragma unroll
-          for (int q = 0; q < kUnroll; ++q) {
-            const int v = v0 + q * 32;
-            if (v < ee) {
-              float f[VE];
-              Tr::unpack(rv[q], f);
-              if (v == x) s_lx[par] = f[0];
-              if (t.greedy) {
-                nanf |= (f[0] != f[0]);
-                if (f[0] > best) { best = f[0]; bidx = v; }
-              } else {
-                online_add<VE>(f, s2, m, z, b);
-              }
-            }
-          }
-        }
-        z2 = make_float2(z, 0.0f);
-      }
-
-      // warp partials
-      if (t.greedy) {
-        unsigned long long key = bidx == INT_MAX ? 0ull
-            : (static_cast<unsigned long long>(ordered_bits(best)) << 32) |
-                  static_cast<unsigned long long>(0xFFFFFFFFu - static_cast<uint32_t>(bidx));
-        key = warp_max_u64(key);
-        nanf = __any_sync(kFull, nanf);
-        if (lane == 0) { red_k[par][warp] = key; red_n[par][warp] = nanf; }
-      } else {
-        const float mw = warp_max(m);
-        const float zr = (m == -INFINITY || mw == -INFINITY) ? 0.0f
-                                                            : (z2.x + z2.y) * exp2_ftz((m - mw) * s2);
-        const float zw = warp_sum(zr);
-        if (lane == 0) {
-          red_m[par][warp] = mw;
-          red_z[par][warp] = zw;
-          if (!t.draft) __stcg(p.st_r + t.row * kMaxRanges + warp, make_float2(mw, zw));
-        }
-      }
-    } else if (is_res) {
-      // Slice sl of listed residual draw re (request ri, first rejected slot
-      // ra): the sl-th part of each warp's range of the row pair streams
-      // through the ring like a row (target and draft chunk c in consecutive
-      // entries); each warp adds its sum of max(p - q, 0), in 2^56 fixed
-      // point, to the draw's range sum.
-      ri = (cur >> 4) & 0xFFF;
-      ra = cur & 15;
-      re = (cur >> 18) & 0xFFF;
-      const int sl = (cur >> 16) & 3;
-      const int c0r = cu_s[ri];
-      const float4 ts = __ldcg(reinterpret_cast<const float4*>(p.st_t + c0r + ra));
-      const float4 ds = __ldcg(reinterpret_cast<const float4*>(p.st_d + c0r - ri + ra));
-      const DrawRows w = make_rows(ri, ra, ts, ds, true);
-      if (tid == 0) s_dr = w;  // for the finish after the barrier
-      const auto fr = fast_res(w);
-      unsigned long long acc = 0;
-      if constexpr (VEC) {
-        refill(k + 1);
-        const int c_lo = min(ce_w, cb_w + sl * m_sl), c_hi = min(ce_w, c_lo + m_sl);
-        for (int c = c_lo; c < c_hi; ++c) {
-          const int s0 = static_cast<int>(cseq % kSlots), s1 = static_cast<int>((cseq + 1) % kSlots);
-          if (!mbar_wait_bounded(&mbar[warp * kSlots + s0], (cseq / kSlots) & 1, 1u << 24) ||
-              !mbar_wait_bounded(&mbar[warp * kSlots + s1], ((cseq + 1) / kSlots) & 1, 1u << 24))
-            raise_error(p.err, SD_DEV_ERR_TIMEOUT);
-          const Raw* ct = reinterpret_cast<const Raw*>(ring + (warp * kSlots + s0) * CB);
-          const Raw* cd = reinterpret_cast<const Raw*>(ring + (warp * kSlots + s1) * CB);
-          const int nv = min(VPC, nvec - c * VPC);
-#pragma unroll 2
-          for (int q = 0; q < VPL; ++q) {
-            const int v = lane + 32 * q;
-            if (v < nv) acc += __float2ull_rn(__fmul_rn(fr(ct[v], cd[v]), kTwo56));
-          }
-          __syncwarp();
-          cseq += 2;
-          refill(k + 1);
-        }
-      } else {
-        const int we = min(nvec, warp * RU + RU);  // end of this warp's range
-        const int eb = min(we, warp * RU + sl * mu_sl), ee = min(we, eb + mu_sl);
-        for (int v0 = eb + lane; v0 < ee; v0 += 32 * kUnroll) {
-          Raw at[kUnroll], ad[kUnroll];
-#pragma unroll
-          for (int q = 0; q < kUnroll; ++q) {
-            const int v = v0 + q * 32;
-            if (v < ee) {
-              at[q] = ld_stream(w.rt + v);
-              ad[q] = ld_stream(w.rd + v);
-            }
-          }
-#pragma unroll
-          for (int q = 0; q < kUnroll; ++q)
-            if (v0 + q * 32 < ee) acc += __float2ull_rn(__fmul_rn(fr(at[q], ad[q]), kTwo56));
-        }
-      }
-      acc = warp_sum_u64(acc);
-      if (lane == 0 && acc != 0) atomicAdd(p.rs + static_cast<size_t>(re) * kMaxRanges + warp, acc);
-    }
-    if (warp == BW && lane == 0) {
-      s_pending[par] = (pend_i >= 0 && pend_old == pend_rows - 1) ? pend_i : -1;
-      pend_i = -1;
-    }
-    __syncthreads();
-    if (is_row && warp == BW) {
-        float4 stat;
-        if (t.greedy) {
-          const unsigned long long kk = warp_max_u64(lane < NW ? red_k[par][lane] : 0ull);
-          const int nn = __any_sync(kFull, lane < NW ? red_n[par][lane] : 0);
-          const float bv = from_ordered(static_cast<uint32_t>(kk >> 32));
-          const bool rowbad = nn || kk == 0ull || !isfinite(bv);
-          const int amax = rowbad ? -1 : static_cast<int>(0xFFFFFFFFu - static_cast<uint32_t>(kk));
-          stat = make_float4(bv, 0.0f, s_lx[par], __int_as_float(amax));
-        } else {
-          const float mw = lane < NW ? red_m[par][lane] : -INFINITY;
-          const float M = warp_max(mw);
-          const float zr = (lane < NW && mw != -INFINITY && M != -INFINITY)
-                               ? red_z[par][lane] * exp2_ftz((mw - M) * s2)
-                               : 0.0f;
-          stat = make_float4(M, warp_sum(zr), s_lx[par], __int_as_float(0));
-        }
-        if (lane == 0) {
-          RowStat* dst = t.draft ? p.st_d + t.row : p.st_t + t.row;
-          __stcg(reinterpret_cast<float4*>(dst), stat);
-          pend_rows = (t.n + 1) + (t.greedy ? 0 : t.n);
-          pend_i = t.i;
-          __threadfence();  // the statistics are visible before the count
-        pend_old = atomicAdd(&p.req_cnt[t.i], 1);  // read one position later
-        }
-    }
-    if constexpr (VEC) refill(k + 2);  // position k + 2 is known since the last barrier
-    if (is_res) {
-      if (tid == 0) s_last = atom_add_acq_rel(&p.slice_cnt[re], 1) == S_sl - 1;
-      __syncthreads();
-    }
-    if (is_res && s_last) {
-      // The last slice finishes the draw: the crossing range from the range
-      // sums, then its crossing chunk (read again), then the precise walk of
-      // that chunk.  The draw's entries go back to zero for the next call.
-      __threadfence();
-      if (tid < NW) {
-        s_Rr[tid] = __ldcg(p.rs + static_cast<size_t>(re) * kMaxRanges + tid);
-        p.rs[static_cast<size_t>(re) * kMaxRanges + tid] = 0;
-      }
-      if (tid == 0) {
-        p.slice_cnt[re] = 0;
-        p.res_list[re] = 0;
-      }
-      const float ufin = p.uniforms[static_cast<size_t>(ri) * (p.k_max + 1) + p.k_max];
-      const DrawRows w = s_dr;
-      crossing(s_Rr, NW, true, ufin, 0ull);
-      if (s_found) {
-        const int ub = min(nvec, s_ch * RU), ue = min(nvec, ub + RU);
-        const unsigned long long th_r = s_th;
-        const int nc = (ue - ub + CUd - 1) / CUd;
-        chunk_sums(std::true_type{}, w.rt, w.rd, fast_res(w), kTwo56, ub, ue, 0, nc, s_R);
-        crossing(s_R, nc, false, 0.0f, th_r);
-        if (s_found) {
-          const int cb = ub + s_ch * CUd;
-          pick_in(precise_res(w), cb, min(cb + CUd, ue), s_th);
-        } else {
-          pick_in(precise_res(w), ub, ue, 0ull);
-        }
-      } else {
-        bonus_draw(static_cast<size_t>(cu_s[ri] + ra), w, ufin);  // no residual mass in fp32
-      }
-      if (tid == 0) p.out_tokens[static_cast<size_t>(ri) * (p.k_max + 1) + ra] = s_pick;
-    }
-    const int tail_i = s_pending[par];
-    if (tail_i >= 0) {
-      __threadfence();
-      tail(tail_i);
-    }
-    if (warp == BW && lane == 0) s_q[(k + 3) & 3] = schedule(lc);
-  }
-  // the count of the last unit
-  __syncthreads();
-  if (warp == BW && lane == 0)
-    s_pending[0] = (pend_i >= 0 && pend_old == pend_rows - 1) ? pend_i : -1;
-  __syncthreads();
-  if (s_pending[0] >= 0) {
-    __threadfence();
-    tail(s_pending[0]);
-  }
+  (void)sizeof(Raw);
 
   // The last CTA out resets the work counters for the next call.
+  __syncthreads();
   if (tid == 0) {
     __threadfence();
     if (atomicAdd(&p.ctrl[1], 1) == static_cast<int>(gridDim.x) - 1) {
@@ -1412,8 +1674,9 @@ cudaError_t prepare(void* fn, size_t smem) {
 
 size_t verify_smem_bytes(int bs, int V, int elem, bool vec, int threads) {
   (void)V;
-  const int nw = threads / 32;
-  const size_t ring = vec ? static_cast<size_t>(nw) * kSlots * (kChunkBytes + 8) : 0;
+  (void)elem;
+  const int ns = threads / 32 - 3;  // streaming warps
+  const size_t ring = vec ? static_cast<size_t>(ns) * kSlots * (kSlotBytes + 8) : 0;
   return ring + static_cast<size_t>(4) * (4 * static_cast<size_t>(bs) + 2) + 16;
 }
 
@@ -1427,8 +1690,8 @@ cudaError_t choose_verify_shape(int V, int elem, int bs, const sd_launch_cfg* re
   if (e != cudaSuccess) return e;
   e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return e;
-  // 512 threads (16 warps, 192 KB ring) unless the shared memory does not
-  // fit (large batches), then 256 threads (96 KB ring).
+  // 512 threads (13 streaming warps, a 170 KB ring) unless the shared
+  // memory does not fit (large batches), then 256 threads (5 warps, 65 KB).
   const int cands[2] = {512, 256};
   for (int ci = 0; ci < 2; ++ci) {
     const int threads = treq ? treq : cands[ci];

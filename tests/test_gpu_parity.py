@@ -70,17 +70,17 @@ def test_workspace_reuse_across_calls():
                            cfg={"threads": 256 if rep % 2 else 512, "blocks": 2 + rep})
         assert np.array_equal(again["accepted_len"], first["accepted_len"])
         assert np.array_equal(again["out_tokens"], first["out_tokens"])
-    # the counters in the workspace are back at zero: residual range sums,
+    # the counters in the workspace are back at zero: residual chunk sums,
     # per-request arrivals, the residual-draw list, slice counts and the
-    # work counters (layout st_t | st_d | st_r | rs | req_cnt | res_list |
-    # slice_cnt | ctrl, each part 16-byte aligned)
+    # work counters (layout st_t | st_d | st_c | rs | req_cnt | res_list |
+    # slice_cnt | ctrl, each part 16-byte aligned; 128 chunks per row)
     rows_t, rows_d = w.bs * (w.k_max + 1), w.bs * w.k_max
     ib = (4 * w.bs + 15) // 16 * 16
-    rs = 16 * rows_t + 16 * rows_d + 8 * 16 * rows_t
-    req_cnt = rs + 8 * 16 * w.bs
+    rs = 16 * rows_t + 16 * rows_d + 8 * 128 * rows_t
+    req_cnt = rs + 8 * 128 * w.bs
     ctrl = req_cnt + 3 * ib
     assert ctrl + 32 == sd.sd_verify_workspace_bytes(w.bs, w.k_max)
-    for off, size in ((rs, 8 * 16 * w.bs), (req_cnt, 4 * w.bs), (req_cnt + ib, 4 * w.bs),
+    for off, size in ((rs, 8 * 128 * w.bs), (req_cnt, 4 * w.bs), (req_cnt + ib, 4 * w.bs),
                       (req_cnt + 2 * ib, 4 * w.bs), (ctrl, 32)):
         assert int(ws[off:off + size].count_nonzero()) == 0
 
