@@ -1073,18 +1073,29 @@ struct Control {
 
   // Draw from p of target row c0 + a (its per-chunk statistics give the
   // chunk weights; only the crossing chunk is read again).
-  __device__ int bonus(size_t trow, const DrawRows<Raw>& w, float ufin) const {
+  // This lane's block of the chunk statistics of target row trow (all
+  // requested before any is used).
+  __device__ void load_stats(size_t trow, float2 (&st)[kCpl]) const {
     const float2* stc = p.st_c + trow * kStatStride;
     const int nst = NS * G.spw;
-    // all of a lane's chunk statistics are requested before any is used
     const int cpl = (nst + 31) / 32, b0 = min(nst, lane * cpl), b1 = min(nst, b0 + cpl);
-    float2 st[kCpl];
 #pragma unroll
     for (int q = 0; q < kCpl; ++q) {
       int ub = 0, ue = 0;
       if (q < cpl && b0 + q < b1) stat_units(G, b0 + q, ub, ue);
       st[q] = ub < ue ? __ldcg(stc + b0 + q) : make_float2(-INFINITY, 0.0f);
     }
+  }
+
+  __device__ int bonus(size_t trow, const DrawRows<Raw>& w, float ufin) const {
+    float2 st[kCpl];
+    load_stats(trow, st);
+    return bonus(st, w, ufin);
+  }
+
+  // Draw from p with the row's chunk statistics already in hand.
+  __device__ int bonus(const float2 (&st)[kCpl], const DrawRows<Raw>& w, float ufin) const {
+    const int nst = NS * G.spw;
     unsigned long long wv[kCpl];
 #pragma unroll
     for (int q = 0; q < kCpl; ++q)
@@ -1128,6 +1139,9 @@ struct Control {
     float4 ts_l = make_float4(0.0f, 1.0f, 0.0f, 0.0f), ds_l = make_float4(0.0f, 1.0f, 0.0f, 0.0f);
     if (lane <= n) ts_l = __ldcg(reinterpret_cast<const float4*>(p.st_t + c0 + lane));
     if (lane < n && !greedy) ds_l = __ldcg(reinterpret_cast<const float4*>(p.st_d + d0 + lane));
+    // the bonus row's chunk statistics, in case every slot is accepted
+    float2 st_bonus[kCpl];
+    if (!greedy) load_stats(static_cast<size_t>(c0 + n), st_bonus);
     bool acc = true;
     if (lane < n) {
       const int j = lane;
@@ -1190,8 +1204,7 @@ struct Control {
       } else if (reject) {
         residual = true;
       } else {
-        pick = bonus(static_cast<size_t>(c0 + a), make_rows<T, VEC>(p, C.cu, i, a, tau, ts, ds, false),
-                     ufin);
+        pick = bonus(st_bonus, make_rows<T, VEC>(p, C.cu, i, a, tau, ts, ds, false), ufin);
       }
     }
     // outputs: the accepted draft tokens, the final token (a residual one is
@@ -1219,7 +1232,6 @@ struct Control {
   // complete; find the crossing chunk and walk it.
   __device__ void finish(int e, int i, int a, const float4& ts, const float4& ds, float ufin) const {
     const int c0 = C.cu[i];
-    const DrawRows<Raw> w = make_rows<T, VEC>(p, C.cu, i, a, C.tau[i], ts, ds, true);
     unsigned long long* rs = p.rs + static_cast<size_t>(e) * kStatStride;
     const int nst = NS * G.spw;
     const int cpl = (nst + 31) / 32, b0 = min(nst, lane * cpl), b1 = min(nst, b0 + cpl);
@@ -1230,6 +1242,7 @@ struct Control {
       if (q < cpl && b0 + q < b1) stat_units(G, b0 + q, ub, ue);
       wv[q] = ub < ue ? __ldcg(rs + b0 + q) : 0ull;
     }
+    const DrawRows<Raw> w = make_rows<T, VEC>(p, C.cu, i, a, C.tau[i], ts, ds, true);
     int c;
     unsigned long long th;
     int pick;
