@@ -758,7 +758,7 @@ struct Streamer {
   // Slice unit u: this warp's part of a listed residual draw, summed per
   // statistics chunk in 2^56 fixed point into the draw's chunk sums.
   __device__ void slice(int u, unsigned long long* sbuf) {
-    const int e = (u >> 18) & 0xFFF, s = (u >> 16) & 3, i = (u >> 4) & 0xFFF, a = u & 15;
+    const int s = (u >> 16) & 3, i = (u >> 4) & 0xFFF, a = u & 15;
     const int c0 = C.cu[i];
     const float4 ts = __ldcg(reinterpret_cast<const float4*>(p.st_t + c0 + a));
     const float4 ds = __ldcg(reinterpret_cast<const float4*>(p.st_d + c0 - i + a));
