@@ -213,6 +213,33 @@ sd_status sd_verify_ex(const void* target_logits, const void* draft_logits, sd_d
                        int* out_tokens, float* probs_out, int* err_flag, void* workspace,
                        size_t ws_bytes, const sd_launch_cfg* cfg, void* stream);
 
+/* ------------------------------------------------------------------------
+ * sd_verify_noalloc -- sd_verify without a caller workspace.  The pages have
+ * no counterpart to this entry point: it exists for callers that may not
+ * allocate device memory around the step.
+ *
+ * Same arguments and outputs as sd_verify, minus workspace/ws_bytes.  The
+ * workspace is a file-scope device array of SD_NOALLOC_SCRATCH_BYTES inside
+ * the library (static device memory, no allocation at call time).  Its
+ * address is looked up once per device with cudaGetSymbolAddress on the
+ * first call on that device: make that first call before any stream
+ * capture.  Each call clears, on `stream`, the part of the scratch that must
+ * start at zero (the residual sums and the counters), then runs sd_verify on
+ * it.  Calls that overlap in time on one device share the scratch and race:
+ * issue them on one stream, or order them.
+ * Errors: SD_ERR_UNSUPPORTED when sd_verify_workspace_bytes(bs, k_max)
+ * exceeds SD_NOALLOC_SCRATCH_BYTES (about 1770 requests at k_max = 7; the
+ * reason is in sd_last_error_string()); SD_ERR_CUDA when the lookup or the
+ * clear fails; otherwise as sd_verify.
+ * ---------------------------------------------------------------------- */
+#define SD_NOALLOC_SCRATCH_BYTES (16u << 20) /* 16 MiB */
+
+sd_status sd_verify_noalloc(const void* target_logits, const void* draft_logits, sd_dtype dt,
+                            int V, const int* draft_ids, const float* uniforms,
+                            const float* temps, const int* cu_seqlens, int bs, int k_max,
+                            int* accepted_len, int* out_tokens, float* probs_out, int* err_flag,
+                            void* stream);
+
 /* Launch shape sd_verify_ex would use for (V, dt, bs) and `req` (NULL =
  * automatic) on the current device.  Host-only query. */
 sd_status sd_verify_launch_info(int V, sd_dtype dt, int bs, const sd_launch_cfg* req,
@@ -221,8 +248,9 @@ sd_status sd_verify_launch_info(int V, sd_dtype dt, int bs, const sd_launch_cfg*
 const char* sd_status_string(sd_status s);
 
 /* Name and text of the last CUDA error an entry point returned SD_ERR_CUDA
- * for, on the calling host thread ("no error" if none).  The pointer stays
- * valid until the thread's next failing call. */
+ * for, or the reason sd_verify_noalloc refused a call, on the calling host
+ * thread ("no error" if none).  The pointer stays valid until the thread's
+ * next failing call. */
 const char* sd_last_error_string(void);
 
 int sd_abi_version(void);

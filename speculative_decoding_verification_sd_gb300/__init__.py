@@ -21,7 +21,7 @@ from typing import Optional
 import torch
 
 from . import _lib
-from ._lib import (SD_BF16, SD_DEV_ERR_CONF, SD_DEV_ERR_COST, SD_DEV_ERR_CU_SEQLENS,  # noqa: F401
+from ._lib import (SD_NOALLOC_SCRATCH_BYTES, SD_BF16, SD_DEV_ERR_CONF, SD_DEV_ERR_COST, SD_DEV_ERR_CU_SEQLENS,  # noqa: F401
                    SD_DEV_ERR_DRAFT_ID, SD_DEV_ERR_DRAFT_LENS, SD_DEV_ERR_LOGITS,
                    SD_DEV_ERR_TEMP, SD_DEV_ERR_UNIFORM, SD_ERR_CUDA,
                    SD_ERR_DEVICE_CHECK, SD_ERR_INVALID_ARG, SD_ERR_SHAPE, SD_ERR_UNSUPPORTED,
@@ -29,7 +29,7 @@ from ._lib import (SD_BF16, SD_DEV_ERR_CONF, SD_DEV_ERR_COST, SD_DEV_ERR_CU_SEQL
                    SD_MODE_ADAPTIVE, SD_MODE_ALL_SLOTS, SD_OK, SdError, sd_launch_cfg)
 
 __all__ = [
-    "sd_plan", "sd_verify", "sd_verify_ex", "sd_plan_workspace_bytes",
+    "sd_plan", "sd_verify", "sd_verify_ex", "sd_verify_noalloc", "sd_plan_workspace_bytes",
     "sd_verify_workspace_bytes", "sd_verify_launch_info", "plan", "verify", "PlanResult",
     "VerifyResult", "SdError", "build", "library_path", "verify_workspace",
 ]
@@ -127,6 +127,16 @@ def sd_verify_ex(target_logits, draft_logits, dt, V, draft_ids, uniforms, temps,
                                   _ptr(probs_out), _ptr(err_flag), _ptr(workspace), int(ws_bytes),
                                   _cfg(cfg), _stream(stream))
     return _lib.check("sd_verify_ex", st)
+
+
+def sd_verify_noalloc(target_logits, draft_logits, dt, V, draft_ids, uniforms, temps, cu_seqlens,
+                      bs, k_max, accepted_len, out_tokens, probs_out, err_flag, stream=None):
+    st = _lib.load().sd_verify_noalloc(_ptr(target_logits), _ptr(draft_logits), _dt(dt), int(V),
+                                       _ptr(draft_ids), _ptr(uniforms), _ptr(temps),
+                                       _ptr(cu_seqlens), int(bs), int(k_max), _ptr(accepted_len),
+                                       _ptr(out_tokens), _ptr(probs_out), _ptr(err_flag),
+                                       _stream(stream))
+    return _lib.check("sd_verify_noalloc", st)
 
 
 def sd_verify_launch_info(V, dt, bs, threads=0, blocks=0, blocks_per_sm=0) -> dict:

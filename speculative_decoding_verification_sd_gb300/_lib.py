@@ -35,8 +35,9 @@ SD_MAX_V = 1 << 22
 
 # Every symbol include/sd.h declares.
 EXPORTS = ("sd_plan_workspace_bytes", "sd_plan", "sd_verify_workspace_bytes", "sd_verify",
-           "sd_verify_ex", "sd_verify_launch_info", "sd_status_string", "sd_last_error_string",
-           "sd_abi_version")
+           "sd_verify_ex", "sd_verify_noalloc", "sd_verify_launch_info", "sd_status_string",
+           "sd_last_error_string", "sd_abi_version")
+SD_NOALLOC_SCRATCH_BYTES = 16 << 20  # include/sd.h
 
 
 class sd_launch_cfg(ctypes.Structure):
@@ -82,6 +83,8 @@ def load(path: Path | None = None) -> ctypes.CDLL:
     lib.sd_verify_ex.restype = i32
     lib.sd_verify_ex.argtypes = [P, P, i32, i32, P, P, P, P, i32, i32, P, P, P, P, P, sz,
                                  ctypes.POINTER(sd_launch_cfg), P]
+    lib.sd_verify_noalloc.restype = i32
+    lib.sd_verify_noalloc.argtypes = [P, P, i32, i32, P, P, P, P, i32, i32, P, P, P, P, P]
     lib.sd_verify_launch_info.restype = i32
     lib.sd_verify_launch_info.argtypes = [i32, i32, i32, ctypes.POINTER(sd_launch_cfg),
                                           ctypes.POINTER(sd_launch_cfg), ctypes.POINTER(sz)]
@@ -96,7 +99,7 @@ def status_string(status: int) -> str:
 def check(fn: str, status: int) -> int:
     if status != SD_OK:
         text = status_string(status)
-        if status == SD_ERR_CUDA:
+        if status == SD_ERR_CUDA or (fn == "sd_verify_noalloc" and status == SD_ERR_UNSUPPORTED):
             text += ": " + load().sd_last_error_string().decode()
         raise SdError(fn, status, text)
     return status

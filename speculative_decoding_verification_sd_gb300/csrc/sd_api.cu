@@ -93,6 +93,11 @@ sd_status shape_for(int V, sd_dtype dt, int bs, const sd_launch_cfg* cfg, bool v
 
 }  // namespace
 
+namespace sdk {
+size_t verify_ws_zero_offset(int bs, int k_max) { return ws_layout(bs, k_max).rs; }
+void set_last_error(const char* msg) { snprintf(g_last_error, sizeof g_last_error, "%s", msg); }
+}  // namespace sdk
+
 extern "C" {
 
 int sd_abi_version(void) { return 1; }

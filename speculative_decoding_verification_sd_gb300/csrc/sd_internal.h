@@ -91,4 +91,10 @@ cudaError_t choose_verify_shape(int V, int elem, int bs, const sd_launch_cfg* re
 cudaError_t launch_verify(const VerifyParams& p, int elem, const VerifyShape& shape,
                           cudaStream_t s);
 
+// Offset of the first workspace byte that must be zero before a call (the
+// residual sums and every counter sit in [offset, sd_verify_workspace_bytes)).
+size_t verify_ws_zero_offset(int bs, int k_max);
+// Sets the message sd_last_error_string() returns on this host thread.
+void set_last_error(const char* msg);
+
 }  // namespace sdk

@@ -111,6 +111,21 @@ def test_verify_rejects_bad_arguments_on_host(lib):
                             ctypes.byref(bad_cfg), 0) == sd.SD_ERR_INVALID_ARG
 
 
+def test_noalloc_rejects_on_host(lib):
+    """sd_verify_noalloc refuses bad sizes before any CUDA call."""
+    import speculative_decoding_verification_sd_gb300 as sd
+    P = FAKE
+
+    def call(bs, k_max):
+        return lib.sd_verify_noalloc(P, P, 1, 1024, P, P, P, P, bs, k_max, P, P, None, P, 0)
+
+    assert call(0, 3) == sd.SD_ERR_INVALID_ARG
+    assert call(4, 16) == sd.SD_ERR_UNSUPPORTED
+    assert sd.sd_verify_workspace_bytes(4096, 15) > sd.SD_NOALLOC_SCRATCH_BYTES
+    assert call(4096, 15) == sd.SD_ERR_UNSUPPORTED
+    assert b"static scratch" in lib.sd_last_error_string()
+
+
 def test_binding_refuses_host_tensors(lib):
     import torch
     import speculative_decoding_verification_sd_gb300 as sd
