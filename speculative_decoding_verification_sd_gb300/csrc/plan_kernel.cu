@@ -32,6 +32,8 @@ namespace {
 constexpr int NT = kPlanThreads;
 constexpr int NW = NT / 32;
 constexpr unsigned long long kSentinel = ~0ull;
+constexpr int kBuckets = 4096;     // bucket sort: buckets over the key range
+constexpr int kBucketMax = 256;    // larger buckets fall back to the merge sort
 constexpr float kFix = 281474976710656.0f;  // 2^48
 
 struct PlanShared {
@@ -41,6 +43,8 @@ struct PlanShared {
   int err;
   int B;
   unsigned long long scan_total;
+  unsigned int hmin, hmax;
+  int cmax;
 };
 
 __device__ unsigned long long block_excl_scan_u64(unsigned long long v, PlanShared& sh,
@@ -55,14 +59,14 @@ __device__ unsigned long long block_excl_scan_u64(unsigned long long v, PlanShar
   if (lane == 31) sh.red_u64[warp] = inc;
   __syncthreads();
   if (warp == 0) {
-    unsigned long long w = sh.red_u64[lane];
+    unsigned long long w = lane < NW ? sh.red_u64[lane] : 0ull;
     unsigned long long wi = w;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       unsigned long long t = __shfl_up_sync(kFull, wi, o);
       if (lane >= o) wi += t;
     }
-    sh.red_u64[lane] = wi - w;  // exclusive prefix of warp totals
+    if (lane < NW) sh.red_u64[lane] = wi - w;  // exclusive prefix of warp totals
     if (lane == 31) sh.scan_total = wi;
   }
   __syncthreads();
@@ -79,63 +83,32 @@ __device__ int block_excl_scan_i32(int v, PlanShared& sh, int* total) {
   return static_cast<int>(r);
 }
 
-__device__ unsigned long long block_max_u64(unsigned long long v, PlanShared& sh) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  v = warp_max_u64(v);
-  if (lane == 0) sh.red_u64[warp] = v;
-  __syncthreads();
-  if (warp == 0) {
-    unsigned long long w = warp_max_u64(sh.red_u64[lane]);
-    if (lane == 0) sh.scan_total = w;
-  }
-  __syncthreads();
-  const unsigned long long r = sh.scan_total;
-  __syncthreads();
-  return r;
+// round(s * 2^48) to nearest even for 0 <= s <= 1 (the value
+// __float2ull_rn(s * 2^48) has), in integer arithmetic.
+__device__ __forceinline__ unsigned long long fix48(float s) {
+  const uint32_t b = __float_as_uint(s);
+  const int e = static_cast<int>((b >> 23) & 0xFFu);
+  if (e == 0) return 0ull;  // zero, or below 2^-126
+  const unsigned long long m = (b & 0x7FFFFFu) | 0x800000u;  // s = m * 2^(e - 150)
+  const int sh = e - 150 + 48;
+  if (sh >= 0) return m << sh;
+  if (sh < -25) return 0ull;  // s * 2^48 < 1/4
+  const int k = -sh;
+  const unsigned long long q = m >> k, r = m & ((1ull << k) - 1), half = 1ull << (k - 1);
+  return q + ((r > half || (r == half && (q & 1ull))) ? 1ull : 0ull);
 }
 
-__device__ float block_max_f32(float v, PlanShared& sh) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  v = warp_max(v);
-  if (lane == 0) sh.red_f32[warp] = v;
-  __syncthreads();
-  if (warp == 0) {
-    float w = warp_max(sh.red_f32[lane]);
-    if (lane == 0) sh.red_f32[0] = w;
-  }
-  __syncthreads();
-  const float r = sh.red_f32[0];
-  __syncthreads();
-  return r;
-}
-
-// Exclusive running maximum over the threads' values in thread order.
-__device__ float block_excl_max_scan(float v, PlanShared& sh) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  float inc = v;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const float t = __shfl_up_sync(kFull, inc, o);
-    if (lane >= o) inc = fmaxf(inc, t);
-  }
-  if (lane == 31) sh.red_f32[warp] = inc;
-  __syncthreads();
-  if (warp == 0) {
-    float wi = sh.red_f32[lane];
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const float t = __shfl_up_sync(kFull, wi, o);
-      if (lane >= o) wi = fmaxf(wi, t);
-    }
-    const float ex = __shfl_up_sync(kFull, wi, 1);
-    sh.red_f32[lane] = lane == 0 ? -INFINITY : ex;
-  }
-  __syncthreads();
-  const float lane_ex_raw = __shfl_up_sync(kFull, inc, 1);
-  const float lane_ex = lane == 0 ? -INFINITY : lane_ex_raw;
-  const float r = fmaxf(sh.red_f32[warp], lane_ex);
-  __syncthreads();
-  return r;
+// x correctly rounded to fp32 (nearest even), in integer arithmetic (the
+// value __ull2float_rn(x) has).
+__device__ __forceinline__ float u64_to_f32(unsigned long long x) {
+  if (x < (1ull << 24)) return static_cast<float>(static_cast<uint32_t>(x));
+  const int k = 63 - __clzll(static_cast<long long>(x)) - 23;  // bits dropped
+  unsigned long long q = x >> k;
+  const unsigned long long r = x & ((1ull << k) - 1), half = 1ull << (k - 1);
+  q += (r > half || (r == half && (q & 1ull))) ? 1ull : 0ull;  // q <= 2^24
+  // q * 2^k: q converts exactly; the power of two goes into the exponent field
+  return __uint_as_float(__float_as_uint(static_cast<float>(static_cast<uint32_t>(q))) +
+                         (static_cast<uint32_t>(k) << 23));
 }
 
 // Loads draft lengths, checks them and forms packed offsets off[0..n].
@@ -204,7 +177,7 @@ __device__ unsigned long long* merge_runs(unsigned long long* a, unsigned long l
     const int o_beg = static_cast<int>(threadIdx.x) * ipt;
     const int o_end = min(n, o_beg + ipt);
     for (int o = o_beg; o < o_end;) {
-      const int base = (o / (2 * w)) * (2 * w);
+      const int base = o & ~(2 * w - 1);  // w is a power of two
       const int blk_end = min(base + 2 * w, o_end);
       const unsigned long long* A = a + base;
       const unsigned long long* Bv = a + base + w;
@@ -230,58 +203,172 @@ __device__ unsigned long long* merge_runs(unsigned long long* a, unsigned long l
   return a;
 }
 
-// Budget argmax over B in [0, Bmax] on the sorted keys.  cm receives the
-// monotone cost at T+B.  Returns B* (smallest maximiser).
-__device__ int budget_argmax(const unsigned long long* sorted, int Bmax, int R, int T,
-                             const float* cost, float* cm, PlanShared& sh) {
-  // cost'[n] = max(cost[1..n]): the part below T is a plain maximum.
-  float m0 = -INFINITY;
-  for (int n = 1 + threadIdx.x; n < T; n += NT) m0 = fmaxf(m0, cost[n]);
-  m0 = block_max_f32(m0, sh);
-  // Running maximum over cost[T..T+Bmax] (chunked scan; entries must be > 0).
+// Sort of the n (power of two) keys by distribution: each real key goes to
+// one of kBuckets buckets by its high word (monotone in the key), buckets
+// are laid out by an exclusive scan of their counts, and every key then
+// finds its place inside its bucket by counting the bucket's smaller keys
+// (keys are distinct: the low word is the slot index).  The real keys end
+// up ascending in keys[0..N) (tmp is scratch); sentinels are dropped.
+// Returns false (keys untouched) when a bucket holds more than kBucketMax
+// keys, e.g. many equal survivals; the caller then merges the runs instead.
+__device__ bool bucket_sort(unsigned long long* keys, unsigned long long* tmp, int n, int* cnt,
+                            int* end, PlanShared& sh) {
+  unsigned int lo = 0xFFFFFFFFu, hi = 0u;
+  for (int q = threadIdx.x; q < n; q += NT) {
+    const unsigned long long k = keys[q];
+    if (k != kSentinel) {
+      const unsigned int h = static_cast<unsigned int>(k >> 32);
+      lo = min(lo, h);
+      hi = max(hi, h);
+    }
+  }
+  for (int q = threadIdx.x; q < kBuckets; q += NT) cnt[q] = 0;
+  if (threadIdx.x == 0) { sh.hmin = 0xFFFFFFFFu; sh.hmax = 0u; sh.cmax = 0; }
+  __syncthreads();
+  lo = __reduce_min_sync(kFull, lo);
+  hi = __reduce_max_sync(kFull, hi);
+  if ((threadIdx.x & 31) == 0) {
+    atomicMin(&sh.hmin, lo);
+    atomicMax(&sh.hmax, hi);
+  }
+  __syncthreads();
+  const unsigned int hmin = sh.hmin;
+  if (hmin > sh.hmax) return true;  // no real key
+  const unsigned int range = sh.hmax - hmin;
+  int shift = 0;
+  while ((range >> shift) >= static_cast<unsigned int>(kBuckets)) ++shift;
+  for (int q = threadIdx.x; q < n; q += NT) {
+    const unsigned long long k = keys[q];
+    if (k != kSentinel) atomicAdd(&cnt[(static_cast<unsigned int>(k >> 32) - hmin) >> shift], 1);
+  }
+  __syncthreads();
+  // bucket offsets (exclusive scan, kBuckets / NT consecutive buckets per thread)
+  constexpr int kPer = kBuckets / NT;
+  int c[kPer], local = 0, cm = 0;
+#pragma unroll
+  for (int q = 0; q < kPer; ++q) {
+    c[q] = cnt[threadIdx.x * kPer + q];
+    local += c[q];
+    cm = max(cm, c[q]);
+  }
+  cm = __reduce_max_sync(kFull, cm);
+  if ((threadIdx.x & 31) == 0) atomicMax(&sh.cmax, cm);
+  int run = block_excl_scan_i32(local, sh, nullptr);  // synchronises the block
+  if (sh.cmax > kBucketMax) return false;
+#pragma unroll
+  for (int q = 0; q < kPer; ++q) {
+    run += c[q];
+    cnt[threadIdx.x * kPer + q] = run - c[q];  // the bucket's fill cursor
+    end[threadIdx.x * kPer + q] = run;
+  }
+  __syncthreads();
+  for (int q = threadIdx.x; q < n; q += NT) {
+    const unsigned long long k = keys[q];
+    if (k != kSentinel) tmp[atomicAdd(&cnt[(static_cast<unsigned int>(k >> 32) - hmin) >> shift], 1)] = k;
+  }
+  __syncthreads();
+  const int total = end[kBuckets - 1];
+  // each key's place: its bucket's start plus the bucket's keys below it
+  for (int x = threadIdx.x; x < total; x += NT) {
+    const unsigned long long v = tmp[x];
+    const int bk = static_cast<int>((static_cast<unsigned int>(v >> 32) - hmin) >> shift);
+    const int e = end[bk], b0 = bk > 0 ? end[bk - 1] : 0;
+    int r = 0;
+    for (int y = b0; y < e; ++y) r += tmp[y] < v;
+    keys[b0 + r] = v;
+  }
+  __syncthreads();
+  return true;
+}
+
+// Budget argmax over B in [0, Bmax] on the sorted keys.  cm[b] holds
+// cost[T+b] (loaded at kernel start) and lm each thread's maximum of its share
+// of cost[1..T) (lm_bad: one of those was not finite and positive).  Thread t
+// owns the budgets B in [vb, ve); one combined block scan gives every thread
+// its prefix of the survival sum (exact, 2^48 fixed point) and of the running
+// cost maximum (the monotone cost'[n] = max(cost[1..n])).  Returns B*
+// (smallest maximiser).
+__device__ int budget_argmax(const unsigned long long* sorted, int Bmax, int R, float* cm,
+                             float lm, int lm_bad, PlanShared& sh) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int cnt = Bmax + 1;
   const int chunk = (cnt + NT - 1) / NT;
-  const int beg = min(cnt, static_cast<int>(threadIdx.x) * chunk);
-  const int end = min(cnt, beg + chunk);
-  float lm = -INFINITY;
-  int bad = 0;
-  for (int b = beg; b < end; ++b) {
-    const float c = cost[T + b];
+  const int vb = min(cnt, static_cast<int>(threadIdx.x) * chunk);
+  const int ve = min(cnt, vb + chunk);
+  int bad = lm_bad;
+  float cmax = -INFINITY;
+  unsigned long long ls = 0;
+  for (int B = vb; B < ve; ++B) {
+    const float c = cm[B];
     if (!(isfinite(c) && c > 0.0f)) bad = 1;
-    lm = fmaxf(lm, c);
-    cm[b] = lm;
+    cmax = fmaxf(cmax, c);
+    cm[B] = cmax;  // running maximum within the chunk
+    if (B < Bmax) ls += fix48(__uint_as_float(~static_cast<uint32_t>(sorted[B] >> 32)));
   }
+  // combined scan: exclusive sums, exclusive running maxima, total of lm
+  unsigned long long si = ls;
+  float mi = cmax, m0 = lm;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const unsigned long long ts = __shfl_up_sync(kFull, si, o);
+    const float tm = __shfl_up_sync(kFull, mi, o);
+    if (lane >= o) {
+      si += ts;
+      mi = fmaxf(mi, tm);
+    }
+    m0 = fmaxf(m0, __shfl_xor_sync(kFull, m0, o));
+  }
+  if (lane == 31) {
+    sh.red_u64[warp] = si;
+    sh.red_f32[warp] = mi;
+  }
+  if (lane == 0) sh.red_i32[warp] = __float_as_int(m0);
   if (__syncthreads_or(bad) && threadIdx.x == 0) sh.err |= SD_DEV_ERR_COST;
-  // Exclusive running maximum across the chunks, folded into each chunk.
-  const float excl = fmaxf(block_excl_max_scan(lm, sh), m0);
-  for (int b = beg; b < end; ++b) cm[b] = fmaxf(cm[b], excl);
-  __syncthreads();
-  // E(B) = R + sum_{r<B} s_(r) in 2^-48 fixed point; objective and argmax.
-  const int vchunk = (Bmax + NT - 1) / NT;
-  const int vb = min(Bmax, static_cast<int>(threadIdx.x) * vchunk);
-  const int ve = min(Bmax, vb + vchunk);
-  unsigned long long local = 0;
-  for (int r = vb; r < ve; ++r) {
-    const float s = __uint_as_float(~static_cast<uint32_t>(sorted[r] >> 32));
-    local += __float2ull_rn(s * kFix);
+  if (warp == 0) {
+    unsigned long long ws = lane < NW ? sh.red_u64[lane] : 0ull;
+    float wm = lane < NW ? sh.red_f32[lane] : -INFINITY;
+    float w0 = lane < NW ? __int_as_float(sh.red_i32[lane]) : -INFINITY;
+    const unsigned long long ws_in = ws;
+    const float wm_in = wm;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const unsigned long long ts = __shfl_up_sync(kFull, ws, o);
+      const float tm = __shfl_up_sync(kFull, wm, o);
+      if (lane >= o) {
+        ws += ts;
+        wm = fmaxf(wm, tm);
+      }
+      w0 = fmaxf(w0, __shfl_xor_sync(kFull, w0, o));
+    }
+    const float wm_ex = __shfl_up_sync(kFull, wm, 1);
+    if (lane < NW) {
+      sh.red_u64[lane] = ws - ws_in;                    // exclusive warp sums
+      sh.red_f32[lane] = lane == 0 ? -INFINITY : wm_ex;  // exclusive warp maxima
+    }
+    if (lane == 0) sh.red_i32[0] = __float_as_int(w0);
+    (void)wm_in;
   }
-  unsigned long long E = block_excl_scan_u64(local, sh, nullptr) +
-                         static_cast<unsigned long long>(R) * 281474976710656ull;
+  __syncthreads();
+  const float mi_up = __shfl_up_sync(kFull, mi, 1);  // every lane takes part
+  const float mi_ex = lane == 0 ? -INFINITY : mi_up;
+  const float mpre = fmaxf(fmaxf(sh.red_f32[warp], mi_ex), __int_as_float(sh.red_i32[0]));
+  unsigned long long E = sh.red_u64[warp] + (si - ls) + static_cast<unsigned long long>(R) * 281474976710656ull;
+  // objectives of this thread's budgets; the largest (smallest B on ties) wins
   unsigned long long best = 0;
-  auto consider = [&](int B, unsigned long long e) {
-    const float obj = (__ull2float_rn(e) * (1.0f / kFix)) / cm[B];
+  for (int B = vb; B < ve; ++B) {
+    const float c = fmaxf(cm[B], mpre);
+    const float obj = (u64_to_f32(E) * (1.0f / kFix)) / c;
     const unsigned long long key = (static_cast<unsigned long long>(__float_as_uint(obj)) << 32) |
                                    static_cast<unsigned long long>(0xFFFFFFFFu - static_cast<uint32_t>(B));
     best = key > best ? key : best;
-  };
-  if (threadIdx.x == 0) consider(0, E);
-  for (int r = vb; r < ve; ++r) {
-    const float s = __uint_as_float(~static_cast<uint32_t>(sorted[r] >> 32));
-    E += __float2ull_rn(s * kFix);
-    consider(r + 1, E);
+    if (B < Bmax) E += fix48(__uint_as_float(~static_cast<uint32_t>(sorted[B] >> 32)));
   }
-  best = block_max_u64(best, sh);
-  return static_cast<int>(0xFFFFFFFFu - static_cast<uint32_t>(best & 0xFFFFFFFFull));
+  best = warp_max_u64(best);
+  if (threadIdx.x == 0) sh.scan_total = 0;
+  __syncthreads();
+  if (lane == 0) atomicMax(&sh.scan_total, best);
+  __syncthreads();
+  return static_cast<int>(0xFFFFFFFFu - static_cast<uint32_t>(sh.scan_total & 0xFFFFFFFFull));
 }
 
 __global__ void __launch_bounds__(NT, 1) plan_kernel(const PlanParams p) {
@@ -293,12 +380,27 @@ __global__ void __launch_bounds__(NT, 1) plan_kernel(const PlanParams p) {
   float* cm = reinterpret_cast<float*>(keysB + NPm);        // [NPm + 1]
   int* lens = reinterpret_cast<int*>(cm + NPm + 1);        // [NPm / P]
   int* off = lens + NPm / p.P;                              // [NPm / P + 1]
-  uint8_t* sel = reinterpret_cast<uint8_t*>(off + NPm / p.P + 1);  // [NP]
+  int* bcnt = off + NPm / p.P + 1;                          // [2 * kBuckets]
+  uint8_t* sel = reinterpret_cast<uint8_t*>(bcnt + 2 * kBuckets);  // [NP]
 
   if (threadIdx.x == 0) { sh.err = 0; sh.B = 0; }
+  const int L = p.cost_len - 1;
+  // The cost table is read first, so that its loads overlap the lengths':
+  // cost[T+b] for every budget b the call can reach, and each thread's
+  // maximum of its share of cost[1..T).
+  float lm = -INFINITY;
+  int lm_bad = 0;
+  if (p.mode != SD_MODE_ALL_SLOTS) {
+    for (int n = 1 + threadIdx.x; n < p.T; n += NT) {
+      const float c = p.cost[n];
+      if (!(isfinite(c) && c > 0.0f)) lm_bad = 1;
+      lm = fmaxf(lm, c);
+    }
+    const int bmax = min(NPm, L - p.T);
+    for (int b = threadIdx.x; b <= bmax; b += NT) cm[b] = p.cost[p.T + b];
+  }
   __syncthreads();
 
-  const int L = p.cost_len - 1;
   const int nreq = p.NP / p.P;  // padded request count (power of two)
   // Current slots: lengths and offsets (padded requests have no slots).
   int N = load_lengths(p.lens, p.bs, p.k_max, lens, off, sh);
@@ -316,10 +418,12 @@ __global__ void __launch_bounds__(NT, 1) plan_kernel(const PlanParams p) {
       __syncthreads();
       if (sh.err == 0) {
         build_keys(p.budget_conf, lens, off, nb, p.P, Nb, keysA, reinterpret_cast<float*>(keysB), sh);
-        const unsigned long long* sorted = merge_runs(keysA, keysB, p.NPb, p.P);
+        const unsigned long long* sorted = bucket_sort(keysA, keysB, p.NPb, bcnt, bcnt + kBuckets, sh)
+                                               ? keysA
+                                               : merge_runs(keysA, keysB, p.NPb, p.P);
         const int Bmax_b = min(Nb, L - p.T);
         int Bb = 0;
-        if (sh.err == 0) Bb = budget_argmax(sorted, Bmax_b, p.bs, p.T, p.cost, cm, sh);
+        if (sh.err == 0) Bb = budget_argmax(sorted, Bmax_b, p.bs, cm, lm, lm_bad, sh);
         B = min(Bb, min(N, L - p.T));
       }
       // Restore the current request lengths.
@@ -329,9 +433,11 @@ __global__ void __launch_bounds__(NT, 1) plan_kernel(const PlanParams p) {
     }
     if (sh.err == 0) {
       build_keys(p.conf, lens, off, nreq, p.P, N, keysA, reinterpret_cast<float*>(keysB), sh);
-      const unsigned long long* sorted = merge_runs(keysA, keysB, p.NP, p.P);
+      const unsigned long long* sorted = bucket_sort(keysA, keysB, p.NP, bcnt, bcnt + kBuckets, sh)
+                                             ? keysA
+                                             : merge_runs(keysA, keysB, p.NP, p.P);
       if (!p.budget_conf && sh.err == 0)
-        B = budget_argmax(sorted, min(N, L - p.T), p.bs, p.T, p.cost, cm, sh);
+        B = budget_argmax(sorted, min(N, L - p.T), p.bs, cm, lm, lm_bad, sh);
       // Selection: the B best ranks.
       for (int q = threadIdx.x; q < p.NP; q += NT) sel[q] = 0;
       __syncthreads();
@@ -378,7 +484,7 @@ __global__ void __launch_bounds__(NT, 1) plan_kernel(const PlanParams p) {
 size_t plan_smem_bytes(const PlanParams& p) {
   const size_t NPm = static_cast<size_t>(p.NP > p.NPb ? p.NP : p.NPb);
   return 2 * NPm * 8 + (NPm + 1) * 4 + (NPm / p.P) * 4 + (NPm / p.P + 1) * 4 +
-         static_cast<size_t>(p.NP) + 16;
+         static_cast<size_t>(kBuckets) * 8 + static_cast<size_t>(p.NP) + 16;
 }
 
 cudaError_t launch_plan(const PlanParams& p, cudaStream_t s) {
