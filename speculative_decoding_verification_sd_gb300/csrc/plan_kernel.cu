@@ -1,11 +1,12 @@
 // plan_kernel.cu -- K1: the planning stage of adaptive verification in one
 // CTA of 1024 threads, everything resident in shared memory.
 //
-//   survival   a = sigmoid(conf), s_j = s_{j-1} * a_j front to back
+//   survival   a = sigmoid(conf), s_j = a_0 * ... * a_j along the draft
 //              [fosworld blog "추측 디코딩과 vLLM 적응형 검증", "동작" step 1]
-//   top-B      all slots ranked by (s desc, packed index asc); each request's
-//              survival list is already sorted, so the sort is a merge of
-//              pre-sorted runs (merge path, Odeh et al. 2012)
+//   top-B      all slots ranked by (s desc, packed index asc): a bucket sort
+//              on the key's high word, with a merge of the per-request runs
+//              (each already sorted; merge path, Odeh et al. 2012) when a
+//              bucket overflows
 //              ["동작" step 2; agentlenshq "vLLM DSpark을 활용한 적응형 검증",
 //               "DSpark 신뢰도 스케줄링 메커니즘" / Global Top-B Selection]
 //   budget     B* = smallest argmax_B (R + sum of the B best s) / cost'[T+B],
@@ -34,53 +35,71 @@ constexpr int NW = NT / 32;
 constexpr unsigned long long kSentinel = ~0ull;
 constexpr int kBuckets = 4096;     // bucket sort: buckets over the key range
 constexpr int kBucketMax = 256;    // larger buckets fall back to the merge sort
+constexpr unsigned kOneBits = 0x3F800000u;  // bit pattern of 1.0f
+constexpr int kBucketShift = 15;   // 2^15 ulps a bucket: 256 buckets a binade
+static_assert(kBuckets == 4 * NT, "four bucket counters a thread, moved as one 16-byte vector");
 constexpr float kFix = 281474976710656.0f;  // 2^48
 
 struct PlanShared {
-  unsigned long long red_u64[NW];
-  float red_f32[NW];
-  int red_i32[NW];
+  unsigned long long tot_u64[NW];  // per-warp totals of the block scans
+  float tot_f32[NW];
+  float tot_m0[NW];
+  int tot_i32[NW];
   int err;
-  int B;
-  unsigned long long scan_total;
-  unsigned int hmin, hmax;
-  int cmax;
+  unsigned long long best;         // budget argmax (packed objective, budget)
+  int cmax;                        // largest bucket of the bucket sort
 };
 
-__device__ unsigned long long block_excl_scan_u64(unsigned long long v, PlanShared& sh,
-                                                  unsigned long long* total) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  unsigned long long inc = v;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    unsigned long long t = __shfl_up_sync(kFull, inc, o);
-    if (lane >= o) inc += t;
-  }
-  if (lane == 31) sh.red_u64[warp] = inc;
-  __syncthreads();
-  if (warp == 0) {
-    unsigned long long w = lane < NW ? sh.red_u64[lane] : 0ull;
-    unsigned long long wi = w;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      unsigned long long t = __shfl_up_sync(kFull, wi, o);
-      if (lane >= o) wi += t;
-    }
-    if (lane < NW) sh.red_u64[lane] = wi - w;  // exclusive prefix of warp totals
-    if (lane == 31) sh.scan_total = wi;
-  }
-  __syncthreads();
-  const unsigned long long r = sh.red_u64[warp] + inc - v;
-  if (total) *total = sh.scan_total;
-  __syncthreads();
-  return r;
+__device__ __forceinline__ void cp_async4(void* dst, const void* src) {
+  const unsigned d = static_cast<unsigned>(__cvta_generic_to_shared(dst));
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;\n" ::"r"(d), "l"(src) : "memory");
 }
 
-__device__ int block_excl_scan_i32(int v, PlanShared& sh, int* total) {
-  unsigned long long t;
-  unsigned long long r = block_excl_scan_u64(static_cast<unsigned long long>(v), sh, &t);
-  if (total) *total = static_cast<int>(t);
-  return static_cast<int>(r);
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.wait_all;\n" ::: "memory");
+}
+
+template <typename U>
+__device__ __forceinline__ U warp_incl_scan(U v) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const U t = __shfl_up_sync(kFull, v, o);
+    if (lane >= o) v += t;
+  }
+  return v;
+}
+
+// Exclusive block scan of non-negative ints with one barrier: each warp scans
+// its values, lane 31 publishes the warp total in tot[warp], and after the
+// barrier every warp adds up the totals of the warps before it (and of all
+// warps) with two warp reductions.  tot must not be written again before
+// every thread has passed a later barrier.
+__device__ int block_scan_excl(int v, int* tot, int* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int inc = warp_incl_scan(v);
+  if (lane == 31) tot[warp] = inc;
+  __syncthreads();
+  const unsigned w = lane < NW ? static_cast<unsigned>(tot[lane]) : 0u;
+  const int before = static_cast<int>(__reduce_add_sync(kFull, lane < warp ? w : 0u));
+  if (total) *total = static_cast<int>(__reduce_add_sync(kFull, w));
+  return before + inc - v;
+}
+
+// Sum over the warp of values below 2^62 (the 2^48 fixed-point survival sums),
+// as three 32-bit warp reductions of 24-, 24- and 14-bit pieces.
+__device__ __forceinline__ unsigned long long warp_sum_u62(unsigned long long x) {
+  const unsigned lo = __reduce_add_sync(kFull, static_cast<unsigned>(x & 0xFFFFFFull));
+  const unsigned mid = __reduce_add_sync(kFull, static_cast<unsigned>((x >> 24) & 0xFFFFFFull));
+  const unsigned hi = __reduce_add_sync(kFull, static_cast<unsigned>(x >> 48));
+  return static_cast<unsigned long long>(lo) + (static_cast<unsigned long long>(mid) << 24) +
+         (static_cast<unsigned long long>(hi) << 48);
+}
+
+// Maximum over the warp of floats that are >= 0 or -inf: for those, the
+// order of the bit patterns read as signed ints is the order of the values.
+__device__ __forceinline__ float warp_max_nonneg(float x) {
+  return __int_as_float(__reduce_max_sync(kFull, __float_as_int(x)));
 }
 
 // round(s * 2^48) to nearest even for 0 <= s <= 1 (the value
@@ -111,60 +130,126 @@ __device__ __forceinline__ float u64_to_f32(unsigned long long x) {
                          (static_cast<uint32_t>(k) << 23));
 }
 
-// Loads draft lengths, checks them and forms packed offsets off[0..n].
-// Returns the total slot count N.
-__device__ int load_lengths(const int* lens_g, int n, int k_max, int* lens, int* off,
-                            PlanShared& sh) {
-  const int chunk = (n + NT - 1) / NT;
-  const int beg = min(n, static_cast<int>(threadIdx.x) * chunk);
-  const int end = min(n, beg + chunk);
+// Requests per thread in the contiguous chunks that the lengths are read in
+// (bs <= pow2ceil(bs) <= SD_MAX_PLAN_SLOTS).
+constexpr int kReqPer = SD_MAX_PLAN_SLOTS / NT;
+
+struct Chunk {
+  int beg, end;
+};
+
+__device__ __forceinline__ Chunk req_chunk(int n) {
+  const int c = (n + NT - 1) / NT;
+  const int beg = min(n, static_cast<int>(threadIdx.x) * c);
+  return {beg, min(n, beg + c)};
+}
+
+// Bucket of a key with high word h = ~bits(s), 0 <= s <= 1: 256 buckets for
+// each binade below 1, down to 2^-16; smaller survivals share the last
+// bucket.  Monotone in h, so ascending buckets hold ascending keys.  A NaN
+// survival (bad input, flagged) lands in the last bucket.
+__device__ __forceinline__ int bucket_of(unsigned int h) {
+  const unsigned int d = kOneBits - ~h;
+  return static_cast<int>(min(d >> kBucketShift, static_cast<unsigned int>(kBuckets - 1)));
+}
+
+// Issues the loads of this thread's chunk of draft lengths into registers.
+// The loads are volatile so that they stay ahead of the cost table's (whose
+// use stalls the thread) and all of them travel together.
+__device__ __forceinline__ void fetch_lengths(const int* g, Chunk ch, int (&r)[kReqPer]) {
+#pragma unroll
+  for (int q = 0; q < kReqPer; ++q) r[q] = 0;
+#pragma unroll
+  for (int q = 0; q < kReqPer; ++q) {
+    if (ch.beg + q >= ch.end) break;
+    asm volatile("ld.global.b32 %0, [%1];" : "=r"(r[q]) : "l"(g + ch.beg + q));
+  }
+}
+
+// Checks the fetched lengths of n requests, stores them in lens and forms the
+// packed offsets off[0..nreq] (requests n..nreq are padding with no slots).
+// Returns the total slot count N.  Ends with a barrier.
+__device__ int load_lengths(const int (&r)[kReqPer], Chunk ch, int n, int nreq, int k_max,
+                            uint8_t* lens, int* off, PlanShared& sh) {
   int local = 0, bad = 0;
-  for (int i = beg; i < end; ++i) {
-    int k = lens_g[i];
+#pragma unroll
+  for (int q = 0; q < kReqPer; ++q) {
+    if (ch.beg + q >= ch.end) break;
+    int k = r[q];
     if (k < 0 || k > k_max) { bad = 1; k = 0; }
-    lens[i] = k;
+    lens[ch.beg + q] = static_cast<uint8_t>(k);
     local += k;
   }
-  if (__syncthreads_or(bad) && threadIdx.x == 0) sh.err |= SD_DEV_ERR_DRAFT_LENS;
+  if (bad) atomicOr(&sh.err, SD_DEV_ERR_DRAFT_LENS);
   int total;
-  int run = block_excl_scan_i32(local, sh, &total);
-  for (int i = beg; i < end; ++i) {
-    off[i] = run;
-    run += lens[i];
+  int run = block_scan_excl(local, sh.tot_i32, &total);
+#pragma unroll
+  for (int q = 0; q < kReqPer; ++q) {
+    if (ch.beg + q >= ch.end) break;
+    off[ch.beg + q] = run;
+    run += lens[ch.beg + q];
   }
-  if (threadIdx.x == 0) off[n] = total;
+  for (int i = n + threadIdx.x; i <= nreq; i += NT) {
+    if (i < nreq) lens[i] = 0;
+    off[i] = total;
+  }
   __syncthreads();
   return total;
 }
 
-// Sort keys of n requests, P slots each: high word = ~bits(s) (s >= 0, so a
-// larger survival gives a smaller key), low word = i*P + j (packed order).
-// Unused slots hold the sentinel, which sorts last.  The N packed confidence
-// logits are first copied to shared memory by the whole block (coalesced),
-// then each thread runs the short survival product of its requests.
-__device__ void build_keys(const float* conf, const int* lens, const int* off, int n, int P,
-                           int N, unsigned long long* keys, float* conf_s, PlanShared& sh) {
-  int bad = 0;
-  for (int q = threadIdx.x; q < N; q += NT) {
-    const float c = conf[q];
-    if (!isfinite(c)) bad = 1;
-    conf_s[q] = c;
+// Slots per thread in the key phase (nreq * P <= SD_MAX_PLAN_SLOTS).
+constexpr int kSlotPer = SD_MAX_PLAN_SLOTS / NT;
+
+// Sort keys of nreq requests, P slots each: high word = ~bits(s) (s >= 0, so
+// a larger survival gives a smaller key), low word = q = i*P + j (packed
+// order).  Unused slots hold the sentinel, which sorts last.  One thread per
+// slot: all of a thread's confidence logits are requested first, then each
+// slot takes a_j = sigmoid(c_j) and the survival s_j = a_0 * ... * a_j comes
+// from a product scan over the request's P lanes (log2 P steps: the same
+// factors as the front-to-back product, associated differently, so equal to
+// it within fp32 rounding).  Every real key is counted in its bucket (cnt
+// holds kBuckets zeroed counters).  Ends with a barrier.
+__device__ void build_keys(const float* conf, const uint8_t* lens, const int* off, int nreq, int P,
+                           unsigned long long* keys, int* cnt, PlanShared& sh) {
+  const int n = nreq * P;
+  const int lgP = 31 - __clz(P);
+  float cv[kSlotPer];
+#pragma unroll
+  for (int r = 0; r < kSlotPer; ++r) cv[r] = 0.0f;
+#pragma unroll
+  for (int r = 0; r < kSlotPer; ++r) {
+    if (r * NT >= n) break;
+    const int q = r * NT + static_cast<int>(threadIdx.x);
+    const int i = q >> lgP, j = q & (P - 1);
+    if (q < n && j < lens[i]) cv[r] = conf[off[i] + j];
   }
-  if (__syncthreads_or(bad) && threadIdx.x == 0) sh.err |= SD_DEV_ERR_CONF;
-  for (int i = threadIdx.x; i < n; i += NT) {
-    const int k = lens[i];
-    const float* c = conf_s + off[i];
+  int bad = 0;
+#pragma unroll
+  for (int r = 0; r < kSlotPer; ++r) {
+    if (r * NT >= n) break;  // uniform: the scan below is warp-wide
+    const int q = r * NT + static_cast<int>(threadIdx.x);
+    const int i = q >> lgP, j = q & (P - 1);
+    const bool real = q < n && j < lens[i];
     float s = 1.0f;
-    for (int j = 0; j < P; ++j) {
+    if (real) {
+      if (!isfinite(cv[r])) bad = 1;
+      s = 1.0f / (1.0f + expf(-cv[r]));
+    }
+    for (int d = 1; d < P; d <<= 1) {
+      const float t = __shfl_up_sync(kFull, s, d, P);
+      if (j >= d) s *= t;
+    }
+    if (q < n) {
       unsigned long long key = kSentinel;
-      if (j < k) {
-        s = s * (1.0f / (1.0f + expf(-c[j])));
-        key = (static_cast<unsigned long long>(~__float_as_uint(s)) << 32) |
-              static_cast<unsigned long long>(i * P + j);
+      if (real) {
+        const unsigned int h = ~__float_as_uint(s);
+        key = (static_cast<unsigned long long>(h) << 32) | static_cast<unsigned long long>(q);
+        atomicAdd(&cnt[bucket_of(h)], 1);
       }
-      keys[i * P + j] = key;
+      keys[q] = key;
     }
   }
+  if (bad) atomicOr(&sh.err, SD_DEV_ERR_CONF);
   __syncthreads();
 }
 
@@ -203,76 +288,49 @@ __device__ unsigned long long* merge_runs(unsigned long long* a, unsigned long l
   return a;
 }
 
-// Sort of the n (power of two) keys by distribution: each real key goes to
-// one of kBuckets buckets by its high word (monotone in the key), buckets
-// are laid out by an exclusive scan of their counts, and every key then
-// finds its place inside its bucket by counting the bucket's smaller keys
-// (keys are distinct: the low word is the slot index).  The real keys end
-// up ascending in keys[0..N) (tmp is scratch); sentinels are dropped.
+// Sort of the n (power of two) keys by distribution: build_keys counted each
+// real key in its bucket (bucket_of, monotone in the key); buckets are laid
+// out by an exclusive scan of their counts, the keys are scattered into their
+// buckets, and every key then finds its place inside its bucket by counting
+// the bucket's smaller keys (keys are distinct: the low word is the slot
+// index).  The real keys end up ascending in keys[0..N) (tmp is scratch);
+// sentinels are dropped.  After the scatter cnt[b] is the end of bucket b.
 // Returns false (keys untouched) when a bucket holds more than kBucketMax
 // keys, e.g. many equal survivals; the caller then merges the runs instead.
 __device__ bool bucket_sort(unsigned long long* keys, unsigned long long* tmp, int n, int* cnt,
-                            int* end, PlanShared& sh) {
-  unsigned int lo = 0xFFFFFFFFu, hi = 0u;
-  for (int q = threadIdx.x; q < n; q += NT) {
-    const unsigned long long k = keys[q];
-    if (k != kSentinel) {
-      const unsigned int h = static_cast<unsigned int>(k >> 32);
-      lo = min(lo, h);
-      hi = max(hi, h);
-    }
-  }
-  for (int q = threadIdx.x; q < kBuckets; q += NT) cnt[q] = 0;
-  if (threadIdx.x == 0) { sh.hmin = 0xFFFFFFFFu; sh.hmax = 0u; sh.cmax = 0; }
-  __syncthreads();
-  lo = __reduce_min_sync(kFull, lo);
-  hi = __reduce_max_sync(kFull, hi);
-  if ((threadIdx.x & 31) == 0) {
-    atomicMin(&sh.hmin, lo);
-    atomicMax(&sh.hmax, hi);
-  }
-  __syncthreads();
-  const unsigned int hmin = sh.hmin;
-  if (hmin > sh.hmax) return true;  // no real key
-  const unsigned int range = sh.hmax - hmin;
-  int shift = 0;
-  while ((range >> shift) >= static_cast<unsigned int>(kBuckets)) ++shift;
-  for (int q = threadIdx.x; q < n; q += NT) {
-    const unsigned long long k = keys[q];
-    if (k != kSentinel) atomicAdd(&cnt[(static_cast<unsigned int>(k >> 32) - hmin) >> shift], 1);
-  }
-  __syncthreads();
+                            PlanShared& sh) {
   // bucket offsets (exclusive scan, kBuckets / NT consecutive buckets per thread)
-  constexpr int kPer = kBuckets / NT;
-  int c[kPer], local = 0, cm = 0;
+  constexpr int kPer = 4;
+  const int4 c4 = reinterpret_cast<const int4*>(cnt)[threadIdx.x];
+  const int c[kPer] = {c4.x, c4.y, c4.z, c4.w};
+  int local = 0, cm = 0;
 #pragma unroll
   for (int q = 0; q < kPer; ++q) {
-    c[q] = cnt[threadIdx.x * kPer + q];
     local += c[q];
     cm = max(cm, c[q]);
   }
   cm = __reduce_max_sync(kFull, cm);
   if ((threadIdx.x & 31) == 0) atomicMax(&sh.cmax, cm);
-  int run = block_excl_scan_i32(local, sh, nullptr);  // synchronises the block
-  if (sh.cmax > kBucketMax) return false;
-#pragma unroll
-  for (int q = 0; q < kPer; ++q) {
-    run += c[q];
-    cnt[threadIdx.x * kPer + q] = run - c[q];  // the bucket's fill cursor
-    end[threadIdx.x * kPer + q] = run;
-  }
+  int run = block_scan_excl(local, sh.tot_i32, nullptr);
+  if (sh.cmax > kBucketMax) return false;  // read after the scan's barrier
+  int4 cur;  // the buckets' fill cursors
+  cur.x = run;
+  cur.y = cur.x + c[0];
+  cur.z = cur.y + c[1];
+  cur.w = cur.z + c[2];
+  reinterpret_cast<int4*>(cnt)[threadIdx.x] = cur;
   __syncthreads();
   for (int q = threadIdx.x; q < n; q += NT) {
     const unsigned long long k = keys[q];
-    if (k != kSentinel) tmp[atomicAdd(&cnt[(static_cast<unsigned int>(k >> 32) - hmin) >> shift], 1)] = k;
+    if (k != kSentinel) tmp[atomicAdd(&cnt[bucket_of(static_cast<unsigned int>(k >> 32))], 1)] = k;
   }
   __syncthreads();
-  const int total = end[kBuckets - 1];
+  const int total = cnt[kBuckets - 1];
   // each key's place: its bucket's start plus the bucket's keys below it
   for (int x = threadIdx.x; x < total; x += NT) {
     const unsigned long long v = tmp[x];
-    const int bk = static_cast<int>((static_cast<unsigned int>(v >> 32) - hmin) >> shift);
-    const int e = end[bk], b0 = bk > 0 ? end[bk - 1] : 0;
+    const int bk = bucket_of(static_cast<unsigned int>(v >> 32));
+    const int e = cnt[bk], b0 = bk > 0 ? cnt[bk - 1] : 0;
     int r = 0;
     for (int y = b0; y < e; ++y) r += tmp[y] < v;
     keys[b0 + r] = v;
@@ -286,15 +344,18 @@ __device__ bool bucket_sort(unsigned long long* keys, unsigned long long* tmp, i
 // of cost[1..T) (lm_bad: one of those was not finite and positive).  Thread t
 // owns the budgets B in [vb, ve); one combined block scan gives every thread
 // its prefix of the survival sum (exact, 2^48 fixed point) and of the running
-// cost maximum (the monotone cost'[n] = max(cost[1..n])).  Returns B*
-// (smallest maximiser).
-__device__ int budget_argmax(const unsigned long long* sorted, int Bmax, int R, float* cm,
-                             float lm, int lm_bad, PlanShared& sh) {
+// cost maximum (the monotone cost'[n] = max(cost[1..n])).  fx is scratch for
+// the fixed-point survivals (Bmax entries).  Returns B* (smallest maximiser).
+// Ends with a barrier.
+__device__ int budget_argmax(const unsigned long long* sorted, unsigned long long* fx, int Bmax,
+                             int R, float* cm, float lm, int lm_bad, PlanShared& sh) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int cnt = Bmax + 1;
-  const int chunk = (cnt + NT - 1) / NT;
+  // an odd chunk keeps the strided shared-memory accesses free of bank conflicts
+  const int chunk = ((cnt + NT - 1) / NT) | 1;
   const int vb = min(cnt, static_cast<int>(threadIdx.x) * chunk);
   const int ve = min(cnt, vb + chunk);
+  if (threadIdx.x == 0) sh.best = 0ull;
   int bad = lm_bad;
   float cmax = -INFINITY;
   unsigned long long ls = 0;
@@ -303,11 +364,18 @@ __device__ int budget_argmax(const unsigned long long* sorted, int Bmax, int R, 
     if (!(isfinite(c) && c > 0.0f)) bad = 1;
     cmax = fmaxf(cmax, c);
     cm[B] = cmax;  // running maximum within the chunk
-    if (B < Bmax) ls += fix48(__uint_as_float(~static_cast<uint32_t>(sorted[B] >> 32)));
+    if (B < Bmax) {
+      const unsigned long long f = fix48(__uint_as_float(~static_cast<uint32_t>(sorted[B] >> 32)));
+      fx[B] = f;
+      ls += f;
+    }
   }
-  // combined scan: exclusive sums, exclusive running maxima, total of lm
+  // Combined scan: inclusive sums and running maxima within the warp; the
+  // warp totals go through shared memory, and each warp adds up those of the
+  // warps before it with warp reductions (costs are > 0 when valid; invalid
+  // ones raise the error flag, so their order does not matter).
   unsigned long long si = ls;
-  float mi = cmax, m0 = lm;
+  float mi = cmax;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
     const unsigned long long ts = __shfl_up_sync(kFull, si, o);
@@ -316,43 +384,23 @@ __device__ int budget_argmax(const unsigned long long* sorted, int Bmax, int R, 
       si += ts;
       mi = fmaxf(mi, tm);
     }
-    m0 = fmaxf(m0, __shfl_xor_sync(kFull, m0, o));
   }
+  const float m0 = warp_max_nonneg(lm);
   if (lane == 31) {
-    sh.red_u64[warp] = si;
-    sh.red_f32[warp] = mi;
+    sh.tot_u64[warp] = si;
+    sh.tot_f32[warp] = mi;
   }
-  if (lane == 0) sh.red_i32[warp] = __float_as_int(m0);
-  if (__syncthreads_or(bad) && threadIdx.x == 0) sh.err |= SD_DEV_ERR_COST;
-  if (warp == 0) {
-    unsigned long long ws = lane < NW ? sh.red_u64[lane] : 0ull;
-    float wm = lane < NW ? sh.red_f32[lane] : -INFINITY;
-    float w0 = lane < NW ? __int_as_float(sh.red_i32[lane]) : -INFINITY;
-    const unsigned long long ws_in = ws;
-    const float wm_in = wm;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const unsigned long long ts = __shfl_up_sync(kFull, ws, o);
-      const float tm = __shfl_up_sync(kFull, wm, o);
-      if (lane >= o) {
-        ws += ts;
-        wm = fmaxf(wm, tm);
-      }
-      w0 = fmaxf(w0, __shfl_xor_sync(kFull, w0, o));
-    }
-    const float wm_ex = __shfl_up_sync(kFull, wm, 1);
-    if (lane < NW) {
-      sh.red_u64[lane] = ws - ws_in;                    // exclusive warp sums
-      sh.red_f32[lane] = lane == 0 ? -INFINITY : wm_ex;  // exclusive warp maxima
-    }
-    if (lane == 0) sh.red_i32[0] = __float_as_int(w0);
-    (void)wm_in;
-  }
+  if (lane == 0) sh.tot_m0[warp] = m0;
+  if (bad) atomicOr(&sh.err, SD_DEV_ERR_COST);
   __syncthreads();
-  const float mi_up = __shfl_up_sync(kFull, mi, 1);  // every lane takes part
+  const bool earlier = lane < warp;
+  const unsigned long long w_ex = warp_sum_u62(earlier ? sh.tot_u64[lane] : 0ull);
+  const float wm_ex = warp_max_nonneg(earlier ? sh.tot_f32[lane] : -INFINITY);
+  const float w0 = warp_max_nonneg(lane < NW ? sh.tot_m0[lane] : -INFINITY);
+  const float mi_up = __shfl_up_sync(kFull, mi, 1);
   const float mi_ex = lane == 0 ? -INFINITY : mi_up;
-  const float mpre = fmaxf(fmaxf(sh.red_f32[warp], mi_ex), __int_as_float(sh.red_i32[0]));
-  unsigned long long E = sh.red_u64[warp] + (si - ls) + static_cast<unsigned long long>(R) * 281474976710656ull;
+  const float mpre = fmaxf(fmaxf(wm_ex, mi_ex), w0);
+  unsigned long long E = w_ex + (si - ls) + static_cast<unsigned long long>(R) * 281474976710656ull;
   // objectives of this thread's budgets; the largest (smallest B on ties) wins
   unsigned long long best = 0;
   for (int B = vb; B < ve; ++B) {
@@ -361,116 +409,180 @@ __device__ int budget_argmax(const unsigned long long* sorted, int Bmax, int R, 
     const unsigned long long key = (static_cast<unsigned long long>(__float_as_uint(obj)) << 32) |
                                    static_cast<unsigned long long>(0xFFFFFFFFu - static_cast<uint32_t>(B));
     best = key > best ? key : best;
-    if (B < Bmax) E += fix48(__uint_as_float(~static_cast<uint32_t>(sorted[B] >> 32)));
+    if (B < Bmax) E += fx[B];
   }
-  best = warp_max_u64(best);
-  if (threadIdx.x == 0) sh.scan_total = 0;
+  // warp maximum of the packed keys: the high words first, then the low
+  // words of the lanes that hold the largest high word
+  const unsigned bh = __reduce_max_sync(kFull, static_cast<unsigned>(best >> 32));
+  const unsigned bl = __reduce_max_sync(kFull, static_cast<unsigned>(best >> 32) == bh
+                                                   ? static_cast<unsigned>(best & 0xFFFFFFFFull)
+                                                   : 0u);
+  if (lane == 0) atomicMax(&sh.best, (static_cast<unsigned long long>(bh) << 32) | bl);
   __syncthreads();
-  if (lane == 0) atomicMax(&sh.scan_total, best);
-  __syncthreads();
-  return static_cast<int>(0xFFFFFFFFu - static_cast<uint32_t>(sh.scan_total & 0xFFFFFFFFull));
+  return static_cast<int>(0xFFFFFFFFu - static_cast<uint32_t>(sh.best & 0xFFFFFFFFull));
+}
+
+// Shared-memory layout of one launch (NPm = max(NP, NPb), NRm = NPm / P).
+struct PlanSmem {
+  unsigned long long* keysA;  // [NPm]
+  unsigned long long* keysB;  // [NPm]
+  float* cm;                  // [NPm + 1] cost[T+b], then its running maximum
+  int* off;                   // [NRm + 1]
+  int* cnt;                   // [kBuckets]
+  uint8_t* lens;              // [NRm]
+  uint8_t* sel;               // [NP]
+};
+
+__host__ __device__ inline size_t plan_layout(int NP, int NPb, int P, unsigned char* base,
+                                              PlanSmem* m) {
+  const size_t NPm = static_cast<size_t>(NP > NPb ? NP : NPb);
+  const size_t NRm = NPm / static_cast<size_t>(P);
+  size_t o = 0;
+  auto take = [&o](size_t bytes) {  // each part starts on a 16-byte boundary
+    const size_t at = o;
+    o = (o + bytes + 15) / 16 * 16;
+    return at;
+  };
+  const size_t keysA = take(NPm * 8);
+  const size_t keysB = take(NPm * 8);
+  const size_t cm = take((NPm + 1) * 4);
+  const size_t off = take((NRm + 1) * 4);
+  const size_t cnt = take(static_cast<size_t>(kBuckets) * 4);
+  const size_t lens = take(NRm);
+  const size_t sel = take(static_cast<size_t>(NP));
+  if (m) {
+    m->keysA = reinterpret_cast<unsigned long long*>(base + keysA);
+    m->keysB = reinterpret_cast<unsigned long long*>(base + keysB);
+    m->cm = reinterpret_cast<float*>(base + cm);
+    m->off = reinterpret_cast<int*>(base + off);
+    m->cnt = reinterpret_cast<int*>(base + cnt);
+    m->lens = base + lens;
+    m->sel = base + sel;
+  }
+  return o;
+}
+
+// Sorts the keys of one slot set; returns the buffer that holds them ascending.
+// Both ways end with a barrier; the bucket counters are then zeroed again
+// for a later build_keys (which runs after further barriers).
+__device__ const unsigned long long* sort_keys(const PlanSmem& m, int n, int P, PlanShared& sh) {
+  const unsigned long long* sorted =
+      bucket_sort(m.keysA, m.keysB, n, m.cnt, sh) ? m.keysA : merge_runs(m.keysA, m.keysB, n, P);
+  reinterpret_cast<int4*>(m.cnt)[threadIdx.x] = int4{0, 0, 0, 0};  // kBuckets == 4 * NT
+  if (threadIdx.x == 0) sh.cmax = 0;
+  return sorted;
 }
 
 __global__ void __launch_bounds__(NT, 1) plan_kernel(const PlanParams p) {
   extern __shared__ __align__(16) unsigned char smem[];
   __shared__ PlanShared sh;
+  PlanSmem m;
+  plan_layout(p.NP, p.NPb, p.P, smem, &m);
   const int NPm = max(p.NP, p.NPb);
-  unsigned long long* keysA = reinterpret_cast<unsigned long long*>(smem);
-  unsigned long long* keysB = keysA + NPm;
-  float* cm = reinterpret_cast<float*>(keysB + NPm);        // [NPm + 1]
-  int* lens = reinterpret_cast<int*>(cm + NPm + 1);        // [NPm / P]
-  int* off = lens + NPm / p.P;                              // [NPm / P + 1]
-  int* bcnt = off + NPm / p.P + 1;                          // [2 * kBuckets]
-  uint8_t* sel = reinterpret_cast<uint8_t*>(bcnt + 2 * kBuckets);  // [NP]
-
-  if (threadIdx.x == 0) { sh.err = 0; sh.B = 0; }
+  const int nreq = p.NP / p.P;  // padded request counts (powers of two)
+  const int nb = p.NPb / p.P;
   const int L = p.cost_len - 1;
-  // The cost table is read first, so that its loads overlap the lengths':
-  // cost[T+b] for every budget b the call can reach, and each thread's
-  // maximum of its share of cost[1..T).
+  const bool adaptive = p.mode != SD_MODE_ALL_SLOTS;
+
+  // Every global input the first steps need is requested at once: the draft
+  // lengths (current, and those of the budget set) into registers, cost[T+b]
+  // for every budget b the call can reach into shared memory, and each
+  // thread's maximum of its share of cost[1..T).
+  const Chunk cc = req_chunk(p.bs);
+  int rc[kReqPer], rb[kReqPer];
+  fetch_lengths(p.lens, cc, rc);
+  Chunk cb = {0, 0};
+  if (p.budget_conf) {
+    cb = req_chunk(p.bs_budget);
+    fetch_lengths(p.budget_lens, cb, rb);
+  }
   float lm = -INFINITY;
   int lm_bad = 0;
-  if (p.mode != SD_MODE_ALL_SLOTS) {
+  if (adaptive) {
+    const int bmax = min(NPm, L - p.T);
+    for (int b = threadIdx.x; b <= bmax; b += NT) cp_async4(m.cm + b, p.cost + p.T + b);
     for (int n = 1 + threadIdx.x; n < p.T; n += NT) {
       const float c = p.cost[n];
       if (!(isfinite(c) && c > 0.0f)) lm_bad = 1;
       lm = fmaxf(lm, c);
     }
-    const int bmax = min(NPm, L - p.T);
-    for (int b = threadIdx.x; b <= bmax; b += NT) cm[b] = p.cost[p.T + b];
   }
+  if (p.NP >= 16) {  // sel starts on a 16-byte boundary
+    for (int q = threadIdx.x; q < p.NP / 16; q += NT) reinterpret_cast<int4*>(m.sel)[q] = int4{0, 0, 0, 0};
+  } else if (threadIdx.x < p.NP) {
+    m.sel[threadIdx.x] = 0;
+  }
+  reinterpret_cast<int4*>(m.cnt)[threadIdx.x] = int4{0, 0, 0, 0};  // kBuckets == 4 * NT
+  if (threadIdx.x == 0) {
+    sh.err = 0;
+    sh.cmax = 0;
+  }
+  cp_async_wait_all();
   __syncthreads();
 
-  const int nreq = p.NP / p.P;  // padded request count (power of two)
-  // Current slots: lengths and offsets (padded requests have no slots).
-  int N = load_lengths(p.lens, p.bs, p.k_max, lens, off, sh);
-  for (int i = p.bs + threadIdx.x; i < nreq; i += NT) { lens[i] = 0; off[i] = N; }
-  __syncthreads();
+  // Current slots: lengths and offsets.
+  int N = load_lengths(rc, cc, p.bs, nreq, p.k_max, m.lens, m.off, sh);
 
   int B = 0;
-  if (p.mode == SD_MODE_ALL_SLOTS) {
+  if (!adaptive) {
     B = N;
   } else {
     if (p.budget_conf) {
-      const int nb = p.NPb / p.P;
-      const int Nb = load_lengths(p.budget_lens, p.bs_budget, p.k_max, lens, off, sh);
-      for (int i = p.bs_budget + threadIdx.x; i < nb; i += NT) { lens[i] = 0; off[i] = Nb; }
-      __syncthreads();
+      const int Nb = load_lengths(rb, cb, p.bs_budget, nb, p.k_max, m.lens, m.off, sh);
       if (sh.err == 0) {
-        build_keys(p.budget_conf, lens, off, nb, p.P, Nb, keysA, reinterpret_cast<float*>(keysB), sh);
-        const unsigned long long* sorted = bucket_sort(keysA, keysB, p.NPb, bcnt, bcnt + kBuckets, sh)
-                                               ? keysA
-                                               : merge_runs(keysA, keysB, p.NPb, p.P);
+        build_keys(p.budget_conf, m.lens, m.off, nb, p.P, m.keysA, m.cnt, sh);
+        const unsigned long long* sorted = sort_keys(m, p.NPb, p.P, sh);
         const int Bmax_b = min(Nb, L - p.T);
         int Bb = 0;
-        if (sh.err == 0) Bb = budget_argmax(sorted, Bmax_b, p.bs, cm, lm, lm_bad, sh);
+        if (sh.err == 0)
+          Bb = budget_argmax(sorted, sorted == m.keysA ? m.keysB : m.keysA, Bmax_b, p.bs, m.cm,
+                             lm, lm_bad, sh);
         B = min(Bb, min(N, L - p.T));
       }
-      // Restore the current request lengths.
-      N = load_lengths(p.lens, p.bs, p.k_max, lens, off, sh);
-      for (int i = p.bs + threadIdx.x; i < nreq; i += NT) { lens[i] = 0; off[i] = N; }
-      __syncthreads();
+      // Back to the current request lengths.
+      N = load_lengths(rc, cc, p.bs, nreq, p.k_max, m.lens, m.off, sh);
     }
     if (sh.err == 0) {
-      build_keys(p.conf, lens, off, nreq, p.P, N, keysA, reinterpret_cast<float*>(keysB), sh);
-      const unsigned long long* sorted = bucket_sort(keysA, keysB, p.NP, bcnt, bcnt + kBuckets, sh)
-                                             ? keysA
-                                             : merge_runs(keysA, keysB, p.NP, p.P);
+      build_keys(p.conf, m.lens, m.off, nreq, p.P, m.keysA, m.cnt, sh);
+      const unsigned long long* sorted = sort_keys(m, p.NP, p.P, sh);
       if (!p.budget_conf && sh.err == 0)
-        B = budget_argmax(sorted, min(N, L - p.T), p.bs, cm, lm, lm_bad, sh);
+        B = budget_argmax(sorted, sorted == m.keysA ? m.keysB : m.keysA, min(N, L - p.T), p.bs,
+                          m.cm, lm, lm_bad, sh);
       // Selection: the B best ranks.
-      for (int q = threadIdx.x; q < p.NP; q += NT) sel[q] = 0;
-      __syncthreads();
       if (sh.err == 0)
         for (int r = threadIdx.x; r < B; r += NT)
-          sel[static_cast<uint32_t>(sorted[r] & 0xFFFFFFFFull)] = 1;
+          m.sel[static_cast<uint32_t>(sorted[r] & 0xFFFFFFFFull)] = 1;
       __syncthreads();
     }
   }
 
   const bool failed = sh.err != 0;
   if (failed) B = 0;
-  // Compaction: mask rows, n_i and cu_seqlens.
-  const int chunk = (p.bs + NT - 1) / NT;
-  const int beg = min(p.bs, static_cast<int>(threadIdx.x) * chunk);
-  const int end = min(p.bs, beg + chunk);
-  int local = 0;
-  for (int i = beg; i < end; ++i) {
-    int n = 0;
+  // Compaction: slot mask, n_i and cu_seqlens, one thread per chunk of requests.
+  int nv[kReqPer], local = 0;
+#pragma unroll
+  for (int q = 0; q < kReqPer; ++q) nv[q] = 0;
+#pragma unroll
+  for (int q = 0; q < kReqPer; ++q) {
+    const int i = cc.beg + q;
+    if (i >= cc.end) break;
+    const int k = failed ? 0 : m.lens[i];
+    uint8_t* mrow = p.mask + static_cast<size_t>(i) * p.k_max;
     for (int j = 0; j < p.k_max; ++j) {
-      uint8_t m = 0;
-      if (!failed && j < lens[i]) m = (p.mode == SD_MODE_ALL_SLOTS) ? 1 : sel[i * p.P + j];
-      p.mask[static_cast<size_t>(i) * p.k_max + j] = m;
-      n += m;
+      const uint8_t v = j < k ? (adaptive ? m.sel[i * p.P + j] : uint8_t{1}) : uint8_t{0};
+      mrow[j] = v;
+      nv[q] += v;
     }
-    p.num_verified[i] = n;
-    local += n + 1;
+    p.num_verified[i] = nv[q];
+    local += nv[q] + 1;
   }
   int total;
-  int run = block_excl_scan_i32(local, sh, &total);
-  for (int i = beg; i < end; ++i) {
-    p.cu[i] = run;
-    run += p.num_verified[i] + 1;
+  int run = block_scan_excl(local, sh.tot_i32, &total);
+#pragma unroll
+  for (int q = 0; q < kReqPer; ++q) {
+    if (cc.beg + q >= cc.end) break;
+    p.cu[cc.beg + q] = run;
+    run += nv[q] + 1;
   }
   if (threadIdx.x == 0) {
     p.cu[p.bs] = total;
@@ -482,9 +594,7 @@ __global__ void __launch_bounds__(NT, 1) plan_kernel(const PlanParams p) {
 }  // namespace
 
 size_t plan_smem_bytes(const PlanParams& p) {
-  const size_t NPm = static_cast<size_t>(p.NP > p.NPb ? p.NP : p.NPb);
-  return 2 * NPm * 8 + (NPm + 1) * 4 + (NPm / p.P) * 4 + (NPm / p.P + 1) * 4 +
-         static_cast<size_t>(kBuckets) * 8 + static_cast<size_t>(p.NP) + 16;
+  return plan_layout(p.NP, p.NPb, p.P, nullptr, nullptr);
 }
 
 cudaError_t launch_plan(const PlanParams& p, cudaStream_t s) {

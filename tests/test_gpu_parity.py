@@ -211,6 +211,30 @@ def test_random_small_plans_match_oracle():
             compare_plan(gpu_plan(pa, k_max), oracle_plan(pa, k_max), f"all-slots {trial}")
 
 
+@pytest.mark.parametrize("bs,k_max", [(8192, 1), (4096, 2), (512, 15), (1, 15), (8192, 0)])
+def test_plans_at_the_slot_limit(bs, k_max):
+    """pow2ceil(bs) * pow2ceil(k_max) at its limit of 8192 slots (the largest
+    shared-memory footprint), with and without a budget set of that size."""
+    rng = np.random.default_rng(bs * 16 + k_max)
+    dl = rng.integers(0, k_max + 1, bs).astype(np.int32)
+    T = 64
+    L = T + int(dl.sum()) + 3
+    cost = (1.0 + 0.002 * np.arange(L + 1)).astype(np.float32)
+    pi = {"draft_lens": dl, "conf": rng.normal(1, 2, dl.sum()).astype(np.float32), "cost": cost,
+          "T": T, "mode": S.MODE_ADAPTIVE, "budget_conf": None, "budget_draft_lens": None}
+    for extra in ({}, {"mode": S.MODE_ALL_SLOTS}):
+        q = dict(pi, **extra)
+        g = gpu_plan(q, k_max)
+        assert g["err"] == 0
+        compare_plan(g, oracle_plan(q, k_max), f"bs={bs} k_max={k_max} {extra}")
+    if k_max > 0:
+        bdl = rng.integers(0, k_max + 1, bs).astype(np.int32)
+        q = dict(pi, budget_conf=rng.normal(1, 2, bdl.sum()).astype(np.float32), budget_draft_lens=bdl)
+        g = gpu_plan(q, k_max)
+        assert g["err"] == 0
+        compare_plan(g, oracle_plan(q, k_max), f"bs={bs} k_max={k_max} budget set")
+
+
 # Mismatches allowed at near-boundary decisions, as a fraction of all
 # decisions.  The pages fix fp32 for the sampling arithmetic; at V = 129280 the
 # mean gap between consecutive CDF values is S / V = 7.7e-6 S, inside the
