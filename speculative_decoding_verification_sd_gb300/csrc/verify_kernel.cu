@@ -181,10 +181,15 @@ struct ChunkOps<uint16_t> {  // 8 bf16 per 16-byte vector
   template <int N>
   __device__ __forceinline__ static void softmax(const uint4 (&r)[N], float s2, float& m,
                                                  float2& z2, float& nb) {
-    uint32_t mx = kNegInf2;
+    // per-vector maxima, then a tree over the vectors (short dependency chains)
+    uint32_t vm[N];
 #pragma unroll
-    for (int q = 0; q < N; ++q) mx = bmax2(mx, bmax2(bmax2(r[q].x, r[q].y), bmax2(r[q].z, r[q].w)));
-    const float lm = fmaxf(bf_lo(mx), bf_hi(mx));
+    for (int q = 0; q < N; ++q) vm[q] = bmax2(bmax2(r[q].x, r[q].y), bmax2(r[q].z, r[q].w));
+#pragma unroll
+    for (int st = 1; st < N; st <<= 1)
+#pragma unroll
+      for (int q = 0; q + st < N; q += 2 * st) vm[q] = bmax2(vm[q], vm[q + st]);
+    const float lm = fmaxf(bf_lo(vm[0]), bf_hi(vm[0]));
     if (lm > m) {
       if (m == -INFINITY) {
         z2 = make_float2(0.0f, 0.0f);
@@ -197,15 +202,19 @@ struct ChunkOps<uint16_t> {  // 8 bf16 per 16-byte vector
     }
     if (m != -INFINITY) {
       const float2 s22 = make_float2(s2, s2), nb2 = make_float2(nb, nb);
+      float2 acc[4];  // four independent partial sums, one per word of the vector
+#pragma unroll
+      for (int h = 0; h < 4; ++h) acc[h] = make_float2(0.0f, 0.0f);
 #pragma unroll
       for (int q = 0; q < N; ++q) {
         const uint32_t w4[4] = {r[q].x, r[q].y, r[q].z, r[q].w};
 #pragma unroll
         for (int h = 0; h < 4; ++h) {
           const float2 t = __ffma2_rn(make_float2(bf_lo(w4[h]), bf_hi(w4[h])), s22, nb2);
-          z2 = __fadd2_rn(z2, make_float2(exp2_ftz(t.x), exp2_ftz(t.y)));
+          acc[h] = __fadd2_rn(acc[h], make_float2(exp2_ftz(t.x), exp2_ftz(t.y)));
         }
       }
+      z2 = __fadd2_rn(z2, __fadd2_rn(__fadd2_rn(acc[0], acc[1]), __fadd2_rn(acc[2], acc[3])));
     }
   }
   // Running argmax of one lane: the first vector whose maximum strictly
@@ -247,9 +256,14 @@ struct ChunkOps<float> {  // 4 fp32 per 16-byte vector
   template <int N>
   __device__ __forceinline__ static void softmax(const float4 (&r)[N], float s2, float& m,
                                                  float2& z2, float& nb) {
-    float lm = -INFINITY;
+    float vm[N];
 #pragma unroll
-    for (int q = 0; q < N; ++q) lm = fmaxf(fmaxf(lm, fmaxf(r[q].x, r[q].y)), fmaxf(r[q].z, r[q].w));
+    for (int q = 0; q < N; ++q) vm[q] = fmaxf(fmaxf(r[q].x, r[q].y), fmaxf(r[q].z, r[q].w));
+#pragma unroll
+    for (int st = 1; st < N; st <<= 1)
+#pragma unroll
+      for (int q = 0; q + st < N; q += 2 * st) vm[q] = fmaxf(vm[q], vm[q + st]);
+    const float lm = vm[0];
     if (lm > m) {
       if (m == -INFINITY) {
         z2 = make_float2(0.0f, 0.0f);
@@ -262,13 +276,15 @@ struct ChunkOps<float> {  // 4 fp32 per 16-byte vector
     }
     if (m != -INFINITY) {
       const float2 s22 = make_float2(s2, s2), nb2 = make_float2(nb, nb);
+      float2 a0 = make_float2(0.0f, 0.0f), a1 = make_float2(0.0f, 0.0f);  // independent sums
 #pragma unroll
       for (int q = 0; q < N; ++q) {
         const float2 t0 = __ffma2_rn(make_float2(r[q].x, r[q].y), s22, nb2);
         const float2 t1 = __ffma2_rn(make_float2(r[q].z, r[q].w), s22, nb2);
-        z2 = __fadd2_rn(z2, make_float2(exp2_ftz(t0.x), exp2_ftz(t0.y)));
-        z2 = __fadd2_rn(z2, make_float2(exp2_ftz(t1.x), exp2_ftz(t1.y)));
+        a0 = __fadd2_rn(a0, make_float2(exp2_ftz(t0.x), exp2_ftz(t0.y)));
+        a1 = __fadd2_rn(a1, make_float2(exp2_ftz(t1.x), exp2_ftz(t1.y)));
       }
+      z2 = __fadd2_rn(z2, __fadd2_rn(a0, a1));
     }
   }
   template <int N>
@@ -582,7 +598,10 @@ struct Streamer {
   __device__ void refill() {
     while (iseq - cseq < static_cast<uint32_t>(kSlots)) {
       if (fk_cached != fk) {
-        if (fk > ld_acquire_cta(C.pub)) break;
+        // every lane acquires the counter and all act on the smallest value
+        // seen, so the lanes take the same trips through this loop and each
+        // has synchronised with the publication it acts on
+        if (fk > __reduce_min_sync(kFull, ld_acquire_cta(C.pub))) break;
         const int u = C.q[fk % kDepth];
         if (u == kEnd) break;
         f_two = false;
@@ -620,12 +639,14 @@ struct Streamer {
       ++iseq;
       ++fe;
     }
+    __syncwarp();  // lane 0's copies are issued before any lane waits on them
   }
 
   // Waits for ring entry `seq`; returns its data.
   __device__ const Raw* entry(uint32_t seq, int* err) {
     const int slot = static_cast<int>(seq % kSlots);
-    if (!mbar_wait_bounded(&bar[slot], (seq / kSlots) & 1, 1u << 24)) raise_error(err, SD_DEV_ERR_TIMEOUT);
+    const bool ok = __all_sync(kFull, mbar_wait_bounded(&bar[slot], (seq / kSlots) & 1, 1u << 24));
+    if (!ok && lane == 0) raise_error(err, SD_DEV_ERR_TIMEOUT);
     return reinterpret_cast<const Raw*>(ring + slot * kSlotBytes);
   }
 
@@ -902,8 +923,12 @@ struct Control {
         bulk_load_nohint(cbuf, w.rt + ub, bytes, cbar);
         if (two) bulk_load_nohint(cbuf + kSlotBytes, w.rd + ub, bytes, cbar);
       }
-      if (!mbar_wait_bounded(cbar, cphase & 1, 1u << 24) && lane == 0)
-        raise_error(p.err, SD_DEV_ERR_TIMEOUT);
+      // The copies are issued before any lane starts waiting for them: lanes
+      // left to spin ahead of lane 0 could hold the warp until their wait
+      // gives up and then read the buffer before it has landed.
+      __syncwarp();
+      const bool ok = __all_sync(kFull, mbar_wait_bounded(cbar, cphase & 1, 1u << 24));
+      if (!ok && lane == 0) raise_error(p.err, SD_DEV_ERR_TIMEOUT);
       ++cphase;
       w.rt = reinterpret_cast<const Raw*>(cbuf);
       w.rd = two ? reinterpret_cast<const Raw*>(cbuf + kSlotBytes) : w.rt;
