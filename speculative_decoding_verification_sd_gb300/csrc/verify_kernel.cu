@@ -336,9 +336,9 @@ __device__ __forceinline__ unsigned long long warp_scan_u64(unsigned long long v
 }
 
 // 2^(d * s2) with d = l - M given as (d_hi, d_lo) and s2 = s2_hi + s2_lo: the
-// exponent is formed in double-float so its rounding does not depend on |d|.
-// Written with explicitly rounded intrinsics so that every call site computes
-// bit-identical values (the final draw recomputes weights it summed before).
+// exponent is formed in double-float so its rounding does not depend on |d|
+// (the accept test's p(x) and q(x)).  Written with explicitly rounded
+// intrinsics so that its value does not depend on how it is compiled.
 __device__ __forceinline__ float exp2_df(float d_hi, float d_lo, float s2_hi, float s2_lo) {
   const float t_hi = __fmul_rn(d_hi, s2_hi);
   const float t_lo = __fadd_rn(__fmaf_rn(d_hi, s2_hi, -t_hi),
@@ -471,16 +471,18 @@ __device__ __forceinline__ bool is_slice(int u) { return u >= kResBase && u < kW
 
 // ---------------------------------------------------------------------------
 // Weight functions of the final draws.  A draw from p (target row rt, max
-// Mt, scale s2 = log2(e)/tau, also as the double-float s2h + s2l) weighs an
-// element 2^((l - Mt) s2) <= 1 (2^40 fixed point); a residual draw adds the
-// draft row rd (max Md) and both 1/Z and weighs max(p - q, 0) <= 1 (2^56).
-// fast_*: the fp32 sum over one unit, for chunk sums; precise_*: each
-// element with a double-float exponent, for the walk of the crossing chunk.
+// Mt, scale s2 = log2(e)/tau) weighs an element 2^((l - Mt) s2) <= 1 (2^40
+// fixed point); a residual draw adds the draft row rd (max Md) and both 1/Z
+// and weighs max(p - q, 0) <= 1 (2^56).  All in fp32 with the hardware
+// exponent; a unit's weight is the fixed-point value of its fp32 sum (what
+// the residual slices add into the chunk sums, so the walk of the crossing
+// chunk retraces those sums exactly), an element's weight its own fixed-point
+// value.
 template <typename Raw>
 struct DrawRows {
   const Raw* rt;  // unit u at rt[u - off] (off > 0: a staged copy in shared memory)
   const Raw* rd;
-  float Mt, Md, iZt, iZd, s2, s2h, s2l;
+  float Mt, Md, iZt, iZd, s2;
   int off;
 };
 
@@ -501,10 +503,16 @@ __device__ __forceinline__ DrawRows<typename VT<T, VEC>::Raw> make_rows(
   w.iZt = 1.0f / ts.y;
   w.iZd = 1.0f / ds.y;
   w.s2 = kLog2e / tau;
-  w.s2h = kLog2eHi / tau;
-  w.s2l = (fmaf(-w.s2h, tau, kLog2eHi) + kLog2eLo) / tau;
   w.off = 0;
   return w;
+}
+
+// max(p - q, 0) of one element
+__device__ __forceinline__ float res_weight(float f, float g, float s2, float bt, float bd,
+                                            float iZt, float iZd) {
+  const float et = exp2_ftz(fmaf(f, s2, -bt));
+  const float ed = exp2_ftz(fmaf(g, s2, -bd));
+  return fmaxf(fmaf(et, iZt, -__fmul_rn(ed, iZd)), 0.0f);
 }
 
 template <typename T, bool VEC>
@@ -518,45 +526,51 @@ __device__ __forceinline__ float fast_res(const DrawRows<typename VT<T, VEC>::Ra
   const float bt = w.Mt * w.s2, bd = w.Md * w.s2;
   float ws = 0.0f;
 #pragma unroll
-  for (int e = 0; e < Tr::VE; ++e) {
-    const float et = exp2_ftz(fmaf(f[e], w.s2, -bt));
-    const float ed = exp2_ftz(fmaf(g[e], w.s2, -bd));
-    ws += fmaxf(fmaf(et, w.iZt, -__fmul_rn(ed, w.iZd)), 0.0f);
-  }
+  for (int e = 0; e < Tr::VE; ++e) ws += res_weight(f[e], g[e], w.s2, bt, bd, w.iZt, w.iZd);
   return ws;
 }
 
+// Residual draw: unit u's weight, and its elements' weights.
 template <typename T, bool VEC>
-__device__ __forceinline__ void precise_p(const DrawRows<typename VT<T, VEC>::Raw>& w, int u,
-                                          unsigned long long (&wi)[VT<T, VEC>::VE]) {
-  using Tr = VT<T, VEC>;
-  float f[Tr::VE];
-  Tr::unpack(w.rt[u - w.off], f);
-#pragma unroll
-  for (int e = 0; e < Tr::VE; ++e) {
-    float h, l;
-    two_diff(f[e], w.Mt, h, l);
-    wi[e] = __float2ull_rn(__fmul_rn(exp2_df(h, l, w.s2h, w.s2l), kTwo40));
-  }
+__device__ __forceinline__ unsigned long long unit_res(const DrawRows<typename VT<T, VEC>::Raw>& w,
+                                                       int u) {
+  return __float2ull_rn(__fmul_rn(fast_res<T, VEC>(w, w.rt[u - w.off], w.rd[u - w.off]), kTwo56));
 }
-
 template <typename T, bool VEC>
-__device__ __forceinline__ void precise_res(const DrawRows<typename VT<T, VEC>::Raw>& w, int u,
-                                            unsigned long long (&wi)[VT<T, VEC>::VE]) {
+__device__ __forceinline__ void elem_res(const DrawRows<typename VT<T, VEC>::Raw>& w, int u,
+                                         unsigned long long (&wi)[VT<T, VEC>::VE]) {
   using Tr = VT<T, VEC>;
   float f[Tr::VE], g[Tr::VE];
   Tr::unpack(w.rt[u - w.off], f);
   Tr::unpack(w.rd[u - w.off], g);
+  const float bt = w.Mt * w.s2, bd = w.Md * w.s2;
 #pragma unroll
-  for (int e = 0; e < Tr::VE; ++e) {
-    float h, l;
-    two_diff(f[e], w.Mt, h, l);
-    const float et = exp2_df(h, l, w.s2h, w.s2l);
-    two_diff(g[e], w.Md, h, l);
-    const float ed = exp2_df(h, l, w.s2h, w.s2l);
-    const float x = fmaxf(__fmaf_rn(et, w.iZt, -__fmul_rn(ed, w.iZd)), 0.0f);
-    wi[e] = __float2ull_rn(__fmul_rn(x, kTwo56));
-  }
+  for (int e = 0; e < Tr::VE; ++e)
+    wi[e] = __float2ull_rn(__fmul_rn(res_weight(f[e], g[e], w.s2, bt, bd, w.iZt, w.iZd), kTwo56));
+}
+
+// Draw from p: unit u's weight, and its elements' weights.
+template <typename T, bool VEC>
+__device__ __forceinline__ unsigned long long unit_p(const DrawRows<typename VT<T, VEC>::Raw>& w,
+                                                     int u) {
+  using Tr = VT<T, VEC>;
+  float f[Tr::VE];
+  Tr::unpack(w.rt[u - w.off], f);
+  const float bt = w.Mt * w.s2;
+  float ws = 0.0f;
+#pragma unroll
+  for (int e = 0; e < Tr::VE; ++e) ws += exp2_ftz(fmaf(f[e], w.s2, -bt));
+  return __float2ull_rn(__fmul_rn(ws, kTwo40));
+}
+template <typename T, bool VEC>
+__device__ __forceinline__ void elem_p(const DrawRows<typename VT<T, VEC>::Raw>& w, int u,
+                                       unsigned long long (&wi)[VT<T, VEC>::VE]) {
+  using Tr = VT<T, VEC>;
+  float f[Tr::VE];
+  Tr::unpack(w.rt[u - w.off], f);
+  const float bt = w.Mt * w.s2;
+#pragma unroll
+  for (int e = 0; e < Tr::VE; ++e) wi[e] = __float2ull_rn(__fmul_rn(exp2_ftz(fmaf(f[e], w.s2, -bt)), kTwo40));
 }
 
 // ---------------------------------------------------------------------------
@@ -964,10 +978,15 @@ struct Control {
   }
   // Next unit for this CTA: a listed slice first, else a row; kEnd once
   // nothing is left anywhere; kWait when a draw may still be listed.
-  __device__ int schedule() {
+  // `depth` is the number of units published behind the one being folded.
+  // Once the rows have run out, a CTA takes a slice only when nothing is
+  // queued behind its current unit, so that a late draw's slices go to idle
+  // CTAs and start at once instead of waiting behind queued rows.
+  __device__ int schedule(int depth) {
     const unsigned long long lc = load_lc();
     const int avail = static_cast<int>(lc & 0xFFFFFFFFull) * G.S_sl;
-    if (held < 0 && static_cast<int>(lc >> 32) < avail) held = atomicAdd(&p.ctrl[3], 1);
+    const bool deep = rows_done && depth > 0;
+    if (!deep && held < 0 && static_cast<int>(lc >> 32) < avail) held = atomicAdd(&p.ctrl[3], 1);
     if (held >= 0 && held < avail) {
       const int h = held;
       held = -1;
@@ -980,8 +999,9 @@ struct Control {
         return u;
       }
       rows_done = true;
+      if (depth > 0) return kWait;  // as above: slices only with nothing queued
     }
-    if (!decided()) return kWait;
+    if (deep || !decided()) return kWait;
     const unsigned long long f = load_lc();  // the final list
     const int fin = static_cast<int>(f & 0xFFFFFFFFull) * G.S_sl;
     if (held < 0) {
@@ -1031,16 +1051,32 @@ struct Control {
     return true;
   }
 
-  // The element of units [ub, ue) where the precise running weight passes
-  // th; the last positive weight when the threshold lies past them (the
-  // fast and precise weights differ by rounding).  Each lane takes a block
-  // of at most kWalk units: it first prefetches the block into L1, then sums
-  // each unit, keeping the sums in shared memory, so the lane holding the
-  // crossing recomputes one unit only.  Longer ranges go in rounds.
-  template <typename PF, typename FF>
-  __device__ int walk(PF pfn, FF pref, int ub, int ue, unsigned long long th) const {
+  // The element of units [ub, ue) where the running weight passes th:
+  // usum(u) is unit u's weight, elem(u, wi) its elements' weights.  Each lane
+  // takes a block of at most kWalk units: it first prefetches the block into
+  // L1, then sums each unit, keeping the sums in shared memory, so the lane
+  // holding the crossing recomputes one unit only.  Longer ranges go in
+  // rounds.  When the threshold lies past the units or past the crossing
+  // unit's elements (their fixed-point values need not add up to the unit's
+  // exactly), the last positive weight is taken.
+  template <typename UF, typename EF, typename FF>
+  __device__ int walk(UF usum, EF elem, FF pref, int ub, int ue, unsigned long long th) const {
     unsigned long long* us = s_walk + lane * kWalk;
-    int lastpos = -1;
+    // the element of unit u where the running weight from 0 passes r, else its last positive one
+    auto pick_in = [&](int u, unsigned long long r) {
+      unsigned long long wi[VE];
+      elem(u, wi);
+      unsigned long long acc = 0;
+      int last = u * VE + VE - 1, hit = -1;
+#pragma unroll
+      for (int e = 0; e < VE; ++e) {
+        if (wi[e] > 0) last = u * VE + e;
+        if (hit < 0 && acc + wi[e] > r) hit = u * VE + e;
+        acc += wi[e];
+      }
+      return hit >= 0 ? hit : last;
+    };
+    int lastu = -1;
     for (int rb = ub; rb < ue; rb += 32 * kWalk) {
       const int re = min(ue, rb + 32 * kWalk);
       const int upl = (re - rb + 31) / 32;
@@ -1049,14 +1085,8 @@ struct Control {
       unsigned long long sv = 0;
 #pragma unroll 1
       for (int u = b0; u < b1; ++u) {
-        unsigned long long wi[VE];
-        pfn(u, wi);
-        unsigned long long su = 0;
-#pragma unroll
-        for (int e = 0; e < VE; ++e) {
-          su += wi[e];
-          if (wi[e] > 0) lastpos = u * VE + e;
-        }
+        const unsigned long long su = usum(u);
+        if (su > 0) lastu = u;
         us[u - b0] = su;
         sv += su;
       }
@@ -1074,26 +1104,16 @@ struct Control {
             }
             acc += us[v - b0];
           }
-          unsigned long long wi[VE];
-          pfn(u, wi);
-          pk = u * VE + VE - 1;
-          bool hit_e = false;
-#pragma unroll
-          for (int e = 0; e < VE; ++e) {
-            acc += wi[e];
-            if (!hit_e && acc > th) {
-              pk = u * VE + e;
-              hit_e = true;
-            }
-          }
+          pk = pick_in(u, th - acc);
         }
         const unsigned hit = __ballot_sync(kFull, pk >= 0);
         return __shfl_sync(kFull, pk, __ffs(hit) - 1);
       }
       th -= tot;
     }
-    const int lp = static_cast<int>(warp_max_u64(static_cast<unsigned long long>(lastpos + 1))) - 1;
-    return lp >= 0 ? lp : ub * VE;
+    const int lu = static_cast<int>(warp_max_u64(static_cast<unsigned long long>(lastu + 1))) - 1;
+    if (lu < 0) return ub * VE;
+    return pick_in(lu, ~0ull);  // every lane: the same unit, the same answer
   }
 
   // Draw from p of target row c0 + a (its per-chunk statistics give the
@@ -1137,7 +1157,8 @@ struct Control {
     stat_units(G, c, ub, ue);
     DrawRows<Raw> ws = w;
     const bool staged = stage(ws, false, ub, ue);
-    return walk([&](int u, unsigned long long (&wi)[VE]) { precise_p<T, VEC>(ws, u, wi); },
+    return walk([&](int u) { return unit_p<T, VEC>(ws, u); },
+                [&](int u, unsigned long long (&wi)[VE]) { elem_p<T, VEC>(ws, u, wi); },
                 [&](int u) {
                   if (!staged) prefetch_l1(ws.rt + u);
                 },
@@ -1276,7 +1297,8 @@ struct Control {
       stat_units(G, c, ub, ue);
       DrawRows<Raw> ws = w;
       const bool staged = stage(ws, true, ub, ue);
-      pick = walk([&](int u, unsigned long long (&wi)[VE]) { precise_res<T, VEC>(ws, u, wi); },
+      pick = walk([&](int u) { return unit_res<T, VEC>(ws, u); },
+                  [&](int u, unsigned long long (&wi)[VE]) { elem_res<T, VEC>(ws, u, wi); },
                   [&](int u) {
                     if (!staged) {
                       prefetch_l1(ws.rt + u);
@@ -1421,7 +1443,7 @@ struct Control {
       bool progress = false;
       if (!end_pub && k_pub < k_done + kWindow - 1) {
         int e = kWait;
-        if (lane == 0) e = schedule();
+        if (lane == 0) e = schedule(k_pub - k_done);
         e = __shfl_sync(kFull, e, 0);
         if (e != kWait) {
           if (lane == 0) {
@@ -1533,6 +1555,22 @@ __global__ void __launch_bounds__(NT, 1) verify_kernel(const __grid_constant__ V
   }
   if (badt && blockIdx.x == 0) raise_error(p.err, badt);
   __syncthreads();
+
+  // The small per-request inputs that only the final draws read (uniforms,
+  // draft ids) are brought into L2 and kept there, so that those draws do
+  // not wait behind the row traffic queued at the memory controllers.  Every
+  // address prefetched lies inside its array.
+  {
+    const size_t bu = static_cast<size_t>(p.bs) * (p.k_max + 1) * sizeof(float);
+    const size_t bd = p.draft_ids ? static_cast<size_t>(cu_s[p.bs] - p.bs) * sizeof(int) : 0;
+    const size_t lu = (bu + 127) / 128, ld = (bd + 127) / 128;
+    for (size_t l = static_cast<size_t>(blockIdx.x) * NT + tid; l < lu + ld;
+         l += static_cast<size_t>(gridDim.x) * NT) {
+      const char* a = l < lu ? reinterpret_cast<const char*>(p.uniforms) + l * 128
+                             : reinterpret_cast<const char*>(p.draft_ids) + (l - lu) * 128;
+      asm volatile("prefetch.global.L2::evict_last [%0];" ::"l"(a));
+    }
+  }
 
   // Exclusive prefix of one value per thread (thread order); *total = sum.
   auto block_scan = [&](int v, int* total) {
