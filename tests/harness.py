@@ -17,7 +17,6 @@ import sdsynth as S
 
 ROOT = Path(__file__).resolve().parent.parent
 PROB_RTOL = 1e-5
-NEAR_FRACTION_MAX = 1e-4  # 0.01 % of decisions
 
 
 @dataclass
@@ -29,9 +28,10 @@ class Tally:
     cases: list = field(default_factory=list)
 
     def dump(self):
-        out = ROOT / "gpurun_out"
-        if out.is_dir():
-            (out / "parity_tally.json").write_text(json.dumps(self.__dict__, indent=1))
+        """Writes the tally to $SD_TALLY_DIR/parity_tally.json when that is set."""
+        d = os.environ.get("SD_TALLY_DIR")
+        if d and Path(d).is_dir():
+            (Path(d) / "parity_tally.json").write_text(json.dumps(self.__dict__, indent=1))
 
 
 TALLY = Tally()
