@@ -161,6 +161,18 @@ __device__ __forceinline__ unsigned long long ld_relaxed_u64(const unsigned long
   return v;
 }
 
+// Arrival counters with the ordering on the counter itself: a fence at GPU
+// scope waits for the memory traffic in flight and costs microseconds while
+// the SM streams, an acquire-release read-modify-write does not.
+__device__ __forceinline__ int atom_add_acq_rel(int* p, int v) {
+  int old;
+  asm volatile("atom.add.acq_rel.gpu.global.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
+}
+__device__ __forceinline__ void red_add_release(int* p, int v) {
+  asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
 __device__ __forceinline__ int ld_acquire(const int* p) {
   int v;
   asm volatile("ld.acquire.gpu.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
@@ -323,15 +335,6 @@ constexpr float kTwo64 = 18446744073709551616.0f;     // 2^64
 __device__ __forceinline__ unsigned long long warp_sum_u64(unsigned long long v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(kFull, v, o);
-  return v;
-}
-
-__device__ __forceinline__ unsigned long long warp_scan_u64(unsigned long long v, int lane) {
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const unsigned long long t = __shfl_up_sync(kFull, v, o);
-    if (lane >= o) v += t;
-  }
   return v;
 }
 
@@ -887,6 +890,7 @@ struct Control {
   static constexpr int kCpl = (kStatStride + 31) / 32;  // statistics chunks per lane
   static constexpr int kWalk = 12;                       // units per lane in one walk round
   static constexpr int kJobs = 64;                       // job ring capacity
+  static constexpr int kScratch = 40;                    // per-lane values of a warp-wide search
 
   const VerifyParams& p;
   const Cta& C;
@@ -898,7 +902,7 @@ struct Control {
   unsigned long long (*red_k)[NS];
   int (*red_n)[NS];
   float* s_lx;
-  unsigned long long* s_walk;  // [32][kWalk] unit sums of the walk in hand (per draw warp)
+  unsigned long long* s_walk;  // [32][kWalk] unit sums of the walk in hand, then [kScratch] (per draw warp)
   int* jobs;                   // [kJobs] job ring
   int* jtail;                  // jobs appended
   int* jhead;                  // jobs taken
@@ -1014,6 +1018,40 @@ struct Control {
   }
 
   // ---- warp-wide draw helpers ---------------------------------------------
+  // The searches below share their per-lane values through the warp's
+  // scratch in shared memory (one barrier per exchange) rather than through
+  // chains of shuffles: every lane reads all 32 values and computes the sums
+  // and the search result itself.
+  __device__ unsigned long long* scratch() const { return s_walk + 32 * kWalk; }
+
+  // Sum of the 32 values in sc[0..32) (read by every lane).
+  __device__ static unsigned long long sum32(const unsigned long long* sc) {
+    unsigned long long t = 0;
+#pragma unroll 8
+    for (int l = 0; l < 32; ++l) t += sc[l];
+    return t;
+  }
+  // The first l whose running sum of sc[0..l] exceeds th (th < the total), and
+  // the running sum before it.
+  __device__ static int first_past(const unsigned long long* sc, unsigned long long th,
+                                   unsigned long long& before) {
+    int ln = 31;
+    unsigned long long run = 0;
+    before = 0;
+    bool found = false;
+#pragma unroll 8
+    for (int l = 0; l < 32; ++l) {
+      const unsigned long long nx = run + sc[l];
+      if (!found && nx > th) {
+        ln = l;
+        before = run;
+        found = true;
+      }
+      run = nx;
+    }
+    return ln;
+  }
+
   // The first of n weights (vocabulary order) whose running sum exceeds the
   // threshold: floor(u * S) when use_u, else th_in clamped below S.  Each
   // lane sums a contiguous block exactly in 64 bits.  Returns false when
@@ -1026,28 +1064,38 @@ struct Control {
     unsigned long long ls = 0;
 #pragma unroll
     for (int q = 0; q < kCpl; ++q) ls += wv[q];
-    const unsigned long long inc = warp_scan_u64(ls, lane);
-    const unsigned long long S = __shfl_sync(kFull, inc, 31);
-    if (S == 0) return false;
+    unsigned long long* sc = scratch();
+    sc[lane] = ls;
+    __syncwarp();
+    const unsigned long long S = sum32(sc);
+    if (S == 0) {
+      __syncwarp();  // the scratch is read before it is reused
+      return false;
+    }
     const unsigned long long thr =
         use_u ? __umul64hi(__float2ull_rn(ufin * kTwo64), S) : (th_in < S ? th_in : S - 1);
-    const unsigned cm = __ballot_sync(kFull, inc > thr);
-    const int ln = __ffs(cm) - 1;
-    int c = -1;
-    unsigned long long th = 0;
+    unsigned long long before;
+    const int ln = first_past(sc, thr, before);
+    __syncwarp();  // every lane has read the lane sums
     if (lane == ln) {
-      unsigned long long run = inc - ls;
-      c = b1 - 1;
+      unsigned long long run = before;
+      int c = b1 - 1;
       for (int q = 0; q < kCpl; ++q) {
         if (q < cpl && b0 + q < b1) {
-          if (run + wv[q] > thr) { c = b0 + q; break; }
+          if (run + wv[q] > thr) {
+            c = b0 + q;
+            break;
+          }
           run += wv[q];
         }
       }
-      th = thr - run;
+      sc[32] = static_cast<unsigned long long>(c);
+      sc[33] = thr - run;
     }
-    c_out = __shfl_sync(kFull, c, ln);
-    th_out = __shfl_sync(kFull, th, ln);
+    __syncwarp();
+    c_out = static_cast<int>(sc[32]);
+    th_out = sc[33];
+    __syncwarp();  // read before the scratch is reused
     return true;
   }
 
@@ -1090,12 +1138,15 @@ struct Control {
         us[u - b0] = su;
         sv += su;
       }
-      const unsigned long long inc = warp_scan_u64(sv, lane);
-      const unsigned long long tot = __shfl_sync(kFull, inc, 31);
+      unsigned long long* sc = scratch();
+      sc[lane] = sv;
+      __syncwarp();
+      const unsigned long long tot = sum32(sc);
       if (th < tot) {
-        int pk = -1;
-        if (sv > 0 && inc - sv <= th && th < inc) {
-          unsigned long long acc = inc - sv;
+        unsigned long long acc;
+        const int ln = first_past(sc, th, acc);
+        __syncwarp();  // every lane has read the block sums
+        if (lane == ln) {
           int u = b1 - 1;
           for (int v = b0; v < b1; ++v) {
             if (acc + us[v - b0] > th) {
@@ -1104,14 +1155,24 @@ struct Control {
             }
             acc += us[v - b0];
           }
-          pk = pick_in(u, th - acc);
+          sc[32] = static_cast<unsigned long long>(pick_in(u, th - acc));
         }
-        const unsigned hit = __ballot_sync(kFull, pk >= 0);
-        return __shfl_sync(kFull, pk, __ffs(hit) - 1);
+        __syncwarp();
+        const int pk = static_cast<int>(sc[32]);
+        __syncwarp();  // read before the scratch is reused
+        return pk;
       }
       th -= tot;
+      __syncwarp();  // read before the next round rewrites the scratch
     }
-    const int lu = static_cast<int>(warp_max_u64(static_cast<unsigned long long>(lastu + 1))) - 1;
+    unsigned long long* sc = scratch();
+    sc[lane] = static_cast<unsigned long long>(lastu + 1);
+    __syncwarp();
+    unsigned long long mx = 0;
+#pragma unroll 8
+    for (int l = 0; l < 32; ++l) mx = sc[l] > mx ? sc[l] : mx;
+    __syncwarp();  // read before the scratch is reused
+    const int lu = static_cast<int>(mx) - 1;
     if (lu < 0) return ub * VE;
     return pick_in(lu, ~0ull);  // every lane: the same unit, the same answer
   }
@@ -1188,17 +1249,20 @@ struct Control {
     // the bonus row's chunk statistics, in case every slot is accepted
     float2 st_bonus[kCpl];
     if (!greedy) load_stats(static_cast<size_t>(c0 + n), st_bonus);
+    // Every lane runs the accept test (lanes past the slots repeat the last
+    // slot and discard the result), so the warp does not split here.
     bool acc = true;
-    if (lane < n) {
-      const int j = lane;
+    if (n > 0) {
+      const bool slot = lane < n;
+      const int j = slot ? lane : n - 1;
       const int x = p.draft_ids[d0 + j];
       const bool x_ok = x >= 0 && x < p.V;
-      if (!x_ok) raise_error(p.err, SD_DEV_ERR_DRAFT_ID);
+      if (slot && !x_ok) raise_error(p.err, SD_DEV_ERR_DRAFT_ID);
       const float4 ts = ts_l;
       if (greedy) {
         const int amax = __float_as_int(ts.w);
-        if (amax < 0) raise_error(p.err, SD_DEV_ERR_LOGITS);
-        acc = x_ok && amax >= 0 && x == amax;
+        if (slot && amax < 0) raise_error(p.err, SD_DEV_ERR_LOGITS);
+        acc = !slot || (x_ok && amax >= 0 && x == amax);
       } else {
         const float4 ds = ds_l;
         const bool ok = isfinite(ts.x) && isfinite(ts.y) && ts.y > 0.0f && isfinite(ds.x) &&
@@ -1211,11 +1275,11 @@ struct Control {
           two_diff(ds.z, ds.x, h, l);
           qx = exp2_df(h, l, s2h, s2l) / ds.y;
         }
-        if (!ok) raise_error(p.err, SD_DEV_ERR_LOGITS);
         const float u = urow[j];
-        if (!(u >= 0.0f && u < 1.0f)) raise_error(p.err, SD_DEV_ERR_UNIFORM);
-        acc = ok && x_ok && (u * qx) <= px;
-        if (p.probs_out) {
+        if (slot && !ok) raise_error(p.err, SD_DEV_ERR_LOGITS);
+        if (slot && !(u >= 0.0f && u < 1.0f)) raise_error(p.err, SD_DEV_ERR_UNIFORM);
+        acc = !slot || (ok && x_ok && (u * qx) <= px);
+        if (slot && p.probs_out) {
           p.probs_out[2 * static_cast<size_t>(d0 + j)] = px;
           p.probs_out[2 * static_cast<size_t>(d0 + j) + 1] = qx;
         }
@@ -1267,8 +1331,9 @@ struct Control {
           const int pos = atomicAdd(&p.ctrl[2], 1);
           st_release(&p.res_list[pos], 1 + ((i << 4) | a));  // publishes the outputs too
         }
-        __threadfence();
-        atomicAdd(&p.ctrl[4], 1);  // one more sampling request decided
+        // one more sampling request decided; releases the warp's outputs (the
+        // lanes' writes are ordered before it by the warp barrier above)
+        red_add_release(&p.ctrl[4], 1);
       }
     }
     __syncwarp();
@@ -1352,19 +1417,15 @@ struct Control {
                                         __uint_as_float(static_cast<uint32_t>(v >> 32))));
         }
       }
-      __threadfence();  // every lane's writes of the row before the count
-      __syncwarp();
+      __syncwarp();  // every lane's writes of the row before lane 0's count
       int old = 0;
       if (lane == 0) {
         __stcg(reinterpret_cast<float4*>(t.draft ? p.st_d + t.row : p.st_t + t.row), stat);
-        __threadfence();  // the row's statistics before the count
-        old = atomicAdd(&p.req_cnt[t.i], 1);
+        // releases this row's statistics, acquires those of the rows counted before
+        old = atom_add_acq_rel(&p.req_cnt[t.i], 1);
       }
       old = __shfl_sync(kFull, old, 0);
-      if (old == (t.n + 1) + (t.greedy ? 0 : t.n) - 1) {  // the request's last row: its tail
-        __threadfence();  // the other rows' statistics, counted before this one
-        push_job(t.i);
-      }
+      if (old == (t.n + 1) + (t.greedy ? 0 : t.n) - 1) push_job(t.i);  // the request's last row: its tail
     } else if (is_slice(u)) {
       const int e = (u >> 18) & 0xFFF;
       unsigned long long* rs = p.rs + static_cast<size_t>(e) * kStatStride;
@@ -1372,15 +1433,12 @@ struct Control {
         const unsigned long long v = s_stat[sl][c];
         if (v != 0) atomicAdd(rs + c, v);
       }
-      __threadfence();  // every lane's sums before the count
-      __syncwarp();
+      __syncwarp();  // every lane's sums before lane 0's count
       int old = 0;
-      if (lane == 0) old = atomicAdd(&p.slice_cnt[e], 1);
+      // releases this slice's sums, acquires those of the slices counted before
+      if (lane == 0) old = atom_add_acq_rel(&p.slice_cnt[e], 1);
       old = __shfl_sync(kFull, old, 0);
-      if (old == G.S_sl - 1) {  // the draw's last slice: its finish
-        __threadfence();  // the other slices' sums, counted before this one
-        push_job(kFinishJob | (u & 0x3FFFFFFF));
-      }
+      if (old == G.S_sl - 1) push_job(kFinishJob | (u & 0x3FFFFFFF));  // the draw's last slice: its finish
     }
   }
 
@@ -1421,7 +1479,10 @@ struct Control {
       }
       code = __shfl_sync(kFull, code, 0);
       if (code == kStopJob) break;
-      __threadfence();  // the unit's statistics and sums, counted by the scheduling warp
+      // lane 0 acquired the job, which the scheduling warp released after its
+      // counter had acquired the statistics and sums; the warp barrier orders
+      // the other lanes' reads after that acquire
+      __syncwarp();
       if (code & kFinishJob) {
         const int e = (code >> 18) & 0xFFF, i = (code >> 4) & 0xFFF, a = code & 15;
         const int c0 = C.cu[i];
@@ -1518,7 +1579,7 @@ __global__ void __launch_bounds__(NT, 1) verify_kernel(const __grid_constant__ V
   __shared__ unsigned long long s_stat[kDepth][kStatStride];
   __shared__ int red_i[NW];
   __shared__ int s_count, s_nsamp;
-  __shared__ unsigned long long s_walk[2][32 * Control<T, VEC, NS>::kWalk];
+  __shared__ unsigned long long s_walk[2][32 * Control<T, VEC, NS>::kWalk + Control<T, VEC, NS>::kScratch];
   __shared__ int s_jobs[Control<T, VEC, NS>::kJobs];
   __shared__ int s_jtail, s_jhead, s_jdone;
   __shared__ __align__(128) unsigned char s_chunk[2][2 * kSlotBytes];  // draw warps' staging
