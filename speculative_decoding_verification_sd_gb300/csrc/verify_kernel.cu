@@ -364,12 +364,14 @@ __device__ __forceinline__ void two_diff(float l, float M, float& hi, float& lo)
 // On the vector path a chunk is one bulk copy of at most kSlotBytes.  The
 // statistics chunks group g consecutive chunks of one warp (spw per warp,
 // NS * spw <= kStatStride).  A residual draw is streamed in S_sl slices:
-// slice s takes chunks [s * m_sl, (s + 1) * m_sl) of every warp's range.
+// slice s takes chunks [s * m_sl, (s + 1) * m_sl) of every warp's range
+// (as many slices as make every slice non-empty, at most kMaxSlices).
 struct Geom {
   int nvec, cpw, CU, nch, g, spw, S_sl, m_sl;
 };
 
 constexpr int kSlotBytes = 4352;  // largest chunk of the vector path (272 vectors)
+constexpr int kMaxSlices = 8;     // slices of one residual draw
 
 __device__ __forceinline__ Geom make_geom(int nvec, bool vec, int ns) {
   Geom G;
@@ -386,8 +388,9 @@ __device__ __forceinline__ Geom make_geom(int nvec, bool vec, int ns) {
   const int spw_max = kStatStride / ns;
   G.g = (G.cpw + spw_max - 1) / spw_max;
   G.spw = (G.cpw + G.g - 1) / G.g;
-  G.S_sl = min(4, G.cpw);
+  G.S_sl = min(kMaxSlices, G.cpw);
   G.m_sl = (G.cpw + G.S_sl - 1) / G.S_sl;
+  G.S_sl = (G.cpw + G.m_sl - 1) / G.m_sl;  // no empty slice
   return G;
 }
 
@@ -433,6 +436,7 @@ struct Cta {
   const int* order;  // [bs] request order of the work list
   const int* ustart; // [bs+1] first row unit of order[k]
   int* q;            // [kDepth] queue
+  int* qx;           // [kDepth] of a slice: its draw's request and slot (i << 4 | a)
   int* pub;          // last published position
   int nsamp;         // sampling requests
   int U_rows;        // row units
@@ -464,9 +468,10 @@ __device__ __forceinline__ Unit locate(const Cta& C, int bs, int u) {
   return t;
 }
 
-// Queue entries past the rows: slice s of listed residual draw e, the draw
-// of request i at slot a, as kResBase | e << 18 | s << 16 | i << 4 | a
-// (e, i < 4096, s < 4, a < 16); kEnd closes the queue.
+// Queue entries past the rows: slice s of listed residual draw e, as
+// kResBase | e << 8 | s (e < 4096, s < 256); the draw's request i and slot a
+// travel beside it in the queue's side array, as i << 4 | a.  kEnd closes
+// the queue.
 constexpr int kResBase = 1 << 30;
 constexpr int kEnd = INT_MAX;
 constexpr int kWait = INT_MAX - 1;  // scheduler: nothing to hand out yet
@@ -629,7 +634,8 @@ struct Streamer {
           f_c0 = cb;
           f_n = ce - cb;
         } else if (is_slice(u)) {
-          const int i = (u >> 4) & 0xFFF, a = u & 15, s = (u >> 16) & 3;
+          const int ia = C.qx[fk % kDepth];
+          const int i = (ia >> 4) & 0xFFF, a = ia & 15, s = u & 0xFF;
           const int c0 = C.cu[i];
           f_base = reinterpret_cast<const char*>(p.target) + static_cast<size_t>(c0 + a) * row_bytes();
           f_base2 = reinterpret_cast<const char*>(p.draft) + static_cast<size_t>(c0 - i + a) * row_bytes();
@@ -795,8 +801,8 @@ struct Streamer {
 
   // Slice unit u: this warp's part of a listed residual draw, summed per
   // statistics chunk in 2^56 fixed point into the draw's chunk sums.
-  __device__ void slice(int u, unsigned long long* sbuf) {
-    const int s = (u >> 16) & 3, i = (u >> 4) & 0xFFF, a = u & 15;
+  __device__ void slice(int u, int ia, unsigned long long* sbuf) {
+    const int s = u & 0xFF, i = (ia >> 4) & 0xFFF, a = ia & 15;
     const int c0 = C.cu[i];
     const float4 ts = __ldcg(reinterpret_cast<const float4*>(p.st_t + c0 + a));
     const float4 ds = __ldcg(reinterpret_cast<const float4*>(p.st_d + c0 - i + a));
@@ -863,7 +869,7 @@ struct Streamer {
       if (u == kEnd) break;
       if constexpr (VEC) refill();
       if (u < C.U_rows) row(k, u, red_m, red_z, red_k, red_n, s_lx, s_stat[k % kDepth]);
-      else if (is_slice(u)) slice(u, s_stat[k % kDepth]);
+      else if (is_slice(u)) slice(u, C.qx[k % kDepth], s_stat[k % kDepth]);
       __syncwarp();
       if (lane == 0) mbar_arrive(&pbar[k % kDepth]);
     }
@@ -915,6 +921,7 @@ struct Control {
   // schedule ahead; a slice slot taken before its draw was listed
   bool rows_done = false;
   int stash = 0, held = -1;
+  mutable int last_ia = 0;  // request and slot of the last slice handed out
 
   __device__ Control(const VerifyParams& p_, const Cta& C_, const Geom& G_, int lane_,
                      uint64_t* pbar_, float (*rm)[NS], float (*rz)[NS],
@@ -978,18 +985,19 @@ struct Control {
       raise_error(p.err, SD_DEV_ERR_TIMEOUT);
       return kWait;
     }
-    return kResBase | (e << 18) | (s << 16) | (v - 1);
+    last_ia = v - 1;  // published beside the unit
+    return kResBase | (e << 8) | s;
   }
   // Next unit for this CTA: a listed slice first, else a row; kEnd once
   // nothing is left anywhere; kWait when a draw may still be listed.
-  // `depth` is the number of units published behind the one being folded.
-  // Once the rows have run out, a CTA takes a slice only when nothing is
-  // queued behind its current unit, so that a late draw's slices go to idle
-  // CTAs and start at once instead of waiting behind queued rows.
+  // `depth` is the number of units published behind the one being folded
+  // (-1: none in flight).  Once the rows have run out, a CTA takes a slice
+  // only when it has no unit in flight, so that a late draw's slices go to
+  // idle CTAs and start at once instead of waiting behind a row.
   __device__ int schedule(int depth) {
     const unsigned long long lc = load_lc();
     const int avail = static_cast<int>(lc & 0xFFFFFFFFull) * G.S_sl;
-    const bool deep = rows_done && depth > 0;
+    const bool deep = rows_done && depth >= 0;
     if (!deep && held < 0 && static_cast<int>(lc >> 32) < avail) held = atomicAdd(&p.ctrl[3], 1);
     if (held >= 0 && held < avail) {
       const int h = held;
@@ -1003,7 +1011,7 @@ struct Control {
         return u;
       }
       rows_done = true;
-      if (depth > 0) return kWait;  // as above: slices only with nothing queued
+      if (depth >= 0) return kWait;  // as above: slices only with nothing in flight
     }
     if (deep || !decided()) return kWait;
     const unsigned long long f = load_lc();  // the final list
@@ -1427,7 +1435,7 @@ struct Control {
       old = __shfl_sync(kFull, old, 0);
       if (old == (t.n + 1) + (t.greedy ? 0 : t.n) - 1) push_job(t.i);  // the request's last row: its tail
     } else if (is_slice(u)) {
-      const int e = (u >> 18) & 0xFFF;
+      const int e = (u >> 8) & 0xFFF;
       unsigned long long* rs = p.rs + static_cast<size_t>(e) * kStatStride;
       for (int c = lane; c < NS * G.spw; c += 32) {
         const unsigned long long v = s_stat[sl][c];
@@ -1438,7 +1446,7 @@ struct Control {
       // releases this slice's sums, acquires those of the slices counted before
       if (lane == 0) old = atom_add_acq_rel(&p.slice_cnt[e], 1);
       old = __shfl_sync(kFull, old, 0);
-      if (old == G.S_sl - 1) push_job(kFinishJob | (u & 0x3FFFFFFF));  // the draw's last slice: its finish
+      if (old == G.S_sl - 1) push_job(kFinishJob | (e << 16) | C.qx[sl]);  // the draw's last slice: its finish
     }
   }
 
@@ -1484,7 +1492,7 @@ struct Control {
       // the other lanes' reads after that acquire
       __syncwarp();
       if (code & kFinishJob) {
-        const int e = (code >> 18) & 0xFFF, i = (code >> 4) & 0xFFF, a = code & 15;
+        const int e = (code >> 16) & 0xFFF, i = (code >> 4) & 0xFFF, a = code & 15;
         const int c0 = C.cu[i];
         const float4 ts = __ldcg(reinterpret_cast<const float4*>(p.st_t + c0 + a));
         const float4 ds = __ldcg(reinterpret_cast<const float4*>(p.st_d + c0 - i + a));
@@ -1509,6 +1517,7 @@ struct Control {
         if (e != kWait) {
           if (lane == 0) {
             C.q[(k_pub + 1) % kDepth] = e;
+            if (is_slice(e)) C.qx[(k_pub + 1) % kDepth] = last_ia;
             st_release_cta(C.pub, k_pub + 1);
           }
           ++k_pub;
@@ -1571,6 +1580,7 @@ __global__ void __launch_bounds__(NT, 1) verify_kernel(const __grid_constant__ V
 
   __shared__ uint64_t pbar[kDepth];  // position k done by every streaming warp
   __shared__ int s_q[kDepth];        // the unit of position k at s_q[k % kDepth]
+  __shared__ int s_qx[kDepth];       // beside a slice unit: its draw's request and slot
   __shared__ int s_pub;              // positions 0..s_pub are published
   __shared__ float red_m[kDepth][NS], red_z[kDepth][NS];
   __shared__ unsigned long long red_k[kDepth][NS];
@@ -1707,7 +1717,7 @@ __global__ void __launch_bounds__(NT, 1) verify_kernel(const __grid_constant__ V
   __syncthreads();
 
   const Geom G = make_geom(nvec, VEC, NS);
-  const Cta C{cu_s, tau_s, order, ustart, s_q, &s_pub, s_nsamp, ustart[p.bs]};
+  const Cta C{cu_s, tau_s, order, ustart, s_q, s_qx, &s_pub, s_nsamp, ustart[p.bs]};
   // The first kWindow positions: rows (no draw is listed yet); the row
   // after them is the control warp's first stash.
   int k_pub = -1;
