@@ -920,6 +920,7 @@ struct Control {
   // lane 0's scheduler state: rows ran out; the next row id, fetched one
   // schedule ahead; a slice slot taken before its draw was listed
   bool rows_done = false;
+  bool dealt = false;  // every row was dealt at the start
   int stash = 0, held = -1;
   mutable int last_ia = 0;  // request and slot of the last slice handed out
 
@@ -1007,7 +1008,7 @@ struct Control {
     if (!rows_done) {
       const int u = stash;
       if (u < C.U_rows) {
-        stash = atomicAdd(&p.ctrl[0], 1);  // used by the next schedule
+        stash = dealt ? C.U_rows : atomicAdd(&p.ctrl[0], 1);  // used by the next schedule
         return u;
       }
       rows_done = true;
@@ -1719,16 +1720,25 @@ __global__ void __launch_bounds__(NT, 1) verify_kernel(const __grid_constant__ V
   const Geom G = make_geom(nvec, VEC, NS);
   const Cta C{cu_s, tau_s, order, ustart, s_q, s_qx, &s_pub, s_nsamp, ustart[p.bs]};
   // The first kWindow positions: rows (no draw is listed yet); the row
-  // after them is the control warp's first stash.
+  // after them is the control warp's first stash.  Each CTA claims these
+  // kWindow + 1 rows at once.  When that covers every row of the call, the
+  // rows are dealt position-major instead (CTA b's q-th is unit
+  // q * gridDim.x + b): consecutive claims would give a request's rows to one
+  // CTA, one after another, and every request would finish last.
   int k_pub = -1;
   int stash = 0;
+  bool dealt = false;
   if (warp == NS && lane == 0) {
-    const int u0 = atomicAdd(&p.ctrl[0], kWindow + 1);
-    for (int q = 0; q < kWindow && u0 + q < C.U_rows; ++q) {
-      s_q[q] = u0 + q;
+    const int G = static_cast<int>(gridDim.x), b = static_cast<int>(blockIdx.x);
+    dealt = C.U_rows <= (kWindow + 1) * G;
+    const int u0 = dealt ? 0 : atomicAdd(&p.ctrl[0], kWindow + 1);
+    for (int q = 0; q < kWindow; ++q) {
+      const int u = dealt ? q * G + b : u0 + q;
+      if (u >= C.U_rows) break;
+      s_q[q] = u;
       k_pub = q;
     }
-    stash = u0 + kWindow;
+    stash = dealt ? kWindow * G + b : u0 + kWindow;
     s_pub = k_pub;
   }
   __syncthreads();
@@ -1743,6 +1753,7 @@ __global__ void __launch_bounds__(NT, 1) verify_kernel(const __grid_constant__ V
                           &s_cbar[warp == NS ? 0 : warp - NS - 1]);
     if (warp == NS) {
       K.stash = stash;
+      K.dealt = dealt;
       K.run_sched(__shfl_sync(kFull, k_pub, 0));
     } else {
       K.run_draw();
