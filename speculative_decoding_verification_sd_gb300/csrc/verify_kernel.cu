@@ -322,7 +322,7 @@ struct ChunkOps<float> {  // 4 fp32 per 16-byte vector
 };
 
 constexpr int kUnroll = 8;                 // element path: loads in flight per lane
-constexpr int kSlots = 3;                  // ring slots per streaming warp
+constexpr int kSlots = 2;                  // ring slots per streaming warp
 constexpr uint32_t kSpinLimit = 1u << 22;  // polls (~100 ns apart) before a wait gives up
 constexpr float kLn2 = 0.693147180559945309f;
 // log2(e) split into two floats (hi + lo) for a double-float exponent.
@@ -428,7 +428,7 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
 // once pub >= k; the control warp keeps at most kWindow positions published
 // ahead of the last one it has folded.
 constexpr int kDepth = 4;
-constexpr int kWindow = 3;
+constexpr int kWindow = 2;  // a unit streaming, one published behind it
 
 struct Cta {
   const int* cu;     // [bs+1] cu_seqlens
@@ -1848,8 +1848,8 @@ cudaError_t choose_verify_shape(int V, int elem, int bs, const sd_launch_cfg* re
   if (e != cudaSuccess) return e;
   e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return e;
-  // 512 threads (13 streaming warps, a 170 KB ring) unless the shared
-  // memory does not fit (large batches), then 256 threads (5 warps, 65 KB).
+  // 512 threads (13 streaming warps, a 113 KB ring) unless the shared
+  // memory does not fit (large batches), then 256 threads (5 warps, 44 KB).
   const int cands[2] = {512, 256};
   for (int ci = 0; ci < 2; ++ci) {
     const int threads = treq ? treq : cands[ci];
