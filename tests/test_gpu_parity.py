@@ -85,6 +85,24 @@ def test_workspace_reuse_across_calls():
         assert int(ws[off:off + size].count_nonzero()) == 0
 
 
+def test_repeated_full_size_calls_are_identical():
+    """Forty calls in a row on one workspace at full vocabulary (mixed
+    temperatures, residual draws spread over many CTAs) give identical
+    results: a check for ordering races between the kernel's warps and CTAs."""
+    w = S.WORKLOADS["adaptive_hc"].with_(bs=96, T=96)
+    pi = S.plan_inputs(w, 5, 0)
+    cu = oracle_plan(pi, w.k_max)["cu_seqlens"]
+    vi = S.verify_inputs(w, 5, 0, cu, pi["draft_lens"])
+    first = gpu_verify(w, vi, cu, w.k_max)
+    assert first["err"] == 0
+    ws = first["workspace"]
+    for rep in range(40):
+        again = gpu_verify(w, vi, cu, w.k_max, workspace=ws)
+        assert again["err"] == 0
+        assert np.array_equal(again["accepted_len"], first["accepted_len"]), rep
+        assert np.array_equal(again["out_tokens"], first["out_tokens"]), rep
+
+
 def test_varlen_draft_lengths_and_zero_drafts():
     w = S.WORKLOADS["varlen_mixed"].with_(bs=24, V=5000)
     for step in range(3):
