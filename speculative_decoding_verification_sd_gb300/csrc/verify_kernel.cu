@@ -12,22 +12,26 @@
 // Design (GB300): one persistent CTA per SM, warp-specialised.  The work is
 // a list of rows -- every compacted target row, and the draft row of every
 // verified slot of a sampling request -- plus the residual draws, which are
-// listed as requests are decided.  In each CTA, NT/32 - 1 streaming warps
+// listed as requests are decided.  In each CTA, NT/32 - 3 streaming warps
 // each own a contiguous range of every row and stream it from HBM through a
 // private ring of bulk copies (mbarrier completion) into shared memory,
 // reducing it to softmax statistics at the request's temperature (kept per
 // chunk for target rows) or to the argmax, plus the logit at the draft
-// token.  They never wait for one another.  The control warp hands out the
-// queue (a row from a global counter, or a slice of a listed residual draw),
-// folds each unit once every streaming warp has arrived on the unit's
-// barrier, stores the row statistics and counts the row for its request;
-// the CTA that counts a request's last row takes its accept decisions and
-// draws its final token: the argmax, a bonus token from p (the chunk
+// token.  They never wait for one another.  The scheduling warp hands out
+// the queue (a row from a global counter, or a slice of a listed residual
+// draw), folds each unit once every streaming warp has arrived on the
+// unit's barrier, stores the row statistics and counts the row for its
+// request; when it counts a request's last row it queues the request's tail
+// for one of the CTA's two draw warps, which takes the accept decisions and
+// draws the final token: the argmax, a bonus token from p (the chunk
 // statistics locate the crossing chunk, which alone is read again), or --
 // after a rejection -- lists a residual draw, whose row pair is streamed
 // again in slices by whichever CTAs claim them; the CTA that folds the last
 // slice finishes the inverse CDF.  Inverse-CDF sums are exact 64-bit fixed
-// point, so the crossing chunk does not depend on summation order.
+// point, so the crossing chunk does not depend on summation order.  The
+// ordering between CTAs rides on the arrival counters (acquire-release
+// read-modify-writes), not on GPU-scope fences, which wait for the memory
+// traffic in flight.
 #include <algorithm>
 #include <atomic>
 #include <climits>
@@ -884,10 +888,11 @@ struct Streamer {
 };
 
 // ---------------------------------------------------------------------------
-// The control warp: hands out the queue, folds each finished unit, runs the
-// tail of every request whose last row it folds, and finishes every
-// residual draw whose last slice it folds.  Scheduling is lane 0's; folds,
-// tails and draws use the whole warp.
+// The control warps.  The scheduling warp hands out the queue, folds each
+// finished unit, and queues the tail of every request whose last row it
+// folds and the finish of every residual draw whose last slice it folds; the
+// two draw warps take those jobs.  Scheduling is lane 0's; folds, tails and
+// draws use the whole warp.
 template <typename T, bool VEC, int NS>
 struct Control {
   using Tr = VT<T, VEC>;
