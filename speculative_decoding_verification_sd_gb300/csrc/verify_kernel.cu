@@ -1260,9 +1260,6 @@ struct Control {
     float4 ts_l = make_float4(0.0f, 1.0f, 0.0f, 0.0f), ds_l = make_float4(0.0f, 1.0f, 0.0f, 0.0f);
     if (lane <= n) ts_l = __ldcg(reinterpret_cast<const float4*>(p.st_t + c0 + lane));
     if (lane < n && !greedy) ds_l = __ldcg(reinterpret_cast<const float4*>(p.st_d + d0 + lane));
-    // the bonus row's chunk statistics, in case every slot is accepted
-    float2 st_bonus[kCpl];
-    if (!greedy) load_stats(static_cast<size_t>(c0 + n), st_bonus);
     // Every lane runs the accept test (lanes past the slots repeat the last
     // slot and discard the result), so the warp does not split here.
     bool acc = true;
@@ -1328,7 +1325,10 @@ struct Control {
       } else if (reject) {
         residual = true;
       } else {
-        pick = bonus(st_bonus, make_rows<T, VEC>(p, C.cu, i, a, tau, ts, ds, false), ufin);
+        // every slot accepted: a bonus draw from the next row (its chunk
+        // statistics are read only here; most sampling requests reject)
+        pick = bonus(static_cast<size_t>(c0 + n), make_rows<T, VEC>(p, C.cu, i, a, tau, ts, ds, false),
+                     ufin);
       }
     }
     // outputs: the accepted draft tokens, the final token (a residual one is
