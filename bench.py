@@ -69,6 +69,27 @@ def dist_env():
     return rank, world, local
 
 
+def reduce_over_ranks(elapsed_ms, units, device, world):
+    """Weak scaling over replicas: the job takes as long as the slowest rank
+    (max of the elapsed times) and does the work of all ranks (sum of the
+    units).  Returns (max elapsed ms, total units); one rank returns its own."""
+    if world <= 1:
+        return float(elapsed_ms), float(units)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(elapsed_ms)], device=device, dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    u = torch.tensor([float(units)], device=device, dtype=torch.float64)
+    dist.all_reduce(u, op=dist.ReduceOp.SUM)
+    return float(t.item()), float(u.item())
+
+
+def whole_job_rate(total_units, steps, elapsed_ms):
+    """Units per second of the whole job: every rank's units of every step over
+    the slowest rank's time."""
+    return total_units * steps / (elapsed_ms / 1e3)
+
+
 def hbm_peak():
     try:
         d = json.loads(PEAKS.read_text())
@@ -372,17 +393,8 @@ def run_ours(args, w, rank, world, local):
     bytes_small = ((bs + 1) * 4 + bs * 4 + B * 4 + bs * (k + 1) * 4 + bs * 4 + bs * (k + 1) * 4
                    + 2 * 16 * rows_read)
     bytes_alg = bytes_rows + bytes_small
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([elapsed_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed_ms = float(t.item())
-        u = torch.tensor([verified], device=dev, dtype=torch.float64)
-        dist.all_reduce(u)
-        total_verified = float(u.item())
-    else:
-        total_verified = float(verified)
-    value = total_verified * args.steps / (elapsed_ms / 1e3)
+    elapsed_ms, total_verified = reduce_over_ranks(elapsed_ms, verified, dev, world)
+    value = whole_job_rate(total_verified, args.steps, elapsed_ms)
     rows_avg_ms = sum(rows_ms) / len(rows_ms)
     achieved = bytes_alg / (rows_avg_ms / 1e3) / 1e9
     peak, peak_kind = hbm_peak()
@@ -420,10 +432,8 @@ def run_ours(args, w, rank, world, local):
     if not args.no_e2e:
         e2e = run_e2e(args, w, sd, dev, stream, pi, vi, cu, ws_bytes, cfg, rows_cap)
         if world > 1 and e2e is not None:
-            import torch.distributed as dist
-            t = torch.tensor([e2e["_ms"]], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e2e["value"] = total_verified * args.steps / (float(t.item()) / 1e3)
+            e2e_ms, _ = reduce_over_ranks(e2e["_ms"], 0, dev, world)
+            e2e["value"] = whole_job_rate(total_verified, args.steps, e2e_ms)
         if e2e is not None:
             e2e.pop("_ms", None)
 
