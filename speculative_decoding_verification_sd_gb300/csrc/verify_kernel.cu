@@ -661,7 +661,9 @@ struct Streamer {
       const uint32_t bytes = static_cast<uint32_t>(min(static_cast<size_t>(G.CU) * 16, row_bytes() - off));
       if (lane == 0) {
         mbar_arrive_expect_tx(&bar[slot], bytes);
-        bulk_load_nohint(ring + slot * kSlotBytes, base + off, bytes, &bar[slot]);
+        // logits are read once: first out of L2, so the small per-call data
+        // (statistics, counters, the next call's planner inputs) stays
+        bulk_load(ring + slot * kSlotBytes, base + off, bytes, &bar[slot], policy_evict_first());
       }
       ++iseq;
       ++fe;
