@@ -180,8 +180,9 @@ sd_status sd_plan(const float* conf_logits, const float* budget_conf,
  *                  no logit is read and outputs are accepted_len = 0,
  *                  out_tokens = -1.
  *   workspace      device scratch of sd_verify_workspace_bytes(bs, k_max)
- *                  bytes, 16-byte aligned: per-row statistics, per-request
- *                  arrival counts and a work counter.  It must be zero-filled
+ *                  bytes, 16-byte aligned: per-row and per-chunk statistics,
+ *                  residual chunk sums, per-request arrival counts, the list
+ *                  of residual draws and work counters.  It must be zero-filled
  *                  once before its first use (e.g. cudaMemsetAsync); every
  *                  call leaves the counters at zero again.  One call at a time
  *                  per workspace.

@@ -87,7 +87,7 @@ struct VT<uint16_t, false> {
   }
 };
 
-// Streaming loads: read once, keep out of L1 (L2 keeps them for the final draw).
+// Element-path loads of the logits through the read-only data path.
 template <typename Raw>
 __device__ __forceinline__ Raw ld_stream(const Raw* p) {
   return __ldg(p);
