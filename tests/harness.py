@@ -141,6 +141,9 @@ def compare_verify(g, o, cu, k_max, requests=None, what=""):
                 f"request {i} differs away from any boundary {what}: gpu a={g['accepted_len'][i]} "
                 f"{g['out_tokens'][i]} oracle a={o['accepted_len'][i]} {o['out_tokens'][i]}")
             near_mis += 1
+            TALLY.cases.append({"what": what, "request": int(i), "near_flags": int(o["near"][i]),
+                                "gpu": [int(g["accepted_len"][i])] + [int(x) for x in g["out_tokens"][i]],
+                                "oracle": [int(o["accepted_len"][i])] + [int(x) for x in o["out_tokens"][i]]})
     TALLY.decisions += o["decisions"]
     TALLY.near_mismatches += near_mis
     if g["probs"] is not None:
