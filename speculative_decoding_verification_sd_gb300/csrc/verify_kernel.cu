@@ -104,32 +104,33 @@ __device__ __forceinline__ float from_ordered(uint32_t u) {
 
 // One thread's values into its running (max, scaled sum) at scale s2:
 // z = sum 2^((l - m) * s2) with m the running maximum.  The exponent
-// arguments and the sum use packed fp32x2 arithmetic.
+// argument is formed as (l - m) * s2 (the rounding of m * s2 in l * s2 - m * s2
+// would scale the whole sum; the vector path keeps that form and undoes the
+// scale with bias_fix).  The arguments and the sum use packed fp32x2
+// arithmetic.
 template <int VE>
-__device__ __forceinline__ void online_add(const float (&f)[VE], float s2, float& m, float& z,
-                                           float& b) {
+__device__ __forceinline__ void online_add(const float (&f)[VE], float s2, float& m, float& z) {
   float vm = f[0];
 #pragma unroll
   for (int e = 1; e < VE; ++e) vm = fmaxf(vm, f[e]);
   if (vm > m) {
     z = (m == -INFINITY) ? 0.0f : z * exp2_ftz((m - vm) * s2);
     m = vm;
-    b = m * s2;
   }
   if (m != -INFINITY) {
     if constexpr (VE % 2 == 0) {
       const float2 s22 = make_float2(s2, s2);
-      const float2 nb2 = make_float2(-b, -b);
+      const float2 nm2 = make_float2(-m, -m);
       float2 acc = make_float2(0.0f, 0.0f);
 #pragma unroll
       for (int e = 0; e < VE; e += 2) {
-        const float2 t = __ffma2_rn(make_float2(f[e], f[e + 1]), s22, nb2);
+        const float2 t = __fmul2_rn(__fadd2_rn(make_float2(f[e], f[e + 1]), nm2), s22);
         acc = __fadd2_rn(acc, make_float2(exp2_ftz(t.x), exp2_ftz(t.y)));
       }
       z += acc.x + acc.y;
     } else {
 #pragma unroll
-      for (int e = 0; e < VE; ++e) z += exp2_ftz(fmaf(f[e], s2, -b));
+      for (int e = 0; e < VE; ++e) z += exp2_ftz((f[e] - m) * s2);
     }
   }
 }
@@ -183,6 +184,18 @@ __device__ __forceinline__ int ld_acquire(const int* p) {
   return v;
 }
 
+constexpr float kLn2 = 0.693147180559945309f;
+
+// The hot loops form each exponent with one fused multiply-add, l * s2 - b
+// with b = RN(M * s2).  That shifts every argument by the same amount, the
+// rounding error of b: (l - M) * s2 = (l * s2 - b) - fma(M, s2, -b), where
+// the fma is exact (the error of a rounded product is representable).  The
+// shift is undone once per sum (or folded into a scale) by the factor
+// 2^-fma(M, s2, -b) = 1 + c, |c| < 1e-6; this returns c.
+__device__ __forceinline__ float bias_fix(float M, float s2, float b) {
+  return __fmul_rn(-__fmaf_rn(M, s2, -b), kLn2);
+}
+
 // Running softmax statistics of one lane over a chunk: (m, z2) with
 // z2.x + z2.y = sum 2^((l - m) * s2); the chunk's maximum is folded in once.
 template <typename T>
@@ -196,7 +209,7 @@ struct ChunkOps<uint16_t> {  // 8 bf16 per 16-byte vector
   }
   template <int N>
   __device__ __forceinline__ static void softmax(const uint4 (&r)[N], float s2, float& m,
-                                                 float2& z2, float& nb) {
+                                                 float2& z2) {
     // per-vector maxima, then a tree over the vectors (short dependency chains)
     uint32_t vm[N];
 #pragma unroll
@@ -214,10 +227,10 @@ struct ChunkOps<uint16_t> {  // 8 bf16 per 16-byte vector
         z2 = __fmul2_rn(z2, make_float2(sc, sc));
       }
       m = lm;
-      nb = -m * s2;
     }
     if (m != -INFINITY) {
-      const float2 s22 = make_float2(s2, s2), nb2 = make_float2(nb, nb);
+      const float b = __fmul_rn(m, s2);
+      const float2 s22 = make_float2(s2, s2), nb2 = make_float2(-b, -b);
       float2 acc[4];  // four independent partial sums, one per word of the vector
 #pragma unroll
       for (int h = 0; h < 4; ++h) acc[h] = make_float2(0.0f, 0.0f);
@@ -230,7 +243,9 @@ struct ChunkOps<uint16_t> {  // 8 bf16 per 16-byte vector
           acc[h] = __fadd2_rn(acc[h], make_float2(exp2_ftz(t.x), exp2_ftz(t.y)));
         }
       }
-      z2 = __fadd2_rn(z2, __fadd2_rn(__fadd2_rn(acc[0], acc[1]), __fadd2_rn(acc[2], acc[3])));
+      const float2 sum = __fadd2_rn(__fadd2_rn(acc[0], acc[1]), __fadd2_rn(acc[2], acc[3]));
+      const float c = bias_fix(m, s2, b);
+      z2 = __ffma2_rn(sum, make_float2(c, c), __fadd2_rn(z2, sum));
     }
   }
   // Running argmax of one lane: the first vector whose maximum strictly
@@ -271,7 +286,7 @@ struct ChunkOps<float> {  // 4 fp32 per 16-byte vector
   }
   template <int N>
   __device__ __forceinline__ static void softmax(const float4 (&r)[N], float s2, float& m,
-                                                 float2& z2, float& nb) {
+                                                 float2& z2) {
     float vm[N];
 #pragma unroll
     for (int q = 0; q < N; ++q) vm[q] = fmaxf(fmaxf(r[q].x, r[q].y), fmaxf(r[q].z, r[q].w));
@@ -288,10 +303,10 @@ struct ChunkOps<float> {  // 4 fp32 per 16-byte vector
         z2 = __fmul2_rn(z2, make_float2(sc, sc));
       }
       m = lm;
-      nb = -m * s2;
     }
     if (m != -INFINITY) {
-      const float2 s22 = make_float2(s2, s2), nb2 = make_float2(nb, nb);
+      const float b = __fmul_rn(m, s2);
+      const float2 s22 = make_float2(s2, s2), nb2 = make_float2(-b, -b);
       float2 a0 = make_float2(0.0f, 0.0f), a1 = make_float2(0.0f, 0.0f);  // independent sums
 #pragma unroll
       for (int q = 0; q < N; ++q) {
@@ -300,7 +315,9 @@ struct ChunkOps<float> {  // 4 fp32 per 16-byte vector
         a0 = __fadd2_rn(a0, make_float2(exp2_ftz(t0.x), exp2_ftz(t0.y)));
         a1 = __fadd2_rn(a1, make_float2(exp2_ftz(t1.x), exp2_ftz(t1.y)));
       }
-      z2 = __fadd2_rn(z2, __fadd2_rn(a0, a1));
+      const float2 sum = __fadd2_rn(a0, a1);
+      const float c = bias_fix(m, s2, b);
+      z2 = __ffma2_rn(sum, make_float2(c, c), __fadd2_rn(z2, sum));
     }
   }
   template <int N>
@@ -328,7 +345,6 @@ struct ChunkOps<float> {  // 4 fp32 per 16-byte vector
 constexpr int kUnroll = 8;                 // element path: loads in flight per lane
 constexpr int kSlots = 2;                  // ring slots per streaming warp
 constexpr uint32_t kSpinLimit = 1u << 22;  // polls (~100 ns apart) before a wait gives up
-constexpr float kLn2 = 0.693147180559945309f;
 // log2(e) split into two floats (hi + lo) for a double-float exponent.
 constexpr float kLog2eHi = 1.44269502162933349609375f;
 constexpr float kLog2eLo = 1.925963033500011079e-08f;
@@ -494,7 +510,10 @@ template <typename Raw>
 struct DrawRows {
   const Raw* rt;  // unit u at rt[u - off] (off > 0: a staged copy in shared memory)
   const Raw* rd;
-  float Mt, Md, iZt, iZd, s2;
+  float Mt, Md, s2;
+  float bt, bd;    // RN(Mt * s2), RN(Md * s2): exponent arguments l * s2 - b
+  float iZt, iZd;  // 1 / Z, each times the correction of its bias (bias_fix)
+  float sp;        // 2^40 times the target bias's correction (draws from p)
   int off;
 };
 
@@ -512,14 +531,21 @@ __device__ __forceinline__ DrawRows<typename VT<T, VEC>::Raw> make_rows(
                : w.rt;
   w.Mt = ts.x;
   w.Md = ds.x;
-  w.iZt = 1.0f / ts.y;
-  w.iZd = 1.0f / ds.y;
   w.s2 = kLog2e / tau;
+  w.bt = __fmul_rn(w.Mt, w.s2);
+  w.bd = __fmul_rn(w.Md, w.s2);
+  // no correction for a non-finite maximum (the weights are not finite then)
+  const float ct = fabsf(w.bt) < INFINITY ? bias_fix(w.Mt, w.s2, w.bt) : 0.0f;
+  const float cd = fabsf(w.bd) < INFINITY ? bias_fix(w.Md, w.s2, w.bd) : 0.0f;
+  const float izt = 1.0f / ts.y, izd = 1.0f / ds.y;
+  w.iZt = __fmaf_rn(izt, ct, izt);
+  w.iZd = __fmaf_rn(izd, cd, izd);
+  w.sp = __fmaf_rn(kTwo40, ct, kTwo40);
   w.off = 0;
   return w;
 }
 
-// max(p - q, 0) of one element
+// max(p - q, 0) of one element (biases bt, bd; iZt, iZd carry their corrections)
 __device__ __forceinline__ float res_weight(float f, float g, float s2, float bt, float bd,
                                             float iZt, float iZd) {
   const float et = exp2_ftz(fmaf(f, s2, -bt));
@@ -535,10 +561,9 @@ __device__ __forceinline__ float fast_res(const DrawRows<typename VT<T, VEC>::Ra
   float f[Tr::VE], g[Tr::VE];
   Tr::unpack(ra, f);
   Tr::unpack(rb, g);
-  const float bt = w.Mt * w.s2, bd = w.Md * w.s2;
   float ws = 0.0f;
 #pragma unroll
-  for (int e = 0; e < Tr::VE; ++e) ws += res_weight(f[e], g[e], w.s2, bt, bd, w.iZt, w.iZd);
+  for (int e = 0; e < Tr::VE; ++e) ws += res_weight(f[e], g[e], w.s2, w.bt, w.bd, w.iZt, w.iZd);
   return ws;
 }
 
@@ -555,10 +580,9 @@ __device__ __forceinline__ void elem_res(const DrawRows<typename VT<T, VEC>::Raw
   float f[Tr::VE], g[Tr::VE];
   Tr::unpack(w.rt[u - w.off], f);
   Tr::unpack(w.rd[u - w.off], g);
-  const float bt = w.Mt * w.s2, bd = w.Md * w.s2;
 #pragma unroll
   for (int e = 0; e < Tr::VE; ++e)
-    wi[e] = __float2ull_rn(__fmul_rn(res_weight(f[e], g[e], w.s2, bt, bd, w.iZt, w.iZd), kTwo56));
+    wi[e] = __float2ull_rn(__fmul_rn(res_weight(f[e], g[e], w.s2, w.bt, w.bd, w.iZt, w.iZd), kTwo56));
 }
 
 // Draw from p: unit u's weight, and its elements' weights.
@@ -568,11 +592,10 @@ __device__ __forceinline__ unsigned long long unit_p(const DrawRows<typename VT<
   using Tr = VT<T, VEC>;
   float f[Tr::VE];
   Tr::unpack(w.rt[u - w.off], f);
-  const float bt = w.Mt * w.s2;
   float ws = 0.0f;
 #pragma unroll
-  for (int e = 0; e < Tr::VE; ++e) ws += exp2_ftz(fmaf(f[e], w.s2, -bt));
-  return __float2ull_rn(__fmul_rn(ws, kTwo40));
+  for (int e = 0; e < Tr::VE; ++e) ws += exp2_ftz(fmaf(f[e], w.s2, -w.bt));
+  return __float2ull_rn(__fmul_rn(ws, w.sp));
 }
 template <typename T, bool VEC>
 __device__ __forceinline__ void elem_p(const DrawRows<typename VT<T, VEC>::Raw>& w, int u,
@@ -580,9 +603,8 @@ __device__ __forceinline__ void elem_p(const DrawRows<typename VT<T, VEC>::Raw>&
   using Tr = VT<T, VEC>;
   float f[Tr::VE];
   Tr::unpack(w.rt[u - w.off], f);
-  const float bt = w.Mt * w.s2;
 #pragma unroll
-  for (int e = 0; e < Tr::VE; ++e) wi[e] = __float2ull_rn(__fmul_rn(exp2_ftz(fmaf(f[e], w.s2, -bt)), kTwo40));
+  for (int e = 0; e < Tr::VE; ++e) wi[e] = __float2ull_rn(__fmul_rn(exp2_ftz(fmaf(f[e], w.s2, -w.bt)), w.sp));
 }
 
 // ---------------------------------------------------------------------------
@@ -743,16 +765,16 @@ struct Streamer {
         if (t.greedy) {
           ChunkOps<T>::argmax(rv, u0 + lane, best, bvec, bv, nanf);
         } else {
-          float m = -INFINITY, nb = 0.0f;
+          float m = -INFINITY;
           float2 z2 = make_float2(0.0f, 0.0f);
-          ChunkOps<T>::softmax(rv, s2, m, z2, nb);
+          ChunkOps<T>::softmax(rv, s2, m, z2);
           chunk_reduce(m, z2.x + z2.y, s2, mc, zc);
         }
         __syncwarp();
         ++cseq;
         refill();
       } else {
-        float m = -INFINITY, z = 0.0f, b = 0.0f;
+        float m = -INFINITY, z = 0.0f;
         for (int v0 = u0 + lane; v0 < u0 + nv; v0 += 32 * kUnroll) {
           Raw rv[kUnroll];
 #pragma unroll
@@ -769,7 +791,7 @@ struct Streamer {
                 nanf |= (f[0] != f[0]);
                 if (f[0] > best) { best = f[0]; bidx = v; }
               } else {
-                online_add<VE>(f, s2, m, z, b);
+                online_add<VE>(f, s2, m, z);
               }
             }
           }
