@@ -26,7 +26,7 @@ _SRC = _HERE / "sd_oracle.cpp"
 _LIB = _HERE / "libsd_oracle.so"
 
 F32, BF16 = 0, 1
-MODE_ADAPTIVE, MODE_ALL_SLOTS = 0, 1
+MODE_ADAPTIVE, MODE_ALL_SLOTS, MODE_UNIFORM_K = 0, 1, 2
 NEAR_TOPB, NEAR_BUDGET = 1, 2
 NEAR_ACCEPT, NEAR_CDF, DEGENERATE_RESIDUAL = 1, 2, 4
 
@@ -93,7 +93,9 @@ def survival(conf, draft_lens):
 def plan(conf, draft_lens, k_max, cost=None, T=0, mode=MODE_ADAPTIVE,
          budget_conf=None, budget_draft_lens=None):
     """Planning stage.  Returns a dict with B, slot_mask, num_verified,
-    cu_seqlens, obj (objective per B of the budget set) and near flags."""
+    cu_seqlens, obj (objective per B of the budget set; per K in uniform-K
+    mode) and near flags.  In uniform-K mode B is the number of verified
+    slots and K* = max(num_verified)."""
     dl = _c(draft_lens, np.int32)
     bs = len(dl)
     conf = _c(conf, np.float32)
@@ -109,6 +111,8 @@ def plan(conf, draft_lens, k_max, cost=None, T=0, mode=MODE_ADAPTIVE,
     if mode == MODE_ADAPTIVE and cost is not None:
         nbud = int(bdl.sum()) if bdl is not None else int(dl.sum())
         nobj = max(1, min(nbud, len(cost) - 1 - T) + 1)
+    elif mode == MODE_UNIFORM_K:
+        nobj = int(dl.max()) + 1 if bs else 1
     obj = np.full(nobj, np.nan, np.float64)
     rc = _load().oracle_plan(_ptr(conf), _ptr(dl), bs, k_max, _ptr(bconf), _ptr(bdl),
                              0 if bdl is None else len(bdl), _ptr(cost),

@@ -11,6 +11,9 @@
 //
 //   planning  (adaptive verification):
 //     [fosworld blog "추측 디코딩과 vLLM 적응형 검증", section "동작", steps 1-3]
+//     uniform-K mode: [discuss.pytorch.kr "DSD feat. Cohere", section
+//      "동적 추측 디코딩(DSD)의 핵심 아이디어": one draft length K for the
+//      whole batch, chosen to maximise goodput = AL / ITL]
 //     [agentlenshq "vLLM DSpark을 활용한 적응형 검증", section
 //      "DSpark 신뢰도 스케줄링 메커니즘": Global Top-B Selection,
 //      Budget Calculation, Execution Pipeline]
@@ -30,7 +33,10 @@
 //   O6  B in [0, min(N, cost_len-1-T)], ties in the objective -> smallest B
 //   O7  cost forced monotone: cost'[n] = max(cost[1..n]); cost[0] unused
 //   O10 optional previous-step confidences size the budget, current ones
-//       assign the slots
+//       assign the slots (adaptive mode only)
+//   O24 uniform K: AL(K) = R + sum_i sum_{j < min(K, K_i)} s_{i,j} (the same
+//       survival estimates), ITL(K) = cost'[T + sum_i min(K, K_i)]; K ranges
+//       over 0..max_i K_i with T + tokens <= cost_len-1; ties -> smallest K
 //   O11 p = softmax(target/tau), q = softmax(draft/tau), same tau; tau = 0
 //       is greedy
 //   O12 uniforms[i][j] (j < k_max) test slot j, uniforms[i][k_max] is the
@@ -57,7 +63,7 @@ constexpr double kNearRel = 1e-5;
 
 enum { ORC_OK = 0, ORC_ERR_ARG = -1, ORC_ERR_DATA = -5 };
 enum { ORC_F32 = 0, ORC_BF16 = 1 };
-enum { ORC_MODE_ADAPTIVE = 0, ORC_MODE_ALL_SLOTS = 1 };
+enum { ORC_MODE_ADAPTIVE = 0, ORC_MODE_ALL_SLOTS = 1, ORC_MODE_UNIFORM_K = 2 };
 
 // Near flags of the plan.
 enum { NEAR_TOPB = 1, NEAR_BUDGET = 2 };
@@ -135,6 +141,46 @@ BudgetResult budget_argmax(const std::vector<float>& key, const std::vector<int>
   if (Bmax >= 1 && best - runner <= kNearRel * std::fabs(best)) r.near |= NEAR_BUDGET;
   if (obj_out)
     for (int B = 0; B <= Bmax; ++B) obj_out[B] = obj[static_cast<size_t>(B)];
+  return r;
+}
+
+// Uniform draft length (DSD, O24): every request verifies the first
+// min(K, K_i) slots of its draft.  For each K, AL(K) is R plus the survival
+// of those slots and ITL(K) the monotone cost of the step's T + (their
+// number) tokens; the smallest K with the largest AL / ITL wins.  obj_out
+// [max_i K_i + 1] receives the objective per K (NaN where the cost table is
+// too short).
+BudgetResult uniform_argmax(const std::vector<float>& key, const int* draft_lens, int bs, int T,
+                            const std::vector<double>& cost_mono, int cost_len, double* obj_out) {
+  const int L = cost_len - 1;
+  int Kcap = 0;
+  for (int i = 0; i < bs; ++i) Kcap = std::max(Kcap, draft_lens[i]);
+  std::vector<double> obj(static_cast<size_t>(Kcap) + 1,
+                          std::numeric_limits<double>::quiet_NaN());
+  for (int K = 0; K <= Kcap; ++K) {
+    double E = static_cast<double>(bs);
+    int tokens = 0;
+    size_t off = 0;
+    for (int i = 0; i < bs; ++i) {
+      const int n = std::min(K, draft_lens[i]);
+      for (int j = 0; j < n; ++j) E += static_cast<double>(key[off + static_cast<size_t>(j)]);
+      tokens += n;
+      off += static_cast<size_t>(draft_lens[i]);
+    }
+    if (T + tokens > L) break;  // tokens grow with K: no larger K fits either
+    obj[static_cast<size_t>(K)] = E / cost_mono[static_cast<size_t>(T + tokens)];
+  }
+  BudgetResult r;
+  double best = obj[0];
+  for (int K = 1; K <= Kcap; ++K)
+    if (obj[static_cast<size_t>(K)] > best) { best = obj[static_cast<size_t>(K)]; r.B = K; }
+  double runner = -std::numeric_limits<double>::infinity();
+  for (int K = 0; K <= Kcap; ++K)
+    if (K != r.B && !std::isnan(obj[static_cast<size_t>(K)]))
+      runner = std::max(runner, obj[static_cast<size_t>(K)]);
+  if (best - runner <= kNearRel * std::fabs(best)) r.near |= NEAR_BUDGET;
+  if (obj_out)
+    for (int K = 0; K <= Kcap; ++K) obj_out[K] = obj[static_cast<size_t>(K)];
   return r;
 }
 
@@ -230,7 +276,8 @@ int oracle_plan(const float* conf, const int* draft_lens, int bs, int k_max,
                 double* obj_out, int* near_out) {
   if (!draft_lens || !B_out || !slot_mask || !num_verified || !cu_seqlens) return ORC_ERR_ARG;
   if (bs < 1 || k_max < 0) return ORC_ERR_ARG;
-  if (mode != ORC_MODE_ADAPTIVE && mode != ORC_MODE_ALL_SLOTS) return ORC_ERR_ARG;
+  if (mode != ORC_MODE_ADAPTIVE && mode != ORC_MODE_ALL_SLOTS && mode != ORC_MODE_UNIFORM_K)
+    return ORC_ERR_ARG;
   for (int i = 0; i < bs; ++i)
     if (draft_lens[i] < 0 || draft_lens[i] > k_max) return ORC_ERR_DATA;
   int N = 0;
@@ -241,7 +288,36 @@ int oracle_plan(const float* conf, const int* draft_lens, int bs, int k_max,
   std::vector<uint8_t> selected(static_cast<size_t>(N), 0);
   int near = 0;
   int B = N;
-  if (mode == ORC_MODE_ADAPTIVE) {
+  if (mode == ORC_MODE_UNIFORM_K) {
+    if (!conf || !cost || T < 1 || cost_len < T + 1) return ORC_ERR_ARG;
+    const int L = cost_len - 1;
+    std::vector<double> cost_mono(static_cast<size_t>(cost_len), 0.0);
+    double run = -std::numeric_limits<double>::infinity();
+    for (int n = 1; n < cost_len; ++n) {
+      run = std::max(run, static_cast<double>(cost[n]));
+      cost_mono[static_cast<size_t>(n)] = run;
+    }
+    std::vector<double> s;
+    survival(conf, draft_lens, bs, s);
+    std::vector<float> key(s.size());
+    for (size_t q = 0; q < s.size(); ++q) {
+      if (!std::isfinite(s[q])) return ORC_ERR_DATA;
+      key[q] = static_cast<float>(s[q]);
+    }
+    // the entries a budget of up to min(N, L-T) slots reads, as in adaptive mode
+    for (int n = T; n <= T + std::min(N, L - T); ++n)
+      if (!std::isfinite(cost[n]) || !(cost[n] > 0.0f)) return ORC_ERR_DATA;
+    BudgetResult kr = uniform_argmax(key, draft_lens, bs, T, cost_mono, cost_len, obj_out);
+    near |= kr.near;
+    B = 0;
+    size_t off = 0;
+    for (int i = 0; i < bs; ++i) {
+      const int n = std::min(kr.B, draft_lens[i]);
+      for (int j = 0; j < n; ++j) selected[off + static_cast<size_t>(j)] = 1;
+      B += n;
+      off += static_cast<size_t>(draft_lens[i]);
+    }
+  } else if (mode == ORC_MODE_ADAPTIVE) {
     if (!conf || !cost || T < 1 || cost_len < T + 1) return ORC_ERR_ARG;
     if (budget_conf && (!budget_draft_lens || bs_budget < 1)) return ORC_ERR_ARG;
     const int L = cost_len - 1;
