@@ -267,7 +267,8 @@ def run_reference(args, w, rank, world):
 def config_of(w):
     return {"workload": w.name, "bs": w.bs, "k_max": w.k_max, "V": w.V,
             "logits": "fp32" if w.dtype == S.F32 else "bf16", "T": w.T,
-            "mode": "adaptive" if w.mode == S.MODE_ADAPTIVE else "all_slots",
+            "mode": {S.MODE_ADAPTIVE: "adaptive", S.MODE_ALL_SLOTS: "all_slots",
+                     S.MODE_UNIFORM_K: "uniform_k"}[w.mode],
             "parallelism": "replicas (independent batch per GPU)",
             "l2": "two alternating input sets, each larger than L2"}
 

@@ -55,7 +55,8 @@ typedef enum { SD_F32 = 0, SD_BF16 = 1 } sd_dtype;
 
 typedef enum {
   SD_MODE_ADAPTIVE = 0,  /* budget chosen by the cost model ([AV-page] Budget Calculation) */
-  SD_MODE_ALL_SLOTS = 1  /* every drafted slot verified (fixed-K speculative decoding) */
+  SD_MODE_ALL_SLOTS = 1, /* every drafted slot verified (fixed-K speculative decoding) */
+  SD_MODE_UNIFORM_K = 2  /* one draft length K for the batch, by goodput ([DSD-page]) */
 } sd_mode;
 
 /* Device error bits (OR-ed into *err_flag). */
@@ -99,11 +100,23 @@ typedef enum {
  *        (bs + sum of the B largest s) / cost'[T+B];
  *   a slot is selected iff its rank < B*.
  *
+ * SD_MODE_UNIFORM_K ([DSD-page] discuss.pytorch.kr "DSD feat. Cohere",
+ * "동적 추측 디코딩(DSD)의 핵심 아이디어": one draft length for the whole
+ * batch, chosen to maximise goodput = AL / ITL) computes instead, with
+ * n(K) = sum_i min(K, draft_lens[i]):
+ *   K* = smallest argmax over K in [0, max_i draft_lens[i]] with
+ *        n(K) <= cost_len-1-T of
+ *        (bs + sum_i sum_{j < min(K, draft_lens[i])} s_{i,j}) / cost'[T+n(K)];
+ *   slot (i,j) is selected iff j < K*; B* = n(K*).  K* is max_i n_i.
+ * The same survival s, cost' and error checks as the adaptive mode (the cost
+ * entries T..T+min(N, cost_len-1-T) must be finite and > 0).
+ *
  * Arguments
  *   conf_logits      [N] fp32, packed by request: slot (i,j) at
  *                    offset_i + j, offset = exclusive scan of draft_lens.
  *                    Unused (may be NULL) in SD_MODE_ALL_SLOTS.
- *   budget_conf      [N'] fp32 previous-step confidences packed by
+ *   budget_conf      (SD_MODE_ADAPTIVE only; ignored in the other modes)
+ *                    [N'] fp32 previous-step confidences packed by
  *                    budget_draft_lens [bs_budget], or NULL to size the budget
  *                    from conf_logits.  When given, B* is computed from them
  *                    (same T, R = bs) and clipped to min(N, cost_len-1-T);
@@ -111,9 +124,10 @@ typedef enum {
  *   draft_lens       [bs] int32, 0 <= draft_lens[i] <= k_max.
  *   cost_table       [cost_len] fp32, cost of a step of n tokens at index n.
  *                    Unused (may be NULL) in SD_MODE_ALL_SLOTS.
- *   T                non-draft tokens of the step (>= 1 in adaptive mode).
+ *   T                non-draft tokens of the step (>= 1 in the adaptive and
+ *                    uniform-K modes).
  * Outputs
- *   B_out            [1] int32: B*.
+ *   B_out            [1] int32: B* (the number of verified draft slots).
  *   slot_mask        [bs*k_max] uint8: slot (i,j) at i*k_max+j, 1 = verified.
  *   num_verified     [bs] int32: n_i (a prefix of request i's draft).
  *   cu_seqlens       [bs+1] int32: cu[0] = 0, cu[i+1] = cu[i] + n_i + 1

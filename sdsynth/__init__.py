@@ -32,7 +32,7 @@ _SRC = _HERE / "synth.c"
 _LIB = _HERE / "libsdsynth.so"
 
 F32, BF16 = 0, 1
-MODE_ADAPTIVE, MODE_ALL_SLOTS = 0, 1
+MODE_ADAPTIVE, MODE_ALL_SLOTS, MODE_UNIFORM_K = 0, 1, 2
 ST_CONF, ST_UNIFORM, ST_LENS = 10, 11, 12
 
 
@@ -213,6 +213,8 @@ WORKLOADS = {
         conf_mean=lambda j: 2.0 - 0.6 * j, conf_sd=1.0, T=1024,
         cost=cost_linear_stairs(1.0, 0.003, 32, 8192)),
 }
+# adaptive_hc's requests planned with one draft length for the whole batch
+WORKLOADS["uniform_hc"] = WORKLOADS["adaptive_hc"].with_(name="uniform_hc", mode=MODE_UNIFORM_K)
 
 WORKLOAD_ORDER = ("tiny", "dense_fixed_k", "adaptive_hc", "varlen_mixed", "stress")
 
@@ -232,7 +234,7 @@ def plan_inputs(w: Workload, seed: int, step: int = 0) -> dict:
     dl = draft_lens(w, seed, step)
     out = {"draft_lens": dl, "bs": w.bs, "k_max": w.k_max, "T": w.T, "mode": w.mode,
            "cost": w.cost, "conf": None, "budget_conf": None, "budget_draft_lens": None}
-    if w.mode == MODE_ADAPTIVE:
+    if w.mode != MODE_ALL_SLOTS:
         out["conf"] = conf_logits(w, seed, step, dl)
         if w.budget_from_previous and step > 0:
             pdl = draft_lens(w, seed, step - 1)

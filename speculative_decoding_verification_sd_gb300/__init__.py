@@ -26,7 +26,7 @@ from ._lib import (SD_NOALLOC_SCRATCH_BYTES, SD_BF16, SD_DEV_ERR_CONF, SD_DEV_ER
                    SD_DEV_ERR_TEMP, SD_DEV_ERR_UNIFORM, SD_ERR_CUDA,
                    SD_ERR_DEVICE_CHECK, SD_ERR_INVALID_ARG, SD_ERR_SHAPE, SD_ERR_UNSUPPORTED,
                    SD_F32, SD_MAX_K, SD_MAX_PLAN_SLOTS, SD_MAX_V, SD_MAX_VERIFY_BS,
-                   SD_MODE_ADAPTIVE, SD_MODE_ALL_SLOTS, SD_OK, SdError, sd_launch_cfg)
+                   SD_MODE_ADAPTIVE, SD_MODE_ALL_SLOTS, SD_MODE_UNIFORM_K, SD_OK, SdError, sd_launch_cfg)
 
 __all__ = [
     "sd_plan", "sd_verify", "sd_verify_ex", "sd_verify_noalloc", "sd_plan_workspace_bytes",

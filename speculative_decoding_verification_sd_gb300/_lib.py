@@ -16,7 +16,7 @@ LIB_PATH = PKG / "libsdverify.so"
 SD_OK, SD_ERR_INVALID_ARG, SD_ERR_SHAPE, SD_ERR_UNSUPPORTED, SD_ERR_CUDA, SD_ERR_DEVICE_CHECK = (
     0, -1, -2, -3, -4, -5)
 SD_F32, SD_BF16 = 0, 1
-SD_MODE_ADAPTIVE, SD_MODE_ALL_SLOTS = 0, 1
+SD_MODE_ADAPTIVE, SD_MODE_ALL_SLOTS, SD_MODE_UNIFORM_K = 0, 1, 2
 
 SD_DEV_ERR_DRAFT_LENS = 0x001
 SD_DEV_ERR_CONF = 0x002

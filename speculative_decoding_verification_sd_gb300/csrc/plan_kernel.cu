@@ -13,6 +13,11 @@
 //              cost' = running max of the table (forced monotone)
 //              ["동작" step 3; same page, Budget Calculation, and
 //               "기술적 구현 및 CUDA Graphs" / Cost Modeling, CUDA Graph Padding]
+//   uniform K  (the other planning mode) one draft length K for the batch:
+//              K* = smallest argmax_K (R + survival of each request's first
+//              min(K, K_i) slots) / cost'[T + their number]
+//              [discuss.pytorch.kr "DSD feat. Cohere", "동적 추측 디코딩(DSD)의
+//               핵심 아이디어": goodput = AL / ITL]
 //   compaction slot mask, n_i and cu_seqlens (n_i drafts + 1 row per request)
 //              [same page, Execution Pipeline: assignment on the GPU without a
 //               host round trip]
@@ -39,6 +44,7 @@ constexpr unsigned kOneBits = 0x3F800000u;  // bit pattern of 1.0f
 constexpr int kBucketShift = 15;   // 2^15 ulps a bucket: 256 buckets a binade
 static_assert(kBuckets == 4 * NT, "four bucket counters a thread, moved as one 16-byte vector");
 constexpr float kFix = 281474976710656.0f;  // 2^48
+constexpr int kMaxP = 16;          // pow2ceil(SD_MAX_K)
 
 struct PlanShared {
   unsigned long long tot_u64[NW];  // per-warp totals of the block scans
@@ -48,6 +54,8 @@ struct PlanShared {
   int err;
   unsigned long long best;         // budget argmax (packed objective, budget)
   int cmax;                        // largest bucket of the bucket sort
+  unsigned long long col_s[kMaxP]; // uniform K: survival sum of position j (2^48)
+  int col_n[kMaxP];                // uniform K: requests that draft position j
 };
 
 __device__ __forceinline__ void cp_async4(void* dst, const void* src) {
@@ -422,6 +430,78 @@ __device__ int budget_argmax(const unsigned long long* sorted, unsigned long lon
   return static_cast<int>(0xFFFFFFFFu - static_cast<uint32_t>(sh.best & 0xFFFFFFFFull));
 }
 
+// Uniform draft length.  keys: build_keys' output in packed order (slot
+// (i, j) at i * P + j, sentinel where request i has no slot j).  The
+// survival of each position j is summed over the requests (2^48 fixed
+// point, exact) with the number of requests that reach it; warp K then forms
+// AL(K) = R + sum_{j<K} col_s[j] and the token count n(K) = sum_{j<K}
+// col_n[j], and takes the objective AL(K) / cost'[T + n(K)] for every K up
+// to the longest draft whose tokens fit the table.  cm[b] holds cost[T+b]
+// (b <= Bmax, each checked here) and lm each thread's maximum of its share
+// of cost[1..T).  sh.col_s / sh.col_n start zeroed.  Returns K* (smallest
+// maximiser) and its token count in *B; after its last barrier it only
+// reads shared state that later steps do not write.
+__device__ int uniform_argmax(const unsigned long long* keys, int NP, int P, int k_max, int Bmax,
+                              int R, const float* cm, float lm, int lm_bad, PlanShared& sh,
+                              int* B) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  if (threadIdx.x == 0) sh.best = 0ull;
+  // P divides NT, so every slot a thread visits has the same position j
+  unsigned long long acc = 0;
+  int cnt = 0;
+#pragma unroll
+  for (int r = 0; r < kSlotPer; ++r) {
+    const int q = r * NT + static_cast<int>(threadIdx.x);
+    if (q >= NP) break;
+    const unsigned long long key = keys[q];
+    if (key != kSentinel) {
+      acc += fix48(__uint_as_float(~static_cast<uint32_t>(key >> 32)));
+      ++cnt;
+    }
+  }
+  for (int o = P; o < 32; o <<= 1) {
+    acc += __shfl_xor_sync(kFull, acc, o);
+    cnt += __shfl_xor_sync(kFull, cnt, o);
+  }
+  if (lane < P && lane < 32) {
+    atomicAdd(&sh.col_s[lane], acc);
+    atomicAdd(&sh.col_n[lane], cnt);
+  }
+  int bad = lm_bad;
+  for (int b = threadIdx.x; b <= Bmax; b += NT) {
+    const float c = cm[b];
+    if (!(isfinite(c) && c > 0.0f)) bad = 1;
+  }
+  const float m0 = warp_max_nonneg(lm);
+  if (lane == 0) sh.tot_m0[warp] = m0;
+  if (bad) atomicOr(&sh.err, SD_DEV_ERR_COST);
+  __syncthreads();
+  const int K = warp;
+  if (K <= k_max && (K == 0 || sh.col_n[K - 1] > 0)) {
+    unsigned long long E = static_cast<unsigned long long>(R) * 281474976710656ull;
+    int n = 0;
+    for (int j = 0; j < K; ++j) {
+      E += sh.col_s[j];
+      n += sh.col_n[j];
+    }
+    if (n <= Bmax) {  // tokens grow with K; Bmax = min(N, cost_len-1-T)
+      float c = warp_max_nonneg(lane < NW ? sh.tot_m0[lane] : -INFINITY);
+      for (int b = lane; b <= n; b += 32) c = fmaxf(c, cm[b]);
+      c = warp_max_nonneg(c);
+      const float obj = (u64_to_f32(E) * (1.0f / kFix)) / c;
+      if (lane == 0)
+        atomicMax(&sh.best, (static_cast<unsigned long long>(__float_as_uint(obj)) << 32) |
+                                static_cast<unsigned long long>(0xFFFFFFFFu - static_cast<uint32_t>(K)));
+    }
+  }
+  __syncthreads();
+  const int Ks = static_cast<int>(0xFFFFFFFFu - static_cast<uint32_t>(sh.best & 0xFFFFFFFFull));
+  int n = 0;
+  for (int j = 0; j < Ks; ++j) n += sh.col_n[j];
+  *B = n;
+  return Ks;
+}
+
 // Shared-memory layout of one launch (NPm = max(NP, NPb), NRm = NPm / P).
 struct PlanSmem {
   unsigned long long* keysA;  // [NPm]
@@ -482,7 +562,8 @@ __global__ void __launch_bounds__(NT, 1) plan_kernel(const PlanParams p) {
   const int nreq = p.NP / p.P;  // padded request counts (powers of two)
   const int nb = p.NPb / p.P;
   const int L = p.cost_len - 1;
-  const bool adaptive = p.mode != SD_MODE_ALL_SLOTS;
+  const bool adaptive = p.mode != SD_MODE_ALL_SLOTS;  // a cost-driven mode
+  const bool uniform = p.mode == SD_MODE_UNIFORM_K;
 
   // Every global input the first steps need is requested at once: the draft
   // lengths (current, and those of the budget set) into registers, cost[T+b]
@@ -517,6 +598,10 @@ __global__ void __launch_bounds__(NT, 1) plan_kernel(const PlanParams p) {
     sh.err = 0;
     sh.cmax = 0;
   }
+  if (threadIdx.x < kMaxP) {
+    sh.col_s[threadIdx.x] = 0ull;
+    sh.col_n[threadIdx.x] = 0;
+  }
   cp_async_wait_all();
   __syncthreads();
 
@@ -524,8 +609,16 @@ __global__ void __launch_bounds__(NT, 1) plan_kernel(const PlanParams p) {
   int N = load_lengths(rc, cc, p.bs, nreq, p.k_max, m.lens, m.off, sh);
 
   int B = 0;
+  int Ks = p.k_max;  // slots j < Ks of each draft, where no top-B mask applies
   if (!adaptive) {
     B = N;
+  } else if (uniform) {
+    if (sh.err == 0) {
+      build_keys(p.conf, m.lens, m.off, nreq, p.P, m.keysA, m.cnt, sh);
+      if (sh.err == 0)
+        Ks = uniform_argmax(m.keysA, p.NP, p.P, p.k_max, min(N, L - p.T), p.bs, m.cm, lm, lm_bad,
+                            sh, &B);
+    }
   } else {
     if (p.budget_conf) {
       const int Nb = load_lengths(rb, cb, p.bs_budget, nb, p.k_max, m.lens, m.off, sh);
@@ -569,7 +662,8 @@ __global__ void __launch_bounds__(NT, 1) plan_kernel(const PlanParams p) {
     const int k = failed ? 0 : m.lens[i];
     uint8_t* mrow = p.mask + static_cast<size_t>(i) * p.k_max;
     for (int j = 0; j < p.k_max; ++j) {
-      const uint8_t v = j < k ? (adaptive ? m.sel[i * p.P + j] : uint8_t{1}) : uint8_t{0};
+      const uint8_t v = j < k ? (adaptive && !uniform ? m.sel[i * p.P + j] : static_cast<uint8_t>(j < Ks))
+                              : uint8_t{0};
       mrow[j] = v;
       nv[q] += v;
     }

@@ -131,17 +131,18 @@ sd_status sd_plan(const float* conf_logits, const float* budget_conf, const int*
   (void)ws_bytes;
   if (bs < 1 || k_max < 0) return SD_ERR_INVALID_ARG;
   if (k_max > SD_MAX_K) return SD_ERR_UNSUPPORTED;
-  if (mode != SD_MODE_ADAPTIVE && mode != SD_MODE_ALL_SLOTS) return SD_ERR_INVALID_ARG;
+  if (mode != SD_MODE_ADAPTIVE && mode != SD_MODE_ALL_SLOTS && mode != SD_MODE_UNIFORM_K)
+    return SD_ERR_INVALID_ARG;
   if (!draft_lens || !B_out || !num_verified || !cu_seqlens || !err_flag) return SD_ERR_INVALID_ARG;
   if (k_max > 0 && !slot_mask) return SD_ERR_INVALID_ARG;
   const int P = pow2ceil(k_max < 1 ? 1 : k_max);
   if (static_cast<long long>(pow2ceil(bs)) * P > SD_MAX_PLAN_SLOTS) return SD_ERR_UNSUPPORTED;
   int NPb = 0;
-  if (mode == SD_MODE_ADAPTIVE) {
+  if (mode != SD_MODE_ALL_SLOTS) {
     if (!conf_logits || !cost_table) return SD_ERR_INVALID_ARG;
     if (T < 1 || cost_len < 1) return SD_ERR_INVALID_ARG;
     if (T >= cost_len) return SD_ERR_SHAPE;
-    if (budget_conf) {
+    if (mode == SD_MODE_ADAPTIVE && budget_conf) {
       if (!budget_draft_lens || bs_budget < 1) return SD_ERR_INVALID_ARG;
       if (static_cast<long long>(pow2ceil(bs_budget)) * P > SD_MAX_PLAN_SLOTS)
         return SD_ERR_UNSUPPORTED;

@@ -253,6 +253,81 @@ def test_plans_at_the_slot_limit(bs, k_max):
         compare_plan(g, oracle_plan(q, k_max), f"bs={bs} k_max={k_max} budget set")
 
 
+# ---------------------------------------------------------------------------
+# uniform-K planning: one draft length for the whole batch
+
+
+def _uniform_pi(dl, conf, cost, T):
+    return {"draft_lens": dl, "conf": conf, "cost": cost, "T": T, "mode": S.MODE_UNIFORM_K,
+            "budget_conf": None, "budget_draft_lens": None}
+
+
+def test_uniform_k_random_small_plans_match_oracle():
+    rng = np.random.default_rng(7)
+    for trial in range(60):
+        bs = int(rng.integers(1, 40))
+        k_max = int(rng.integers(0, 9))
+        dl = rng.integers(0, k_max + 1, bs).astype(np.int32)
+        T = int(rng.integers(1, 50))
+        L = T + int(rng.integers(0, dl.sum() + 3))
+        n = np.arange(L + 1)
+        if trial % 2:  # flat up to a knee, then in proportion to the tokens
+            cost = np.maximum(1.0, n / rng.uniform(1.0, 60.0))
+        else:          # noisy, not monotone: the planner forces it
+            cost = 1.0 + rng.uniform(0, 0.05) * n + rng.uniform(0, 0.3, n.size)
+        pi = _uniform_pi(dl, rng.normal(1, 2, dl.sum()).astype(np.float32), cost.astype(np.float32), T)
+        g = gpu_plan(pi, k_max)
+        assert g["err"] == 0
+        o = oracle_plan(pi, k_max)
+        compare_plan(g, o, f"uniform trial {trial}")
+        assert g["B"] == int(g["num_verified"].sum())
+
+
+@pytest.mark.parametrize("bs,k_max", [(8192, 1), (4096, 2), (512, 15), (1, 15), (8192, 0)])
+def test_uniform_k_at_the_slot_limit(bs, k_max):
+    rng = np.random.default_rng(bs * 16 + k_max + 1)
+    dl = rng.integers(0, k_max + 1, bs).astype(np.int32)
+    T = bs
+    n = np.arange(T + int(dl.sum()) + 4)
+    conf = rng.normal(1, 2, dl.sum()).astype(np.float32)
+    for cost in (1.0 + 0.002 * n, np.maximum(1.0, n / (1.5 * bs))):
+        pi = _uniform_pi(dl, conf, cost.astype(np.float32), T)
+        g = gpu_plan(pi, k_max)
+        assert g["err"] == 0
+        compare_plan(g, oracle_plan(pi, k_max), f"uniform bs={bs} k_max={k_max}")
+
+
+def test_uniform_k_full_size():
+    _full("uniform_hc", 2024, 24)
+    w = S.WORKLOADS["stress"].with_(mode=S.MODE_UNIFORM_K)
+    pi = S.plan_inputs(w, 31337, 0)
+    g = gpu_plan(pi, w.k_max)
+    assert g["err"] == 0
+    compare_plan(g, oracle_plan(pi, w.k_max), "uniform stress")
+
+
+def test_uniform_k_device_checks_and_budget_set_ignored():
+    w = S.WORKLOADS["uniform_hc"].with_(bs=40)
+    pi = S.plan_inputs(w, 4, 0)
+    base = gpu_plan(pi, w.k_max)
+    assert base["err"] == 0
+    # previous-step confidences apply to the adaptive mode only
+    q = dict(pi, budget_conf=pi["conf"][::-1].copy(), budget_draft_lens=pi["draft_lens"])
+    other = gpu_plan(q, w.k_max)
+    assert other["err"] == 0 and other["B"] == base["B"]
+    assert np.array_equal(other["slot_mask"], base["slot_mask"])
+    pi_nan = dict(pi, conf=pi["conf"].copy())
+    pi_nan["conf"][3] = np.nan
+    g = gpu_plan(pi_nan, w.k_max)
+    assert g["err"] & sd.SD_DEV_ERR_CONF
+    assert g["B"] == 0 and list(g["cu_seqlens"]) == list(range(w.bs + 1))
+    pi_cost = dict(pi, cost=pi["cost"].copy())
+    pi_cost["cost"][w.T + 2] = np.inf
+    g = gpu_plan(pi_cost, w.k_max)
+    assert g["err"] & sd.SD_DEV_ERR_COST
+    assert g["B"] == 0 and not g["slot_mask"].any()
+
+
 # Mismatches allowed at near-boundary decisions, as a fraction of all
 # decisions.  The pages fix fp32 for the sampling arithmetic; at V = 129280 the
 # mean gap between consecutive CDF values is S / V = 7.7e-6 S, inside the
