@@ -79,6 +79,14 @@ def test_plan_rejects_bad_arguments_on_host(lib):
     assert call(T=65) == sd.SD_ERR_SHAPE
     assert call(bs=2048, k_max=7) == sd.SD_ERR_UNSUPPORTED
     assert call(budget_conf=P, budget_draft_lens=None) == sd.SD_ERR_INVALID_ARG
+    # the uniform-K mode needs the same inputs as the adaptive one
+    U = sd.SD_MODE_UNIFORM_K
+    assert call(mode=U, conf_logits=None) == sd.SD_ERR_INVALID_ARG
+    assert call(mode=U, cost_table=None) == sd.SD_ERR_INVALID_ARG
+    assert call(mode=U, T=0) == sd.SD_ERR_INVALID_ARG
+    assert call(mode=U, T=65) == sd.SD_ERR_SHAPE
+    assert call(mode=U, bs=2048, k_max=7) == sd.SD_ERR_UNSUPPORTED
+    assert call(mode=3) == sd.SD_ERR_INVALID_ARG
 
 
 def test_verify_rejects_bad_arguments_on_host(lib):
