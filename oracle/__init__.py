@@ -62,7 +62,9 @@ def _load():
         lib.oracle_verify.argtypes = [P, P, i32, i32, P, P, P, P, i32, i32, P, i32,
                                       P, P, P, P, P, P]
         lib.oracle_softmax.argtypes = [P, i32, i32, ctypes.c_double, P]
-        for f in (lib.oracle_survival, lib.oracle_plan, lib.oracle_verify, lib.oracle_softmax):
+        lib.oracle_calibrate.argtypes = [P, P, P, P, i32, i32, ctypes.c_double, P, P, P, P, P]
+        for f in (lib.oracle_survival, lib.oracle_plan, lib.oracle_verify, lib.oracle_softmax,
+                  lib.oracle_calibrate):
             f.restype = i32
         _lib = lib
     return _lib
@@ -79,6 +81,28 @@ def _c(a, dtype):
 def _check(rc, what):
     if rc != 0:
         raise OracleError(f"{what} returned {rc}")
+
+
+def calibrate(conf, draft_lens, num_verified, accepted_len, k_max, lr, w, b):
+    """One online-calibration step of the per-position logistic acceptance
+    model a = sigmoid(w_j c + b_j) from one step's verification outcomes.
+    Returns the updated w, b (fp64), the gradients and the observation counts."""
+    dl = _c(draft_lens, np.int32)
+    bs = len(dl)
+    conf = _c(conf, np.float32)
+    nv = _c(num_verified, np.int32)
+    acc = _c(accepted_len, np.int32)
+    w2 = np.array(w, np.float64, copy=True).reshape(k_max)
+    b2 = np.array(b, np.float64, copy=True).reshape(k_max)
+    gw = np.zeros(k_max, np.float64)
+    gb = np.zeros(k_max, np.float64)
+    cnt = np.zeros(k_max, np.int32)
+    if conf is not None and conf.size == 0:
+        conf = np.zeros(1, np.float32)
+    _check(_load().oracle_calibrate(_ptr(conf), _ptr(dl), _ptr(nv), _ptr(acc), bs, k_max,
+                                    float(lr), _ptr(w2), _ptr(b2), _ptr(gw), _ptr(gb), _ptr(cnt)),
+           "oracle_calibrate")
+    return {"w": w2, "b": b2, "grad_w": gw, "grad_b": gb, "count": cnt}
 
 
 def survival(conf, draft_lens):

@@ -46,6 +46,10 @@
 //   O15 residual mass S <= 0 or non-finite -> sample from p with the same u
 //   O16 argmax ties -> lowest index
 //   O17 draft rows of greedy requests are never read
+//   O25 online calibration: per position j a logistic model
+//       a = sigmoid(w_j * c + b_j) of the confidence logit c, moved by one
+//       gradient step on the mean logistic loss of the step's observed slots
+//       (those up to and including the first rejection)
 //
 // Near-boundary flags: decisions within 1e-5 relative of their boundary are
 // reported so that a test can tell an fp32 rounding disagreement from a bug.
@@ -509,6 +513,63 @@ int oracle_softmax(const void* row, int dtype, int V, double tau, double* p_out)
   std::vector<double> p;
   softmax_row(row, dtype, 0, V, tau, p);
   std::copy(p.begin(), p.end(), p_out);
+  return ORC_OK;
+}
+
+// Online calibration of the acceptance estimate (fosworld blog, the table
+// under "동작": for model-based drafts a small logistic model predicts
+// acceptance from the draft's logits and is corrected continuously with the
+// verification outcomes; reading O25).  Slot (i, j) of the packed conf
+// (offsets = exclusive scan of draft_lens) is observed when
+// j < num_verified[i] and j <= accepted_len[i]: it was accepted (y = 1) when
+// j < accepted_len[i], and it is the first rejection (y = 0) at
+// j = accepted_len[i].  Later slots were never tested.  With m_j observed
+// slots at position j, z = w_j * c + b_j and e = sigmoid(z) - y:
+//   grad_w[j] = (1/m_j) sum e * c,  grad_b[j] = (1/m_j) sum e
+// (the gradient of the mean of -[y log a + (1-y) log(1-a)]), and
+//   w_j -= lr * grad_w[j],  b_j -= lr * grad_b[j]   (positions with m_j = 0
+// keep their parameters; their gradient is reported as 0).
+//   w, b      [k_max] in/out;  grad_w, grad_b [k_max] out (or NULL);
+//   count     [k_max] out m_j (or NULL).
+int oracle_calibrate(const float* conf, const int* draft_lens, const int* num_verified,
+                     const int* accepted_len, int bs, int k_max, double lr, double* w,
+                     double* b, double* grad_w, double* grad_b, int* count) {
+  if (!draft_lens || !num_verified || !accepted_len || !w || !b) return ORC_ERR_ARG;
+  if (bs < 1 || k_max < 0 || !std::isfinite(lr) || lr < 0.0) return ORC_ERR_ARG;
+  size_t N = 0;
+  for (int i = 0; i < bs; ++i) {
+    if (draft_lens[i] < 0 || draft_lens[i] > k_max) return ORC_ERR_DATA;
+    if (num_verified[i] < 0 || num_verified[i] > draft_lens[i]) return ORC_ERR_DATA;
+    if (accepted_len[i] < 0 || accepted_len[i] > num_verified[i]) return ORC_ERR_DATA;
+    N += static_cast<size_t>(draft_lens[i]);
+  }
+  if (N > 0 && !conf) return ORC_ERR_ARG;
+  std::vector<double> ge(static_cast<size_t>(k_max), 0.0), gc(static_cast<size_t>(k_max), 0.0);
+  std::vector<int> m(static_cast<size_t>(k_max), 0);
+  size_t off = 0;
+  for (int i = 0; i < bs; ++i) {
+    const int observed = std::min(num_verified[i], accepted_len[i] + 1);
+    for (int j = 0; j < observed; ++j) {
+      const double c = static_cast<double>(conf[off + static_cast<size_t>(j)]);
+      if (!std::isfinite(c)) return ORC_ERR_DATA;
+      const double y = j < accepted_len[i] ? 1.0 : 0.0;
+      const double e = sigmoid(w[j] * c + b[j]) - y;
+      ge[static_cast<size_t>(j)] += e;
+      gc[static_cast<size_t>(j)] += e * c;
+      m[static_cast<size_t>(j)] += 1;
+    }
+    off += static_cast<size_t>(draft_lens[i]);
+  }
+  for (int j = 0; j < k_max; ++j) {
+    const size_t q = static_cast<size_t>(j);
+    const double gw = m[q] ? gc[q] / m[q] : 0.0;
+    const double gb = m[q] ? ge[q] / m[q] : 0.0;
+    w[j] -= lr * gw;
+    b[j] -= lr * gb;
+    if (grad_w) grad_w[j] = gw;
+    if (grad_b) grad_b[j] = gb;
+    if (count) count[j] = m[q];
+  }
   return ORC_OK;
 }
 
