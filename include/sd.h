@@ -69,6 +69,7 @@ typedef enum {
 #define SD_DEV_ERR_UNIFORM 0x040         /* a uniform outside [0, 1) */
 #define SD_DEV_ERR_LOGITS 0x080          /* a logit row holds NaN/+inf or no finite value */
 #define SD_DEV_ERR_TIMEOUT 0x100         /* a bounded wait for a staged copy gave up */
+#define SD_DEV_ERR_OUTCOME 0x200         /* num_verified / accepted_len out of range (calibration) */
 
 /* Limits of this build. */
 #define SD_MAX_K 15            /* k_max <= 15: at most 16 query rows per request */
@@ -259,6 +260,52 @@ sd_status sd_verify_noalloc(const void* target_logits, const void* draft_logits,
  * automatic) on the current device.  Host-only query. */
 sd_status sd_verify_launch_info(int V, sd_dtype dt, int bs, const sd_launch_cfg* req,
                                 sd_launch_cfg* chosen, size_t* smem_bytes);
+
+/* ------------------------------------------------------------------------
+ * sd_calibrate / sd_calibrate_apply -- online calibration of the
+ * per-position acceptance estimate.
+ *
+ * Passage: [AV-blog] the table under "동작" (for model-based drafts the
+ * per-position acceptance estimate comes from a small logistic model on the
+ * draft's logits, corrected continuously with the verification results).
+ * Model: a_{i,j} = sigmoid(w_j * c_{i,j} + b_j) of the confidence logit;
+ * w = 1, b = 0 is the estimate sd_plan uses on raw logits.
+ *
+ * sd_calibrate: one gradient step from one step's outcomes.  Slot (i,j) was
+ * observed when j < num_verified[i] and j <= accepted_len[i]; its label is 1
+ * for j < accepted_len[i] (accepted) and 0 at j = accepted_len[i] (the first
+ * rejection).  With m_j observed slots at position j and
+ * e = sigmoid(w_j c + b_j) - label:
+ *   w_j -= lr * (1/m_j) * sum e * c,   b_j -= lr * (1/m_j) * sum e
+ * (the gradient of the mean logistic loss); positions with m_j = 0 keep
+ * their parameters.  Sums in fp32 within a warp and fp64 across warps, in a
+ * fixed order: repeated calls give identical results.
+ *
+ * sd_calibrate_apply: conf_out[slot] = fma(w_j, conf_logits[slot], b_j) for
+ * every drafted slot, the calibrated logits to pass to sd_plan as
+ * conf_logits (conf_out may equal conf_logits).
+ *
+ * Arguments
+ *   conf_logits   [N] fp32 packed by draft_lens as for sd_plan.
+ *   draft_lens    [bs] int32, 0 <= draft_lens[i] <= k_max.
+ *   num_verified  [bs] int32, 0 <= num_verified[i] <= draft_lens[i] (sd_plan's).
+ *   accepted_len  [bs] int32, 0 <= accepted_len[i] <= num_verified[i] (sd_verify's).
+ *   lr            learning rate, finite and >= 0.
+ *   w, b          [k_max] fp32 on the device, updated in place (sd_calibrate).
+ *   conf_out      [N] fp32 (sd_calibrate_apply).
+ *   err_flag      [1] int32, sticky bits: SD_DEV_ERR_DRAFT_LENS,
+ *                 SD_DEV_ERR_OUTCOME, SD_DEV_ERR_CONF (a non-finite observed
+ *                 logit).  On any of them nothing is updated (or written).
+ * Limits as sd_plan: 1 <= bs, 0 <= k_max <= SD_MAX_K,
+ * pow2ceil(bs)*pow2ceil(k_max) <= SD_MAX_PLAN_SLOTS.  k_max = 0 returns
+ * SD_OK without a launch.  One CTA, one launch, asynchronous on `stream`.
+ * ---------------------------------------------------------------------- */
+sd_status sd_calibrate(const float* conf_logits, const int* draft_lens, const int* num_verified,
+                       const int* accepted_len, int bs, int k_max, float lr, float* w, float* b,
+                       int* err_flag, void* stream);
+sd_status sd_calibrate_apply(const float* conf_logits, const int* draft_lens, int bs, int k_max,
+                             const float* w, const float* b, float* conf_out, int* err_flag,
+                             void* stream);
 
 const char* sd_status_string(sd_status s);
 

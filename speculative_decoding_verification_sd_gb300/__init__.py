@@ -4,8 +4,11 @@ verification.
 Two stages, both hand-written sm_103a CUDA kernels behind the C ABI of
 ``include/sd.h`` (``libsdverify.so``):
 
-  sd_plan    survival -> global top-B -> budget argmax -> varlen compaction
-  sd_verify  vocab-wide speculative rejection sampling on compacted logits
+  sd_plan       survival -> global top-B (or one K for the batch) -> budget
+                argmax -> varlen compaction
+  sd_verify     vocab-wide speculative rejection sampling on compacted logits
+  sd_calibrate  one online step of the per-position acceptance model (and
+                sd_calibrate_apply: the calibrated logits for the next plan)
 
 This module is the Python binding: the ``sd_*`` functions mirror the C entry
 points one to one (argument marshalling only; tensors are passed as device
@@ -22,7 +25,7 @@ import torch
 
 from . import _lib
 from ._lib import (SD_NOALLOC_SCRATCH_BYTES, SD_BF16, SD_DEV_ERR_CONF, SD_DEV_ERR_COST, SD_DEV_ERR_CU_SEQLENS,  # noqa: F401
-                   SD_DEV_ERR_DRAFT_ID, SD_DEV_ERR_DRAFT_LENS, SD_DEV_ERR_LOGITS,
+                   SD_DEV_ERR_DRAFT_ID, SD_DEV_ERR_DRAFT_LENS, SD_DEV_ERR_LOGITS, SD_DEV_ERR_OUTCOME,
                    SD_DEV_ERR_TEMP, SD_DEV_ERR_UNIFORM, SD_ERR_CUDA,
                    SD_ERR_DEVICE_CHECK, SD_ERR_INVALID_ARG, SD_ERR_SHAPE, SD_ERR_UNSUPPORTED,
                    SD_F32, SD_MAX_K, SD_MAX_PLAN_SLOTS, SD_MAX_V, SD_MAX_VERIFY_BS,
@@ -30,7 +33,8 @@ from ._lib import (SD_NOALLOC_SCRATCH_BYTES, SD_BF16, SD_DEV_ERR_CONF, SD_DEV_ER
 
 __all__ = [
     "sd_plan", "sd_verify", "sd_verify_ex", "sd_verify_noalloc", "sd_plan_workspace_bytes",
-    "sd_verify_workspace_bytes", "sd_verify_launch_info", "plan", "verify", "PlanResult",
+    "sd_verify_workspace_bytes", "sd_verify_launch_info", "sd_calibrate", "sd_calibrate_apply",
+    "plan", "verify", "PlanResult",
     "VerifyResult", "SdError", "build", "library_path", "verify_workspace",
 ]
 
@@ -106,6 +110,21 @@ def sd_verify(target_logits, draft_logits, dt, V, draft_ids, uniforms, temps, cu
                                _ptr(probs_out), _ptr(err_flag), _ptr(workspace), int(ws_bytes),
                                _stream(stream))
     return _lib.check("sd_verify", st)
+
+
+def sd_calibrate(conf_logits, draft_lens, num_verified, accepted_len, bs, k_max, lr, w, b,
+                 err_flag, stream=None):
+    st = _lib.load().sd_calibrate(_ptr(conf_logits), _ptr(draft_lens), _ptr(num_verified),
+                                  _ptr(accepted_len), int(bs), int(k_max), float(lr), _ptr(w),
+                                  _ptr(b), _ptr(err_flag), _stream(stream))
+    return _lib.check("sd_calibrate", st)
+
+
+def sd_calibrate_apply(conf_logits, draft_lens, bs, k_max, w, b, conf_out, err_flag, stream=None):
+    st = _lib.load().sd_calibrate_apply(_ptr(conf_logits), _ptr(draft_lens), int(bs), int(k_max),
+                                        _ptr(w), _ptr(b), _ptr(conf_out), _ptr(err_flag),
+                                        _stream(stream))
+    return _lib.check("sd_calibrate_apply", st)
 
 
 def _cfg(cfg):

@@ -27,6 +27,7 @@ SD_DEV_ERR_TEMP = 0x020
 SD_DEV_ERR_UNIFORM = 0x040
 SD_DEV_ERR_LOGITS = 0x080
 SD_DEV_ERR_TIMEOUT = 0x100
+SD_DEV_ERR_OUTCOME = 0x200
 
 SD_MAX_K = 15
 SD_MAX_PLAN_SLOTS = 8192
@@ -35,8 +36,8 @@ SD_MAX_V = 1 << 22
 
 # Every symbol include/sd.h declares.
 EXPORTS = ("sd_plan_workspace_bytes", "sd_plan", "sd_verify_workspace_bytes", "sd_verify",
-           "sd_verify_ex", "sd_verify_noalloc", "sd_verify_launch_info", "sd_status_string",
-           "sd_last_error_string", "sd_abi_version")
+           "sd_verify_ex", "sd_verify_noalloc", "sd_verify_launch_info", "sd_calibrate",
+           "sd_calibrate_apply", "sd_status_string", "sd_last_error_string", "sd_abi_version")
 SD_NOALLOC_SCRATCH_BYTES = 16 << 20  # include/sd.h
 
 
@@ -85,6 +86,10 @@ def load(path: Path | None = None) -> ctypes.CDLL:
                                  ctypes.POINTER(sd_launch_cfg), P]
     lib.sd_verify_noalloc.restype = i32
     lib.sd_verify_noalloc.argtypes = [P, P, i32, i32, P, P, P, P, i32, i32, P, P, P, P, P]
+    lib.sd_calibrate.restype = i32
+    lib.sd_calibrate.argtypes = [P, P, P, P, i32, i32, ctypes.c_float, P, P, P, P]
+    lib.sd_calibrate_apply.restype = i32
+    lib.sd_calibrate_apply.argtypes = [P, P, i32, i32, P, P, P, P, P]
     lib.sd_verify_launch_info.restype = i32
     lib.sd_verify_launch_info.argtypes = [i32, i32, i32, ctypes.POINTER(sd_launch_cfg),
                                           ctypes.POINTER(sd_launch_cfg), ctypes.POINTER(sz)]

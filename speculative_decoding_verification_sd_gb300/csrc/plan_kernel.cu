@@ -21,6 +21,11 @@
 //   compaction slot mask, n_i and cu_seqlens (n_i drafts + 1 row per request)
 //              [same page, Execution Pipeline: assignment on the GPU without a
 //               host round trip]
+//   calibration (calib_kernel) one online step of the per-position
+//              acceptance model a = sigmoid(w_j c + b_j), and the calibrated
+//              logits w_j c + b_j that the planner then takes as its input
+//              [fosworld blog, the table under "동작": a small logistic model
+//               on the draft's logits, corrected with the verification results]
 //
 // The prefix sums of the ranked survival values are exact integer sums of
 // the fp32 keys scaled by 2^48 (at most 8192 terms <= 1, so they fit in 62
@@ -28,6 +33,7 @@
 #include <atomic>
 #include <mutex>
 
+#include "calib.h"
 #include "sd_device.cuh"
 #include "sd_internal.h"
 
@@ -685,6 +691,112 @@ __global__ void __launch_bounds__(NT, 1) plan_kernel(const PlanParams p) {
   }
 }
 
+// Online calibration of the per-position acceptance model a = sigmoid(w_j c
+// + b_j), one CTA.
+// apply = 0: one gradient step on the mean logistic loss of the slots the
+//   step observed: slot (i, j) with j < num_verified[i] and j <=
+//   accepted_len[i], label 1 below accepted_len[i] and 0 at it (the first
+//   rejection); positions without observations keep their parameters.  One
+//   thread per slot i * P + j as in the planner's key phase, so each thread
+//   sees a single position; the per-position sums go through warp shuffles
+//   and then over the warps in a fixed order in fp64, so the result does not
+//   depend on timing.  The parameters are written after the last barrier and
+//   only when no input check failed.
+// apply = 1: conf_out[slot] = fma(w_j, c, b_j) for every drafted slot (may
+//   be in place); nothing is written when a draft length is out of range.
+__global__ void __launch_bounds__(NT, 1) calib_kernel(const CalibParams p) {
+  extern __shared__ __align__(16) unsigned char smem[];
+  __shared__ PlanShared sh;
+  __shared__ float part_e[NW][kMaxP];
+  __shared__ float part_ec[NW][kMaxP];
+  __shared__ int part_n[NW][kMaxP];
+  const int nreq = p.NP / p.P;
+  int* off = reinterpret_cast<int*>(smem);                               // [nreq + 1]
+  uint8_t* lens = smem + static_cast<size_t>(nreq + 1) * sizeof(int);  // [nreq]
+  const Chunk cc = req_chunk(p.bs);
+  int rc[kReqPer];
+  fetch_lengths(p.lens, cc, rc);
+  if (threadIdx.x == 0) sh.err = 0;
+  __syncthreads();
+  load_lengths(rc, cc, p.bs, nreq, p.k_max, lens, off, sh);
+  const bool ok = sh.err == 0;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int lgP = 31 - __clz(p.P);
+  const int j = static_cast<int>(threadIdx.x) & (p.P - 1);  // P divides NT
+  float wj = 0.0f, bj = 0.0f;
+  if (ok && j < p.k_max) {
+    wj = p.w[j];
+    bj = p.b[j];
+  }
+  float se = 0.0f, sec = 0.0f;
+  int n = 0, bad = 0;
+  if (ok && !p.apply) {  // every request's outcome, also those with no drafted slot
+    for (int i = cc.beg; i < cc.end; ++i) {
+      const int nv = p.nv[i], ac = p.acc[i];
+      if (nv < 0 || nv > lens[i] || ac < 0 || ac > nv) bad |= SD_DEV_ERR_OUTCOME;
+    }
+  }
+  if (ok) {
+    for (int r = 0; r < kSlotPer; ++r) {
+      const int q = r * NT + static_cast<int>(threadIdx.x);
+      if (q >= p.NP) break;
+      const int i = q >> lgP;
+      if (i >= p.bs || j >= lens[i]) continue;
+      const int at = off[i] + j;
+      const float c = p.conf[at];
+      if (p.apply) {
+        p.conf_out[at] = fmaf(wj, c, bj);
+        continue;
+      }
+      const int nv = p.nv[i], ac = p.acc[i];
+      if (nv < 0 || nv > lens[i] || ac < 0 || ac > nv) {
+        bad |= SD_DEV_ERR_OUTCOME;
+        continue;
+      }
+      if (j >= min(nv, ac + 1)) continue;  // never tested
+      if (!isfinite(c)) {
+        bad |= SD_DEV_ERR_CONF;
+        continue;
+      }
+      const float e = 1.0f / (1.0f + expf(-fmaf(wj, c, bj))) - (j < ac ? 1.0f : 0.0f);
+      se += e;
+      sec = fmaf(e, c, sec);
+      ++n;
+    }
+  }
+  if (p.apply) {  // uniform over the block: no barrier follows
+    if (threadIdx.x == 0 && sh.err) raise_error(p.err, sh.err);
+    return;
+  }
+  for (int o = p.P; o < 32; o <<= 1) {  // lanes with the same position
+    se += __shfl_xor_sync(kFull, se, o);
+    sec += __shfl_xor_sync(kFull, sec, o);
+    n += __shfl_xor_sync(kFull, n, o);
+  }
+  if (lane < p.P) {
+    part_e[warp][lane] = se;
+    part_ec[warp][lane] = sec;
+    part_n[warp][lane] = n;
+  }
+  if (bad) atomicOr(&sh.err, bad);
+  __syncthreads();
+  if (static_cast<int>(threadIdx.x) < p.k_max) {  // thread j holds w_j, b_j
+    double E = 0.0, EC = 0.0;
+    int m = 0;
+    for (int v = 0; v < NW; ++v) {
+      E += static_cast<double>(part_e[v][threadIdx.x]);
+      EC += static_cast<double>(part_ec[v][threadIdx.x]);
+      m += part_n[v][threadIdx.x];
+    }
+    if (sh.err == 0 && m > 0) {
+      const double lr = static_cast<double>(p.lr);
+      p.w[threadIdx.x] = static_cast<float>(static_cast<double>(wj) - lr * (EC / m));
+      p.b[threadIdx.x] = static_cast<float>(static_cast<double>(bj) - lr * (E / m));
+    }
+  }
+  if (threadIdx.x == 0 && sh.err) raise_error(p.err, sh.err);
+}
+
 }  // namespace
 
 size_t plan_smem_bytes(const PlanParams& p) {
@@ -719,6 +831,19 @@ cudaError_t launch_plan(const PlanParams& p, cudaStream_t s) {
   }
   if (smem > static_cast<size_t>(lim)) return cudaErrorInvalidValue;
   plan_kernel<<<1, NT, smem, s>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_calibrate(const CalibParams& p, cudaStream_t s) {
+  const int nreq = p.NP / p.P;
+  // offsets and lengths of the padded requests: at most 8193 * 4 + 8192 bytes
+  const size_t smem = static_cast<size_t>(nreq + 1) * sizeof(int) + static_cast<size_t>(nreq);
+  if (smem > 32 * 1024) {
+    const cudaError_t e = cudaFuncSetAttribute(
+        calib_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+  }
+  calib_kernel<<<1, NT, smem, s>>>(p);
   return cudaGetLastError();
 }
 

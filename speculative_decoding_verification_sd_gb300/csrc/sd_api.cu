@@ -3,9 +3,11 @@
 // No entry point allocates device memory or synchronises the stream.
 #include <cuda_runtime.h>
 
+#include <cmath>
 #include <cstdio>
 #include <mutex>
 
+#include "calib.h"
 #include "sd_internal.h"
 
 namespace {
@@ -171,6 +173,68 @@ sd_status sd_plan(const float* conf_logits, const float* budget_conf, const int*
   p.err = err_flag;
   return note(sdk::launch_plan(p, static_cast<cudaStream_t>(stream))) == cudaSuccess ? SD_OK
                                                                                     : SD_ERR_CUDA;
+}
+
+// Host checks shared by the two calibration calls; fills the shape fields.
+static sd_status calib_shape(int bs, int k_max, sdk::CalibParams& p) {
+  if (bs < 1 || k_max < 0) return SD_ERR_INVALID_ARG;
+  if (k_max > SD_MAX_K) return SD_ERR_UNSUPPORTED;
+  const int P = pow2ceil(k_max < 1 ? 1 : k_max);
+  if (static_cast<long long>(pow2ceil(bs)) * P > SD_MAX_PLAN_SLOTS) return SD_ERR_UNSUPPORTED;
+  p.bs = bs;
+  p.k_max = k_max;
+  p.P = P;
+  p.NP = pow2ceil(bs) * P;
+  return SD_OK;
+}
+
+sd_status sd_calibrate(const float* conf_logits, const int* draft_lens, const int* num_verified,
+                       const int* accepted_len, int bs, int k_max, float lr, float* w, float* b,
+                       int* err_flag, void* stream) {
+  sdk::CalibParams p{};
+  const sd_status st = calib_shape(bs, k_max, p);
+  if (st != SD_OK) return st;
+  if (!(std::isfinite(lr) && lr >= 0.0f)) return SD_ERR_INVALID_ARG;
+  if (!draft_lens || !num_verified || !accepted_len || !err_flag) return SD_ERR_INVALID_ARG;
+  if (k_max > 0 && (!conf_logits || !w || !b)) return SD_ERR_INVALID_ARG;
+  if (k_max == 0) return SD_OK;
+  p.conf = conf_logits;
+  p.lens = draft_lens;
+  p.nv = num_verified;
+  p.acc = accepted_len;
+  p.lr = lr;
+  p.w = w;
+  p.b = b;
+  p.conf_out = nullptr;
+  p.apply = 0;
+  p.err = err_flag;
+  return note(sdk::launch_calibrate(p, static_cast<cudaStream_t>(stream))) == cudaSuccess
+             ? SD_OK
+             : SD_ERR_CUDA;
+}
+
+sd_status sd_calibrate_apply(const float* conf_logits, const int* draft_lens, int bs, int k_max,
+                             const float* w, const float* b, float* conf_out, int* err_flag,
+                             void* stream) {
+  sdk::CalibParams p{};
+  const sd_status st = calib_shape(bs, k_max, p);
+  if (st != SD_OK) return st;
+  if (!draft_lens || !err_flag) return SD_ERR_INVALID_ARG;
+  if (k_max > 0 && (!conf_logits || !w || !b || !conf_out)) return SD_ERR_INVALID_ARG;
+  if (k_max == 0) return SD_OK;
+  p.conf = conf_logits;
+  p.lens = draft_lens;
+  p.nv = nullptr;
+  p.acc = nullptr;
+  p.lr = 0.0f;
+  p.w = const_cast<float*>(w);  // read only when apply = 1
+  p.b = const_cast<float*>(b);
+  p.conf_out = conf_out;
+  p.apply = 1;
+  p.err = err_flag;
+  return note(sdk::launch_calibrate(p, static_cast<cudaStream_t>(stream))) == cudaSuccess
+             ? SD_OK
+             : SD_ERR_CUDA;
 }
 
 size_t sd_verify_workspace_bytes(int bs, int k_max) {

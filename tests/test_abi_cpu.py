@@ -119,6 +119,41 @@ def test_verify_rejects_bad_arguments_on_host(lib):
                             ctypes.byref(bad_cfg), 0) == sd.SD_ERR_INVALID_ARG
 
 
+def test_calibration_rejects_bad_arguments_on_host(lib):
+    """sd_calibrate / sd_calibrate_apply refuse bad arguments before any CUDA
+    call; k_max = 0 is a no-op that returns before any launch."""
+    import speculative_decoding_verification_sd_gb300 as sd
+    P = FAKE
+
+    def upd(**kw):
+        a = dict(conf=P, dl=P, nv=P, acc=P, bs=4, k_max=3, lr=0.1, w=P, b=P, err=P)
+        a.update(kw)
+        return lib.sd_calibrate(a["conf"], a["dl"], a["nv"], a["acc"], a["bs"], a["k_max"],
+                                a["lr"], a["w"], a["b"], a["err"], 0)
+
+    def app(**kw):
+        a = dict(conf=P, dl=P, bs=4, k_max=3, w=P, b=P, out=P, err=P)
+        a.update(kw)
+        return lib.sd_calibrate_apply(a["conf"], a["dl"], a["bs"], a["k_max"], a["w"], a["b"],
+                                      a["out"], a["err"], 0)
+
+    assert upd(bs=0) == sd.SD_ERR_INVALID_ARG
+    assert upd(k_max=-1) == sd.SD_ERR_INVALID_ARG
+    assert upd(k_max=16) == sd.SD_ERR_UNSUPPORTED
+    assert upd(bs=2048, k_max=7) == sd.SD_ERR_UNSUPPORTED
+    assert upd(lr=-0.5) == sd.SD_ERR_INVALID_ARG
+    assert upd(lr=float("nan")) == sd.SD_ERR_INVALID_ARG
+    assert upd(lr=float("inf")) == sd.SD_ERR_INVALID_ARG
+    for k in ("dl", "nv", "acc", "err", "conf", "w", "b"):
+        assert upd(**{k: None}) == sd.SD_ERR_INVALID_ARG, k
+    assert upd(k_max=0, conf=None, w=None, b=None) == sd.SD_OK
+    assert app(bs=0) == sd.SD_ERR_INVALID_ARG
+    assert app(k_max=16) == sd.SD_ERR_UNSUPPORTED
+    for k in ("dl", "err", "conf", "w", "b", "out"):
+        assert app(**{k: None}) == sd.SD_ERR_INVALID_ARG, k
+    assert app(k_max=0, conf=None, w=None, b=None, out=None) == sd.SD_OK
+
+
 def test_noalloc_rejects_on_host(lib):
     """sd_verify_noalloc refuses bad sizes before any CUDA call."""
     import speculative_decoding_verification_sd_gb300 as sd
