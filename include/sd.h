@@ -115,7 +115,9 @@ typedef enum {
  * Arguments
  *   conf_logits      [N] fp32, packed by request: slot (i,j) at
  *                    offset_i + j, offset = exclusive scan of draft_lens.
- *                    Unused (may be NULL) in SD_MODE_ALL_SLOTS.
+ *                    Unused (may be NULL) in SD_MODE_ALL_SLOTS.  Raw
+ *                    confidence logits, or sd_calibrate_apply's calibrated
+ *                    ones (the survival then uses the calibrated estimate).
  *   budget_conf      (SD_MODE_ADAPTIVE only; ignored in the other modes)
  *                    [N'] fp32 previous-step confidences packed by
  *                    budget_draft_lens [bs_budget], or NULL to size the budget
