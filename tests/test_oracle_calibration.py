@@ -11,7 +11,8 @@ rejection).  The pins tie it to:
 - the loss itself: the reported gradient equals central finite differences of
   the mean logistic loss, evaluated with scipy's log-sigmoid;
 - constructed outcomes: which slots count, with which label, by hand;
-- statistics: steps on outcomes drawn from a known model recover that model.
+- statistics: steps on outcomes drawn from a known model recover that model;
+- descent: a small step lowers each observed position's loss by about lr·|grad|².
 """
 import numpy as np
 import pytest
@@ -138,3 +139,26 @@ def test_calibrate_rejects_bad_inputs():
     nan[0] = np.nan  # an observed slot
     with pytest.raises(oracle.OracleError):
         oracle.calibrate(**dict(ok, conf=nan))
+
+
+@pytest.mark.parametrize("trial", range(20))
+def test_a_small_step_lowers_each_positions_loss(trial):
+    """The update is a descent step: with a small rate, the mean logistic loss
+    of every observed position goes down (or stays, when its gradient is 0)."""
+    rng = np.random.default_rng(RNG_SEED + 500 + trial)
+    k_max = int(rng.integers(1, 8))
+    dl, nv, acc, conf = _random_step(rng, int(rng.integers(8, 64)), k_max)
+    w0 = rng.normal(1.0, 0.5, k_max)
+    b0 = rng.normal(0.0, 1.0, k_max)
+    r = oracle.calibrate(conf, dl, nv, acc, k_max, 1e-3, w0, b0)
+    obs = _observed(dl, nv, acc)
+    c64 = conf.astype(np.float64)
+    for j in range(k_max):
+        if r["count"][j] == 0:
+            continue
+        before = _mean_loss(c64, obs, j, w0[j], b0[j])
+        after = _mean_loss(c64, obs, j, r["w"][j], r["b"][j])
+        assert after <= before + 1e-15
+        g2 = r["grad_w"][j] ** 2 + r["grad_b"][j] ** 2
+        # first order: the decrease is about lr * |grad|^2
+        assert before - after == pytest.approx(1e-3 * g2, rel=0.05, abs=1e-12)
