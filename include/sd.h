@@ -46,7 +46,7 @@ typedef enum {
   SD_OK = 0,
   SD_ERR_INVALID_ARG = -1,  /* NULL pointer, negative size, unknown enum value */
   SD_ERR_SHAPE = -2,        /* sizes inconsistent with each other (e.g. T >= cost_len) */
-  SD_ERR_UNSUPPORTED = -3,  /* valid but beyond this build's limits (SD_MAX_*) */
+  SD_ERR_UNSUPPORTED = -3,  /* valid but beyond this library's limits (SD_MAX_*) */
   SD_ERR_CUDA = -4,         /* a CUDA runtime call or launch failed */
   SD_ERR_DEVICE_CHECK = -5  /* reserved for callers mapping err_flag to a status */
 } sd_status;
@@ -71,7 +71,7 @@ typedef enum {
 #define SD_DEV_ERR_TIMEOUT 0x100         /* a bounded wait for a staged copy gave up */
 #define SD_DEV_ERR_OUTCOME 0x200         /* num_verified / accepted_len out of range (calibration) */
 
-/* Limits of this build. */
+/* Limits of this library. */
 #define SD_MAX_K 15            /* k_max <= 15: at most 16 query rows per request */
 #define SD_MAX_PLAN_SLOTS 8192 /* pow2ceil(bs) * pow2ceil(k_max) <= 8192 for sd_plan */
 #define SD_MAX_VERIFY_BS 4096  /* bs <= 4096 for sd_verify */
@@ -137,7 +137,7 @@ typedef enum {
  *                    (n_i verified drafts plus one target/bonus row).
  *   err_flag         [1] int32, sticky SD_DEV_ERR_* bits.  On a device error
  *                    the outputs describe B = 0 (n_i = 0, cu[i] = i).
- *   workspace        unused by this build (ws_bytes may be 0).
+ *   workspace        unused by this library (ws_bytes may be 0).
  * Limits: 1 <= bs, 0 <= k_max <= SD_MAX_K, pow2ceil(bs)*pow2ceil(k_max)
  * <= SD_MAX_PLAN_SLOTS (SD_ERR_UNSUPPORTED otherwise).  One CTA, one launch.
  * ---------------------------------------------------------------------- */
