@@ -8,9 +8,13 @@ The arithmetic lives in ``sd_oracle.cpp`` (sequential C++17, fp64, no shared
 code with the CUDA library).  This module only compiles it and marshals numpy
 arrays through ctypes.
 
-Pins: every function here is pinned by ``tests/test_oracle_pins.py`` against the
-pages' worked examples (tests/golden/), brute force on tiny inputs, closed forms
-and statistical tests.
+Pins: every function here is pinned against things fixed outside it:
+``tests/test_oracle_pins.py`` (the pages' worked examples in tests/golden/,
+brute force on tiny inputs, closed forms, statistical tests),
+``tests/test_oracle_uniform_k.py`` (the uniform-K planning mode),
+``tests/test_oracle_calibration.py`` (the calibration step: finite differences of
+its loss, hand-built outcomes, recovery of a generating model) and
+``tests/test_oracle_plan_properties.py`` (planner invariants over random inputs).
 """
 from __future__ import annotations
 

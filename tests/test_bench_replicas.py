@@ -69,3 +69,12 @@ def test_rank_environment_defaults_to_one_process(monkeypatch):
     monkeypatch.setenv("WORLD_SIZE", "2")
     monkeypatch.setenv("LOCAL_RANK", "1")
     assert bench.dist_env() == (1, 2, 1)
+
+
+def test_every_workload_has_a_config_line():
+    import sdsynth as S
+    for name, w in S.WORKLOADS.items():
+        c = bench.config_of(w)
+        assert c["workload"] == name
+        assert c["mode"] in ("adaptive", "all_slots", "uniform_k")
+    assert bench.config_of(S.WORKLOADS["uniform_hc"])["mode"] == "uniform_k"
