@@ -78,3 +78,13 @@ def test_every_workload_has_a_config_line():
         assert c["workload"] == name
         assert c["mode"] in ("adaptive", "all_slots", "uniform_k")
     assert bench.config_of(S.WORKLOADS["uniform_hc"])["mode"] == "uniform_k"
+
+
+def test_oracle_all_cores_leg_runs_on_the_host():
+    """The all-cores oracle timing (spawned processes, requests dealt
+    round-robin) returns a positive rate and the process count it used."""
+    import sdsynth as S
+    r = bench.oracle_all_cores(S.WORKLOADS["tiny"], 7, 1.0, workers=2)
+    assert "error" not in r
+    assert r["cores"] == 2 and r["value"] > 0 and r["kind"] == "oracle"
+    assert bench.all_cores_or_error(S.WORKLOADS["tiny"].with_(name="no_such_workload"), 7, 1.0)["error"]
