@@ -68,14 +68,15 @@ typedef enum {
 #define SD_DEV_ERR_TEMP 0x020            /* a temperature < 0 or not finite */
 #define SD_DEV_ERR_UNIFORM 0x040         /* a uniform outside [0, 1) */
 #define SD_DEV_ERR_LOGITS 0x080          /* a logit row holds NaN/+inf or no finite value */
-#define SD_DEV_ERR_TIMEOUT 0x100         /* a bounded wait for a staged copy gave up */
+#define SD_DEV_ERR_TIMEOUT 0x100         /* a bounded device-side wait gave up */
 #define SD_DEV_ERR_OUTCOME 0x200         /* num_verified / accepted_len out of range (calibration) */
 
 /* Limits of this library. */
 #define SD_MAX_K 15            /* k_max <= 15: at most 16 query rows per request */
 #define SD_MAX_PLAN_SLOTS 8192 /* pow2ceil(bs) * pow2ceil(k_max) <= 8192 for sd_plan */
 #define SD_MAX_VERIFY_BS 4096  /* bs <= 4096 for sd_verify */
-#define SD_MAX_V (1 << 22)     /* V <= 4,194,304 */
+#define SD_MAX_V (1 << 20)     /* V <= 1,048,576 ... */
+#define SD_MAX_ROW_BYTES (2 << 20) /* ... and V * element size <= 2 MiB (fp32: V <= 524,288) */
 
 /* ------------------------------------------------------------------------
  * sd_plan -- planning stage of adaptive verification.
@@ -164,50 +165,59 @@ sd_status sd_plan(const float* conf_logits, const float* budget_conf,
  * For request i with n_i = cu[i+1]-cu[i]-1 verified drafts, temperature
  * tau_i, target rows t_j (j = 0..n_i) and draft rows d_j (j < n_i):
  *   tau_i > 0: p_j = softmax(t_j/tau_i), q_j = softmax(d_j/tau_i);
- *              slot j accepted iff uniforms[i][j] * q_j(x_j) <= p_j(x_j).
+ *              slot j accepted iff uniforms[i][j] * q_j(x_j) <= p_j(x_j)
+ *              (p_j(x_j), q_j(x_j) rounded to fp32, the product in fp32).
  *   tau_i = 0: slot j accepted iff x_j == argmax t_j (lowest index on ties);
  *              draft rows are not read.
  *   a_i = first rejected slot, else n_i.
  *   final token y_i: tau_i = 0: argmax t_{a_i}; tau_i > 0: inverse CDF with
  *   u = uniforms[i][k_max] (smallest k with sum_{l<=k} w_l > u * sum w) over
  *   w = max(p_{a_i} - q_{a_i}, 0) after a rejection, or w = p_{n_i} (bonus)
- *   when every slot was accepted; if that residual has no positive mass in
- *   fp32, w = p_{a_i}.
+ *   when every slot was accepted; if that residual has no positive mass,
+ *   w = p_{a_i}.  The weights are summed in exact 64-bit fixed point (2^-56);
+ *   an element heavier than 2^-12 of its row's largest weight is formed to
+ *   about 1e-10 relative, the others in fp32.
  *   out_tokens[i] = (x_0 .. x_{a_i-1}, y_i, -1 ...), accepted_len[i] = a_i.
  *
  * Arguments
  *   target_logits  [rows_cap, V] fp32 or bf16, row-major, compacted: the row of
  *                  (i,j) is cu_seqlens[i]+j.  rows_cap >= bs*(k_max+1) is the
  *                  caller's allocation; only rows < cu_seqlens[bs] are read.
- *   draft_logits   [bs*k_max, V] same dtype, compacted: row of (i,j) is
- *                  cu_seqlens[i]-i+j.  Only rows of requests with tau > 0 are
- *                  read.  May be NULL if every temperature is 0.
+ *   draft_logits   [bs*k_max, V] same dtype.  Compacted: the row of (i,j) is
+ *                  cu_seqlens[i]-i+j; with SD_VERIFY_DRAFT_PADDED (see
+ *                  sd_verify_ex) it is i*k_max+j, the uncompacted layout a
+ *                  draft forward over every drafted slot leaves.  Only rows of
+ *                  requests with tau > 0 are read.  May be NULL if every
+ *                  temperature is 0.
  *   dt, V          element type and vocabulary size.
- *   draft_ids      [bs*k_max] int32, compacted like the draft rows.
+ *   draft_ids      [bs*k_max] int32, indexed like the draft rows.
  *   uniforms       [bs, k_max+1] fp32 in [0,1): slot tests then the final draw.
  *   temps          [bs] fp32 >= 0.
  *   cu_seqlens     [bs+1] int32 from sd_plan (or the caller).
  * Outputs
  *   accepted_len   [bs] int32; out_tokens [bs, k_max+1] int32, -1 padded.
  *   probs_out      [bs*k_max, 2] fp32 or NULL: (p_j(x_j), q_j(x_j)) of every
- *                  verified slot of a tau > 0 request, at the draft-row
- *                  index (diagnostics; entries of greedy requests and of
- *                  unverified slots untouched).
+ *                  verified slot of a tau > 0 request whose rows were read, at
+ *                  the draft-row index (diagnostics; with early exit the slots
+ *                  after the first rejection may be left untouched; entries of
+ *                  greedy requests and of unverified slots are untouched).
  *   err_flag       [1] int32, sticky SD_DEV_ERR_* bits.  On SD_DEV_ERR_CU_SEQLENS
  *                  no logit is read and outputs are accepted_len = 0,
- *                  out_tokens = -1.
- *   workspace      device scratch of sd_verify_workspace_bytes(bs, k_max)
- *                  bytes, 16-byte aligned: per-row and per-chunk statistics,
- *                  residual chunk sums, per-request arrival counts, the list
- *                  of residual draws and work counters.  It must be zero-filled
- *                  once before its first use (e.g. cudaMemsetAsync); every
- *                  call leaves the counters at zero again.  One call at a time
- *                  per workspace.
- * Layout: rows are read with 16-byte vector loads when V*elem is a multiple
- * of 16 and both logits base pointers are 16-byte aligned, element by
+ *                  out_tokens = -1.  On SD_DEV_ERR_TIMEOUT every request's
+ *                  outputs are accepted_len = 0, out_tokens = (0, -1, ...).
+ *   workspace      device scratch of sd_verify_workspace_bytes(bs, k_max, V, dt)
+ *                  bytes, 256-byte aligned: per-segment and per-row statistics,
+ *                  per-sub-chunk sums of the final draws, per-request and
+ *                  per-slot counters.  It must be zero-filled once before its
+ *                  first use (e.g. cudaMemsetAsync); every call leaves the
+ *                  counters at zero again.  One call at a time per workspace.
+ * Layout: rows are staged with 16-byte bulk copies when V*elem is a multiple
+ * of 16 and both logits base pointers are 16-byte aligned, read element by
  * element otherwise (same results, slower).
+ * Limits: 1 <= bs <= SD_MAX_VERIFY_BS, 0 <= k_max <= SD_MAX_K,
+ * V <= SD_MAX_V, V * elem <= SD_MAX_ROW_BYTES (SD_ERR_UNSUPPORTED otherwise).
  * ---------------------------------------------------------------------- */
-size_t sd_verify_workspace_bytes(int bs, int k_max);
+size_t sd_verify_workspace_bytes(int bs, int k_max, int V, sd_dtype dt);
 
 sd_status sd_verify(const void* target_logits, const void* draft_logits, sd_dtype dt, int V,
                     const int* draft_ids, const float* uniforms, const float* temps,
@@ -215,16 +225,24 @@ sd_status sd_verify(const void* target_logits, const void* draft_logits, sd_dtyp
                     int* out_tokens, float* probs_out, int* err_flag, void* workspace,
                     size_t ws_bytes, void* stream);
 
-/* Launch tuning of the sampling kernel; 0 in any field = automatic.  Results
- * do not depend on it. */
+/* Options of sd_verify_ex.  Outputs never depend on `blocks`; the flags below
+ * change what is read, never the accepted lengths or tokens. */
+#define SD_VERIFY_EARLY_EXIT 0x1   /* skip the rows of slots after a request's known
+                                      first rejection ([AV-blog] "뒤 자리 수락률이 급하게
+                                      떨어지는 이유": later positions are rarely reached) */
+#define SD_VERIFY_DRAFT_PADDED 0x2 /* draft rows and draft ids at i*k_max+j (uncompacted) */
+#define SD_VERIFY_TEST_STALL 0x100 /* test hook: stream no row, so the end-of-call wait
+                                      runs out (after wait_limit_us) and the time-out path runs */
 typedef struct {
-  int threads;        /* threads per CTA: 256 or 512 */
-  int blocks;         /* persistent CTAs launched (capped at what fits at once) */
-  int blocks_per_sm;  /* CTAs per SM to aim for */
-  int reserved;       /* must be 0 */
+  int blocks;     /* persistent CTAs (0 = one per SM; capped at one per SM) */
+  int flags;      /* SD_VERIFY_* bits */
+  int wait_limit_us; /* microseconds a device-side wait may last before it gives up
+                        (0 = the default, 1 s); the drain of in-flight copies at exit
+                        is bounded separately */
+  int reserved;   /* must be 0 */
 } sd_launch_cfg;
 
-/* sd_verify with an explicit launch shape (cfg may be NULL). */
+/* sd_verify with options (cfg may be NULL: defaults). */
 sd_status sd_verify_ex(const void* target_logits, const void* draft_logits, sd_dtype dt, int V,
                        const int* draft_ids, const float* uniforms, const float* temps,
                        const int* cu_seqlens, int bs, int k_max, int* accepted_len,
@@ -233,22 +251,30 @@ sd_status sd_verify_ex(const void* target_logits, const void* draft_logits, sd_d
 
 /* ------------------------------------------------------------------------
  * sd_verify_noalloc -- sd_verify without a caller workspace.  The pages have
- * no counterpart to this entry point: it exists for callers that may not
- * allocate device memory around the step.
+ * no counterpart to this entry point.  It is for callers that cannot call
+ * cudaMalloc around the verification step: a serving loop that reserved the
+ * device's memory up front (weights, KV cache) and must not allocate while
+ * it runs, or a host process whose allocator is owned by another framework.
  *
  * Same arguments and outputs as sd_verify, minus workspace/ws_bytes.  The
  * workspace is a file-scope device array of SD_NOALLOC_SCRATCH_BYTES inside
- * the library (static device memory, no allocation at call time).  Its
- * address is looked up once per device with cudaGetSymbolAddress on the
- * first call on that device: make that first call before any stream
- * capture.  Each call clears, on `stream`, the part of the scratch that must
- * start at zero (the residual sums and the counters), then runs sd_verify on
- * it.  Calls that overlap in time on one device share the scratch and race:
- * issue them on one stream, or order them.
- * Errors: SD_ERR_UNSUPPORTED when sd_verify_workspace_bytes(bs, k_max)
- * exceeds SD_NOALLOC_SCRATCH_BYTES (about 1770 requests at k_max = 7; the
- * reason is in sd_last_error_string()); SD_ERR_CUDA when the lookup or the
- * clear fails; otherwise as sd_verify.
+ * the library (static device memory, held by every device that loads the
+ * library until the process exits; no allocation at call time).  Host code
+ * cannot name that array directly: its device address is looked up with
+ * cudaGetSymbolAddress, with the device current, on the first call on each
+ * device -- make that first call before any stream capture -- and again on
+ * every later call that is not being captured, so a call after a device
+ * reset or from another context on the device uses the address that is
+ * valid there.  A call under capture uses the address cached by the last
+ * call outside capture on that device.
+ * Each call first checks its arguments as sd_verify does, then clears, on
+ * `stream`, the part of the scratch that must start at zero (the counters),
+ * then runs the sampling kernel on it.  Calls that overlap in time on one
+ * device share the scratch and race: issue them on one stream, or order them.
+ * Errors: SD_ERR_UNSUPPORTED when sd_verify_workspace_bytes(bs, k_max, V, dt)
+ * exceeds SD_NOALLOC_SCRATCH_BYTES (about 1,900 requests at k_max = 7 and
+ * V = 129280 bf16), with the reason in sd_last_error_string(); SD_ERR_CUDA
+ * when the lookup or the clear fails; otherwise as sd_verify.
  * ---------------------------------------------------------------------- */
 #define SD_NOALLOC_SCRATCH_BYTES (16u << 20) /* 16 MiB */
 
@@ -259,9 +285,12 @@ sd_status sd_verify_noalloc(const void* target_logits, const void* draft_logits,
                             void* stream);
 
 /* Launch shape sd_verify_ex would use for (V, dt, bs) and `req` (NULL =
- * automatic) on the current device.  Host-only query. */
+ * defaults) on the current device: CTAs in chosen->blocks, threads per CTA
+ * and ring buffers in *threads and *buffers, dynamic shared memory in
+ * *smem_bytes (each output pointer may be NULL).  Host-only query. */
 sd_status sd_verify_launch_info(int V, sd_dtype dt, int bs, const sd_launch_cfg* req,
-                                sd_launch_cfg* chosen, size_t* smem_bytes);
+                                sd_launch_cfg* chosen, int* threads, int* buffers,
+                                size_t* smem_bytes);
 
 /* ------------------------------------------------------------------------
  * sd_calibrate / sd_calibrate_apply -- online calibration of the
@@ -311,10 +340,12 @@ sd_status sd_calibrate_apply(const float* conf_logits, const int* draft_lens, in
 
 const char* sd_status_string(sd_status s);
 
-/* Name and text of the last CUDA error an entry point returned SD_ERR_CUDA
- * for, or the reason sd_verify_noalloc refused a call, on the calling host
- * thread ("no error" if none).  The pointer stays valid until the thread's
- * next failing call. */
+/* The reason for the last status other than SD_OK that an entry point
+ * returned on the calling host thread: the CUDA error's name and text for
+ * SD_ERR_CUDA, otherwise the failed check ("no error" if none).  Every entry
+ * point resets it to "no error" when it starts, so the text always belongs to
+ * the thread's latest call.  The pointer stays valid until that thread's next
+ * call. */
 const char* sd_last_error_string(void);
 
 int sd_abi_version(void);

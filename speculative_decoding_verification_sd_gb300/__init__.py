@@ -26,10 +26,12 @@ import torch
 from . import _lib
 from ._lib import (SD_NOALLOC_SCRATCH_BYTES, SD_BF16, SD_DEV_ERR_CONF, SD_DEV_ERR_COST, SD_DEV_ERR_CU_SEQLENS,  # noqa: F401
                    SD_DEV_ERR_DRAFT_ID, SD_DEV_ERR_DRAFT_LENS, SD_DEV_ERR_LOGITS, SD_DEV_ERR_OUTCOME,
-                   SD_DEV_ERR_TEMP, SD_DEV_ERR_UNIFORM, SD_ERR_CUDA,
+                   SD_DEV_ERR_TEMP, SD_DEV_ERR_TIMEOUT, SD_DEV_ERR_UNIFORM, SD_ERR_CUDA,
                    SD_ERR_DEVICE_CHECK, SD_ERR_INVALID_ARG, SD_ERR_SHAPE, SD_ERR_UNSUPPORTED,
-                   SD_F32, SD_MAX_K, SD_MAX_PLAN_SLOTS, SD_MAX_V, SD_MAX_VERIFY_BS,
-                   SD_MODE_ADAPTIVE, SD_MODE_ALL_SLOTS, SD_MODE_UNIFORM_K, SD_OK, SdError, sd_launch_cfg)
+                   SD_F32, SD_MAX_K, SD_MAX_PLAN_SLOTS, SD_MAX_ROW_BYTES, SD_MAX_V, SD_MAX_VERIFY_BS,
+                   SD_MODE_ADAPTIVE, SD_MODE_ALL_SLOTS, SD_MODE_UNIFORM_K, SD_OK,
+                   SD_VERIFY_DRAFT_PADDED, SD_VERIFY_EARLY_EXIT, SD_VERIFY_TEST_STALL, SdError,
+                   sd_launch_cfg)
 
 __all__ = [
     "sd_plan", "sd_verify", "sd_verify_ex", "sd_verify_noalloc", "sd_plan_workspace_bytes",
@@ -86,8 +88,8 @@ def sd_plan_workspace_bytes(bs: int, k_max: int) -> int:
     return _lib.load().sd_plan_workspace_bytes(bs, k_max)
 
 
-def sd_verify_workspace_bytes(bs: int, k_max: int) -> int:
-    return _lib.load().sd_verify_workspace_bytes(bs, k_max)
+def sd_verify_workspace_bytes(bs: int, k_max: int, V: int, dt) -> int:
+    return _lib.load().sd_verify_workspace_bytes(int(bs), int(k_max), int(V), _dt(dt))
 
 
 def sd_plan(conf_logits, budget_conf, budget_draft_lens, bs_budget, draft_lens, bs, k_max,
@@ -128,12 +130,13 @@ def sd_calibrate_apply(conf_logits, draft_lens, bs, k_max, w, b, conf_out, err_f
 
 
 def _cfg(cfg):
+    """sd_launch_cfg from a dict with any of blocks, flags, wait_limit_us."""
     if cfg is None:
         return None
     if isinstance(cfg, sd_launch_cfg):
         return ctypes.byref(cfg)
-    c = sd_launch_cfg(int(cfg.get("threads", 0)), int(cfg.get("blocks", 0)),
-                      int(cfg.get("blocks_per_sm", 0)), 0)
+    c = sd_launch_cfg(int(cfg.get("blocks", 0)), int(cfg.get("flags", 0)),
+                      int(cfg.get("wait_limit_us", 0)), 0)
     return ctypes.byref(c)
 
 
@@ -158,19 +161,23 @@ def sd_verify_noalloc(target_logits, draft_logits, dt, V, draft_ids, uniforms, t
     return _lib.check("sd_verify_noalloc", st)
 
 
-def sd_verify_launch_info(V, dt, bs, threads=0, blocks=0, blocks_per_sm=0) -> dict:
-    req = sd_launch_cfg(threads, blocks, blocks_per_sm, 0)
+def sd_verify_launch_info(V, dt, bs, blocks=0, flags=0) -> dict:
+    req = sd_launch_cfg(int(blocks), int(flags), 0, 0)
     out = sd_launch_cfg()
+    threads, buffers = ctypes.c_int(0), ctypes.c_int(0)
     smem = ctypes.c_size_t(0)
     st = _lib.load().sd_verify_launch_info(int(V), _dt(dt), int(bs), ctypes.byref(req),
-                                           ctypes.byref(out), ctypes.byref(smem))
+                                           ctypes.byref(out), ctypes.byref(threads),
+                                           ctypes.byref(buffers), ctypes.byref(smem))
     _lib.check("sd_verify_launch_info", st)
-    return {"threads": out.threads, "blocks": out.blocks, "smem_bytes": smem.value}
+    return {"blocks": out.blocks, "threads": threads.value, "buffers": buffers.value,
+            "smem_bytes": smem.value}
 
 
-def verify_workspace(bs: int, k_max: int, device=None) -> torch.Tensor:
-    """A zero-filled workspace for sd_verify (zero-filled once; calls keep it so)."""
-    return torch.zeros(sd_verify_workspace_bytes(bs, k_max), dtype=torch.uint8,
+def verify_workspace(bs: int, k_max: int, V: int, dt, device=None) -> torch.Tensor:
+    """A zero-filled workspace for sd_verify (zero-filled once; calls keep it
+    so).  torch's CUDA allocations are 256-byte aligned, as the call requires."""
+    return torch.zeros(sd_verify_workspace_bytes(bs, k_max, V, dt), dtype=torch.uint8,
                        device=device or torch.device("cuda"))
 
 
@@ -223,7 +230,7 @@ def verify(target: torch.Tensor, draft: Optional[torch.Tensor], dt, V: int,
            draft_ids: torch.Tensor, uniforms: torch.Tensor, temps: torch.Tensor,
            cu_seqlens: torch.Tensor, k_max: int, probs: bool = False,
            err: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
-           stream=None) -> VerifyResult:
+           cfg=None, stream=None) -> VerifyResult:
     dev = target.device
     bs = cu_seqlens.numel() - 1
     acc = torch.empty(bs, dtype=torch.int32, device=dev)
@@ -232,7 +239,7 @@ def verify(target: torch.Tensor, draft: Optional[torch.Tensor], dt, V: int,
     if err is None:
         err = torch.zeros(1, dtype=torch.int32, device=dev)
     if workspace is None:
-        workspace = verify_workspace(bs, k_max, dev)
-    sd_verify(target, draft, dt, V, draft_ids, uniforms, temps, cu_seqlens, bs, k_max, acc, out,
-              pr, err, workspace, workspace.numel(), stream)
+        workspace = verify_workspace(bs, k_max, V, dt, dev)
+    sd_verify_ex(target, draft, dt, V, draft_ids, uniforms, temps, cu_seqlens, bs, k_max, acc,
+                 out, pr, err, workspace, workspace.numel(), cfg=cfg, stream=stream)
     return VerifyResult(acc, out, pr, err)

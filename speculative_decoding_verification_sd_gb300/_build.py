@@ -14,7 +14,7 @@ CSRC = PKG / "csrc"
 INCLUDE = PKG.parent / "include"
 LIB = PKG / "libsdverify.so"
 BUILD_DIR = PKG / "_build"
-SOURCES = ("sd_api.cu", "plan_kernel.cu", "verify_kernel.cu", "noalloc.cu")
+SOURCES = ("sd_api.cu", "plan_kernel.cu", "sampler.cu", "noalloc.cu")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
               "-Xptxas", "-v"]

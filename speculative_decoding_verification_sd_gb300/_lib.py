@@ -32,7 +32,12 @@ SD_DEV_ERR_OUTCOME = 0x200
 SD_MAX_K = 15
 SD_MAX_PLAN_SLOTS = 8192
 SD_MAX_VERIFY_BS = 4096
-SD_MAX_V = 1 << 22
+SD_MAX_V = 1 << 20
+SD_MAX_ROW_BYTES = 2 << 20
+
+SD_VERIFY_EARLY_EXIT = 0x1
+SD_VERIFY_DRAFT_PADDED = 0x2
+SD_VERIFY_TEST_STALL = 0x100
 
 # Every symbol include/sd.h declares.
 EXPORTS = ("sd_plan_workspace_bytes", "sd_plan", "sd_verify_workspace_bytes", "sd_verify",
@@ -42,8 +47,8 @@ SD_NOALLOC_SCRATCH_BYTES = 16 << 20  # include/sd.h
 
 
 class sd_launch_cfg(ctypes.Structure):
-    _fields_ = [("threads", ctypes.c_int), ("blocks", ctypes.c_int),
-                ("blocks_per_sm", ctypes.c_int), ("reserved", ctypes.c_int)]
+    _fields_ = [("blocks", ctypes.c_int), ("flags", ctypes.c_int),
+                ("wait_limit_us", ctypes.c_int), ("reserved", ctypes.c_int)]
 
 
 class SdError(RuntimeError):
@@ -76,7 +81,7 @@ def load(path: Path | None = None) -> ctypes.CDLL:
     lib.sd_plan_workspace_bytes.restype = sz
     lib.sd_plan_workspace_bytes.argtypes = [i32, i32]
     lib.sd_verify_workspace_bytes.restype = sz
-    lib.sd_verify_workspace_bytes.argtypes = [i32, i32]
+    lib.sd_verify_workspace_bytes.argtypes = [i32, i32, i32, i32]
     lib.sd_plan.restype = i32
     lib.sd_plan.argtypes = [P, P, P, i32, P, i32, i32, P, i32, i32, i32, P, P, P, P, P, P, sz, P]
     lib.sd_verify.restype = i32
@@ -92,7 +97,8 @@ def load(path: Path | None = None) -> ctypes.CDLL:
     lib.sd_calibrate_apply.argtypes = [P, P, i32, i32, P, P, P, P, P]
     lib.sd_verify_launch_info.restype = i32
     lib.sd_verify_launch_info.argtypes = [i32, i32, i32, ctypes.POINTER(sd_launch_cfg),
-                                          ctypes.POINTER(sd_launch_cfg), ctypes.POINTER(sz)]
+                                          ctypes.POINTER(sd_launch_cfg), ctypes.POINTER(i32),
+                                          ctypes.POINTER(i32), ctypes.POINTER(sz)]
     _lib = lib
     return lib
 
@@ -102,9 +108,9 @@ def status_string(status: int) -> str:
 
 
 def check(fn: str, status: int) -> int:
+    """Raises SdError for a status other than SD_OK, with the library's
+    reason for it (every entry point records one for the calling thread)."""
     if status != SD_OK:
-        text = status_string(status)
-        if status == SD_ERR_CUDA or (fn == "sd_verify_noalloc" and status == SD_ERR_UNSUPPORTED):
-            text += ": " + load().sd_last_error_string().decode()
+        text = status_string(status) + ": " + load().sd_last_error_string().decode()
         raise SdError(fn, status, text)
     return status

@@ -4,6 +4,7 @@
 #include <cuda_runtime.h>
 
 #include <cmath>
+#include <cstdarg>
 #include <cstdio>
 #include <mutex>
 
@@ -29,80 +30,132 @@ int pow2ceil(int v) {
   return p;
 }
 
-size_t align16(size_t v) { return (v + 15) & ~static_cast<size_t>(15); }
-
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
-
-struct VerifyWs {
-  sdk::RowStat* st_t;
-  sdk::RowStat* st_d;
-  float2* st_c;
-  unsigned long long* rs;
-  int* req_cnt;
-  int* res_list;
-  int* slice_cnt;
-  int* ctrl;
-};
-
-// Workspace layout (each part 16-byte aligned):
-// st_t | st_d | st_c | rs | req_cnt | res_list | slice_cnt | ctrl.
-struct WsLayout {
-  size_t st_t, st_d, st_c, rs, req_cnt, res_list, slice_cnt, ctrl, total;
-};
-
-WsLayout ws_layout(int bs, int k_max) {
-  const size_t rows_t = static_cast<size_t>(bs) * (k_max + 1);
-  const size_t rows_d = static_cast<size_t>(bs) * k_max;
-  const size_t ib = align16(4 * static_cast<size_t>(bs));
-  WsLayout L;
-  L.st_t = 0;
-  L.st_d = L.st_t + 16 * rows_t;
-  L.st_c = L.st_d + 16 * rows_d;
-  L.rs = L.st_c + 8 * sdk::kStatStride * rows_t;
-  L.req_cnt = L.rs + 8 * sdk::kStatStride * static_cast<size_t>(bs);
-  L.res_list = L.req_cnt + ib;
-  L.slice_cnt = L.res_list + ib;
-  L.ctrl = L.slice_cnt + ib;
-  L.total = L.ctrl + 32;
-  return L;
-}
-
-size_t verify_ws_bytes(int bs, int k_max) { return ws_layout(bs, k_max).total; }
-
-VerifyWs carve(void* ws, int bs, int k_max) {
-  const WsLayout L = ws_layout(bs, k_max);
-  char* b = static_cast<char*>(ws);
-  VerifyWs w;
-  w.st_t = reinterpret_cast<sdk::RowStat*>(b + L.st_t);
-  w.st_d = reinterpret_cast<sdk::RowStat*>(b + L.st_d);
-  w.st_c = reinterpret_cast<float2*>(b + L.st_c);
-  w.rs = reinterpret_cast<unsigned long long*>(b + L.rs);
-  w.req_cnt = reinterpret_cast<int*>(b + L.req_cnt);
-  w.res_list = reinterpret_cast<int*>(b + L.res_list);
-  w.slice_cnt = reinterpret_cast<int*>(b + L.slice_cnt);
-  w.ctrl = reinterpret_cast<int*>(b + L.ctrl);
-  return w;
-}
-
-sd_status shape_for(int V, sd_dtype dt, int bs, const sd_launch_cfg* cfg, bool vec,
-                    sdk::VerifyShape* shape) {
-  const int elem = dt == SD_F32 ? 4 : 2;
-  bool fits = false;
-  if (note(sdk::choose_verify_shape(V, elem, bs, cfg, vec, shape, &fits)) != cudaSuccess)
-    return SD_ERR_CUDA;
-  return fits ? SD_OK : SD_ERR_UNSUPPORTED;
-}
 
 }  // namespace
 
 namespace sdk {
-size_t verify_ws_zero_offset(int bs, int k_max) { return ws_layout(bs, k_max).rs; }
+
 void set_last_error(const char* msg) { snprintf(g_last_error, sizeof g_last_error, "%s", msg); }
+void clear_last_error() { set_last_error("no error"); }
+
+// Records why a call is refused; returns the status unchanged.
+sd_status refuse(sd_status st, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_last_error, sizeof g_last_error, fmt, ap);
+  va_end(ap);
+  return st;
+}
+
+// 2^(j/16), j = 0..15, each split into two floats (hi + lo) -- the table of
+// the sampler's precise exponent.
+static void exp_table(float2* tab) {
+  for (int j = 0; j < 16; ++j) {
+    const double t = std::exp2(static_cast<double>(j) / 16.0);
+    const float hi = static_cast<float>(t);
+    tab[j] = make_float2(hi, static_cast<float>(t - static_cast<double>(hi)));
+  }
+}
+
+sd_status verify_setup(const void* target_logits, const void* draft_logits, sd_dtype dt, int V,
+                       const int* draft_ids, const float* uniforms, const float* temps,
+                       const int* cu_seqlens, int bs, int k_max, int* accepted_len,
+                       int* out_tokens, float* probs_out, int* err_flag,
+                       const sd_launch_cfg* cfg, VerifyCall* call) {
+  if (bs < 1 || k_max < 0) return refuse(SD_ERR_INVALID_ARG, "bs=%d, k_max=%d: need bs >= 1, k_max >= 0", bs, k_max);
+  if (k_max > SD_MAX_K || bs > SD_MAX_VERIFY_BS)
+    return refuse(SD_ERR_UNSUPPORTED, "bs=%d, k_max=%d beyond SD_MAX_VERIFY_BS=%d / SD_MAX_K=%d", bs,
+                  k_max, SD_MAX_VERIFY_BS, SD_MAX_K);
+  if (dt != SD_F32 && dt != SD_BF16) return refuse(SD_ERR_INVALID_ARG, "unknown dtype %d", static_cast<int>(dt));
+  if (V < 1) return refuse(SD_ERR_INVALID_ARG, "V=%d < 1", V);
+  const int elem = dt == SD_F32 ? 4 : 2;
+  if (V > SD_MAX_V || static_cast<size_t>(V) * elem > static_cast<size_t>(SD_MAX_ROW_BYTES))
+    return refuse(SD_ERR_UNSUPPORTED, "V=%d (%d-byte elements) beyond SD_MAX_V / SD_MAX_ROW_BYTES", V, elem);
+  if (!target_logits || !uniforms || !temps || !cu_seqlens || !err_flag || !accepted_len ||
+      !out_tokens)
+    return refuse(SD_ERR_INVALID_ARG, "a required pointer is NULL");
+  if (k_max > 0 && !draft_ids) return refuse(SD_ERR_INVALID_ARG, "draft_ids is NULL");
+  int blocks = 0, flags = 0, wait_us = 0;
+  if (cfg) {
+    if (cfg->blocks < 0 || cfg->wait_limit_us < 0 || cfg->reserved != 0)
+      return refuse(SD_ERR_INVALID_ARG, "sd_launch_cfg: negative field or reserved != 0");
+    if (cfg->flags & ~(SD_VERIFY_EARLY_EXIT | SD_VERIFY_DRAFT_PADDED | SD_VERIFY_TEST_STALL))
+      return refuse(SD_ERR_INVALID_ARG, "sd_launch_cfg: unknown flag bits 0x%x", cfg->flags);
+    blocks = cfg->blocks;
+    flags = cfg->flags;
+    wait_us = cfg->wait_limit_us;
+  }
+  call->vec = (static_cast<size_t>(V) * elem) % 16 == 0 && aligned16(target_logits) &&
+              (draft_logits == nullptr || aligned16(draft_logits));
+  call->blocks = blocks;
+  const SamplerWs L = sampler_ws_layout(bs, k_max, V, elem);
+  call->elem = elem;
+  call->ws_need = L.total;
+  call->zero_off = L.zero;
+  SamplerParams& p = call->p;
+  p = SamplerParams{};
+  p.target = target_logits;
+  p.draft = draft_logits;
+  p.V = V;
+  p.draft_ids = draft_ids;
+  p.uniforms = uniforms;
+  p.temps = temps;
+  p.cu = cu_seqlens;
+  p.bs = bs;
+  p.k_max = k_max;
+  p.accepted_len = accepted_len;
+  p.out_tokens = out_tokens;
+  p.probs_out = probs_out;
+  p.err = err_flag;
+  p.flags = flags;
+  p.wait_ns = 1000ull * static_cast<uint64_t>(wait_us > 0 ? wait_us : 1000000);
+  const size_t rb = static_cast<size_t>(V) * elem;
+  p.nseg = static_cast<int>((rb + kSegBytes - 1) / kSegBytes);
+  p.nsub = static_cast<int>((rb + kSubBytes - 1) / kSubBytes);
+  exp_table(p.exp_tab);
+  return SD_OK;
+}
+
+sd_status verify_shape(VerifyCall* call) {
+  bool fits = false;
+  if (note(choose_sampler_shape(call->p.V, call->elem, call->p.bs, call->blocks, call->vec,
+                                &call->shape, &fits)) != cudaSuccess)
+    return SD_ERR_CUDA;
+  if (!fits)
+    return refuse(SD_ERR_UNSUPPORTED, "bs=%d: the sampler's shared memory does not fit", call->p.bs);
+  call->p.nbuf = call->shape.nbuf;
+  return SD_OK;
+}
+
+void verify_bind(VerifyCall* call, void* workspace) {
+  const SamplerWs L = sampler_ws_layout(call->p.bs, call->p.k_max, call->p.V, call->elem);
+  char* b = static_cast<char*>(workspace);
+  SamplerParams& p = call->p;
+  p.seg_t = reinterpret_cast<SegRec*>(b + L.seg_t);
+  p.seg_d = reinterpret_cast<SegRec*>(b + L.seg_d);
+  p.ps = reinterpret_cast<PairStat*>(b + L.ps);
+  p.rs = reinterpret_cast<unsigned long long*>(b + L.rs);
+  p.pc = reinterpret_cast<int*>(b + L.pc);
+  p.st = reinterpret_cast<int*>(b + L.st);
+  p.ev = reinterpret_cast<int*>(b + L.ev);
+  p.dl = reinterpret_cast<int*>(b + L.dl);
+  p.dc = reinterpret_cast<int*>(b + L.dc);
+  p.ctrl = reinterpret_cast<int*>(b + L.ctrl);
+}
+
+sd_status verify_launch(const VerifyCall& call, void* stream) {
+  return note(launch_sampler(call.p, call.elem, call.shape, static_cast<cudaStream_t>(stream))) ==
+                 cudaSuccess
+             ? SD_OK
+             : SD_ERR_CUDA;
+}
+
 }  // namespace sdk
 
 extern "C" {
 
-int sd_abi_version(void) { return 1; }
+int sd_abi_version(void) { return 2; }
 
 const char* sd_last_error_string(void) { return g_last_error; }
 
@@ -124,6 +177,37 @@ size_t sd_plan_workspace_bytes(int bs, int k_max) {
   return 0;
 }
 
+// Host checks of sd_plan; records the reason of a refusal.
+static sd_status plan_checks(const float* conf_logits, const float* budget_conf,
+                             const int* budget_draft_lens, int bs_budget, const int* draft_lens,
+                             int bs, int k_max, const float* cost_table, int cost_len, int T,
+                             sd_mode mode, const int* B_out, const uint8_t* slot_mask,
+                             const int* num_verified, const int* cu_seqlens, const int* err_flag) {
+  using sdk::refuse;
+  if (bs < 1 || k_max < 0) return refuse(SD_ERR_INVALID_ARG, "bs=%d, k_max=%d", bs, k_max);
+  if (k_max > SD_MAX_K) return refuse(SD_ERR_UNSUPPORTED, "k_max=%d > SD_MAX_K", k_max);
+  if (mode != SD_MODE_ADAPTIVE && mode != SD_MODE_ALL_SLOTS && mode != SD_MODE_UNIFORM_K)
+    return refuse(SD_ERR_INVALID_ARG, "unknown mode %d", static_cast<int>(mode));
+  if (!draft_lens || !B_out || !num_verified || !cu_seqlens || !err_flag)
+    return refuse(SD_ERR_INVALID_ARG, "a required pointer is NULL");
+  if (k_max > 0 && !slot_mask) return refuse(SD_ERR_INVALID_ARG, "slot_mask is NULL");
+  const int P = pow2ceil(k_max < 1 ? 1 : k_max);
+  if (static_cast<long long>(pow2ceil(bs)) * P > SD_MAX_PLAN_SLOTS)
+    return refuse(SD_ERR_UNSUPPORTED, "pow2ceil(bs)*pow2ceil(k_max) > SD_MAX_PLAN_SLOTS");
+  if (mode != SD_MODE_ALL_SLOTS) {
+    if (!conf_logits || !cost_table) return refuse(SD_ERR_INVALID_ARG, "conf_logits or cost_table is NULL");
+    if (T < 1 || cost_len < 1) return refuse(SD_ERR_INVALID_ARG, "T=%d, cost_len=%d", T, cost_len);
+    if (T >= cost_len) return refuse(SD_ERR_SHAPE, "T=%d >= cost_len=%d", T, cost_len);
+    if (mode == SD_MODE_ADAPTIVE && budget_conf) {
+      if (!budget_draft_lens || bs_budget < 1)
+        return refuse(SD_ERR_INVALID_ARG, "budget_conf without budget_draft_lens / bs_budget");
+      if (static_cast<long long>(pow2ceil(bs_budget)) * P > SD_MAX_PLAN_SLOTS)
+        return refuse(SD_ERR_UNSUPPORTED, "budget set beyond SD_MAX_PLAN_SLOTS");
+    }
+  }
+  return SD_OK;
+}
+
 sd_status sd_plan(const float* conf_logits, const float* budget_conf, const int* budget_draft_lens,
                   int bs_budget, const int* draft_lens, int bs, int k_max, const float* cost_table,
                   int cost_len, int T, sd_mode mode, int* B_out, uint8_t* slot_mask,
@@ -131,26 +215,13 @@ sd_status sd_plan(const float* conf_logits, const float* budget_conf, const int*
                   size_t ws_bytes, void* stream) {
   (void)workspace;
   (void)ws_bytes;
-  if (bs < 1 || k_max < 0) return SD_ERR_INVALID_ARG;
-  if (k_max > SD_MAX_K) return SD_ERR_UNSUPPORTED;
-  if (mode != SD_MODE_ADAPTIVE && mode != SD_MODE_ALL_SLOTS && mode != SD_MODE_UNIFORM_K)
-    return SD_ERR_INVALID_ARG;
-  if (!draft_lens || !B_out || !num_verified || !cu_seqlens || !err_flag) return SD_ERR_INVALID_ARG;
-  if (k_max > 0 && !slot_mask) return SD_ERR_INVALID_ARG;
+  sdk::clear_last_error();
+  const sd_status st = plan_checks(conf_logits, budget_conf, budget_draft_lens, bs_budget,
+                                   draft_lens, bs, k_max, cost_table, cost_len, T, mode, B_out,
+                                   slot_mask, num_verified, cu_seqlens, err_flag);
+  if (st != SD_OK) return st;
   const int P = pow2ceil(k_max < 1 ? 1 : k_max);
-  if (static_cast<long long>(pow2ceil(bs)) * P > SD_MAX_PLAN_SLOTS) return SD_ERR_UNSUPPORTED;
-  int NPb = 0;
-  if (mode != SD_MODE_ALL_SLOTS) {
-    if (!conf_logits || !cost_table) return SD_ERR_INVALID_ARG;
-    if (T < 1 || cost_len < 1) return SD_ERR_INVALID_ARG;
-    if (T >= cost_len) return SD_ERR_SHAPE;
-    if (mode == SD_MODE_ADAPTIVE && budget_conf) {
-      if (!budget_draft_lens || bs_budget < 1) return SD_ERR_INVALID_ARG;
-      if (static_cast<long long>(pow2ceil(bs_budget)) * P > SD_MAX_PLAN_SLOTS)
-        return SD_ERR_UNSUPPORTED;
-      NPb = pow2ceil(bs_budget) * P;
-    }
-  }
+  const int NPb = (mode == SD_MODE_ADAPTIVE && budget_conf) ? pow2ceil(bs_budget) * P : 0;
   sdk::PlanParams p;
   p.conf = conf_logits;
   p.budget_conf = mode == SD_MODE_ADAPTIVE ? budget_conf : nullptr;
@@ -177,10 +248,12 @@ sd_status sd_plan(const float* conf_logits, const float* budget_conf, const int*
 
 // Host checks shared by the two calibration calls; fills the shape fields.
 static sd_status calib_shape(int bs, int k_max, sdk::CalibParams& p) {
-  if (bs < 1 || k_max < 0) return SD_ERR_INVALID_ARG;
-  if (k_max > SD_MAX_K) return SD_ERR_UNSUPPORTED;
+  sdk::clear_last_error();
+  if (bs < 1 || k_max < 0) return sdk::refuse(SD_ERR_INVALID_ARG, "bs=%d, k_max=%d", bs, k_max);
+  if (k_max > SD_MAX_K) return sdk::refuse(SD_ERR_UNSUPPORTED, "k_max=%d > SD_MAX_K", k_max);
   const int P = pow2ceil(k_max < 1 ? 1 : k_max);
-  if (static_cast<long long>(pow2ceil(bs)) * P > SD_MAX_PLAN_SLOTS) return SD_ERR_UNSUPPORTED;
+  if (static_cast<long long>(pow2ceil(bs)) * P > SD_MAX_PLAN_SLOTS)
+    return sdk::refuse(SD_ERR_UNSUPPORTED, "pow2ceil(bs)*pow2ceil(k_max) > SD_MAX_PLAN_SLOTS");
   p.bs = bs;
   p.k_max = k_max;
   p.P = P;
@@ -194,9 +267,11 @@ sd_status sd_calibrate(const float* conf_logits, const int* draft_lens, const in
   sdk::CalibParams p{};
   const sd_status st = calib_shape(bs, k_max, p);
   if (st != SD_OK) return st;
-  if (!(std::isfinite(lr) && lr >= 0.0f)) return SD_ERR_INVALID_ARG;
-  if (!draft_lens || !num_verified || !accepted_len || !err_flag) return SD_ERR_INVALID_ARG;
-  if (k_max > 0 && (!conf_logits || !w || !b)) return SD_ERR_INVALID_ARG;
+  if (!(std::isfinite(lr) && lr >= 0.0f)) return sdk::refuse(SD_ERR_INVALID_ARG, "lr not finite or < 0");
+  if (!draft_lens || !num_verified || !accepted_len || !err_flag)
+    return sdk::refuse(SD_ERR_INVALID_ARG, "a required pointer is NULL");
+  if (k_max > 0 && (!conf_logits || !w || !b))
+    return sdk::refuse(SD_ERR_INVALID_ARG, "conf_logits, w or b is NULL");
   if (k_max == 0) return SD_OK;
   p.conf = conf_logits;
   p.lens = draft_lens;
@@ -219,8 +294,9 @@ sd_status sd_calibrate_apply(const float* conf_logits, const int* draft_lens, in
   sdk::CalibParams p{};
   const sd_status st = calib_shape(bs, k_max, p);
   if (st != SD_OK) return st;
-  if (!draft_lens || !err_flag) return SD_ERR_INVALID_ARG;
-  if (k_max > 0 && (!conf_logits || !w || !b || !conf_out)) return SD_ERR_INVALID_ARG;
+  if (!draft_lens || !err_flag) return sdk::refuse(SD_ERR_INVALID_ARG, "a required pointer is NULL");
+  if (k_max > 0 && (!conf_logits || !w || !b || !conf_out))
+    return sdk::refuse(SD_ERR_INVALID_ARG, "conf_logits, w, b or conf_out is NULL");
   if (k_max == 0) return SD_OK;
   p.conf = conf_logits;
   p.lens = draft_lens;
@@ -237,9 +313,9 @@ sd_status sd_calibrate_apply(const float* conf_logits, const int* draft_lens, in
              : SD_ERR_CUDA;
 }
 
-size_t sd_verify_workspace_bytes(int bs, int k_max) {
-  if (bs < 1 || k_max < 0) return 0;
-  return verify_ws_bytes(bs, k_max);
+size_t sd_verify_workspace_bytes(int bs, int k_max, int V, sd_dtype dt) {
+  if (bs < 1 || k_max < 0 || V < 1 || (dt != SD_F32 && dt != SD_BF16)) return 0;
+  return sdk::sampler_ws_layout(bs, k_max, V, dt == SD_F32 ? 4 : 2).total;
 }
 
 sd_status sd_verify_ex(const void* target_logits, const void* draft_logits, sd_dtype dt, int V,
@@ -247,52 +323,20 @@ sd_status sd_verify_ex(const void* target_logits, const void* draft_logits, sd_d
                        const int* cu_seqlens, int bs, int k_max, int* accepted_len,
                        int* out_tokens, float* probs_out, int* err_flag, void* workspace,
                        size_t ws_bytes, const sd_launch_cfg* cfg, void* stream) {
-  if (bs < 1 || k_max < 0) return SD_ERR_INVALID_ARG;
-  if (k_max > SD_MAX_K || bs > SD_MAX_VERIFY_BS) return SD_ERR_UNSUPPORTED;
-  if (!workspace || !aligned16(workspace)) return SD_ERR_INVALID_ARG;
-  if (ws_bytes < verify_ws_bytes(bs, k_max)) return SD_ERR_SHAPE;
-  if (dt != SD_F32 && dt != SD_BF16) return SD_ERR_INVALID_ARG;
-  if (V < 1) return SD_ERR_INVALID_ARG;
-  if (V > SD_MAX_V) return SD_ERR_UNSUPPORTED;
-  if (!target_logits || !uniforms || !temps || !cu_seqlens || !err_flag || !accepted_len ||
-      !out_tokens)
-    return SD_ERR_INVALID_ARG;
-  if (k_max > 0 && !draft_ids) return SD_ERR_INVALID_ARG;
-  if (cfg && (cfg->threads < 0 || cfg->blocks < 0 || cfg->blocks_per_sm < 0))
-    return SD_ERR_INVALID_ARG;
-  const int elem = dt == SD_F32 ? 4 : 2;
-  const bool vec = (static_cast<size_t>(V) * elem) % 16 == 0 && aligned16(target_logits) &&
-                   (draft_logits == nullptr || aligned16(draft_logits));
-  sdk::VerifyShape shape;
-  sd_status st = shape_for(V, dt, bs, cfg, vec, &shape);
+  sdk::clear_last_error();
+  sdk::VerifyCall call;
+  const sd_status st = sdk::verify_setup(target_logits, draft_logits, dt, V, draft_ids, uniforms,
+                                         temps, cu_seqlens, bs, k_max, accepted_len, out_tokens,
+                                         probs_out, err_flag, cfg, &call);
   if (st != SD_OK) return st;
-  VerifyWs w = carve(workspace, bs, k_max);
-  sdk::VerifyParams p;
-  p.target = target_logits;
-  p.draft = draft_logits;
-  p.V = V;
-  p.draft_ids = draft_ids;
-  p.uniforms = uniforms;
-  p.temps = temps;
-  p.cu = cu_seqlens;
-  p.bs = bs;
-  p.k_max = k_max;
-  p.accepted_len = accepted_len;
-  p.out_tokens = out_tokens;
-  p.probs_out = probs_out;
-  p.err = err_flag;
-  p.st_t = w.st_t;
-  p.st_d = w.st_d;
-  p.st_c = w.st_c;
-  p.rs = w.rs;
-  p.req_cnt = w.req_cnt;
-  p.res_list = w.res_list;
-  p.slice_cnt = w.slice_cnt;
-  p.ctrl = w.ctrl;
-  return note(sdk::launch_verify(p, elem, shape, static_cast<cudaStream_t>(stream))) ==
-                 cudaSuccess
-             ? SD_OK
-             : SD_ERR_CUDA;
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+    return sdk::refuse(SD_ERR_INVALID_ARG, "workspace NULL or not 256-byte aligned");
+  if (ws_bytes < call.ws_need)
+    return sdk::refuse(SD_ERR_SHAPE, "ws_bytes=%zu < %zu", ws_bytes, call.ws_need);
+  const sd_status sh = sdk::verify_shape(&call);
+  if (sh != SD_OK) return sh;
+  sdk::verify_bind(&call, workspace);
+  return sdk::verify_launch(call, stream);
 }
 
 sd_status sd_verify(const void* target_logits, const void* draft_logits, sd_dtype dt, int V,
@@ -306,18 +350,30 @@ sd_status sd_verify(const void* target_logits, const void* draft_logits, sd_dtyp
 }
 
 sd_status sd_verify_launch_info(int V, sd_dtype dt, int bs, const sd_launch_cfg* req,
-                                sd_launch_cfg* chosen, size_t* smem_bytes) {
-  if (V < 1 || bs < 1 || (dt != SD_F32 && dt != SD_BF16) || !chosen) return SD_ERR_INVALID_ARG;
-  if (bs > SD_MAX_VERIFY_BS || V > SD_MAX_V) return SD_ERR_UNSUPPORTED;
+                                sd_launch_cfg* chosen, int* threads, int* buffers,
+                                size_t* smem_bytes) {
+  sdk::clear_last_error();
+  if (V < 1 || bs < 1 || (dt != SD_F32 && dt != SD_BF16) || !chosen)
+    return sdk::refuse(SD_ERR_INVALID_ARG, "invalid V, bs, dtype or NULL output");
   const int elem = dt == SD_F32 ? 4 : 2;
+  if (bs > SD_MAX_VERIFY_BS || V > SD_MAX_V ||
+      static_cast<size_t>(V) * elem > static_cast<size_t>(SD_MAX_ROW_BYTES))
+    return sdk::refuse(SD_ERR_UNSUPPORTED, "beyond this library's limits");
+  if (req && (req->blocks < 0 || req->reserved != 0))
+    return sdk::refuse(SD_ERR_INVALID_ARG, "sd_launch_cfg: negative field or reserved != 0");
   const bool vec = (static_cast<size_t>(V) * elem) % 16 == 0;
-  sdk::VerifyShape shape;
-  sd_status st = shape_for(V, dt, bs, req, vec, &shape);
-  if (st != SD_OK) return st;
-  chosen->threads = shape.threads;
+  sdk::SamplerShape shape;
+  bool fits = false;
+  if (note(sdk::choose_sampler_shape(V, elem, bs, req ? req->blocks : 0, vec, &shape, &fits)) !=
+      cudaSuccess)
+    return SD_ERR_CUDA;
+  if (!fits) return sdk::refuse(SD_ERR_UNSUPPORTED, "the sampler's shared memory does not fit");
   chosen->blocks = shape.blocks;
-  chosen->blocks_per_sm = 0;
+  chosen->flags = req ? req->flags : 0;
+  chosen->wait_limit_us = req ? req->wait_limit_us : 0;
   chosen->reserved = 0;
+  if (threads) *threads = shape.threads;
+  if (buffers) *buffers = shape.nbuf;
   if (smem_bytes) *smem_bytes = shape.smem;
   return SD_OK;
 }

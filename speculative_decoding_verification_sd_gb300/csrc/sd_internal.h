@@ -38,15 +38,50 @@ size_t plan_smem_bytes(const PlanParams& p);
 cudaError_t launch_plan(const PlanParams& p, cudaStream_t s);
 
 // ---------------------------------------------------------------- sampler
-// Statistics of one logit row, 16 bytes: m = max logit, z = sum over the row
-// of 2^((l - m) * log2(e) / tau) (tau > 0), lx = logit at the slot's draft
-// token, amax = lowest index of the maximum (tau = 0; -1 if the row is bad).
-struct __align__(16) RowStat {
-  float m, z, lx;
-  int amax;
+// The sampling kernel cuts every logit row into segments of kSegBytes (one
+// bulk copy each) and every final draw's row(s) into sub-chunks of
+// kSubBytes per row (a target and a draft sub-chunk share one buffer).
+constexpr int kSegBytes = 8192;
+constexpr int kSubBytes = kSegBytes / 2;
+constexpr int kMaxRowBytes = 256 * kSegBytes;  // V * elem <= 2 MiB: at most 256 segments
+
+// Partial statistics of one segment of one row, 16 bytes.  Sampling rows:
+// m = NaN-propagating maximum, z = sum over the segment of
+// 2^((l - m) * log2(e) / tau) (fp64 bits in w2, w3).  Greedy rows: m = the
+// NaN-propagating maximum, w2 = lowest index of the maximum, w3 = 1 if the
+// segment holds NaN or +inf.  lx = the logit at the slot's draft token when
+// that token lies in the segment.
+struct __align__(16) SegRec {
+  float m, lx;
+  uint32_t w2, w3;
 };
 
-struct VerifyParams {
+// Row statistics of one (request, slot) pair: the target row t_j and, for a
+// sampling slot, the draft row d_j.  Z = sum over the row of
+// 2^((l - M) * log2(e) / tau); amax = lowest argmax of t_j (greedy).
+struct __align__(16) PairStat {
+  float Mt, Md;
+  int amax, bad;
+  double Zt, Zd;
+};
+
+// Control words of one call (all zero between calls).
+enum {
+  kCtlRowBlk = 0,   // row blocks claimed
+  kCtlCtas = 1,     // CTAs finished
+  kCtlDraws = 2,    // final draws listed
+  kCtlDrawBlk = 3,  // draw blocks claimed
+  kCtlReqDone = 4,  // requests whose outputs are complete
+  kCtlStop = 5,     // a bounded wait gave up in this call
+  kCtlWords = 8
+};
+
+// Bits of sd_launch_cfg.flags the kernel reads (include/sd.h).
+constexpr int kFlagEarlyExit = SD_VERIFY_EARLY_EXIT;
+constexpr int kFlagDraftPadded = SD_VERIFY_DRAFT_PADDED;
+constexpr int kFlagTestStall = SD_VERIFY_TEST_STALL;
+
+struct SamplerParams {
   const void* target;
   const void* draft;
   int V;
@@ -60,41 +95,74 @@ struct VerifyParams {
   int* out_tokens;
   float* probs_out;
   int* err;
-  RowStat* st_t;  // [bs*(k_max+1)]
-  RowStat* st_d;  // [bs*k_max]
-  float2* st_c;   // [bs*(k_max+1)][kStatStride] per-chunk (max, scaled sum) of target rows
-  unsigned long long* rs;  // [bs][kStatStride] per-chunk residual sums (2^56 fixed point)
-                           //   of the listed residual draws; zero between calls
-  int* req_cnt;   // [bs]   rows finished per request; zero between calls
-  int* res_list;  // [bs]   listed residual draws, 1 + (request << 4 | slot); zero between calls
-  int* slice_cnt; // [bs]   slices finished per listed residual draw; zero between calls
-  int* ctrl;      // [8]    rows handed out, CTAs finished, residual draws listed,
-                  //        residual draws claimed, sampling requests decided;
-                  //        zero between calls
+  int flags;
+  uint64_t wait_ns;  // how long a device-side wait may last before it gives up
+  int nseg;          // segments per row
+  int nsub;          // draw sub-chunks per row
+  int nbuf;          // ring buffers per CTA
+  // workspace
+  SegRec* seg_t;              // [bs*(k_max+1)][nseg], by target row
+  SegRec* seg_d;              // [bs*k_max][nseg], by draft row
+  PairStat* ps;               // [bs*(k_max+1)] by pair i*(k_max+1)+j
+  unsigned long long* rs;     // [2*bs][nsub] sub-chunk sums of each listed draw
+  int* pc;                    // [bs*(k_max+1)] per pair: segments counted, plus
+                              //   skip items << 16                             (zero between calls)
+  int* st;                    // [bs] slot decisions per request               (zero between calls)
+  int* ev;                    // [bs] pair and final-token events per request  (zero between calls)
+  int* dl;                    // [2*bs] listed draws                           (zero between calls)
+  int* dc;                    // [2*bs] sub-chunks counted per draw            (zero between calls)
+  int* ctrl;                  // [kCtlWords]                                   (zero between calls)
+  float2 exp_tab[16];         // 2^(j/16) as (hi, lo) pairs
 };
 
-// Statistics chunks: a row is cut into at most kStatStride chunks whose
-// softmax statistics (target rows) or residual sums (listed draws) are kept,
-// so a final draw reads back one chunk instead of its row.
-constexpr int kStatStride = 128;
+// Workspace layout of the sampling kernel (each part 256-byte aligned); the
+// parts from `zero` on must be zero before a call and are left zero by it.
+struct SamplerWs {
+  size_t seg_t, seg_d, ps, rs, zero, pc, st, ev, dl, dc, ctrl, total;
+};
+SamplerWs sampler_ws_layout(int bs, int k_max, int V, int elem);
 
-struct VerifyShape {
-  int threads, blocks;
+struct SamplerShape {
+  int blocks, threads, nbuf;
   size_t smem;
   bool vec;
 };
 
-// Chooses the launch of the sampling kernel for (V, dtype, bs) on the current
-// device, honouring a user request; *fits = false when nothing fits.
-cudaError_t choose_verify_shape(int V, int elem, int bs, const sd_launch_cfg* req, bool vec,
-                                VerifyShape* out, bool* fits);
-cudaError_t launch_verify(const VerifyParams& p, int elem, const VerifyShape& shape,
-                          cudaStream_t s);
+// Launch shape for (V, elem, bs) on the current device; *fits = false when the
+// ring does not fit.  `blocks` = 0 asks for one CTA per SM.
+cudaError_t choose_sampler_shape(int V, int elem, int bs, int blocks, bool vec,
+                                 SamplerShape* out, bool* fits);
+cudaError_t launch_sampler(const SamplerParams& p, int elem, const SamplerShape& shape,
+                           cudaStream_t s);
 
-// Offset of the first workspace byte that must be zero before a call (the
-// residual sums and every counter sit in [offset, sd_verify_workspace_bytes)).
-size_t verify_ws_zero_offset(int bs, int k_max);
-// Sets the message sd_last_error_string() returns on this host thread.
+// One sd_verify call after its host-side checks: kernel parameters (the
+// workspace pointers still unset), launch shape, workspace size and the
+// offset of its part that must be zero before a call.
+struct VerifyCall {
+  SamplerParams p;
+  SamplerShape shape;
+  int elem, blocks;
+  bool vec;
+  size_t ws_need, zero_off;
+};
+
+// Host-side checks and parameters of a sampling call (sd_verify_ex's
+// arguments minus the workspace), with no CUDA call; records the reason of a
+// refusal.  verify_shape then picks the launch shape on the current device.
+sd_status verify_setup(const void* target_logits, const void* draft_logits, sd_dtype dt, int V,
+                       const int* draft_ids, const float* uniforms, const float* temps,
+                       const int* cu_seqlens, int bs, int k_max, int* accepted_len,
+                       int* out_tokens, float* probs_out, int* err_flag,
+                       const sd_launch_cfg* cfg, VerifyCall* call);
+sd_status verify_shape(VerifyCall* call);
+// Points the call's workspace parts into `workspace` (call->ws_need bytes).
+void verify_bind(VerifyCall* call, void* workspace);
+sd_status verify_launch(const VerifyCall& call, void* stream);
+
+// Sets / clears the message sd_last_error_string() returns on this host thread.
 void set_last_error(const char* msg);
+void clear_last_error();
+// Records why a call is refused (printf format); returns `st` unchanged.
+sd_status refuse(sd_status st, const char* fmt, ...);
 
 }  // namespace sdk
