@@ -92,17 +92,39 @@ def compare_plan(g, o, what=""):
     return same
 
 
-def gpu_verify(w, vi, cu, k_max, cfg=None, rows_cap=None, workspace=None):
-    """Runs the sampling stage through the C ABI with capacity-sized buffers."""
+def padded_rows(rows, cu, k_max, fill):
+    """Compacted draft rows (or ids) to the uncompacted layout: (i, j) at
+    i*k_max + j, the rest `fill`."""
+    bs = len(cu) - 1
+    shape = (max(bs * k_max, 1),) + rows.shape[1:]
+    out = np.full(shape, fill, dtype=rows.dtype)
+    for i in range(bs):
+        n = int(cu[i + 1] - cu[i] - 1)
+        if n:
+            out[i * k_max: i * k_max + n] = rows[cu[i] - i: cu[i] - i + n]
+    return out
+
+
+def gpu_verify(w, vi, cu, k_max, cfg=None, rows_cap=None, workspace=None, padded=False):
+    """Runs the sampling stage through the C ABI with capacity-sized buffers.
+    With ``padded`` the draft rows and ids are passed uncompacted (row of
+    (i, j) at i*k_max + j, SD_VERIFY_DRAFT_PADDED); probabilities are mapped
+    back to the compacted index."""
     import torch
     import speculative_decoding_verification_sd_gb300 as sd
     bs = len(cu) - 1
     rows_cap = rows_cap or bs * (k_max + 1)
+    draft, ids_h = vi["draft"], vi["draft_ids"]
+    cfg = dict(cfg or {})
+    if padded:
+        draft = padded_rows(draft, cu, k_max, 0) if len(draft) else draft
+        ids_h = padded_rows(ids_h, cu, k_max, 0)
+        cfg["flags"] = cfg.get("flags", 0) | sd.SD_VERIFY_DRAFT_PADDED
     tgt = alloc_rows(rows_cap, w.V, w.dtype, vi["target"])
-    dft = alloc_rows(max(bs * k_max, 1), w.V, w.dtype, vi["draft"])
+    dft = alloc_rows(max(bs * k_max, 1), w.V, w.dtype, draft)
     ids = torch.zeros(max(bs * k_max, 1), dtype=torch.int32, device=torch_dev())
-    if len(vi["draft_ids"]):
-        ids[: len(vi["draft_ids"])] = torch.from_numpy(vi["draft_ids"]).to(torch_dev())
+    if len(ids_h):
+        ids[: len(ids_h)] = torch.from_numpy(np.ascontiguousarray(ids_h, np.int32)).to(torch_dev())
     u = torch.from_numpy(vi["uniforms"]).to(torch_dev())
     tp = torch.from_numpy(vi["temps"]).to(torch_dev())
     cu_d = torch.from_numpy(np.asarray(cu, np.int32)).to(torch_dev())
@@ -111,12 +133,19 @@ def gpu_verify(w, vi, cu, k_max, cfg=None, rows_cap=None, workspace=None):
     out = torch.empty((bs, k_max + 1), dtype=torch.int32, device=torch_dev())
     probs = torch.full((max(bs * k_max, 1), 2), float("nan"), dtype=torch.float32, device=torch_dev())
     err = torch.zeros(1, dtype=torch.int32, device=torch_dev())
-    ws = workspace if workspace is not None else sd.verify_workspace(bs, k_max, torch_dev())
+    ws = workspace if workspace is not None else sd.verify_workspace(bs, k_max, w.V, dt, torch_dev())
     sd.sd_verify_ex(tgt, dft, dt, w.V, ids, u, tp, cu_d, bs, k_max, acc, out, probs, err, ws,
                     ws.numel(), cfg=cfg)
     torch.cuda.synchronize()
+    pr = probs.cpu().numpy()
+    if padded:
+        comp = np.full((max(int(cu[-1]) - bs, 1), 2), np.nan, np.float32)
+        for i in range(bs):
+            n = int(cu[i + 1] - cu[i] - 1)
+            comp[cu[i] - i: cu[i] - i + n] = pr[i * k_max: i * k_max + n]
+        pr = comp
     return {"accepted_len": acc.cpu().numpy(), "out_tokens": out.cpu().numpy(),
-            "probs": probs.cpu().numpy(), "err": int(err.item()),
+            "probs": pr, "err": int(err.item()),
             "target_dev": tgt, "draft_dev": dft, "workspace": ws}
 
 

@@ -36,7 +36,7 @@ def test_header_declarations_are_exported(lib):
 
 def test_abi_version_and_status_strings(lib):
     import speculative_decoding_verification_sd_gb300 as sd
-    assert lib.sd_abi_version() == 1
+    assert lib.sd_abi_version() == 2
     for st in (0, -1, -2, -3, -4, -5):
         assert sd._lib.status_string(st)
 
@@ -44,9 +44,13 @@ def test_abi_version_and_status_strings(lib):
 def test_workspace_sizes(lib):
     import speculative_decoding_verification_sd_gb300 as sd
     assert sd.sd_plan_workspace_bytes(256, 7) == 0
-    rows = 256 * 8
-    assert sd.sd_verify_workspace_bytes(256, 7) >= rows * 5
-    assert sd.sd_verify_workspace_bytes(0, 7) == 0
+    # at least one 16-byte record per 8 KB segment of every target and draft row
+    rows = 256 * 8 + 256 * 7
+    segs = -(-129280 * 2 // 8192)
+    assert sd.sd_verify_workspace_bytes(256, 7, 129280, sd.SD_BF16) >= rows * segs * 16
+    assert sd.sd_verify_workspace_bytes(256, 7, 129280, sd.SD_F32) > \
+        sd.sd_verify_workspace_bytes(256, 7, 129280, sd.SD_BF16)
+    assert sd.sd_verify_workspace_bytes(0, 7, 1024, sd.SD_BF16) == 0
 
 
 FAKE = 1 << 20  # a non-null address that is never dereferenced on these paths
@@ -92,7 +96,7 @@ def test_plan_rejects_bad_arguments_on_host(lib):
 def test_verify_rejects_bad_arguments_on_host(lib):
     import speculative_decoding_verification_sd_gb300 as sd
     P = FAKE
-    nb = sd.sd_verify_workspace_bytes(4, 3)
+    nb = sd.sd_verify_workspace_bytes(4, 3, 1024, sd.SD_BF16)
 
     def call(**kw):
         a = dict(t=P, d=P, dt=1, V=1024, ids=P, u=P, temps=P, cu=P, bs=4, k_max=3, acc=P, out=P,
@@ -107,16 +111,22 @@ def test_verify_rejects_bad_arguments_on_host(lib):
     assert call(bs=5000) == sd.SD_ERR_UNSUPPORTED
     assert call(dt=9) == sd.SD_ERR_INVALID_ARG
     assert call(V=0) == sd.SD_ERR_INVALID_ARG
-    assert call(V=(1 << 22) + 1) == sd.SD_ERR_UNSUPPORTED
+    assert call(V=(1 << 20) + 1) == sd.SD_ERR_UNSUPPORTED
+    assert call(dt=0, V=(1 << 19) + 1) == sd.SD_ERR_UNSUPPORTED  # fp32 row over 2 MiB
+    assert b"SD_MAX" in lib.sd_last_error_string()
     assert call(t=None) == sd.SD_ERR_INVALID_ARG
     assert call(acc=None) == sd.SD_ERR_INVALID_ARG
     assert call(out=None) == sd.SD_ERR_INVALID_ARG
     assert call(ws=None) == sd.SD_ERR_INVALID_ARG
-    assert call(ws=P + 4) == sd.SD_ERR_INVALID_ARG  # workspace not 16-byte aligned
+    assert call(ws=P + 16) == sd.SD_ERR_INVALID_ARG  # workspace not 256-byte aligned
     assert call(nb=nb - 1) == sd.SD_ERR_SHAPE
-    bad_cfg = sd.sd_launch_cfg(-1, 0, 0, 0)
-    assert lib.sd_verify_ex(P, P, 1, 1024, P, P, P, P, 4, 3, P, P, None, P, P, nb,
-                            ctypes.byref(bad_cfg), 0) == sd.SD_ERR_INVALID_ARG
+    assert b"ws_bytes" in lib.sd_last_error_string()
+    for bad in (sd.sd_launch_cfg(-1, 0, 0, 0), sd.sd_launch_cfg(0, 0x40, 0, 0),
+                sd.sd_launch_cfg(0, 0, -1, 0), sd.sd_launch_cfg(0, 0, 0, 1)):
+        assert lib.sd_verify_ex(P, P, 1, 1024, P, P, P, P, 4, 3, P, P, None, P, P, nb,
+                                ctypes.byref(bad), 0) == sd.SD_ERR_INVALID_ARG
+    # a refused call leaves its own reason, a later one resets it
+    assert call(bs=0) == sd.SD_ERR_INVALID_ARG and b"bs=0" in lib.sd_last_error_string()
 
 
 def test_calibration_rejects_bad_arguments_on_host(lib):
@@ -159,13 +169,14 @@ def test_noalloc_rejects_on_host(lib):
     import speculative_decoding_verification_sd_gb300 as sd
     P = FAKE
 
-    def call(bs, k_max):
-        return lib.sd_verify_noalloc(P, P, 1, 1024, P, P, P, P, bs, k_max, P, P, None, P, 0)
+    def call(bs, k_max, V=1024):
+        return lib.sd_verify_noalloc(P, P, 1, V, P, P, P, P, bs, k_max, P, P, None, P, 0)
 
     assert call(0, 3) == sd.SD_ERR_INVALID_ARG
     assert call(4, 16) == sd.SD_ERR_UNSUPPORTED
-    assert sd.sd_verify_workspace_bytes(4096, 15) > sd.SD_NOALLOC_SCRATCH_BYTES
-    assert call(4096, 15) == sd.SD_ERR_UNSUPPORTED
+    assert b"no error" not in lib.sd_last_error_string()
+    assert sd.sd_verify_workspace_bytes(4096, 15, 129280, sd.SD_BF16) > sd.SD_NOALLOC_SCRATCH_BYTES
+    assert call(4096, 15, 129280) == sd.SD_ERR_UNSUPPORTED
     assert b"static scratch" in lib.sd_last_error_string()
 
 
@@ -173,7 +184,7 @@ def test_binding_refuses_host_tensors(lib):
     import torch
     import speculative_decoding_verification_sd_gb300 as sd
     with pytest.raises(ValueError):
-        sd.sd_verify_workspace_bytes(1, 1) and sd._ptr(torch.zeros(3))
+        sd.sd_verify_workspace_bytes(1, 1, 16, sd.SD_F32) and sd._ptr(torch.zeros(3))
 
 
 def test_product_path_does_not_import_the_oracle():

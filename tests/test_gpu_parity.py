@@ -1,8 +1,10 @@
 """GPU parity: the C-ABI path against the CPU oracle on identical seeded bytes.
 
-Small cases compare every output; full-size workloads compare the plan
-exactly, the sampled requests one by one against the oracle, and every
-request through invariants (and greedy requests against the target argmax).
+Every case compares every request's accepted length and tokens with the
+oracle (identical unless the oracle flags a near-boundary decision in that
+request), the probabilities p(x), q(x) within 1e-5 relative, the plans
+exactly, and the outputs' invariants -- at small sizes over every launch
+option, and at the full size of every workload.
 """
 import numpy as np
 import pytest
@@ -20,7 +22,7 @@ if not torch.cuda.is_available():
 import speculative_decoding_verification_sd_gb300 as sd  # noqa: E402
 
 
-def _step(w, seed, step=0, cfg=None, requests=None):
+def _step(w, seed, step=0, cfg=None, padded=False):
     pi = S.plan_inputs(w, seed, step)
     o_plan = oracle_plan(pi, w.k_max)
     g_plan = gpu_plan(pi, w.k_max)
@@ -28,12 +30,15 @@ def _step(w, seed, step=0, cfg=None, requests=None):
     compare_plan(g_plan, o_plan, f"{w.name} seed={seed} step={step}")
     cu = o_plan["cu_seqlens"]
     vi = S.verify_inputs(w, seed, step, cu, pi["draft_lens"])
-    g = gpu_verify(w, vi, cu, w.k_max, cfg=cfg)
+    g = gpu_verify(w, vi, cu, w.k_max, cfg=cfg, padded=padded)
     assert g["err"] == 0
-    o = oracle_verify(w, vi, cu, w.k_max, requests=requests)
-    compare_verify(g, o, cu, w.k_max, requests=requests, what=f"{w.name} seed={seed}")
+    o = oracle_verify(w, vi, cu, w.k_max)
+    compare_verify(g, o, cu, w.k_max, what=f"{w.name} seed={seed} step={step} cfg={cfg} padded={padded}")
     check_properties(g, cu, w.k_max, w.V, vi["draft_ids"])
     return pi, o_plan, vi, g, o
+
+
+EE = {"flags": sd.SD_VERIFY_EARLY_EXIT}
 
 
 @pytest.mark.parametrize("seed", range(6))
@@ -46,43 +51,49 @@ SMALL = S.WORKLOADS["adaptive_hc"].with_(bs=12, k_max=5, T=12, name="small")
 
 @pytest.mark.parametrize("dtype", [S.F32, S.BF16])
 @pytest.mark.parametrize("V", [20000, 1003])
-@pytest.mark.parametrize("threads", [256, 512])
 @pytest.mark.parametrize("blocks", [1, 3, 0])
-def test_small_every_launch_shape(dtype, V, threads, blocks):
-    """Many vectors per row with a ragged last round, the 16-byte vector path
+@pytest.mark.parametrize("flags,padded", [(0, False), (1, False), (0, True), (1, True)])
+def test_small_every_launch_shape(dtype, V, blocks, flags, padded):
+    """Many segments per row with a ragged last one, the bulk-copy path
     (V*elem % 16 == 0) and the element path (V = 1003); one CTA doing every
-    row and final draw, a few, or the full persistent grid."""
+    row and final draw, a few, or the full persistent grid; all rows or early
+    exit; compacted or uncompacted draft rows."""
     w = SMALL.with_(V=V, dtype=dtype)
-    _step(w, 100 + threads + blocks, cfg={"threads": threads, "blocks": blocks})
+    _step(w, 100 + 7 * blocks + flags, cfg={"blocks": blocks, "flags": flags}, padded=padded)
+
+
+def _ws_zero_offset(bs, k_max, V, elem):
+    """Offset of the workspace part that must be zero between calls (the
+    layout of include/sd.h's sd_verify workspace: segment records of target
+    and draft rows, pair statistics, draw sums, then the counters; every part
+    256-byte aligned)."""
+    al = lambda v: (v + 255) // 256 * 256
+    rb = V * elem
+    nseg, nsub = -(-rb // 8192), -(-rb // 4096)
+    rows_t, rows_d = bs * (k_max + 1), bs * k_max
+    seg_d = al(rows_t * nseg * 16)
+    ps = al(seg_d + rows_d * nseg * 16)
+    rs = al(ps + rows_t * 32)
+    return al(rs + 2 * bs * nsub * 8)
 
 
 def test_workspace_reuse_across_calls():
-    """The arrival and work counters are left at zero: repeated calls on one
-    workspace give identical results."""
+    """The counters are left at zero: repeated calls on one workspace give
+    identical results, whatever the launch options."""
     w = SMALL.with_(V=20000, dtype=S.BF16, bs=32, T=32)
     pi = S.plan_inputs(w, 9, 0)
     cu = oracle_plan(pi, w.k_max)["cu_seqlens"]
     vi = S.verify_inputs(w, 9, 0, cu, pi["draft_lens"])
     first = gpu_verify(w, vi, cu, w.k_max)
     ws = first["workspace"]
-    for rep in range(3):
+    for rep in range(4):
         again = gpu_verify(w, vi, cu, w.k_max, workspace=ws,
-                           cfg={"threads": 256 if rep % 2 else 512, "blocks": 2 + rep})
+                           cfg={"blocks": 2 + rep, "flags": rep % 2})
         assert np.array_equal(again["accepted_len"], first["accepted_len"])
         assert np.array_equal(again["out_tokens"], first["out_tokens"])
-    # the counters in the workspace are back at zero: residual chunk sums,
-    # per-request arrivals, the residual-draw list, slice counts and the
-    # work counters (layout st_t | st_d | st_c | rs | req_cnt | res_list |
-    # slice_cnt | ctrl, each part 16-byte aligned; 128 chunks per row)
-    rows_t, rows_d = w.bs * (w.k_max + 1), w.bs * w.k_max
-    ib = (4 * w.bs + 15) // 16 * 16
-    rs = 16 * rows_t + 16 * rows_d + 8 * 128 * rows_t
-    req_cnt = rs + 8 * 128 * w.bs
-    ctrl = req_cnt + 3 * ib
-    assert ctrl + 32 == sd.sd_verify_workspace_bytes(w.bs, w.k_max)
-    for off, size in ((rs, 8 * 128 * w.bs), (req_cnt, 4 * w.bs), (req_cnt + ib, 4 * w.bs),
-                      (req_cnt + 2 * ib, 4 * w.bs), (ctrl, 32)):
-        assert int(ws[off:off + size].count_nonzero()) == 0
+    zero = _ws_zero_offset(w.bs, w.k_max, w.V, w.elem)
+    assert zero < ws.numel() == sd.sd_verify_workspace_bytes(w.bs, w.k_max, w.V, sd.SD_BF16)
+    assert int(ws[zero:].count_nonzero()) == 0
 
 
 def test_repeated_full_size_calls_are_identical():
@@ -97,7 +108,7 @@ def test_repeated_full_size_calls_are_identical():
     assert first["err"] == 0
     ws = first["workspace"]
     for rep in range(40):
-        again = gpu_verify(w, vi, cu, w.k_max, workspace=ws)
+        again = gpu_verify(w, vi, cu, w.k_max, workspace=ws, cfg=EE if rep % 2 else None)
         assert again["err"] == 0
         assert np.array_equal(again["accepted_len"], first["accepted_len"]), rep
         assert np.array_equal(again["out_tokens"], first["out_tokens"]), rep
@@ -114,12 +125,11 @@ def test_varlen_draft_lengths_and_zero_drafts():
     _step(w0, 3)
 
 
-def _full(name, seed, n_sample, step=0):
+def _full(name, seed, step=0, cfg=None, padded=False):
+    """Every request of a full-size workload against the oracle; greedy
+    requests also against torch's argmax of the target rows."""
     w = S.WORKLOADS[name]
-    rng = np.random.default_rng(seed)
-    req = sorted(rng.choice(w.bs, size=min(n_sample, w.bs), replace=False).tolist())
-    pi, o_plan, vi, g, o = _step(w, seed, step, requests=req)
-    # Greedy requests emit the target argmax along the accepted path.
+    pi, o_plan, vi, g, o = _step(w, seed, step, cfg=cfg, padded=padded)
     cu = o_plan["cu_seqlens"]
     amax = g["target_dev"][: int(cu[-1])]
     if w.dtype == S.BF16:
@@ -132,24 +142,33 @@ def _full(name, seed, n_sample, step=0):
 
 
 def test_full_adaptive_hc():
-    _full("adaptive_hc", 2024, 24)
+    g = _full("adaptive_hc", 2024)
+    ge = _full("adaptive_hc", 2024, cfg=EE)
+    assert np.array_equal(g["accepted_len"], ge["accepted_len"])
+    assert np.array_equal(g["out_tokens"], ge["out_tokens"])
+
+
+def test_full_adaptive_hc_uncompacted_drafts():
+    _full("adaptive_hc", 77, padded=True)
+    _full("adaptive_hc", 78, cfg=EE, padded=True)
 
 
 def test_full_dense_fixed_k():
-    _full("dense_fixed_k", 5, 12)
+    _full("dense_fixed_k", 5)
+    _full("dense_fixed_k", 6, cfg=EE)
 
 
 def test_full_varlen_mixed_steps():
     w = S.WORKLOADS["varlen_mixed"]
     for step in range(w.steps):  # budget from the previous step's confidences
-        pi = S.plan_inputs(w, 77, step)
-        compare_plan(gpu_plan(pi, w.k_max), oracle_plan(pi, w.k_max), f"varlen step {step}")
-    for step in (0, 1, w.steps - 1):
-        _full("varlen_mixed", 77, 8, step)
+        _full("varlen_mixed", 77, step, cfg=EE if step % 2 else None)
 
 
 def test_full_stress():
-    _full("stress", 31337, 16)
+    g = _full("stress", 31337)
+    ge = _full("stress", 31337, cfg=EE)
+    assert np.array_equal(g["accepted_len"], ge["accepted_len"])
+    assert np.array_equal(g["out_tokens"], ge["out_tokens"])
 
 
 # ---------------------------------------------------------------------------
@@ -298,7 +317,7 @@ def test_uniform_k_at_the_slot_limit(bs, k_max):
 
 
 def test_uniform_k_full_size():
-    _full("uniform_hc", 2024, 24)
+    _full("uniform_hc", 2024)
     w = S.WORKLOADS["stress"].with_(mode=S.MODE_UNIFORM_K)
     pi = S.plan_inputs(w, 31337, 0)
     g = gpu_plan(pi, w.k_max)
@@ -328,14 +347,34 @@ def test_uniform_k_device_checks_and_budget_set_ignored():
     assert g["B"] == 0 and not g["slot_mask"].any()
 
 
+def test_wait_that_runs_out_sets_the_flag_and_leaves_wellformed_outputs():
+    """A device-side wait made to run out (the test hook streams no row, so
+    the end-of-call wait for the requests' outputs gives up after 20 ms): the
+    kernel returns, raises SD_DEV_ERR_TIMEOUT, writes well-formed
+    outputs, and leaves the workspace ready -- the next call on it is exact."""
+    w = SMALL.with_(V=8192, dtype=S.BF16, bs=16, T=16)
+    pi = S.plan_inputs(w, 21, 0)
+    cu = oracle_plan(pi, w.k_max)["cu_seqlens"]
+    vi = S.verify_inputs(w, 21, 0, cu, pi["draft_lens"])
+    g = gpu_verify(w, vi, cu, w.k_max, cfg={"flags": sd.SD_VERIFY_TEST_STALL, "wait_limit_us": 20000})
+    assert g["err"] & sd.SD_DEV_ERR_TIMEOUT
+    assert np.all(g["accepted_len"] == 0)
+    assert np.all(g["out_tokens"][:, 0] == 0) and np.all(g["out_tokens"][:, 1:] == -1)
+    again = gpu_verify(w, vi, cu, w.k_max, workspace=g["workspace"])
+    assert again["err"] == 0
+    o = oracle_verify(w, vi, cu, w.k_max)
+    compare_verify(again, o, cu, w.k_max, what="after a time-out")
+
+
 # Mismatches allowed at near-boundary decisions, as a fraction of all
-# decisions.  The pages fix fp32 for the sampling arithmetic; at V = 129280 the
-# mean gap between consecutive CDF values is S / V = 7.7e-6 S, inside the
-# 1e-5 S band, so nearly every inverse-CDF pick is a near decision, and an fp32
-# weight (relative error ~1e-7) against the fp64 oracle moves the pick to a
-# neighbour with probability of order V * 1e-8 per pick.  The bound is five
-# times that estimate; the measured rate is written by TALLY.dump().
-NEAR_MISMATCH_BOUND = 5e-3
+# decisions: the 0.01 % the target sets.  At V = 129280 nearly every
+# inverse-CDF pick is a near decision (the mean gap between consecutive CDF
+# values, S / V, is inside the 1e-5 S band).  The sampler forms the weights
+# that carry the mass (above 2^-12 of the row maximum) to about 1e-10 and
+# sums in exact fixed point, which an fp64 emulation puts at 3e-5 to 7e-5
+# mismatches per draw at V = 256000.  The measured rate is written by
+# TALLY.dump(); tests/test_gpu_parity_rate.py measures it over 1e5 decisions.
+NEAR_MISMATCH_BOUND = 1e-4
 
 
 def test_zz_near_boundary_budget():

@@ -64,7 +64,7 @@ def _both(w, t, dt, ws):
 def test_noalloc_matches_workspace_entry_point_two_calls(name, bs, k_max, V, dtype):
     w = S.WORKLOADS["adaptive_hc"].with_(bs=bs, k_max=k_max, T=bs, V=V, dtype=dtype, name=name)
     t, dt = _inputs(w, 5)
-    ws = sd.verify_workspace(w.bs, w.k_max)
+    ws = sd.verify_workspace(w.bs, w.k_max, w.V, dt)
     for _ in range(2):  # two calls in a row on both entry points
         _both(w, t, dt, ws)
 
@@ -75,15 +75,17 @@ def test_noalloc_after_a_larger_batch():
     small = S.WORKLOADS["adaptive_hc"].with_(bs=8, k_max=3, T=8, V=8192, name="small")
     for w in (big, small, big):
         t, dt = _inputs(w, 11)
-        _both(w, t, dt, sd.verify_workspace(w.bs, w.k_max))
+        _both(w, t, dt, sd.verify_workspace(w.bs, w.k_max, w.V, dt))
 
 
 def test_noalloc_rejects_a_batch_beyond_the_scratch():
-    bs, k_max = 4096, 15
-    assert sd.sd_verify_workspace_bytes(bs, k_max) > sd.SD_NOALLOC_SCRATCH_BYTES
+    """Refused on the host before any launch (the tensors below are too small
+    for the sizes named: no kernel may ever run on them)."""
+    bs, k_max, V = 4096, 15, 129280
+    assert sd.sd_verify_workspace_bytes(bs, k_max, V, sd.SD_BF16) > sd.SD_NOALLOC_SCRATCH_BYTES
     dev = torch.device("cuda:0")
     x = torch.zeros(16, dtype=torch.int32, device=dev)
     with pytest.raises(sd.SdError) as ei:
-        sd.sd_verify_noalloc(x, x, sd.SD_BF16, 1024, x, x, x, x, bs, k_max, x, x, None, x)
+        sd.sd_verify_noalloc(x, x, sd.SD_BF16, V, x, x, x, x, bs, k_max, x, x, None, x)
     assert ei.value.status == sd.SD_ERR_UNSUPPORTED
     assert "static scratch" in str(ei.value)
