@@ -51,9 +51,9 @@ def parse():
     ap.add_argument("--workload", default="adaptive_hc", choices=sorted(S.WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--seed", type=int, default=2026)
-    ap.add_argument("--threads", type=int, default=0)
-    ap.add_argument("--blocks", type=int, default=0)
-    ap.add_argument("--blocks-per-sm", type=int, default=0)
+    ap.add_argument("--blocks", type=int, default=0, help="sampler CTAs (0 = one per SM)")
+    ap.add_argument("--early-exit", action="store_true",
+                    help="skip rows of slots after a request's first rejection")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
@@ -98,7 +98,7 @@ def hbm_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-KERNEL_SOURCES = ("verify_kernel.cu", "sd_device.cuh", "sd_internal.h")
+KERNEL_SOURCES = ("sampler.cu", "sd_device.cuh", "sd_internal.h")
 
 
 def profiled_traffic(workload):
@@ -404,9 +404,9 @@ def run_ours(args, w, rank, world, local):
     d_t = torch.from_numpy(temps).to(dev)
     d_acc = torch.zeros(bs, dtype=torch.int32, device=dev)
     d_out = torch.zeros((bs, k + 1), dtype=torch.int32, device=dev)
-    ws_bytes = sd.sd_verify_workspace_bytes(bs, k)
-    d_ws = sd.verify_workspace(bs, k, dev)
-    cfg = {"threads": args.threads, "blocks": args.blocks, "blocks_per_sm": args.blocks_per_sm}
+    ws_bytes = sd.sd_verify_workspace_bytes(bs, k, w.V, dtype)
+    d_ws = sd.verify_workspace(bs, k, w.V, dtype, dev)
+    cfg = {"blocks": args.blocks, "flags": sd.SD_VERIFY_EARLY_EXIT if args.early_exit else 0}
 
     def step(s, ev=None):
         tgt, dft = sets[s & 1]
@@ -538,8 +538,7 @@ def run_ours(args, w, rank, world, local):
             "mean_acceptance_length": 1.0 + accepted / bs,
             "per_position_cumulative_acceptance": [round(x, 4) for x in pos],
             "device_err_flag": err, "input_generation_s": gen_s,
-            "launch": sd.sd_verify_launch_info(w.V, dtype, bs, args.threads, args.blocks,
-                                               args.blocks_per_sm),
+            "launch": sd.sd_verify_launch_info(w.V, dtype, bs, args.blocks, cfg["flags"]),
         },
     }
     if rank == 0:
@@ -588,7 +587,7 @@ def run_e2e(args, w, sd, dev, stream, pi, vi, cu, ws_bytes, cfg, rows_cap):
     d_err = torch.zeros(1, dtype=torch.int32, device=dev)
     d_acc = torch.zeros(bs, dtype=torch.int32, device=dev)
     d_out = torch.zeros((bs, k + 1), dtype=torch.int32, device=dev)
-    d_ws = sd.verify_workspace(bs, k, dev)
+    d_ws = sd.verify_workspace(bs, k, w.V, dtype, dev)
     h2d = 0
     for h in (h_conf, h_lens, h_cost, h_tgt, h_dft, h_ids, h_u, h_t):
         if h is not None:

@@ -175,7 +175,7 @@ sd_status sd_plan(const float* conf_logits, const float* budget_conf,
  *   w = max(p_{a_i} - q_{a_i}, 0) after a rejection, or w = p_{n_i} (bonus)
  *   when every slot was accepted; if that residual has no positive mass,
  *   w = p_{a_i}.  The weights are summed in exact 64-bit fixed point (2^-56);
- *   an element heavier than 2^-12 of its row's largest weight is formed to
+ *   an element heavier than 2^-10 of its row's largest weight is formed to
  *   about 1e-10 relative, the others in fp32.
  *   out_tokens[i] = (x_0 .. x_{a_i-1}, y_i, -1 ...), accepted_len[i] = a_i.
  *
@@ -206,9 +206,9 @@ sd_status sd_plan(const float* conf_logits, const float* budget_conf,
  *                  out_tokens = -1.  On SD_DEV_ERR_TIMEOUT every request's
  *                  outputs are accepted_len = 0, out_tokens = (0, -1, ...).
  *   workspace      device scratch of sd_verify_workspace_bytes(bs, k_max, V, dt)
- *                  bytes, 256-byte aligned: per-segment and per-row statistics,
- *                  per-sub-chunk sums of the final draws, per-request and
- *                  per-slot counters.  It must be zero-filled once before its
+ *                  bytes, 256-byte aligned: per-row statistics, per-chunk
+ *                  sums of the final draws, per-request and per-slot
+ *                  counters.  It must be zero-filled once before its
  *                  first use (e.g. cudaMemsetAsync); every call leaves the
  *                  counters at zero again.  One call at a time per workspace.
  * Layout: rows are staged with 16-byte bulk copies when V*elem is a multiple

@@ -9,32 +9,31 @@
 //            accepted prefix draw a bonus token from p of the next row.
 //   tau = 0: accept iff x_j == argmax p_j; the correction/bonus is the argmax.
 //
-// Design (GB300).  Every logit row is cut into 8 KB segments.  The work list
-// is ordered by slot position ("waves"): wave j holds, for every request that
-// verifies slot j, its target row t_j and (tau > 0) its draft row d_j, then
-// the rows t_j that are a request's bonus row, then greedy requests' rows.
-// One persistent CTA per SM: a producer warp claims blocks of segments from a
-// global counter and streams each segment with one bulk copy into a ring of
-// shared-memory buffers; eight consumer warps take the buffers in order and
-// reduce each segment to partial softmax statistics (or an argmax).  The
-// consumer that counts a pair's last segment combines the pair's statistics
-// and takes slot j's accept decision at once; the decision that settles a
-// request (its first rejection with every earlier slot accepted, or a fully
-// accepted prefix and its bonus row) lists the request's final draw.  The
-// draw's row(s) were streamed moments before, so its sub-chunks are read
-// again from L2, not HBM; their inverse-CDF weights are summed in exact
-// 64-bit fixed point, and the consumer that counts the last sub-chunk finds
-// the crossing sub-chunk and walks it.  With SD_VERIFY_EARLY_EXIT the
-// producer skips rows of slots after a request's known first rejection.
+// Design (GB300).  One persistent CTA per SM: a scheduler warp claims units
+// of work into a small queue in shared memory, and twelve streaming warps
+// take every unit together.  A unit is one logit row (claimed in slot order,
+// "waves": slot j's rows of every request before slot j + 1's) or one final
+// draw.  Streaming warp w copies its own slice of the unit's row(s) with
+// bulk copies into two buffers of its own (the next chunk lands while the
+// current one is reduced, across unit boundaries) and reduces each chunk to
+// softmax statistics or an argmax.  The last warp to finish a row combines
+// the twelve partials and counts the row into its (request, slot) pair; the
+// row that completes a pair takes the slot's accept decision, and the
+// decision that settles a request lists the request's final draw.  A draw is
+// a unit like a row: every warp sums its slice's inverse-CDF weights in
+// exact 64-bit fixed point, and the last one finds the crossing chunk and
+// walks it.  With SD_VERIFY_EARLY_EXIT the scheduler drops rows of slots
+// after a request's settled first rejection before they are streamed.
 //
 // Precision.  Row statistics use the hardware base-2 exponent on an argument
 // d * s2 with d = l - m exact and s2 = log2(e)/tau carried in two floats; the
-// per-segment sums are compensated and combined in fp64.  A final draw's
-// weights are fp32 except where an element weighs more than 2^-12 of its
-// row's maximum: there the weight is formed in double-float from a 16-entry
-// table of 2^(j/16) and a short series (Tang's table-driven method), so the
-// elements that carry the distribution's mass match the fp64 definition to
-// about 1e-10.
+// per-chunk sums are compensated and combined in double-float.  A final
+// draw's weights are fp32 except where an element weighs more than 2^-10 of
+// its row's maximum: there the weight is formed in double-float from a
+// 16-entry table of 2^(j/16) and a short series (Tang's table-driven
+// method), so the elements that carry the distribution's mass match the
+// fp64 definition to about 1e-10.  No fp64 arithmetic is used: this GPU
+// runs it, and 64-bit conversions, at 1/64 of the fp32 rate.
 #include <atomic>
 #include <climits>
 #include <cmath>
@@ -47,34 +46,25 @@ namespace sdk {
 
 namespace {
 
-constexpr int kNC = 8;                    // consumer warps per CTA
-constexpr int kThreads = (kNC + 1) * 32;  // + the producer warp
-constexpr int kMaxBufs = 24;              // ring buffers per CTA (at most)
-constexpr int kRowBlock = 4;              // segments per row claim
-constexpr int kSubBlock = 4;              // sub-chunks per draw claim
+constexpr int kNW = kSamplerWarps;         // streaming warps per CTA
+constexpr int kThreads = (kNW + 1) * 32;   // + the scheduler warp
+constexpr int kQ = 4;                      // positions of the per-CTA unit queue
+constexpr int kChunk = kSegBytes;          // bytes of a row chunk (one bulk copy)
+constexpr int kHalf = kSubBytes;           // bytes per row of a draw chunk
 constexpr uint64_t kDrainNs = 2000000000ull;  // bound of the exit drain of in-flight copies (2 s)
-constexpr uint32_t kPollHintNs = 10000;       // suspend hint of one poll of an mbarrier (10 us)
-constexpr float kBigT = -12.0f;           // weights above 2^-12 of the row maximum: precise
-constexpr float kTwo56 = 72057594037927936.0f;
+constexpr float kBigT = -10.0f;           // weights above 2^-10 of the row maximum: precise
+constexpr int kHeavyList = 128;           // per-warp list of heavy elements handled in one pass
 constexpr float kTwo64 = 18446744073709551616.0f;
 // log2(e) and ln(2), each split into two floats (hi + lo).
 constexpr float kLog2eHi = 1.44269502162933349609375f;
 constexpr float kLog2eLo = 1.925963033500011079e-08f;
 constexpr float kLn2Hi = 0.693147182464599609375f;
 constexpr float kLn2Lo = -1.904654299957768e-09f;
-constexpr double kLog2eD = 1.4426950408889634074;
 
-// Item kinds handed from the producer to the consumers.
-enum { kEnd = 0, kRow = 1, kSkip = 2, kSub = 3 };
+// Units of work handed from the scheduler warp to the streaming warps.
+enum { kUEnd = 0, kURow = 1, kUDraw = 2 };
 // Kinds of a final draw.
 enum { kDrawResid = 0, kDrawP = 1 };
-
-struct Desc {
-  int kind;
-  int a;  // kRow / kSkip: i | j << 12 | draft << 16;  kSub: draw index e
-  int b;  // kRow: segment;  kSkip: segments skipped;  kSub: sub-chunk
-  int c;  // kSub: the draw's list entry (1 + (i << 6 | a << 2 | kind))
-};
 
 // ---------------------------------------------------------------------------
 // Memory-order and arithmetic helpers.
@@ -109,20 +99,19 @@ __device__ __forceinline__ uint64_t now_ns() {
   asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
   return t;
 }
-// One poll of an mbarrier phase, suspending the thread at most ~hint ns.
+// One poll of an mbarrier phase (the hardware may hold the thread briefly
+// while the phase is incomplete; no suspend hint, which measurably left
+// warps asleep well after their phase had completed).
 __device__ __forceinline__ bool mbar_poll(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(ok)
-      : "r"(smem_addr(bar)), "r"(parity), "r"(kPollHintNs)
+      : "r"(smem_addr(bar)), "r"(parity)
       : "memory");
   return ok != 0;
-}
-__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
 }
 __device__ __forceinline__ float fmax_nan(float a, float b) {
   float d;
@@ -142,11 +131,6 @@ __device__ __forceinline__ unsigned long long warp_sum_u64(unsigned long long v)
   for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(kFull, v, o);
   return v;
 }
-__device__ __forceinline__ double warp_sum_f64(double v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(kFull, v, o);
-  return v;
-}
 __device__ __forceinline__ float warp_max_nan(float v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v = fmax_nan(v, __shfl_xor_sync(kFull, v, o));
@@ -162,6 +146,34 @@ __device__ __forceinline__ void two_sum(float a, float b, float& s, float& e) {
 __device__ __forceinline__ void fast_two_sum(float a, float b, float& s, float& e) {
   s = __fadd_rn(a, b);
   e = __fsub_rn(b, __fsub_rn(s, a));
+}
+
+// Double-float (hi + lo) sum and product, ~2^-44 relative; fast_two_sum
+// needs |hi| of the result to dominate, which holds for these non-negative
+// sums and products.
+__device__ __forceinline__ void ff_add(float ah, float al, float bh, float bl, float& sh, float& sl) {
+  float s, e;
+  two_sum(ah, bh, s, e);
+  e = __fadd_rn(e, __fadd_rn(al, bl));
+  fast_two_sum(s, e, sh, sl);
+}
+__device__ __forceinline__ void ff_mul(float ah, float al, float bh, float bl, float& ph, float& pl) {
+  const float p = __fmul_rn(ah, bh);
+  const float c = __fmaf_rn(ah, bl, __fmaf_rn(al, bh, __fmaf_rn(ah, bh, -p)));
+  fast_two_sum(p, c, ph, pl);
+}
+// 1 / (zh + zl) as a double-float: a rounded reciprocal and one correction.
+__device__ __forceinline__ void ff_recip(float zh, float zl, float& ih, float& il) {
+  ih = __frcp_rn(zh);
+  const float e = __fmaf_rn(-zl, ih, __fmaf_rn(-zh, ih, 1.0f));
+  il = __fmul_rn(e, ih);
+}
+__device__ __forceinline__ void warp_sum_ff(float& h, float& l) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float oh = __shfl_xor_sync(kFull, h, o), ol = __shfl_xor_sync(kFull, l, o);
+    ff_add(h, l, oh, ol, h, l);
+  }
 }
 
 // s2 = log2(e) / tau as s2h + s2l with s2h rounded down, so s2l > 0 and an
@@ -285,7 +297,7 @@ __device__ __forceinline__ void load_unit(const void* src, int q, int n, bool l2
 // Final-draw weights.  A draw from p weighs element k with p_k; a residual
 // draw with max(p_k - q_k, 0); in 2^56 fixed point.  A unit's value is the
 // fixed-point value of the fp32 sum (in element order) of its elements that
-// weigh less than 2^-12 of their row's maximum, plus the double-float value
+// weigh less than 2^-10 of their row's maximum, plus the double-float value
 // of each heavier element.  The sub-chunk sums and the walk of the crossing
 // sub-chunk use these same functions, so the walk retraces the sums exactly.
 struct DrawCtx {
@@ -293,6 +305,18 @@ struct DrawCtx {
   float izth, iztl, izdh, izdl;  // 1 / Z as (hi, lo)
   bool resid;
 };
+
+// x * 2^56 truncated to an integer (0 <= x < 256) from two 32-bit
+// conversions: this GPU converts to 64-bit integers at 1/8 of the 32-bit
+// rate.  y = x * 2^24 and its fraction are exact, so for x >= 2^-32 the
+// result is x * 2^56 exactly.
+__device__ __forceinline__ unsigned long long fixed56(float x) {
+  const float y = __fmul_rn(x, 16777216.0f);
+  const float yt = truncf(y);
+  const uint32_t hi = __float2uint_rz(yt);
+  const uint32_t lo = __float2uint_rz(__fmul_rn(__fsub_rn(y, yt), 4294967296.0f));
+  return (static_cast<unsigned long long>(hi) << 32) | lo;
+}
 
 // fp32 weight of one element; *big when it must be formed precisely.
 __device__ __forceinline__ float elem_fast(const DrawCtx& c, float lt, float ld, bool& big) {
@@ -336,23 +360,58 @@ __device__ __forceinline__ unsigned long long elem_precise(const DrawCtx& c, flo
     fast_two_sum(rh, rl, ph, pl);  // |rl| small against rh unless both are tiny
   }
   if (!(ph > 0.0f)) return 0ull;
-  const long long v = __float2ll_rn(__fmul_rn(ph, kTwo56)) + __float2ll_rn(__fmul_rn(pl, kTwo56));
+  // The table-driven exponent leaves its series' tail in the low word, up
+  // to ~2^-12 of the high one: renormalise so |pl| <= ulp(ph) / 2, then ph
+  // at 2^-56 and the small correction pl at 2^-48 (|pl * 2^48| <= 2^24).
+  fast_two_sum(ph, pl, ph, pl);
+  const long long v = static_cast<long long>(fixed56(ph)) +
+                      static_cast<long long>(__float2int_rn(__fmul_rn(pl, 281474976710656.0f))) * 256ll;
   return v > 0 ? static_cast<unsigned long long>(v) : 0ull;
 }
 
+// Two elements at once in packed fp32x2 arithmetic; each half is rounded
+// exactly as elem_fast rounds its element (the packed operations are the
+// same IEEE operations per half).
+__device__ __forceinline__ float2 pair_fast(const DrawCtx& c, float2 lt, float2 ld, bool& b0, bool& b1) {
+  const float2 dt = __fadd2_rn(lt, make_float2(-c.Mt, -c.Mt));
+  const float2 tt = __ffma2_rn(dt, make_float2(c.s2h, c.s2h), __fmul2_rn(dt, make_float2(c.s2l, c.s2l)));
+  const float2 wt = make_float2(exp2_ftz(tt.x), exp2_ftz(tt.y));
+  b0 = tt.x > kBigT;
+  b1 = tt.y > kBigT;
+  if (!c.resid)
+    return __ffma2_rn(wt, make_float2(c.izth, c.izth), __fmul2_rn(wt, make_float2(c.iztl, c.iztl)));
+  const float2 dd = __fadd2_rn(ld, make_float2(-c.Md, -c.Md));
+  const float2 td = __ffma2_rn(dd, make_float2(c.s2h, c.s2h), __fmul2_rn(dd, make_float2(c.s2l, c.s2l)));
+  const float2 wd = make_float2(exp2_ftz(td.x), exp2_ftz(td.y));
+  b0 = b0 || td.x > kBigT;
+  b1 = b1 || td.y > kBigT;
+  const float2 qd = __ffma2_rn(wd, make_float2(c.izdh, c.izdh), __fmul2_rn(wd, make_float2(c.izdl, c.izdl)));
+  const float2 r = __ffma2_rn(wt, make_float2(c.izth, c.izth),
+                              __ffma2_rn(wt, make_float2(c.iztl, c.iztl), make_float2(-qd.x, -qd.y)));
+  return make_float2(fmaxf(r.x, 0.0f), fmaxf(r.y, 0.0f));
+}
+
+// A unit's fast value: the fixed-point value of the fp32 sum (a balanced
+// tree, in element order) of its elements that weigh less than 2^-10 of
+// their row's maximum; *bigm marks the others.
 template <int VE>
 __device__ __forceinline__ unsigned long long unit_fast(const DrawCtx& c, const float (&ft)[VE],
                                                         const float (&fd)[VE], uint32_t& bigm) {
-  float s = 0.0f;
+  float r[VE];
   bigm = 0;
 #pragma unroll
-  for (int e = 0; e < VE; ++e) {
-    bool big;
-    const float r = elem_fast(c, ft[e], fd[e], big);
-    if (big) bigm |= 1u << e;
-    else s = __fadd_rn(s, r);
+  for (int e = 0; e < VE; e += 2) {
+    bool b0, b1;
+    const float2 pr = pair_fast(c, make_float2(ft[e], ft[e + 1]), make_float2(fd[e], fd[e + 1]), b0, b1);
+    r[e] = b0 ? 0.0f : pr.x;
+    r[e + 1] = b1 ? 0.0f : pr.y;
+    bigm |= (b0 ? 1u << e : 0u) | (b1 ? 1u << (e + 1) : 0u);
   }
-  return __float2ull_rn(__fmul_rn(s, kTwo56));
+#pragma unroll
+  for (int w = 1; w < VE; w *= 2)
+#pragma unroll
+    for (int e = 0; e < VE; e += 2 * w) r[e] = __fadd_rn(r[e], r[e + w]);
+  return fixed56(r[0]);
 }
 
 template <int VE>
@@ -374,7 +433,7 @@ struct Cta {
   const int* WS;     // [nw+1] first unit of wave j
   const int* Pj;     // [nw] sampling requests with n > j
   const int* Ej;     // [nw] sampling requests with n == j
-  int nsamp, nw, U, BPU, BPD;
+  int nsamp, nw, U;
   const float2* tab;  // shared-memory copy of the exponent table
 };
 
@@ -438,31 +497,78 @@ __device__ __forceinline__ int settled(int s, int n) {
 // ---------------------------------------------------------------------------
 // The kernel.
 
+__device__ __forceinline__ uint64_t policy_evict_normal() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+
+// One unit of the per-CTA queue.
+struct Unit {
+  int kind;
+  int a;  // row: i | j << 12 | draft << 16;  draw: the draw's index e
+  int b;  // row: the row's index;  draw: its list entry 1 + (i << 6 | a << 2 | kind)
+  int c;  // draw: which of its kDrawParts parts
+};
+
+// What a streaming warp needs of a unit.
+struct UInfo {
+  int kind;
+  int i, j, n;
+  bool isd, greedy;
+  float tau;
+  const char* src_t;  // row unit: the row;  draw: the target row t_a
+  const char* src_d;  // residual draw: the draft row d_a (else null)
+  int e, a, dkind;    // draw unit
+  int part;           // draw unit: which part of the draw's chunks
+  int x;              // row unit of a slot j < n: the slot's draft token (else -1)
+};
+
 template <typename T, bool VEC>
 struct Sampler {
   using E = ET<T>;
   static constexpr int VE = E::VE;
-  static constexpr int kSegE = kSegBytes / static_cast<int>(sizeof(T));  // elements per segment
-  static constexpr int kSubE = kSubBytes / static_cast<int>(sizeof(T));  // elements per sub-chunk
-  static constexpr int kUPL = kSubE / VE / 32;                           // sub-chunk units per lane
+  static constexpr int kUPL = kHalf / static_cast<int>(sizeof(T)) / VE / 32;  // draw-chunk units per lane
 
   const SamplerParams& p;
-  const Cta& C;
-  unsigned char* ring;
-  uint64_t* full;
-  uint64_t* empty;
-  Desc* desc;
-  int* ticket;
-  volatile int* seen;  // [nbuf] phases of each buffer whose wait has passed
+  Cta C;
+  // per-CTA queue in shared memory
+  Unit* q_ent;         // [kQ]
+  volatile int* q_seq; // [kQ] position published in each slot
+  volatile int* q_fin; // [kQ] position whose unit is complete in each slot
+  int* q_cnt;          // [kQ] streaming warps done with the slot's position (grows by kNW a use)
+  uint4* q_rec;        // [kQ][kNW] per-warp partial statistics of a row unit
+  unsigned char* bufs; // [kNW][2][kChunk]
+  unsigned short* heavy;  // [kNW][kHeavyList] heavy elements of a draw chunk
+  uint64_t* full;      // [kNW][2]
   volatile int* stop;
-  int lane;
+  int lane, warp;
+  int R;               // row bytes
 
-  __device__ size_t row_bytes() const { return static_cast<size_t>(p.V) * sizeof(T); }
   __device__ const char* trow_ptr(long long r) const {
-    return static_cast<const char*>(p.target) + static_cast<size_t>(r) * row_bytes();
+    return static_cast<const char*>(p.target) + static_cast<size_t>(r) * static_cast<size_t>(R);
   }
   __device__ const char* drow_ptr(long long r) const {
-    return static_cast<const char*>(p.draft) + static_cast<size_t>(r) * row_bytes();
+    return static_cast<const char*>(p.draft) + static_cast<size_t>(r) * static_cast<size_t>(R);
+  }
+  __device__ int sl_begin(int w) const { return min(w * p.slice, R); }
+  __device__ int sl_end(int w) const { return min((w + 1) * p.slice, R); }
+  __device__ int nchunks(int kind, int w) const {
+    const int len = sl_end(w) - sl_begin(w);
+    const int cb = kind == kURow ? kChunk : kHalf;
+    return len > 0 ? (len + cb - 1) / cb : 0;
+  }
+  // Warp w's chunks of unit f: [cbase, cbase + ucount) of its slice (a draw
+  // part takes its share of every warp's draw chunks).
+  __device__ int cbase(const UInfo& f, int w) const {
+    if (f.kind == kURow) return 0;
+    const int per = (p.ncd + kDrawParts - 1) / kDrawParts;
+    return min(f.part * per, nchunks(kUDraw, w));
+  }
+  __device__ int ucount(const UInfo& f, int w) const {
+    if (f.kind == kURow) return nchunks(kURow, w);
+    const int per = (p.ncd + kDrawParts - 1) / kDrawParts;
+    return min((f.part + 1) * per, nchunks(kUDraw, w)) - cbase(f, w);
   }
 
   __device__ void halt() const {
@@ -473,41 +579,129 @@ struct Sampler {
     }
   }
 
-  // ---- consumer: one segment of a row --------------------------------------
-  // Writes the segment's record; returns nothing (the caller counts it).
-  __device__ void segment(const void* src, int n_el, bool greedy, float tau, int xo,
-                          SegRec* rec, int e0) const {
+  __device__ UInfo info(const Unit& u) const {
+    UInfo f;
+    f.kind = u.kind;
+    f.src_d = nullptr;
+    f.x = -1;
+    f.e = f.a = f.dkind = f.part = 0;
+    f.isd = false;
+    if (u.kind == kURow) {
+      f.i = u.a & 0xFFF;
+      f.j = (u.a >> 12) & 0xF;
+      f.isd = ((u.a >> 16) & 1) != 0;
+      f.n = n_of(p, f.i);
+      f.tau = eff_tau(p, f.i);
+      f.greedy = !(f.tau > 0.0f);
+      f.src_t = f.isd ? drow_ptr(u.b) : trow_ptr(u.b);
+      if (f.j < f.n) f.x = __ldg(p.draft_ids + drow_of(p, f.i, f.j));
+    } else {
+      f.e = u.a;
+      f.part = u.c;
+      const int code = u.b - 1;
+      f.i = (code >> 6) & 0xFFF;
+      f.a = (code >> 2) & 0xF;
+      f.dkind = code & 3;
+      f.j = f.a;
+      f.n = n_of(p, f.i);
+      f.tau = eff_tau(p, f.i);
+      f.greedy = false;
+      f.src_t = trow_ptr(trow_of(p, f.i, f.a));
+      if (f.dkind == kDrawResid) f.src_d = drow_ptr(drow_of(p, f.i, f.a));
+    }
+    return f;
+  }
+
+  // ---- per-warp bulk copies ----------------------------------------------
+  __device__ unsigned char* buf_of(int g) const {
+    return bufs + (static_cast<size_t>(warp) * 2 + (g & 1)) * kChunk;
+  }
+  __device__ uint64_t* bar_of(int g) const { return full + warp * 2 + (g & 1); }
+
+  // Lane 0: chunk c of unit f into buffer g & 1 (vector path only).
+  __device__ void issue(const UInfo& f, int c, int g, uint64_t pol_first, uint64_t pol_normal) const {
+    const int cb = f.kind == kURow ? kChunk : kHalf;
+    const int off = sl_begin(warp) + (cbase(f, warp) + c) * cb;
+    const uint32_t by = static_cast<uint32_t>(min(cb, sl_end(warp) - off));
+    unsigned char* dst = buf_of(g);
+    uint64_t* bar = bar_of(g);
+    if (f.kind == kURow) {
+      mbar_arrive_expect_tx(bar, by);
+      bulk_load(dst, f.src_t + off, by, bar, f.greedy ? pol_first : pol_normal);
+    } else {
+      mbar_arrive_expect_tx(bar, f.src_d ? 2 * by : by);
+      bulk_load(dst, f.src_t + off, by, bar, pol_first);
+      if (f.src_d) bulk_load(dst + kHalf, f.src_d + off, by, bar, pol_first);
+    }
+  }
+
+  // Lane 0: waits for chunk g's copy (bounded).
+  __device__ bool wait_chunk(int g) const {
+    uint64_t* bar = bar_of(g);
+    const uint32_t par = static_cast<uint32_t>(g >> 1) & 1u;
+    if (mbar_poll(bar, par)) return true;
+    const uint64_t end = now_ns() + p.wait_ns;
+    for (;;) {
+      if (mbar_poll(bar, par)) return true;
+      if (*stop || now_ns() > end) return false;
+    }
+  }
+
+  // ---- row chunks -----------------------------------------------------------
+  // Per-warp partial of a row unit: sampling rows keep (m, z = zh + zl) with
+  // z = sum of 2^((l - m) s2) over the chunks so far; greedy rows keep the
+  // key (ordered value << 32 | ~index) of the best element and a bad flag.
+  struct Part {
+    float m, zh, zl, lx;
+    unsigned long long key;
+    int bad;
+  };
+
+  // Rescales the double-float z = (zh, zl), taken relative to m_from, to
+  // m_to >= m_from: z * 2^((m_from - m_to) s2).
+  __device__ void rescale(float& zh, float& zl, float m_from, float m_to, float s2h, float s2l) const {
+    float dh, dl;
+    two_sum(m_from, -m_to, dh, dl);
+    const float th = __fmul_rn(dh, s2h);
+    const float tl = __fadd_rn(__fmaf_rn(dh, s2h, -th), __fmaf_rn(dh, s2l, __fmul_rn(dl, s2h)));
+    float fh, fl;
+    exp2_precise(th, tl, C.tab, fh, fl);
+    ff_mul(zh, zl, fh, fl, zh, zl);
+  }
+
+  // One chunk of a row unit: n_el elements at src (staged copy or global
+  // row), e0 = the chunk's first element in the row.
+  __device__ void row_chunk(const void* src, int n_el, int e0, const UInfo& f, float s2h, float s2l,
+                            Part& P) const {
     const int nu = (n_el + VE - 1) / VE;
-    SegRec out;
-    out.lx = 0.0f;
-    if (greedy) {
+    if (f.greedy) {
       float best = -INFINITY;
       int bidx = INT_MAX, bad = 0;
       for (int q = lane; q < nu; q += 32) {
-        float f[VE];
+        float fv[VE];
         float vm;
         if constexpr (VEC) {
           const typename E::V raw = static_cast<const typename E::V*>(src)[q];
           vm = E::vmax_nan(raw);
           if (vm > best) {
-            E::unpack(raw, f);
+            E::unpack(raw, fv);
             int e = VE - 1;
 #pragma unroll
             for (int k = VE - 1; k >= 0; --k)
-              if (f[k] == vm) e = k;
+              if (fv[k] == vm) e = k;
             best = vm;
             bidx = q * VE + e;
           }
         } else {
-          load_unit<T, false>(src, q, n_el, false, f);
-          vm = f[0];
+          load_unit<T, false>(src, q, n_el, false, fv);
+          vm = fv[0];
 #pragma unroll
-          for (int k = 1; k < VE; ++k) vm = fmax_nan(vm, f[k]);
+          for (int k = 1; k < VE; ++k) vm = fmax_nan(vm, fv[k]);
           if (vm > best) {
             int e = VE - 1;
 #pragma unroll
             for (int k = VE - 1; k >= 0; --k)
-              if (f[k] == vm) e = k;
+              if (fv[k] == vm) e = k;
             best = vm;
             bidx = q * VE + e;
           }
@@ -516,113 +710,66 @@ struct Sampler {
       }
       unsigned long long key = bidx == INT_MAX ? 0ull
           : (static_cast<unsigned long long>(ordered_bits(best)) << 32) |
-                static_cast<unsigned long long>(0xFFFFFFFFu - static_cast<uint32_t>(bidx));
+                static_cast<unsigned long long>(0xFFFFFFFFu - static_cast<uint32_t>(e0 + bidx));
       key = warp_max_u64(key);
-      bad = __any_sync(kFull, bad);
-      out.m = key ? __uint_as_float((static_cast<uint32_t>(key >> 32) & 0x80000000u)
-                                        ? (static_cast<uint32_t>(key >> 32) & 0x7FFFFFFFu)
-                                        : ~static_cast<uint32_t>(key >> 32))
-                  : -INFINITY;
-      out.w2 = key ? static_cast<uint32_t>(e0) + (0xFFFFFFFFu - static_cast<uint32_t>(key)) : 0u;
-      out.w3 = bad ? 1u : 0u;
-    } else {
-      float vm = -INFINITY;
-      for (int q = lane; q < nu; q += 32) {
-        if constexpr (VEC) {
-          vm = fmax_nan(vm, E::vmax_nan(static_cast<const typename E::V*>(src)[q]));
-        } else {
-          float f[VE];
-          load_unit<T, false>(src, q, n_el, false, f);
-#pragma unroll
-          for (int k = 0; k < VE; ++k) vm = fmax_nan(vm, f[k]);
-        }
-      }
-      const float m = warp_max_nan(vm);
-      double z = 0.0;
-      if (isfinite(m)) {
-        float s2h, s2l;
-        scale_of(tau, s2h, s2l);
-        float ks = 0.0f, kc = 0.0f;
-        for (int q = lane; q < nu; q += 32) {
-          float f[VE];
-          load_unit<T, VEC>(src, q, n_el, false, f);
-          float2 acc = make_float2(0.0f, 0.0f);
-#pragma unroll
-          for (int k = 0; k < VE; k += 2) {
-            const float2 d = __fadd2_rn(make_float2(f[k], f[k + 1]), make_float2(-m, -m));
-            const float2 t = __ffma2_rn(d, make_float2(s2h, s2h),
-                                        __fmul2_rn(d, make_float2(s2l, s2l)));
-            acc = __fadd2_rn(acc, make_float2(exp2_ftz(t.x), exp2_ftz(t.y)));
-          }
-          comp_add(ks, kc, __fadd_rn(acc.x, acc.y));
-        }
-        z = warp_sum_f64(static_cast<double>(ks) + static_cast<double>(kc));
-      }
-      out.m = m;
-      const unsigned long long zb = static_cast<unsigned long long>(__double_as_longlong(z));
-      out.w2 = static_cast<uint32_t>(zb);
-      out.w3 = static_cast<uint32_t>(zb >> 32);
+      P.key = max(P.key, key);
+      P.bad |= __any_sync(kFull, bad);
+      return;
     }
-    if (lane == 0) {
-      if (xo >= 0 && xo < n_el) {
-        if constexpr (VEC) out.lx = E::at(src, xo);
-        else out.lx = E::ldg(src, xo);
+    float vm = -INFINITY;
+    for (int q = lane; q < nu; q += 32) {
+      if constexpr (VEC) {
+        vm = fmax_nan(vm, E::vmax_nan(static_cast<const typename E::V*>(src)[q]));
+      } else {
+        float fv[VE];
+        load_unit<T, false>(src, q, n_el, false, fv);
+#pragma unroll
+        for (int k = 0; k < VE; ++k) vm = fmax_nan(vm, fv[k]);
       }
-      __stcg(reinterpret_cast<uint4*>(rec), *reinterpret_cast<const uint4*>(&out));
+    }
+    const float mc = warp_max_nan(vm);
+    if (f.x >= e0 && f.x < e0 + n_el && lane == 0) {
+      if constexpr (VEC) P.lx = E::at(src, f.x - e0);
+      else P.lx = E::ldg(src, f.x - e0);
+    }
+    if (!(mc == mc) || mc == INFINITY) {  // NaN or +inf: the row is bad
+      P.bad = 1;
+      return;
+    }
+    if (mc == -INFINITY) return;  // nothing finite in this chunk
+    float ks = 0.0f, kc = 0.0f;
+    for (int q = lane; q < nu; q += 32) {
+      float fv[VE];
+      load_unit<T, VEC>(src, q, n_el, false, fv);
+      float2 acc = make_float2(0.0f, 0.0f);
+#pragma unroll
+      for (int k = 0; k < VE; k += 2) {
+        const float2 d = __fadd2_rn(make_float2(fv[k], fv[k + 1]), make_float2(-mc, -mc));
+        const float2 t = __ffma2_rn(d, make_float2(s2h, s2h), __fmul2_rn(d, make_float2(s2l, s2l)));
+        acc = __fadd2_rn(acc, make_float2(exp2_ftz(t.x), exp2_ftz(t.y)));
+      }
+      comp_add(ks, kc, __fadd_rn(acc.x, acc.y));
+    }
+    float zh, zl;
+    fast_two_sum(ks, kc, zh, zl);
+    warp_sum_ff(zh, zl);
+    if (P.m == -INFINITY) {
+      P.m = mc;
+      P.zh = zh;
+      P.zl = zl;
+    } else if (mc > P.m) {
+      rescale(P.zh, P.zl, P.m, mc, s2h, s2l);
+      ff_add(P.zh, P.zl, zh, zl, P.zh, P.zl);
+      P.m = mc;
+    } else {
+      rescale(zh, zl, mc, P.m, s2h, s2l);
+      ff_add(P.zh, P.zl, zh, zl, P.zh, P.zl);
     }
   }
 
-  // ---- consumer: pair (i, j) complete -----------------------------------
-  // Combines a row's segment records: max M (NaN/+inf/no finite value ->
-  // bad), Z in fp64, lx, and the lowest argmax (greedy).
-  __device__ void combine(const SegRec* recs, bool greedy, double s2d, int xseg, float& M,
-                          double& Z, float& lx, int& amax, int& bad) const {
-    float mv = -INFINITY;
-    int b = 0;
-    unsigned long long key = 0ull;
-    for (int s = lane; s < p.nseg; s += 32) {
-      const uint4 r = __ldcg(reinterpret_cast<const uint4*>(recs + s));
-      const float m = __uint_as_float(r.x);
-      b |= (m != m) | (m == INFINITY);
-      if (greedy) {
-        b |= r.w != 0u;
-        if (m != -INFINITY && m == m)
-          key = max(key, (static_cast<unsigned long long>(ordered_bits(m)) << 32) |
-                             static_cast<unsigned long long>(0xFFFFFFFFu - r.z));
-      }
-      mv = fmaxf(mv, m);
-    }
-    b = __any_sync(kFull, b);
-    M = warp_max(mv);
-    if (M == -INFINITY) b = 1;
-    bad = b;
-    amax = -1;
-    if (greedy) {
-      key = warp_max_u64(key);
-      amax = key ? static_cast<int>(0xFFFFFFFFu - static_cast<uint32_t>(key)) : -1;
-      Z = 1.0;
-    } else {
-      double z = 0.0;
-      if (!b) {
-        for (int s = lane; s < p.nseg; s += 32) {
-          const uint4 r = __ldcg(reinterpret_cast<const uint4*>(recs + s));
-          const float m = __uint_as_float(r.x);
-          if (m != -INFINITY) {
-            const double zs = __longlong_as_double(static_cast<long long>(
-                (static_cast<unsigned long long>(r.w) << 32) | r.z));
-            z += zs * exp2((static_cast<double>(m) - static_cast<double>(M)) * s2d);
-          }
-        }
-      }
-      Z = warp_sum_f64(z);
-    }
-    lx = 0.0f;
-    if (xseg >= 0) lx = __uint_as_float(__ldcg(reinterpret_cast<const unsigned int*>(recs + xseg) + 1));
-  }
-
-  // Writes every output of request i except a residual or bonus draw's
-  // token (written by the draw's finish); counts one event of request i
-  // and the request as done when `done`.
+  // ---- outputs and per-request bookkeeping --------------------------------
+  // Writes every output of request i except a final draw's token (written
+  // when the draw finishes).
   __device__ void write_prefix(int i, int a, int y, bool write_y) const {
     const int k1 = p.k_max + 1;
     int* o = p.out_tokens + static_cast<size_t>(i) * k1;
@@ -634,30 +781,113 @@ struct Sampler {
     if (lane == 0) p.accepted_len[i] = a;
   }
 
-  // Event of request i (pair decisions and the final token): the last one
-  // resets the request's words for the next call.
-  __device__ void event(int i, int n, int count) const {
-    if (lane == 0) {
-      const int old = atom_add_acq_rel(p.ev + i, count);
-      if (old + count == n + 2) {
-        p.st[i] = 0;
-        p.ev[i] = 0;
-      }
+  // One event of request i (a pair decided or skipped, or the final
+  // token); the last of its n + 2 events resets the request's words for the
+  // next call.  Called by one thread.
+  __device__ static void event1(const SamplerParams& q, int i, int n) {
+    const int old = atom_add_acq_rel(q.ev + i, 1);
+    if (old + 1 == n + 2) {
+      q.st[i] = 0;
+      q.ev[i] = 0;
     }
-  }
-
-  __device__ void request_done(int i, int n) const {
-    __syncwarp();
-    if (lane == 0) red_release_add(p.ctrl + kCtlReqDone, 1);
-    event(i, n, 1);
   }
 
   __device__ static void red_release_add(int* q, int v) {
     asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(q), "r"(v) : "memory");
   }
 
-  // `skipped`: early exit dropped some of the pair's segments (its slot is
-  // after the request's first rejection), so it has no statistics.
+  __device__ void request_done(int i, int n) const {
+    __syncwarp();
+    if (lane == 0) {
+      red_release_add(p.ctrl + kCtlReqDone, 1);
+      event1(p, i, n);
+    }
+  }
+
+  __device__ void list_draw(int i, int a, int kind) const {
+    if (lane == 0) {
+      const int e = atomicAdd(p.ctrl + kCtlDraws, 1);
+      if (e < 2 * p.bs) st_release(p.dl + e, 1 + ((i << 6) | (a << 2) | kind));
+      else raise_error(p.err, SD_DEV_ERR_TIMEOUT);  // cannot happen: at most two draws a request
+    }
+  }
+
+  __device__ const RowStat* tstat(int i, int j) const { return p.rst + trow_of(p, i, j); }
+  __device__ const RowStat* dstat(int i, int j) const {
+    return p.rst + static_cast<size_t>(p.bs) * (p.k_max + 1) + drow_of(p, i, j);
+  }
+
+  // ---- row unit complete: combine the warps' partials ---------------------
+  // Called by the last streaming warp to finish the unit; writes the row's
+  // statistics and counts the row into its pair.
+  // r = warp `lane`'s record (lanes < kNW), read before the slot was released.
+  __device__ void row_finish(const uint4 r, const UInfo& f) const {
+    RowStat rs;
+    rs.izh = 1.0f;
+    rs.izl = 0.0f;
+    rs.lx = 0.0f;
+    rs.amax = -1;
+    rs.r0 = rs.r1 = 0;
+    if (f.greedy) {
+      // record: key (lo, hi), bad
+      const unsigned long long key = lane < kNW
+          ? (static_cast<unsigned long long>(r.y) << 32) | r.x : 0ull;
+      const int bad = __any_sync(kFull, lane < kNW && r.z != 0u);
+      const unsigned long long best = warp_max_u64(key);
+      rs.amax = best ? static_cast<int>(0xFFFFFFFFu - static_cast<uint32_t>(best)) : -1;
+      const uint32_t ob = static_cast<uint32_t>(best >> 32);
+      rs.M = best ? __uint_as_float((ob & 0x80000000u) ? (ob & 0x7FFFFFFFu) : ~ob) : -INFINITY;
+      rs.bad = bad || best == 0ull;
+    } else {
+      // record: m (NaN when the warp saw NaN or +inf), zh, zl, lx
+      const float m = lane < kNW ? __uint_as_float(r.x) : -INFINITY;
+      int bad = __any_sync(kFull, m != m);
+      const float M = warp_max(m == m ? m : -INFINITY);
+      if (M == -INFINITY) bad = 1;
+      float zh = 0.0f, zl = 0.0f;
+      if (!bad && m != -INFINITY) {
+        float s2h, s2l;
+        scale_of(f.tau, s2h, s2l);
+        zh = __uint_as_float(r.y);
+        zl = __uint_as_float(r.z);
+        rescale(zh, zl, m, M, s2h, s2l);
+      }
+      warp_sum_ff(zh, zl);
+      rs.M = M;
+      rs.bad = bad;
+      if (!bad) ff_recip(zh, zl, rs.izh, rs.izl);
+      // lx: kept by the warp whose slice holds the draft token
+      if (f.x >= 0 && f.x < p.V) {
+        const int wx = static_cast<int>((static_cast<long long>(f.x) * sizeof(T)) / p.slice);
+        rs.lx = __shfl_sync(kFull, __uint_as_float(r.w), wx);
+      }
+    }
+    const size_t row = f.isd ? static_cast<size_t>(p.bs) * (p.k_max + 1) + drow_of(p, f.i, f.j)
+                             : static_cast<size_t>(trow_of(p, f.i, f.j));
+    if (lane == 0) {
+      __stcg(reinterpret_cast<uint4*>(p.rst + row), *reinterpret_cast<const uint4*>(&rs));
+      __stcg(reinterpret_cast<uint4*>(p.rst + row) + 1, *(reinterpret_cast<const uint4*>(&rs) + 1));
+    }
+    count_row(f.i, f.j, f.n, f.greedy, 1);
+  }
+
+  // Counts `add` into pair (i, j): a row (1) or a skipped row (1 + 1 << 16);
+  // the count that completes the pair finishes it (warp-wide).
+  __device__ void count_row(int i, int j, int n, bool greedy, int add) const {
+    const int pid = i * (p.k_max + 1) + j;
+    const int total = (!greedy && j < n) ? 2 : 1;
+    int now = 0;
+    if (lane == 0) now = atom_add_acq_rel(p.pc + pid, add) + add;
+    now = __shfl_sync(kFull, now, 0);
+    if ((now & 0xFFFF) == total) {
+      __syncwarp();
+      pair_finish(i, j, (now >> 16) != 0);
+    }
+  }
+
+  // ---- pair (i, j) complete ------------------------------------------------
+  // `skipped`: early exit dropped one of its rows (the slot is after the
+  // request's first rejection), so it has no decision.
   __device__ void pair_finish(int i, int j, bool skipped) const {
     const int n = n_of(p, i);
     const float tau = eff_tau(p, i);
@@ -665,65 +895,58 @@ struct Sampler {
     const bool has_d = !greedy && j < n;
     const int pid = i * (p.k_max + 1) + j;
     int bits = 0;
-    int xseg = -1, x = -1;
-    bool x_ok = false;
-    if (j < n) {
-      x = __ldg(p.draft_ids + drow_of(p, i, j));
-      x_ok = x >= 0 && x < p.V;
-      if (x_ok) xseg = x / kSegE;
-    }
-    if (!skipped) {
-      const double s2d = greedy ? 0.0 : kLog2eD / static_cast<double>(tau);
-      float Mt, Md = 0.0f, lxt, lxd = 0.0f;
-      double Zt, Zd = 1.0;
-      int amax, badt, badd = 0, dummy;
-      combine(p.seg_t + static_cast<size_t>(trow_of(p, i, j)) * p.nseg, greedy, s2d, xseg, Mt, Zt,
-              lxt, amax, badt);
-      if (has_d)
-        combine(p.seg_d + static_cast<size_t>(drow_of(p, i, j)) * p.nseg, false, s2d, xseg, Md, Zd,
-                lxd, dummy, badd);
-      const int bad = badt | badd;
-      if (lane == 0) {
-        PairStat ps;
-        ps.Mt = Mt;
-        ps.Md = Md;
-        ps.amax = amax;
-        ps.bad = bad;
-        ps.Zt = Zt;
-        ps.Zd = Zd;
-        __stcg(reinterpret_cast<uint4*>(p.ps + pid), *reinterpret_cast<const uint4*>(&ps));
-        __stcg(reinterpret_cast<uint4*>(p.ps + pid) + 1, *(reinterpret_cast<const uint4*>(&ps) + 1));
-        if (bad) raise_error(p.err, SD_DEV_ERR_LOGITS);
-        if (j < n && !x_ok) raise_error(p.err, SD_DEV_ERR_DRAFT_ID);
-        if (j == n) {
-          bits = 0x8000;  // the bonus row is in
-        } else if (greedy) {
-          const bool acc = !bad && x_ok && x == amax;
-          bits = acc ? (1 << j) : (1 << (16 + j));
-        } else {
-          bool acc = false;
-          float pf = 0.0f, qf = 0.0f;
-          const float u = p.uniforms[static_cast<size_t>(i) * (p.k_max + 1) + j];
-          if (!(u >= 0.0f && u < 1.0f)) raise_error(p.err, SD_DEV_ERR_UNIFORM);
-          if (!bad && x_ok) {
-            // p(x) = 2^((lx - M) s2) / Z in fp64, rounded to fp32; the
-            // comparison u * q <= p is taken in fp32 on those values
-            pf = static_cast<float>(
-                exp2((static_cast<double>(lxt) - static_cast<double>(Mt)) * s2d) / Zt);
-            qf = static_cast<float>(
-                exp2((static_cast<double>(lxd) - static_cast<double>(Md)) * s2d) / Zd);
-            acc = __fmul_rn(u, qf) <= pf;
-          }
-          if (p.probs_out) {
-            const size_t dr = static_cast<size_t>(drow_of(p, i, j));
-            p.probs_out[2 * dr] = pf;
-            p.probs_out[2 * dr + 1] = qf;
-          }
-          bits = acc ? (1 << j) : (1 << (16 + j));
+    if (!skipped && lane == 0) {
+      RowStat t, d;
+      *reinterpret_cast<uint4*>(&t) = __ldcg(reinterpret_cast<const uint4*>(tstat(i, j)));
+      *(reinterpret_cast<uint4*>(&t) + 1) = __ldcg(reinterpret_cast<const uint4*>(tstat(i, j)) + 1);
+      d.M = 0.0f;
+      d.izh = 1.0f;
+      d.izl = 0.0f;
+      d.lx = 0.0f;
+      d.bad = 0;
+      if (has_d) {
+        *reinterpret_cast<uint4*>(&d) = __ldcg(reinterpret_cast<const uint4*>(dstat(i, j)));
+        *(reinterpret_cast<uint4*>(&d) + 1) = __ldcg(reinterpret_cast<const uint4*>(dstat(i, j)) + 1);
+      }
+      const int bad = t.bad | d.bad;
+      int x = -1;
+      bool x_ok = false;
+      if (j < n) {
+        x = __ldg(p.draft_ids + drow_of(p, i, j));
+        x_ok = x >= 0 && x < p.V;
+      }
+      if (bad) raise_error(p.err, SD_DEV_ERR_LOGITS);
+      if (j < n && !x_ok) raise_error(p.err, SD_DEV_ERR_DRAFT_ID);
+      if (j == n) {
+        bits = 0x8000;  // the bonus row is in
+      } else if (greedy) {
+        const bool acc = !bad && x_ok && x == t.amax;
+        bits = acc ? (1 << j) : (1 << (16 + j));
+      } else {
+        bool acc = false;
+        float pf = 0.0f, qf = 0.0f;
+        const float u = p.uniforms[static_cast<size_t>(i) * (p.k_max + 1) + j];
+        if (!(u >= 0.0f && u < 1.0f)) raise_error(p.err, SD_DEV_ERR_UNIFORM);
+        if (!bad && x_ok) {
+          // p(x) = 2^((lx - M) s2) / Z in double-float, rounded once to
+          // fp32; the comparison u * q <= p is taken in fp32 on those values
+          float s2h, s2l, h, l;
+          scale_of(tau, s2h, s2l);
+          prob_precise(t.lx, t.M, s2h, s2l, t.izh, t.izl, C.tab, h, l);
+          pf = __fadd_rn(h, l);
+          prob_precise(d.lx, d.M, s2h, s2l, d.izh, d.izl, C.tab, h, l);
+          qf = __fadd_rn(h, l);
+          acc = __fmul_rn(u, qf) <= pf;
         }
+        if (p.probs_out) {
+          const size_t dr = static_cast<size_t>(drow_of(p, i, j));
+          p.probs_out[2 * dr] = pf;
+          p.probs_out[2 * dr + 1] = qf;
+        }
+        bits = acc ? (1 << j) : (1 << (16 + j));
       }
     }
-    // reset the pair's counter for the next call (every segment was counted)
+    // reset the pair's counter for the next call (every row was counted)
     if (lane == 0) p.pc[pid] = 0;
     int old = 0;
     if (lane == 0 && bits) old = atom_or_acq_rel(p.st + i, bits);
@@ -732,16 +955,16 @@ struct Sampler {
     const int now = settled(old | bits, n);
     const bool settles = bits && settled(old, n) < 0 && now >= 0;
     if (settles) settle(i, n, now, greedy);
-    event(i, n, 1);
+    if (lane == 0) event1(p, i, n);
   }
 
   // Request i has its accepted length a: write the outputs, or list its draw.
   __device__ void settle(int i, int n, int a, bool greedy) const {
-    const int pid = i * (p.k_max + 1) + a;
-    const uint4 w0 = __ldcg(reinterpret_cast<const uint4*>(p.ps + pid));
-    const int amax = static_cast<int>(w0.z);
-    const int bad = static_cast<int>(w0.w);
+    const uint4 t1 = __ldcg(reinterpret_cast<const uint4*>(tstat(i, a)) + 1);
+    int bad = static_cast<int>(t1.y);
+    if (!greedy && a < n) bad |= static_cast<int>(__ldcg(reinterpret_cast<const uint4*>(dstat(i, a)) + 1).y);
     if (greedy) {
+      const int amax = static_cast<int>(t1.x);
       write_prefix(i, a, bad || amax < 0 ? 0 : amax, true);
       request_done(i, n);
       return;
@@ -756,35 +979,29 @@ struct Sampler {
     list_draw(i, a, a < n ? kDrawResid : kDrawP);
   }
 
-  __device__ void list_draw(int i, int a, int kind) const {
-    if (lane == 0) {
-      const int e = atomicAdd(p.ctrl + kCtlDraws, 1);
-      st_release(p.dl + e, 1 + ((i << 6) | (a << 2) | kind));
-    }
-  }
-
-  // ---- consumer: draws ----------------------------------------------------
+  // ---- final draws -----------------------------------------------------------
   __device__ DrawCtx draw_ctx(int i, int a, int kind) const {
-    const int pid = i * (p.k_max + 1) + a;
-    const uint4 w0 = __ldcg(reinterpret_cast<const uint4*>(p.ps + pid));
-    const uint4 w1 = __ldcg(reinterpret_cast<const uint4*>(p.ps + pid) + 1);
-    const double Zt = __longlong_as_double(static_cast<long long>((static_cast<unsigned long long>(w1.y) << 32) | w1.x));
-    const double Zd = __longlong_as_double(static_cast<long long>((static_cast<unsigned long long>(w1.w) << 32) | w1.z));
+    const uint4 t0 = __ldcg(reinterpret_cast<const uint4*>(tstat(i, a)));
     DrawCtx c;
-    c.Mt = __uint_as_float(w0.x);
-    c.Md = __uint_as_float(w0.y);
-    scale_of(eff_tau(p, i), c.s2h, c.s2l);
-    const double izt = 1.0 / Zt, izd = 1.0 / Zd;
-    c.izth = static_cast<float>(izt);
-    c.iztl = static_cast<float>(izt - static_cast<double>(c.izth));
-    c.izdh = static_cast<float>(izd);
-    c.izdl = static_cast<float>(izd - static_cast<double>(c.izdh));
+    c.Mt = __uint_as_float(t0.x);
+    c.izth = __uint_as_float(t0.y);
+    c.iztl = __uint_as_float(t0.z);
+    c.Md = 0.0f;
+    c.izdh = 0.0f;
+    c.izdl = 0.0f;
     c.resid = kind == kDrawResid;
+    if (c.resid) {
+      const uint4 d0 = __ldcg(reinterpret_cast<const uint4*>(dstat(i, a)));
+      c.Md = __uint_as_float(d0.x);
+      c.izdh = __uint_as_float(d0.y);
+      c.izdl = __uint_as_float(d0.z);
+    }
+    scale_of(eff_tau(p, i), c.s2h, c.s2l);
     return c;
   }
 
-  // Fixed-point sum of sub-chunk s of draw (i, a, kind); the data is in the
-  // staged buffer `buf` (vector path) or read from the rows (element path).
+  // Fixed-point sum of one draw chunk of n_el elements (target at tsrc,
+  // draft at dsrc for a residual draw).
   __device__ unsigned long long sub_sum(const DrawCtx& c, const void* tsrc, const void* dsrc,
                                         int n_el) const {
     const int nu = (n_el + VE - 1) / VE;
@@ -806,28 +1023,57 @@ struct Sampler {
         bigm |= static_cast<uint64_t>(bm) << (k * VE);
       }
     }
-    while (bigm) {
-      const int bit = __ffsll(static_cast<long long>(bigm)) - 1;
-      bigm &= bigm - 1;
-      const int q = lane + 32 * (bit / VE);
-      const int k = q * VE + bit % VE;
-      const float lt = VEC ? E::at(tsrc, k) : E::ldg(tsrc, k);
-      const float ld = c.resid ? (VEC ? E::at(dsrc, k) : E::ldg(dsrc, k)) : 0.0f;
-      acc += elem_precise(c, lt, ld, C.tab);
+    // The heavy elements, compacted into the warp's list and spread over all
+    // lanes (a lane's own count varies a lot; the warp's total is small).
+    unsigned short* hl = heavy + warp * kHeavyList;
+    for (;;) {
+      const int cnt = __popcll(bigm);
+      int off = cnt;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int t = __shfl_up_sync(kFull, off, o);
+        if (lane >= o) off += t;
+      }
+      const int total = __shfl_sync(kFull, off, 31);
+      if (total == 0) break;
+      off -= cnt;  // exclusive
+      while (bigm && off < kHeavyList) {
+        const int bit = __ffsll(static_cast<long long>(bigm)) - 1;
+        bigm &= bigm - 1;
+        hl[off++] = static_cast<unsigned short>((lane + 32 * (bit / VE)) * VE + bit % VE);
+      }
+      __syncwarp();
+      const int nl = min(total, kHeavyList);
+      for (int n = lane; n < nl; n += 32) {
+        const int k = hl[n];
+        const float lt = VEC ? E::at(tsrc, k) : E::ldg(tsrc, k);
+        const float ld = c.resid ? (VEC ? E::at(dsrc, k) : E::ldg(dsrc, k)) : 0.0f;
+        acc += elem_precise(c, lt, ld, C.tab);
+      }
+      __syncwarp();
     }
     return warp_sum_u64(acc);
   }
 
-  // Finish of draw e (every sub-chunk summed): threshold floor(u * S), the
-  // crossing sub-chunk, then the walk of its units and elements.
-  __device__ void finish(int e, int i, int a, int kind) const {
-    const int n = n_of(p, i);
-    const unsigned long long* rs = p.rs + static_cast<size_t>(e) * p.nsub;
-    const int spl = (p.nsub + 31) / 32;
-    const int b0 = min(p.nsub, lane * spl), b1 = min(p.nsub, b0 + spl);
+  __device__ void finish_token(int e, int i, int n, int a, int y) const {
+    if (lane == 0) {
+      p.out_tokens[static_cast<size_t>(i) * (p.k_max + 1) + a] = y;
+      p.dl[e] = 0;
+    }
+    request_done(i, n);
+  }
+
+  // Draw unit complete (every warp's chunk sums are in): threshold
+  // floor(u * S), the crossing chunk, then the walk of its units and elements.
+  __device__ void draw_finish(const UInfo& f) const {
+    const int e = f.e, i = f.i, a = f.a, kind = f.dkind, n = f.n;
+    const unsigned long long* rs = p.rs + static_cast<size_t>(e) * kNW * p.ncd;
+    const int total = kNW * p.ncd;
+    const int spl = (total + 31) / 32;
+    const int b0 = min(total, lane * spl), b1 = min(total, b0 + spl);
     unsigned long long ls = 0ull;
-    for (int s = b0; s < b1; ++s) ls += __ldcg(rs + s);
-    // inclusive scan over lanes
+    for (int q = b0; q < b1; ++q)
+      if (q % p.ncd < nchunks(kUDraw, q / p.ncd)) ls += __ldcg(rs + q);
     unsigned long long inc = ls;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -840,9 +1086,8 @@ struct Sampler {
     if (S == 0ull) {
       if (kind == kDrawResid) {  // no residual mass in fp32: draw from p of the same row
         __syncwarp();
-        if (lane == 0) p.dc[e] = 0;
-        list_draw(i, a, kDrawP);
         if (lane == 0) p.dl[e] = 0;
+        list_draw(i, a, kDrawP);
         return;
       }
       if (lane == 0) raise_error(p.err, SD_DEV_ERR_LOGITS);
@@ -851,51 +1096,42 @@ struct Sampler {
     }
     const float uc = fminf(fmaxf(u, 0.0f), 0.99999994f);
     const unsigned long long th = __umul64hi(__float2ull_rn(__fmul_rn(uc, kTwo64)), S);
-    // the lane whose block holds the crossing
+    // the lane whose range holds the crossing
     const unsigned hit = __ballot_sync(kFull, inc > th);
     const int L = __ffs(hit) - 1;  // exists: inc[31] = S > th
     unsigned long long before = __shfl_sync(kFull, inc - ls, L);
-    int c = 0;
+    int cq = 0;
     if (lane == L) {
-      c = b1 - 1;
+      cq = b1 - 1;
       unsigned long long run = before;
-      for (int s = b0; s < b1; ++s) {
-        const unsigned long long v = __ldcg(rs + s);
+      for (int q = b0; q < b1; ++q) {
+        const unsigned long long v = q % p.ncd < nchunks(kUDraw, q / p.ncd) ? __ldcg(rs + q) : 0ull;
         if (run + v > th) {
-          c = s;
+          cq = q;
           break;
         }
         run += v;
       }
       before = run;
     }
-    c = __shfl_sync(kFull, c, L);
+    cq = __shfl_sync(kFull, cq, L);
     before = __shfl_sync(kFull, before, L);
-    const int y = walk(draw_ctx(i, a, kind), i, a, kind, c, th - before);
+    const int w = cq / p.ncd, cc = cq % p.ncd;
+    const int off = sl_begin(w) + cc * kHalf;
+    const int n_el = min(kHalf, sl_end(w) - off) / static_cast<int>(sizeof(T));
+    const int y = walk(draw_ctx(i, a, kind), i, a, off / static_cast<int>(sizeof(T)), n_el, th - before);
     finish_token(e, i, n, a, y);
   }
 
-  __device__ void finish_token(int e, int i, int n, int a, int y) const {
-    if (lane == 0) {
-      p.out_tokens[static_cast<size_t>(i) * (p.k_max + 1) + a] = y;
-      p.dl[e] = 0;
-      p.dc[e] = 0;
-    }
-    request_done(i, n);
-  }
-
-  // The element of sub-chunk c where the running weight passes th (from the
-  // sub-chunk's start); past the last element's weight, the last positive one.
-  __device__ int walk(const DrawCtx& c, int i, int a, int kind, int sc, unsigned long long th) const {
-    const int k0 = sc * kSubE;
-    const int n_el = min(kSubE, p.V - k0);
+  // The element of the chunk of n_el elements at k0 where the running weight
+  // passes th (from the chunk's start); past the last element's weight, the
+  // last positive one.
+  __device__ int walk(const DrawCtx& c, int i, int a, int k0, int n_el, unsigned long long th) const {
     const int nu = (n_el + VE - 1) / VE;
     const char* tb = trow_ptr(trow_of(p, i, a)) + static_cast<size_t>(k0) * sizeof(T);
     const char* db = c.resid ? drow_ptr(drow_of(p, i, a)) + static_cast<size_t>(k0) * sizeof(T) : tb;
-    (void)kind;
     unsigned long long v[kUPL];
-    unsigned long long ls = 0ull;
-    int lastu = -1;
+    uint64_t bigm = 0ull;
 #pragma unroll
     for (int k = 0; k < kUPL; ++k) {
       const int q = lane * kUPL + k;
@@ -908,10 +1144,40 @@ struct Sampler {
 #pragma unroll
           for (int e = 0; e < VE; ++e) fd[e] = 0.0f;
         }
-        v[k] = unit_value<VE>(c, ft, fd, C.tab);
-        if (v[k]) lastu = q;
+        uint32_t bm;
+        v[k] = unit_fast<VE>(c, ft, fd, bm);
+        bigm |= static_cast<uint64_t>(bm) << (k * VE);
       }
+    }
+    while (bigm) {  // the heavy elements, four per pass, each added to its unit
+      int kk[4], ku[4];
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        kk[t] = -1;
+        ku[t] = -1;
+        if (bigm) {
+          const int bit = __ffsll(static_cast<long long>(bigm)) - 1;
+          bigm &= bigm - 1;
+          ku[t] = bit / VE;
+          kk[t] = (lane * kUPL + ku[t]) * VE + bit % VE;
+        }
+      }
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        const int k = kk[t] < 0 ? 0 : kk[t];
+        const float lt = VEC ? E::at(tb, k) : E::ldg(tb, k);
+        const float ld = c.resid ? (VEC ? E::at(db, k) : E::ldg(db, k)) : 0.0f;
+        const unsigned long long pv = elem_precise(c, lt, ld, C.tab);
+#pragma unroll
+        for (int u2 = 0; u2 < kUPL; ++u2) v[u2] += ku[t] == u2 ? pv : 0ull;
+      }
+    }
+    unsigned long long ls = 0ull;
+    int lastu = -1;
+#pragma unroll
+    for (int k = 0; k < kUPL; ++k) {
       ls += v[k];
+      if (v[k]) lastu = lane * kUPL + k;
     }
     unsigned long long inc = ls;
 #pragma unroll
@@ -943,9 +1209,10 @@ struct Sampler {
       rem = ~0ull;
       if (q < 0) return k0;
     }
-    // elements of unit q, each with its own fixed-point weight
-    int pick = -1;
-    if (lane == 0) {
+    // the elements of unit q, one per lane (lanes < VE), each with its own
+    // fixed-point weight; the first whose running weight passes rem
+    unsigned long long w = 0ull;
+    {
       float ft[VE], fd[VE];
       load_unit<T, VEC>(tb, q, n_el, true, ft);
       if (c.resid) load_unit<T, VEC>(db, q, n_el, true, fd);
@@ -953,319 +1220,320 @@ struct Sampler {
 #pragma unroll
         for (int e = 0; e < VE; ++e) fd[e] = 0.0f;
       }
-      unsigned long long run = 0ull;
-      int last = -1;
+      float lt = ft[0], ld = fd[0];
 #pragma unroll
-      for (int e = 0; e < VE; ++e) {
-        bool big;
-        const float r = elem_fast(c, ft[e], fd[e], big);
-        const unsigned long long w = big ? elem_precise(c, ft[e], fd[e], C.tab)
-                                         : __float2ull_rn(__fmul_rn(r, kTwo56));
-        if (w > 0ull) last = e;
-        if (pick < 0 && run + w > rem) pick = e;
-        run += w;
+      for (int e = 1; e < VE; ++e)
+        if (lane == e) {
+          lt = ft[e];
+          ld = fd[e];
+        }
+      bool big;
+      const float r = elem_fast(c, lt, ld, big);
+      w = big ? elem_precise(c, lt, ld, C.tab) : fixed56(r);
+      if (lane >= VE) w = 0ull;
+    }
+    unsigned long long run = w;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const unsigned long long t = __shfl_up_sync(kFull, run, o);
+      if (lane >= o) run += t;
+    }
+    const unsigned pass = __ballot_sync(kFull, lane < VE && run > rem);
+    const unsigned pos = __ballot_sync(kFull, lane < VE && w > 0ull);
+    const int e = pass ? __ffs(pass) - 1 : (pos ? 31 - __clz(pos) : 0);
+    return k0 + q * VE + e;
+  }
+
+  // ---- streaming warps -------------------------------------------------------
+  // Waits (lane 0, bounded) until position k is published in its slot.
+  __device__ bool wait_entry(int k) const {
+    bool ok = true;
+    if (lane == 0 && q_seq[k % kQ] != k) {
+      const uint64_t end = now_ns() + p.wait_ns;
+      for (;;) {
+        if (q_seq[k % kQ] == k) break;
+        if (*stop || now_ns() > end) {
+          ok = false;
+          break;
+        }
+        __nanosleep(64);
       }
-      if (pick < 0) pick = last >= 0 ? last : 0;
-      pick = k0 + q * VE + pick;
     }
-    return __shfl_sync(kFull, pick, 0);
+    ok = __shfl_sync(kFull, ok, 0) != 0;
+    __threadfence_block();  // the entry's fields after its published position
+    __syncwarp();
+    return ok;
   }
 
-  // ---- consumer loop ---------------------------------------------------------
-  __device__ bool wait_full(int b, uint32_t par) const {
-    if (mbar_poll(&full[b], par)) return true;
-    const uint64_t end = now_ns() + p.wait_ns;
-    for (;;) {
-      if (mbar_poll(&full[b], par)) return true;
-      if (*stop || now_ns() > end) return false;
+  // Warp w's part of position k is done: its record (row units), the count,
+  // and, by the last warp, the unit's finish.
+  __device__ void finalize(int k, const UInfo& f, const Part& P) const {
+    const int slot = k % kQ;
+    if (lane == 0) {
+      if (f.kind == kURow) {
+        uint4 r;
+        if (f.greedy) {
+          r = make_uint4(static_cast<uint32_t>(P.key), static_cast<uint32_t>(P.key >> 32),
+                         static_cast<uint32_t>(P.bad), 0u);
+        } else {
+          r = make_uint4(__float_as_uint(P.bad ? NAN : P.m), __float_as_uint(P.zh),
+                         __float_as_uint(P.zl), __float_as_uint(P.lx));
+        }
+        q_rec[slot * kNW + warp] = r;
+      } else {
+        __threadfence();  // the chunk sums, read back through L2 by the finishing warp
+      }
     }
-  }
-
-  // Ticket t is phase m = t / nbuf of buffer b = t % nbuf.  A consumer can
-  // run a whole ring ahead of a slow copy (the items between may complete at
-  // once), and a parity wait on phase m while phase m - 1 is still pending
-  // would return on phase m - 2.  So the consumer first waits until the
-  // consumer of phase m - 1 has passed its own wait.
-  __device__ bool wait_turn(int b, int m) const {
-    if (seen[b] >= m) return true;
-    const uint64_t end = now_ns() + p.wait_ns;
-    for (;;) {
-      if (seen[b] >= m) return true;
-      if (*stop || now_ns() > end) return false;
-      __nanosleep(32);
+    int last = 0;
+    if (lane == 0) {
+      __threadfence_block();
+      last = (atomicAdd(q_cnt + slot, 1) % kNW) == kNW - 1;
     }
-  }
-
-  __device__ void consume() const {
-    for (;;) {
-      int t = 0;
-      if (lane == 0) t = atomicAdd(ticket, 1);
-      t = __shfl_sync(kFull, t, 0);
-      const int b = t % p.nbuf;
-      const int m = t / p.nbuf;
-      bool ok = false;
+    last = __shfl_sync(kFull, last, 0);
+    if (last) {
+      __threadfence_block();
+      // the finish needs nothing more of the slot: release it first, so the
+      // scheduler can reuse it while this warp finishes the unit
+      const uint4 r = (f.kind == kURow && lane < kNW) ? q_rec[slot * kNW + lane] : make_uint4(0u, 0u, 0u, 0u);
+      __syncwarp();
       if (lane == 0) {
-        ok = wait_turn(b, m) && wait_full(b, static_cast<uint32_t>(m) & 1u);
-        if (ok) seen[b] = m + 1;
+        __threadfence_block();
+        q_fin[slot] = k;
       }
-      ok = __shfl_sync(kFull, ok, 0);
-      if (!ok) {
-        halt();
-        return;
-      }
-      __syncwarp();  // lane 0's wait (acquire) covers the warp's reads
-      const Desc d = desc[b];
-      if (d.kind == kEnd) return;
-      const void* buf = ring + static_cast<size_t>(b) * kSegBytes;
-      if (d.kind == kRow || d.kind == kSkip) {
-        const int i = d.a & 0xFFF, j = (d.a >> 12) & 0xF, isd = (d.a >> 16) & 1;
-        const int n = n_of(p, i);
-        const float tau = eff_tau(p, i);
-        const bool greedy = !(tau > 0.0f);
-        const int pid = i * (p.k_max + 1) + j;
-        // One atomic counts the item: its segments, and (a skip item) one
-        // unit at bit 16, so the count that completes the pair also says
-        // whether any of its segments were dropped.
-        int add = 1;
-        if (d.kind == kRow) {
-          const int s = d.b;
-          const int e0 = s * kSegE;
-          const int n_el = min(kSegE, p.V - e0);
-          int xo = -1;
-          if (j < n) {
-            const int x = __ldg(p.draft_ids + drow_of(p, i, j));
-            if (x >= e0 && x < e0 + n_el) xo = x - e0;
-          }
-          const long long r = isd ? drow_of(p, i, j) : trow_of(p, i, j);
-          const void* src = VEC ? buf : static_cast<const void*>((isd ? drow_ptr(r) : trow_ptr(r)) +
-                                                                 static_cast<size_t>(e0) * sizeof(T));
-          SegRec* rec = (isd ? p.seg_d : p.seg_t) + static_cast<size_t>(r) * p.nseg + s;
-          segment(src, n_el, greedy, tau, xo, rec, e0);
-        } else {
-          add = d.b + (1 << 16);
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[b]);
-        const int total = p.nseg * ((!greedy && j < n) ? 2 : 1);
-        int now = 0;
-        if (lane == 0) now = atom_add_acq_rel(p.pc + pid, add) + add;
-        now = __shfl_sync(kFull, now, 0);
-        if ((now & 0xFFFF) == total) {
-          __syncwarp();
-          pair_finish(i, j, (now >> 16) != 0);
-        }
-      } else {  // kSub
-        const int e = d.a, s = d.b;
-        const int code = d.c - 1;
-        const int i = (code >> 6) & 0xFFF, a = (code >> 2) & 0xF, kind = code & 3;
-        const DrawCtx c = draw_ctx(i, a, kind);
-        const int k0 = s * kSubE;
-        const int n_el = min(kSubE, p.V - k0);
-        const void* tsrc;
-        const void* dsrc;
-        if constexpr (VEC) {
-          tsrc = buf;
-          dsrc = static_cast<const char*>(buf) + kSubBytes;
-        } else {
-          tsrc = trow_ptr(trow_of(p, i, a)) + static_cast<size_t>(k0) * sizeof(T);
-          dsrc = c.resid ? static_cast<const void*>(drow_ptr(drow_of(p, i, a)) + static_cast<size_t>(k0) * sizeof(T))
-                         : tsrc;
-        }
-        const unsigned long long sum = sub_sum(c, tsrc, dsrc, n_el);
-        __syncwarp();
+      if (f.kind == kURow) {
+        row_finish(r, f);
+      } else {
+        int parts = 0;
         if (lane == 0) {
-          mbar_arrive(&empty[b]);
-          __stcg(p.rs + static_cast<size_t>(e) * p.nsub + s, sum);
+          __threadfence();
+          parts = atom_add_acq_rel(p.dpc + f.e, 1) + 1;
         }
-        __syncwarp();
-        int old = 0;
-        if (lane == 0) old = atom_add_acq_rel(p.dc + e, 1);
-        old = __shfl_sync(kFull, old, 0);
-        if (old == p.nsub - 1) {
-          __syncwarp();
-          finish(e, i, a, kind);
+        parts = __shfl_sync(kFull, parts, 0);
+        if (parts == kDrawParts) {
+          if (lane == 0) p.dpc[f.e] = 0;
+          draw_finish(f);
         }
       }
     }
   }
 
-  // ---- producer (lane 0 of the producer warp) ------------------------------
-  struct Prod {
-    int k = 0;             // items published
+  __device__ static Part fresh_part() {
+    Part P;
+    P.m = -INFINITY;
+    P.zh = P.zl = P.lx = 0.0f;
+    P.key = 0ull;
+    P.bad = 0;
+    return P;
+  }
+
+  __device__ void stream() const {
+    const uint64_t pol_first = policy_evict_first();    // rows read once, and draws
+    const uint64_t pol_normal = policy_evict_normal();  // sampling rows a draw may read again
+    int ik = 0, ic = 0, gi = 0;  // issue cursor: position, its next chunk; chunks issued
+    int ck = 0, cc = 0, gc = 0;  // compute cursor: position, its next chunk; chunks computed
+    bool iend = false, fi_ok = false, fc_ok = false;
+    UInfo fi{}, fc{};
+    Part P = fresh_part();
+    float s2h = 0.0f, s2l = 0.0f;
+    DrawCtx dctx{};
+    for (;;) {
+      // 1. keep two chunks in flight, across unit boundaries (vector path)
+      if constexpr (VEC) {
+        while (!iend && gi - gc < 2) {
+          if (!fi_ok) {
+            int pub = 0;
+            if (lane == 0) pub = q_seq[ik % kQ] == ik;
+            if (!__shfl_sync(kFull, pub, 0)) break;
+            __threadfence_block();
+            __syncwarp();
+            const Unit u = q_ent[ik % kQ];
+            if (u.kind == kUEnd) {
+              iend = true;
+              break;
+            }
+            fi = info(u);
+            fi_ok = true;
+            ic = 0;
+          }
+          if (ic >= ucount(fi, warp)) {
+            ++ik;
+            fi_ok = false;
+            continue;
+          }
+          if (lane == 0) issue(fi, ic, gi, pol_first, pol_normal);
+          ++ic;
+          ++gi;
+        }
+      }
+      // 2. the compute cursor's unit
+      if (!fc_ok) {
+        if (!wait_entry(ck)) {
+          halt();
+          break;
+        }
+        const Unit u = q_ent[ck % kQ];
+        if (u.kind == kUEnd) break;
+        fc = info(u);
+        fc_ok = true;
+        cc = 0;
+        P = fresh_part();
+        if (fc.kind == kURow) {
+          if (!fc.greedy) scale_of(fc.tau, s2h, s2l);
+        } else {
+          dctx = draw_ctx(fc.i, fc.a, fc.dkind);
+        }
+      }
+      if (cc < ucount(fc, warp)) {
+        const int cb = fc.kind == kURow ? kChunk : kHalf;
+        const int off = sl_begin(warp) + (cbase(fc, warp) + cc) * cb;
+        const int n_el = min(cb, sl_end(warp) - off) / static_cast<int>(sizeof(T));
+        const void* st_src;
+        const void* sd_src;
+        if constexpr (VEC) {
+          if (gc == gi) continue;  // its copy is issued in step 1 of the next pass
+          int ok = 1;
+          if (lane == 0) ok = wait_chunk(gc);
+          if (!__shfl_sync(kFull, ok, 0)) {
+            halt();
+            break;
+          }
+          __syncwarp();
+          st_src = buf_of(gc);
+          sd_src = buf_of(gc) + kHalf;
+        } else {
+          st_src = fc.src_t + off;
+          sd_src = fc.src_d ? fc.src_d + off : nullptr;
+        }
+        if (fc.kind == kURow) {
+          row_chunk(st_src, n_el, off / static_cast<int>(sizeof(T)), fc, s2h, s2l, P);
+        } else {
+          const unsigned long long sum = sub_sum(dctx, st_src, sd_src, n_el);
+          if (lane == 0) __stcg(p.rs + (static_cast<size_t>(fc.e) * kNW + warp) * p.ncd + cbase(fc, warp) + cc, sum);
+        }
+        if constexpr (VEC) fence_proxy_async();  // this buffer's reads before the copy into it
+        __syncwarp();
+        ++gc;
+        ++cc;
+        continue;
+      }
+      finalize(ck, fc, P);
+      ++ck;
+      fc_ok = false;
+    }
+    // No bulk copy may be in flight when the warp leaves.
+    if constexpr (VEC) {
+      if (lane == 0) {
+        const uint64_t end = now_ns() + kDrainNs;
+        for (int g = gc; g < gi; ++g)
+          while (!mbar_poll(bar_of(g), static_cast<uint32_t>(g >> 1) & 1u) && now_ns() <= end) {
+          }
+      }
+      __syncwarp();
+    }
+  }
+
+  // ---- scheduler warp (lane 0) -----------------------------------------------
+  // Pair (i, j)'s row dropped by early exit: counted with the skip mark; the
+  // count that completes the pair ends it without a decision.
+  __device__ void skip_row(int i, int j, int n) const {
+    const bool greedy = !(eff_tau(p, i) > 0.0f);
+    const int pid = i * (p.k_max + 1) + j;
+    const int total = (!greedy && j < n) ? 2 : 1;
+    const int add = 1 + (1 << 16);
+    const int now = atom_add_acq_rel(p.pc + pid, add) + add;
+    if ((now & 0xFFFF) == total) {
+      p.pc[pid] = 0;
+      event1(p, i, n);
+    }
+  }
+
+  struct Sched {
+    int rb_next = -1;  // the next row unit, claimed one step ahead
     bool rows_done = false;
-    int held = -1;         // a claimed draw block whose draw is not listed yet
-    int rb_next = -1;      // the next row block, claimed one step ahead
-    // the row block in hand
-    int seg = 0, seg_end = 0;
-    Loc loc{};
-    long long row = 0;
-    bool greedy = false;
+    int held = -1;     // a claimed draw index not listed yet
+    int taken_seen = 0;
   };
 
-  // Waits until buffer b may be refilled for item k.
-  __device__ bool wait_empty(int k) const {
-    if (k < p.nbuf) return true;
-    const int b = k % p.nbuf;
-    const uint32_t par = static_cast<uint32_t>(k / p.nbuf - 1) & 1u;
-    if (mbar_poll(&empty[b], par)) return true;
-    const uint64_t end = now_ns() + p.wait_ns;
+  // The next unit for the queue: parts of listed draws, else rows in slot
+  // order; END once every request's outputs are in (or a wait gave up).
+  __device__ Unit claim(Sched& S) const {
+    uint64_t idle_end = 0;
     for (;;) {
-      if (mbar_poll(&empty[b], par)) return true;
-      if (*stop || now_ns() > end) return false;
-    }
-  }
-
-  __device__ bool publish(Prod& P, const Desc& d, const char* src0, uint32_t bytes0,
-                          const char* src1, uint32_t bytes1, bool evict) const {
-    if (!wait_empty(P.k)) return false;
-    const int b = P.k % p.nbuf;
-    desc[b] = d;
-    unsigned char* dst = ring + static_cast<size_t>(b) * kSegBytes;
-    if (VEC && (bytes0 + bytes1) > 0) {
-      mbar_arrive_expect_tx(&full[b], bytes0 + bytes1);
-      const uint64_t pol = evict ? policy_evict_first() : policy_evict_normal();
-      if (bytes0) bulk_load(dst, src0, bytes0, &full[b], pol);
-      if (bytes1) bulk_load(dst + kSubBytes, src1, bytes1, &full[b], pol);
-    } else {
-      mbar_arrive(&full[b]);
-    }
-    ++P.k;
-    return true;
-  }
-
-  __device__ static uint64_t policy_evict_normal() {
-    uint64_t pol;
-    asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(pol));
-    return pol;
-  }
-
-  // Takes the next row block into P (returns 1), or finds the rows done
-  // (0), or gives up on a wait (-1).  A block that early exit drops is
-  // handed out as one skip item and never left in P.
-  __device__ int next_row_block(Prod& P) const {
-    const int total = C.U * C.BPU;
-    for (;;) {
-      const int rb = P.rb_next;
-      if (rb < 0 || rb >= total || (p.flags & kFlagTestStall)) {
-        P.rows_done = true;
-        P.seg = P.seg_end = 0;
-        return 0;
-      }
-      P.rb_next = atomicAdd(p.ctrl + kCtlRowBlk, 1);  // one step ahead
-      const int u = rb / C.BPU, g = rb - u * C.BPU;
-      P.loc = locate(C, u);
-      P.seg = g * kRowBlock;
-      P.seg_end = min(p.nseg, P.seg + kRowBlock);
-      const int i = P.loc.i, j = P.loc.j;
-      P.greedy = !(eff_tau(p, i) > 0.0f);
-      P.row = P.loc.isd ? drow_of(p, i, j) : trow_of(p, i, j);
-      if (p.flags & kFlagEarlyExit) {
-        const int a = settled(ld_relaxed(p.st + i), n_of(p, i));
-        if (a >= 0 && j > a) {  // after the request's first rejection: not needed
-          Desc d{kSkip, i | (j << 12) | (P.loc.isd << 16), P.seg_end - P.seg, 0};
-          P.seg = P.seg_end = 0;
-          if (!publish(P, d, nullptr, 0, nullptr, 0, false)) return -1;
-          continue;
-        }
-      }
-      return 1;
-    }
-  }
-
-  __device__ void produce() const {
-    Prod P;
-    P.rb_next = atomicAdd(p.ctrl + kCtlRowBlk, 1);
-    const size_t rbytes = row_bytes();
-    uint64_t idle_end = 0;  // while nothing is handed out: when to give up
-    bool failed = false;
-    for (;;) {
-      if (*stop) {
-        failed = true;
-        break;
-      }
-      // 1. blocks of listed draws first
+      if (*stop) return Unit{kUEnd, 0, 0, 0};
+      // parts of listed draws first: a request's last step
       const int nd = ld_relaxed(p.ctrl + kCtlDraws);
-      if (P.held < 0 && ld_relaxed(p.ctrl + kCtlDrawBlk) < nd * C.BPD)
-        P.held = atomicAdd(p.ctrl + kCtlDrawBlk, 1);
-      if (P.held >= 0 && P.held / C.BPD < ld_relaxed(p.ctrl + kCtlDraws)) {
-        const int e = P.held / C.BPD, blk = P.held - e * C.BPD;
-        P.held = -1;
+      if (S.held < 0 && S.taken_seen < nd * kDrawParts) {
+        S.held = atomicAdd(p.ctrl + kCtlDrawTaken, 1);  // a part of a draw
+        S.taken_seen = S.held + 1;
+        if (S.held >= 2 * p.bs * kDrawParts) S.held = -1;  // past the draw list (never listed)
+      }
+      if (S.held >= 0 && S.held / kDrawParts < nd) {
+        const int e = S.held / kDrawParts;
         int code = ld_acquire(p.dl + e);
         for (const uint64_t end = now_ns() + p.wait_ns; code == 0 && now_ns() <= end;)
           code = ld_acquire(p.dl + e);
         if (code == 0) {
-          failed = true;
+          halt();
+          return Unit{kUEnd, 0, 0, 0};
+        }
+        const Unit u{kUDraw, e, code, S.held - e * kDrawParts};
+        S.held = -1;
+        return u;
+      }
+      // then rows in slot order
+      while (!S.rows_done) {
+        const int rb = S.rb_next;
+        if (rb < 0 || rb >= C.U || (p.flags & kFlagTestStall)) {
+          S.rows_done = true;
           break;
         }
-        const int cc = code - 1;
-        const int i = (cc >> 6) & 0xFFF, a = (cc >> 2) & 0xF, kind = cc & 3;
-        const char* tb = trow_ptr(trow_of(p, i, a));
-        const char* db = kind == kDrawResid ? drow_ptr(drow_of(p, i, a)) : nullptr;
-        const int s1 = min(p.nsub, (blk + 1) * kSubBlock);
-        for (int s = blk * kSubBlock; s < s1; ++s) {
-          const size_t off = static_cast<size_t>(s) * kSubBytes;
-          const uint32_t by = static_cast<uint32_t>(min(static_cast<size_t>(kSubBytes), rbytes - off));
-          Desc d{kSub, e, s, code};
-          if (!publish(P, d, tb + off, VEC ? by : 0u, db ? db + off : nullptr, (VEC && db) ? by : 0u,
-                       true)) {
-            failed = true;
-            break;
+        S.rb_next = atomicAdd(p.ctrl + kCtlRow, 1);
+        const Loc L = locate(C, rb);
+        const int n = n_of(p, L.i);
+        if (p.flags & kFlagEarlyExit) {
+          const int a = settled(ld_relaxed(p.st + L.i), n);
+          if (a >= 0 && L.j > a) {  // after the request's first rejection: not needed
+            skip_row(L.i, L.j, n);
+            continue;
           }
         }
-        if (failed) break;
-        idle_end = 0;
-        continue;
+        const long long row = L.isd ? drow_of(p, L.i, L.j) : trow_of(p, L.i, L.j);
+        return Unit{kURow, L.i | (L.j << 12) | (L.isd << 16), static_cast<int>(row), 0};
       }
-      // 2. row segments
-      if (!P.rows_done) {
-        if (P.seg >= P.seg_end) {
-          const int got = next_row_block(P);
-          if (got < 0 || *stop) {
-            failed = true;
-            break;
-          }
-          if (got == 0) continue;
-        }
-        const int s = P.seg++;
-        const size_t off = static_cast<size_t>(s) * kSegBytes;
-        const uint32_t by = static_cast<uint32_t>(min(static_cast<size_t>(kSegBytes), rbytes - off));
-        const char* base = P.loc.isd ? drow_ptr(P.row) : trow_ptr(P.row);
-        Desc d{kRow, P.loc.i | (P.loc.j << 12) | (P.loc.isd << 16), s, 0};
-        if (!publish(P, d, base + off, VEC ? by : 0u, nullptr, 0u, P.greedy)) {
-          failed = true;
-          break;
-        }
-        idle_end = 0;
-        continue;
-      }
-      // 3. nothing to hand out: done once every request's outputs are in
-      if (ld_acquire(p.ctrl + kCtlReqDone) >= p.bs) break;
+      if (ld_acquire(p.ctrl + kCtlReqDone) >= p.bs) return Unit{kUEnd, 0, 0, 0};
       const uint64_t t = now_ns();
-      if (idle_end == 0) idle_end = t + p.wait_ns;
-      if (t > idle_end) {
-        failed = true;
-        break;
-      }
-      __nanosleep(128);
-    }
-    if (failed) halt();
-    // one end marker per consumer warp
-    for (int w = 0; w < kNC && !*stop; ++w) {
-      Desc d{kEnd, 0, 0, 0};
-      if (!publish(P, d, nullptr, 0, nullptr, 0, false)) {
+      if (idle_end == 0) {
+        idle_end = t + p.wait_ns;
+      } else if (t > idle_end) {
         halt();
-        break;
+        return Unit{kUEnd, 0, 0, 0};
       }
+      __nanosleep(200);
     }
-    // No bulk copy may be in flight when the CTA exits: wait for the last
-    // item of every buffer (a copy of valid memory always lands; the bound
-    // does not depend on the caller's wait limit).
-    const uint64_t drain_end = now_ns() + kDrainNs;
-    for (int k = max(0, P.k - p.nbuf); k < P.k; ++k) {
-      const int b = k % p.nbuf;
-      const uint32_t par = static_cast<uint32_t>(k / p.nbuf) & 1u;
-      while (!mbar_poll(&full[b], par) && now_ns() <= drain_end) {
+  }
+
+  __device__ void schedule() const {
+    Sched S;
+    S.rb_next = atomicAdd(p.ctrl + kCtlRow, 1);
+    for (int k = 0;; ++k) {
+      const int slot = k % kQ;
+      bool ok = true;
+      if (k >= kQ && q_fin[slot] != k - kQ) {  // the slot's previous unit must be complete
+        const uint64_t end = now_ns() + p.wait_ns;
+        while (q_fin[slot] != k - kQ) {
+          if (*stop || now_ns() > end) {
+            ok = false;
+            break;
+          }
+          __nanosleep(64);
+        }
       }
+      if (!ok) halt();
+      const Unit u = ok ? claim(S) : Unit{kUEnd, 0, 0, 0};
+      q_ent[slot] = u;
+      __threadfence_block();
+      q_seq[slot] = k;
+      if (u.kind == kUEnd) break;
     }
   }
 };
@@ -1275,31 +1543,32 @@ struct Sampler {
 template <typename T, bool VEC>
 __global__ void __launch_bounds__(kThreads, 1) sampler_kernel(const __grid_constant__ SamplerParams p) {
   extern __shared__ __align__(128) unsigned char smem[];
-  __shared__ uint64_t s_full[kMaxBufs], s_empty[kMaxBufs];
-  __shared__ Desc s_desc[kMaxBufs];
-  __shared__ int s_ticket, s_stop, s_bad, s_last;
-  __shared__ int s_seen[kMaxBufs];
+  __shared__ uint64_t s_full[kNW * 2];
+  __shared__ Unit s_ent[kQ];
+  __shared__ int s_seq[kQ], s_fin[kQ], s_cnt[kQ];
+  __shared__ uint4 s_rec[kQ * kNW];
+  __shared__ int s_stop, s_last;
   __shared__ int s_hist[32], s_base[32];
   __shared__ int s_WS[SD_MAX_K + 3], s_P[SD_MAX_K + 2], s_E[SD_MAX_K + 2];
   __shared__ float2 s_tab[16];
+  __shared__ unsigned short s_heavy[kNW * kHeavyList];
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int bs = p.bs, K1 = p.k_max + 1;
-  unsigned char* ring = smem;
-  int* order = reinterpret_cast<int*>(smem + static_cast<size_t>(p.nbuf) * kSegBytes);  // [bs]
-  // the ring doubles as scratch for the request lengths while the tables are built
+  unsigned char* bufs = smem;
+  int* order = reinterpret_cast<int*>(smem + static_cast<size_t>(kNW) * 2 * kChunk);  // [bs]
+  // the buffers double as scratch for the request lengths while the tables are built
   int* nscr = reinterpret_cast<int*>(smem);  // [bs] bin of request i
 
-  if (tid == 0) {
-    s_bad = 0;
-    s_ticket = 0;
-    s_stop = 0;
-  }
+  if (tid == 0) s_stop = 0;
   if (tid < 32) s_hist[tid] = 0;
-  if (tid < kMaxBufs) s_seen[tid] = 0;
+  if (tid < kQ) {
+    s_seq[tid] = -1;
+    s_fin[tid] = -1;
+    s_cnt[tid] = 0;
+  }
   if (tid < 16) s_tab[tid] = p.exp_tab[tid];
   __syncthreads();
-
   // ---- per-call checks of the compaction (the same verdict in every CTA)
   int bad = 0;
   if (tid == 0 && __ldg(p.cu) != 0) bad = 1;
@@ -1370,16 +1639,13 @@ __global__ void __launch_bounds__(kThreads, 1) sampler_kernel(const __grid_const
       s_WS[K1] = ws;
     }
   }
-  // the bins were kept in the ring; later bulk copies write there
+  // the bins were kept in the buffers; later bulk copies write there
   fence_proxy_async();
-  // One thread initialises every ring barrier and then fences: the fence
+  // One thread initialises every buffer barrier and then fences: the fence
   // makes the initialising thread's own inits visible to the bulk copies'
   // completions (async proxy), so the inits and the fence share a thread.
   if (tid == 0) {
-    for (int b = 0; b < p.nbuf; ++b) {
-      mbar_init(&s_full[b], 1);
-      mbar_init(&s_empty[b], 1);
-    }
+    for (int b = 0; b < 2 * kNW; ++b) mbar_init(&s_full[b], 1);
     fence_mbar_init();
   }
   __syncthreads();
@@ -1393,17 +1659,16 @@ __global__ void __launch_bounds__(kThreads, 1) sampler_kernel(const __grid_const
   for (int b = 0; b < 16; ++b) C.nsamp += s_hist[b];
   C.nw = K1;
   C.U = s_WS[K1];
-  C.BPU = (p.nseg + kRowBlock - 1) / kRowBlock;
-  C.BPD = (p.nsub + kSubBlock - 1) / kSubBlock;
   C.tab = s_tab;
 
-  Sampler<T, VEC> S{p, C, ring, s_full, s_empty, s_desc, &s_ticket, s_seen, &s_stop, lane};
-  if (warp < kNC) {
-    S.consume();
+  Sampler<T, VEC> S{p, C, s_ent, s_seq, s_fin, s_cnt, s_rec, bufs, s_heavy, s_full, &s_stop, lane, warp,
+                    p.V * static_cast<int>(sizeof(T))};
+  if (warp < kNW) {
+    S.stream();
   } else {
-    if (lane == 0) S.produce();
-    // The CTA barrier below is warp-aligned: the producer warp reaches it
-    // converged, after lane 0 has drained its copies.
+    if (lane == 0) S.schedule();
+    // The CTA barrier below is warp-aligned: the scheduler warp reaches it
+    // converged.
     __syncwarp();
   }
 
@@ -1429,7 +1694,7 @@ __global__ void __launch_bounds__(kThreads, 1) sampler_kernel(const __grid_const
       }
       for (int e = tid; e < 2 * bs; e += kThreads) {
         p.dl[e] = 0;
-        p.dc[e] = 0;
+        p.dpc[e] = 0;
       }
     }
     __syncthreads();
@@ -1484,25 +1749,30 @@ cudaError_t prepare(void* fn, int* limit) {
 
 }  // namespace
 
+void sampler_geometry(int V, int elem, int* slice, int* ncr, int* ncd) {
+  const long long R = static_cast<long long>(V) * elem;
+  const long long sl = ((R + kNW - 1) / kNW + 15) / 16 * 16;
+  *slice = static_cast<int>(sl > 0 ? sl : 16);
+  *ncr = static_cast<int>((*slice + kChunk - 1) / kChunk);
+  *ncd = static_cast<int>((*slice + kHalf - 1) / kHalf);
+}
+
 SamplerWs sampler_ws_layout(int bs, int k_max, int V, int elem) {
   auto al = [](size_t v) { return (v + 255) & ~static_cast<size_t>(255); };
   const size_t rows_t = static_cast<size_t>(bs) * (k_max + 1);
   const size_t rows_d = static_cast<size_t>(bs) * k_max;
-  const size_t rb = static_cast<size_t>(V) * elem;
-  const size_t nseg = (rb + kSegBytes - 1) / kSegBytes;
-  const size_t nsub = (rb + kSubBytes - 1) / kSubBytes;
+  int slice, ncr, ncd;
+  sampler_geometry(V, elem, &slice, &ncr, &ncd);
   SamplerWs L;
-  L.seg_t = 0;
-  L.seg_d = al(L.seg_t + rows_t * nseg * sizeof(SegRec));
-  L.ps = al(L.seg_d + rows_d * nseg * sizeof(SegRec));
-  L.rs = al(L.ps + rows_t * sizeof(PairStat));
-  L.zero = al(L.rs + 2 * static_cast<size_t>(bs) * nsub * 8);
+  L.rst = 0;
+  L.rs = al(L.rst + (rows_t + rows_d) * sizeof(RowStat));
+  L.zero = al(L.rs + 2 * static_cast<size_t>(bs) * kNW * ncd * 8);
   L.pc = L.zero;
   L.st = al(L.pc + rows_t * 4);
   L.ev = al(L.st + static_cast<size_t>(bs) * 4);
   L.dl = al(L.ev + static_cast<size_t>(bs) * 4);
-  L.dc = al(L.dl + 2 * static_cast<size_t>(bs) * 4);
-  L.ctrl = al(L.dc + 2 * static_cast<size_t>(bs) * 4);
+  L.dpc = al(L.dl + 2 * static_cast<size_t>(bs) * 4);
+  L.ctrl = al(L.dpc + 2 * static_cast<size_t>(bs) * 4);
   L.total = al(L.ctrl + kCtlWords * 4);
   return L;
 }
@@ -1521,18 +1791,14 @@ cudaError_t choose_sampler_shape(int V, int elem, int bs, int blocks, bool vec,
   e = prepare(fn, &lim);
   if (e != cudaSuccess) return e;
   const size_t tables = (static_cast<size_t>(bs) * 4 + 127) & ~static_cast<size_t>(127);
-  if (tables + 4 * static_cast<size_t>(kSegBytes) > static_cast<size_t>(lim)) return cudaSuccess;
-  int nbuf = static_cast<int>((static_cast<size_t>(lim) - tables) / kSegBytes);
-  nbuf = std::min(nbuf, kMaxBufs);
-  // A consumer waits on its buffer's phase by parity, which is unambiguous
-  // only while no consumer can run a whole ring ahead of the producer.
-  if (nbuf < kNC + 2) return cudaSuccess;
-  // the ring also holds the request bins while the tables are built
-  if (static_cast<size_t>(nbuf) * kSegBytes < static_cast<size_t>(bs) * 4) return cudaSuccess;
-  out->nbuf = nbuf;
+  const size_t need = static_cast<size_t>(kNW) * 2 * kChunk + tables;
+  if (need > static_cast<size_t>(lim)) return cudaSuccess;
+  // the buffers also hold the request bins while the tables are built
+  if (static_cast<size_t>(kNW) * 2 * kChunk < static_cast<size_t>(bs) * 4) return cudaSuccess;
+  out->nbuf = 2 * kNW;
   out->threads = kThreads;
   out->blocks = blocks > 0 ? std::min(blocks, sms) : sms;
-  out->smem = static_cast<size_t>(nbuf) * kSegBytes + tables;
+  out->smem = need;
   out->vec = vec;
   *fits = true;
   return cudaSuccess;

@@ -110,9 +110,7 @@ sd_status verify_setup(const void* target_logits, const void* draft_logits, sd_d
   p.err = err_flag;
   p.flags = flags;
   p.wait_ns = 1000ull * static_cast<uint64_t>(wait_us > 0 ? wait_us : 1000000);
-  const size_t rb = static_cast<size_t>(V) * elem;
-  p.nseg = static_cast<int>((rb + kSegBytes - 1) / kSegBytes);
-  p.nsub = static_cast<int>((rb + kSubBytes - 1) / kSubBytes);
+  sampler_geometry(V, elem, &p.slice, &p.ncr, &p.ncd);
   exp_table(p.exp_tab);
   return SD_OK;
 }
@@ -124,7 +122,6 @@ sd_status verify_shape(VerifyCall* call) {
     return SD_ERR_CUDA;
   if (!fits)
     return refuse(SD_ERR_UNSUPPORTED, "bs=%d: the sampler's shared memory does not fit", call->p.bs);
-  call->p.nbuf = call->shape.nbuf;
   return SD_OK;
 }
 
@@ -132,15 +129,13 @@ void verify_bind(VerifyCall* call, void* workspace) {
   const SamplerWs L = sampler_ws_layout(call->p.bs, call->p.k_max, call->p.V, call->elem);
   char* b = static_cast<char*>(workspace);
   SamplerParams& p = call->p;
-  p.seg_t = reinterpret_cast<SegRec*>(b + L.seg_t);
-  p.seg_d = reinterpret_cast<SegRec*>(b + L.seg_d);
-  p.ps = reinterpret_cast<PairStat*>(b + L.ps);
+  p.rst = reinterpret_cast<RowStat*>(b + L.rst);
   p.rs = reinterpret_cast<unsigned long long*>(b + L.rs);
   p.pc = reinterpret_cast<int*>(b + L.pc);
   p.st = reinterpret_cast<int*>(b + L.st);
   p.ev = reinterpret_cast<int*>(b + L.ev);
   p.dl = reinterpret_cast<int*>(b + L.dl);
-  p.dc = reinterpret_cast<int*>(b + L.dc);
+  p.dpc = reinterpret_cast<int*>(b + L.dpc);
   p.ctrl = reinterpret_cast<int*>(b + L.ctrl);
 }
 

@@ -38,41 +38,34 @@ size_t plan_smem_bytes(const PlanParams& p);
 cudaError_t launch_plan(const PlanParams& p, cudaStream_t s);
 
 // ---------------------------------------------------------------- sampler
-// The sampling kernel cuts every logit row into segments of kSegBytes (one
-// bulk copy each) and every final draw's row(s) into sub-chunks of
-// kSubBytes per row (a target and a draft sub-chunk share one buffer).
+// The sampling kernel streams every logit row with all its streaming warps:
+// warp w takes bytes [w * slice, (w + 1) * slice) of the row, in chunks of
+// kSegBytes (one bulk copy each).  A final draw's row(s) are taken in
+// chunks of kSubBytes per row (a target and a draft chunk share a buffer).
 constexpr int kSegBytes = 8192;
 constexpr int kSubBytes = kSegBytes / 2;
-constexpr int kMaxRowBytes = 256 * kSegBytes;  // V * elem <= 2 MiB: at most 256 segments
+constexpr int kMaxRowBytes = 256 * kSegBytes;  // V * elem <= 2 MiB
+constexpr int kSamplerWarps = 12;              // streaming warps per CTA (plus one scheduler warp)
+constexpr int kDrawParts = 3;                  // a final draw's chunks are summed as this many units
 
-// Partial statistics of one segment of one row, 16 bytes.  Sampling rows:
-// m = NaN-propagating maximum, z = sum over the segment of
-// 2^((l - m) * log2(e) / tau) (fp64 bits in w2, w3).  Greedy rows: m = the
-// NaN-propagating maximum, w2 = lowest index of the maximum, w3 = 1 if the
-// segment holds NaN or +inf.  lx = the logit at the slot's draft token when
-// that token lies in the segment.
-struct __align__(16) SegRec {
-  float m, lx;
-  uint32_t w2, w3;
-};
-
-// Row statistics of one (request, slot) pair: the target row t_j and, for a
-// sampling slot, the draft row d_j.  Z = sum over the row of
-// 2^((l - M) * log2(e) / tau); amax = lowest argmax of t_j (greedy).
-struct __align__(16) PairStat {
-  float Mt, Md;
-  int amax, bad;
-  double Zt, Zd;
+// Statistics of one logit row, 32 bytes.  M = maximum, 1/Z as a
+// double-float (izh + izl) with Z = sum over the row of
+// 2^((l - M) * log2(e) / tau) (sampling rows), lx = the logit at the
+// slot's draft token, amax = lowest argmax (greedy rows), bad = the row
+// holds NaN or +inf or no finite value.
+struct __align__(16) RowStat {
+  float M, izh, izl, lx;
+  int amax, bad, r0, r1;
 };
 
 // Control words of one call (all zero between calls).
 enum {
-  kCtlRowBlk = 0,   // row blocks claimed
-  kCtlCtas = 1,     // CTAs finished
-  kCtlDraws = 2,    // final draws listed
-  kCtlDrawBlk = 3,  // draw blocks claimed
-  kCtlReqDone = 4,  // requests whose outputs are complete
-  kCtlStop = 5,     // a bounded wait gave up in this call
+  kCtlRow = 0,        // row units claimed
+  kCtlCtas = 1,       // CTAs finished
+  kCtlDraws = 2,      // final draws listed
+  kCtlDrawTaken = 3,  // listed draws claimed by a CTA
+  kCtlReqDone = 4,    // requests whose outputs are complete
+  kCtlStop = 5,       // a bounded wait gave up in this call
   kCtlWords = 8
 };
 
@@ -97,20 +90,18 @@ struct SamplerParams {
   int* err;
   int flags;
   uint64_t wait_ns;  // how long a device-side wait may last before it gives up
-  int nseg;          // segments per row
-  int nsub;          // draw sub-chunks per row
-  int nbuf;          // ring buffers per CTA
+  int slice;         // bytes of a row per streaming warp (a multiple of 16)
+  int ncr;           // row chunks per warp (at most)
+  int ncd;           // draw chunks per warp (at most)
   // workspace
-  SegRec* seg_t;              // [bs*(k_max+1)][nseg], by target row
-  SegRec* seg_d;              // [bs*k_max][nseg], by draft row
-  PairStat* ps;               // [bs*(k_max+1)] by pair i*(k_max+1)+j
-  unsigned long long* rs;     // [2*bs][nsub] sub-chunk sums of each listed draw
-  int* pc;                    // [bs*(k_max+1)] per pair: segments counted, plus
-                              //   skip items << 16                             (zero between calls)
+  RowStat* rst;               // [bs*(k_max+1) + bs*k_max]: target rows, then draft rows
+  unsigned long long* rs;     // [2*bs][kSamplerWarps][ncd] chunk sums of each listed draw
+  int* pc;                    // [bs*(k_max+1)] per pair: rows counted, plus
+                              //   skipped rows << 16                           (zero between calls)
   int* st;                    // [bs] slot decisions per request               (zero between calls)
   int* ev;                    // [bs] pair and final-token events per request  (zero between calls)
   int* dl;                    // [2*bs] listed draws                           (zero between calls)
-  int* dc;                    // [2*bs] sub-chunks counted per draw            (zero between calls)
+  int* dpc;                   // [2*bs] parts of each listed draw summed       (zero between calls)
   int* ctrl;                  // [kCtlWords]                                   (zero between calls)
   float2 exp_tab[16];         // 2^(j/16) as (hi, lo) pairs
 };
@@ -118,9 +109,11 @@ struct SamplerParams {
 // Workspace layout of the sampling kernel (each part 256-byte aligned); the
 // parts from `zero` on must be zero before a call and are left zero by it.
 struct SamplerWs {
-  size_t seg_t, seg_d, ps, rs, zero, pc, st, ev, dl, dc, ctrl, total;
+  size_t rst, rs, zero, pc, st, ev, dl, dpc, ctrl, total;
 };
 SamplerWs sampler_ws_layout(int bs, int k_max, int V, int elem);
+// Per-warp slice of a row and the chunk counts it gives.
+void sampler_geometry(int V, int elem, int* slice, int* ncr, int* ncd);
 
 struct SamplerShape {
   int blocks, threads, nbuf;
@@ -129,7 +122,7 @@ struct SamplerShape {
 };
 
 // Launch shape for (V, elem, bs) on the current device; *fits = false when the
-// ring does not fit.  `blocks` = 0 asks for one CTA per SM.
+// shared memory does not fit.  `blocks` = 0 asks for one CTA per SM.
 cudaError_t choose_sampler_shape(int V, int elem, int bs, int blocks, bool vec,
                                  SamplerShape* out, bool* fits);
 cudaError_t launch_sampler(const SamplerParams& p, int elem, const SamplerShape& shape,

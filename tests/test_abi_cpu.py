@@ -44,10 +44,10 @@ def test_abi_version_and_status_strings(lib):
 def test_workspace_sizes(lib):
     import speculative_decoding_verification_sd_gb300 as sd
     assert sd.sd_plan_workspace_bytes(256, 7) == 0
-    # at least one 16-byte record per 8 KB segment of every target and draft row
+    # at least a 32-byte statistics record per target and draft row, and the
+    # per-warp chunk sums of up to two final draws per request
     rows = 256 * 8 + 256 * 7
-    segs = -(-129280 * 2 // 8192)
-    assert sd.sd_verify_workspace_bytes(256, 7, 129280, sd.SD_BF16) >= rows * segs * 16
+    assert sd.sd_verify_workspace_bytes(256, 7, 129280, sd.SD_BF16) >= rows * 32 + 2 * 256 * 12 * 8
     assert sd.sd_verify_workspace_bytes(256, 7, 129280, sd.SD_F32) > \
         sd.sd_verify_workspace_bytes(256, 7, 129280, sd.SD_BF16)
     assert sd.sd_verify_workspace_bytes(0, 7, 1024, sd.SD_BF16) == 0
@@ -175,8 +175,8 @@ def test_noalloc_rejects_on_host(lib):
     assert call(0, 3) == sd.SD_ERR_INVALID_ARG
     assert call(4, 16) == sd.SD_ERR_UNSUPPORTED
     assert b"no error" not in lib.sd_last_error_string()
-    assert sd.sd_verify_workspace_bytes(4096, 15, 129280, sd.SD_BF16) > sd.SD_NOALLOC_SCRATCH_BYTES
-    assert call(4096, 15, 129280) == sd.SD_ERR_UNSUPPORTED
+    assert sd.sd_verify_workspace_bytes(4096, 15, 1 << 20, sd.SD_BF16) > sd.SD_NOALLOC_SCRATCH_BYTES
+    assert call(4096, 15, 1 << 20) == sd.SD_ERR_UNSUPPORTED
     assert b"static scratch" in lib.sd_last_error_string()
 
 

@@ -64,17 +64,17 @@ def test_small_every_launch_shape(dtype, V, blocks, flags, padded):
 
 def _ws_zero_offset(bs, k_max, V, elem):
     """Offset of the workspace part that must be zero between calls (the
-    layout of include/sd.h's sd_verify workspace: segment records of target
-    and draft rows, pair statistics, draw sums, then the counters; every part
-    256-byte aligned)."""
+    sd_verify workspace: a 32-byte statistics record per target and draft
+    row, then the chunk sums of up to two draws per request -- twelve
+    streaming warps, each with ceil(slice / 4 KB) chunks of a row slice of
+    ceil(V * elem / 12) bytes rounded up to 16 -- then the counters; every
+    part 256-byte aligned)."""
     al = lambda v: (v + 255) // 256 * 256
-    rb = V * elem
-    nseg, nsub = -(-rb // 8192), -(-rb // 4096)
     rows_t, rows_d = bs * (k_max + 1), bs * k_max
-    seg_d = al(rows_t * nseg * 16)
-    ps = al(seg_d + rows_d * nseg * 16)
-    rs = al(ps + rows_t * 32)
-    return al(rs + 2 * bs * nsub * 8)
+    sl = (-(-V * elem // 12) + 15) // 16 * 16
+    ncd = -(-sl // 4096)
+    rs = al((rows_t + rows_d) * 32)
+    return al(rs + 2 * bs * 12 * ncd * 8)
 
 
 def test_workspace_reuse_across_calls():

@@ -81,7 +81,7 @@ def test_noalloc_after_a_larger_batch():
 def test_noalloc_rejects_a_batch_beyond_the_scratch():
     """Refused on the host before any launch (the tensors below are too small
     for the sizes named: no kernel may ever run on them)."""
-    bs, k_max, V = 4096, 15, 129280
+    bs, k_max, V = 4096, 15, 1 << 20
     assert sd.sd_verify_workspace_bytes(bs, k_max, V, sd.SD_BF16) > sd.SD_NOALLOC_SCRATCH_BYTES
     dev = torch.device("cuda:0")
     x = torch.zeros(16, dtype=torch.int32, device=dev)
