@@ -59,6 +59,8 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-plan-graph", action="store_true",
                     help="skip the planner CUDA-graph timing (1000 launches)")
+    ap.add_argument("--no-detail", action="store_true",
+                    help="skip the per-workload blocks and the early-exit comparison")
     return ap.parse_args()
 
 
@@ -99,25 +101,28 @@ def hbm_peak():
 
 
 KERNEL_SOURCES = ("sampler.cu", "sd_device.cuh", "sd_internal.h")
+TRAFFIC = ROOT / "profiles" / "dram_traffic.json"
+
+
+def kernel_sources_hash():
+    import hashlib
+    src = ROOT / "speculative_decoding_verification_sd_gb300" / "csrc"
+    return hashlib.sha256(b"".join((src / n).read_bytes() for n in KERNEL_SOURCES)).hexdigest()[:16]
 
 
 def profiled_traffic(workload):
-    """DRAM bytes (read + write) per sampling launch from the committed ncu
-    summary of this workload, or None when the kernel sources have changed
-    since those counters were taken."""
-    import hashlib
-    import re
-    f = ROOT / "profiles" / f"verify_kernel_{workload}.md"
-    if not f.exists():
+    """DRAM bytes (read + write) per sampling launch, from the ncu capture
+    recorded in profiles/dram_traffic.json for this workload, or None when
+    the kernel sources have changed since those counters were taken (or no
+    capture exists)."""
+    try:
+        d = json.loads(TRAFFIC.read_text())
+    except (OSError, ValueError):
         return None
-    text = f.read_text()
-    mh = re.search(r"kernel_sources_sha256_16:\s*([0-9a-f]{16})", text)
-    mt = re.search(r"traffic_bytes_per_launch:\s*(\d+)", text)
-    if not mh or not mt:
+    e = d.get("workloads", {}).get(workload)
+    if not e or e.get("kernel_sources_sha256_16") != kernel_sources_hash():
         return None
-    src = ROOT / "speculative_decoding_verification_sd_gb300" / "csrc"
-    h = hashlib.sha256(b"".join((src / n).read_bytes() for n in KERNEL_SOURCES)).hexdigest()
-    return int(mt.group(1)) if h[:16] == mh.group(1) else None
+    return int(e["traffic_bytes_per_launch"])
 
 
 class ClockSampler:
@@ -340,6 +345,187 @@ def config_of(w):
 # GPU arm
 
 
+class GpuStep:
+    """One workload's step on the device: sd_plan + sd_verify on inputs
+    already resident in HBM (two input sets, each larger than L2, alternating
+    between steps), with the bytes the sampling stage must read."""
+
+    def __init__(self, w, seed, dev, stream, step=0):
+        import torch
+        import speculative_decoding_verification_sd_gb300 as sd
+        self.sd, self.torch, self.w, self.dev, self.stream = sd, torch, w, dev, stream
+        bs, k = w.bs, w.k_max
+        self.dtype = sd.SD_F32 if w.dtype == S.F32 else sd.SD_BF16
+        tdt = torch.float32 if w.dtype == S.F32 else torch.int16
+        self.rows_cap = bs * (k + 1)
+
+        def host(a, t):
+            return None if a is None else torch.from_numpy(np.ascontiguousarray(a, t))
+
+        pi = S.plan_inputs(w, seed, step)
+        self.pi = pi
+        self.d_lens = host(pi["draft_lens"], np.int32).to(dev)
+        self.d_conf = host(pi["conf"], np.float32).to(dev) if pi["conf"] is not None else None
+        self.d_cost = host(pi["cost"], np.float32).to(dev) if pi["cost"] is not None else None
+        self.cost_len = 0 if pi["cost"] is None else len(pi["cost"])
+        # the previous step's confidences and lengths, where the budget comes from them
+        self.d_bconf = host(pi["budget_conf"], np.float32).to(dev) if pi["budget_conf"] is not None else None
+        self.d_blens = host(pi["budget_draft_lens"], np.int32).to(dev) if pi["budget_draft_lens"] is not None else None
+        self.bs_budget = 0 if pi["budget_draft_lens"] is None else len(pi["budget_draft_lens"])
+        self.d_B = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.d_mask = torch.zeros((bs, max(k, 1)), dtype=torch.uint8, device=dev)
+        self.d_nv = torch.zeros(bs, dtype=torch.int32, device=dev)
+        self.d_cu = torch.zeros(bs + 1, dtype=torch.int32, device=dev)
+        self.d_err = torch.zeros(1, dtype=torch.int32, device=dev)
+        # The plan fixes the compacted layout the "target forward" would have
+        # produced; the logits rows are built in that layout.
+        self.plan()
+        torch.cuda.synchronize()
+        cu = self.d_cu.cpu().numpy()
+        self.cu = cu
+        self.n = np.diff(cu) - 1
+        t0 = time.perf_counter()
+        vi = S.verify_inputs(w, seed, step, cu, pi["draft_lens"])
+        self.gen_s = time.perf_counter() - t0
+        self.vi = vi
+        self.temps = vi["temps"]
+        self.B = int(cu[-1]) - bs
+        self.rows_t = int(cu[-1])
+        self.sets = []
+        for _ in range(2):
+            tgt = torch.empty((self.rows_cap, w.V), dtype=tdt, device=dev)
+            dft = torch.empty((max(bs * k, 1), w.V), dtype=tdt, device=dev)
+            tgt[: self.rows_t].copy_(torch.from_numpy(vi["target"].view(np.int16) if w.dtype == S.BF16 else vi["target"]))
+            if self.B > 0:
+                dft[: self.B].copy_(torch.from_numpy(vi["draft"].view(np.int16) if w.dtype == S.BF16 else vi["draft"]))
+            self.sets.append((tgt, dft))
+        self.d_ids = torch.zeros(max(bs * k, 1), dtype=torch.int32, device=dev)
+        if self.B > 0:
+            self.d_ids[: self.B] = torch.from_numpy(vi["draft_ids"]).to(dev)
+        self.d_u = torch.from_numpy(vi["uniforms"]).to(dev)
+        self.d_t = torch.from_numpy(self.temps).to(dev)
+        self.d_acc = torch.zeros(bs, dtype=torch.int32, device=dev)
+        self.d_out = torch.zeros((bs, k + 1), dtype=torch.int32, device=dev)
+        self.ws_bytes = sd.sd_verify_workspace_bytes(bs, k, w.V, self.dtype)
+        self.d_ws = sd.verify_workspace(bs, k, w.V, self.dtype, dev)
+
+    def plan(self, stream=None):
+        w = self.w
+        self.sd.sd_plan(self.d_conf, self.d_bconf, self.d_blens, self.bs_budget, self.d_lens, w.bs,
+                        w.k_max, self.d_cost,
+                        self.cost_len, w.T, w.mode, self.d_B, self.d_mask, self.d_nv, self.d_cu,
+                        self.d_err, None, 0, stream if stream is not None else self.stream)
+
+    def step(self, s, cfg, ev=None):
+        tgt, dft = self.sets[s & 1]
+        w = self.w
+        if ev:
+            ev[0].record(self.stream)
+        self.plan()
+        if ev:
+            ev[1].record(self.stream)
+        self.sd.sd_verify_ex(tgt, dft, self.dtype, w.V, self.d_ids, self.d_u, self.d_t, self.d_cu,
+                             w.bs, w.k_max, self.d_acc, self.d_out, None, self.d_err, self.d_ws,
+                             self.ws_bytes, cfg=cfg, stream=self.stream)
+        if ev:
+            ev[2].record(self.stream)
+
+    def run(self, steps, warmup, cfg, barrier=None):
+        """Times `steps` steps after `warmup`; returns (elapsed ms, per-step
+        plan ms, per-step verify ms)."""
+        torch = self.torch
+        for s in range(warmup):
+            self.step(s, cfg)
+        (barrier or torch.cuda.synchronize)()
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0.record(self.stream)
+        for s in range(steps):
+            self.step(s, cfg, evs[s])
+        t1.record(self.stream)
+        (barrier or torch.cuda.synchronize)()
+        return (t0.elapsed_time(t1), [e[0].elapsed_time(e[1]) for e in evs],
+                [e[1].elapsed_time(e[2]) for e in evs])
+
+    def bytes_alg(self):
+        """Algorithmic bytes of one sampling launch: every target row
+        (n_i + 1 of request i) and the draft rows of sampling requests, each
+        read once in full, plus the small inputs and outputs."""
+        w, n = self.w, self.n
+        sampled = self.temps > 0
+        rows_read = int((n + 1).sum() + n[sampled].sum())
+        small = ((w.bs + 1) * 4 + w.bs * 4 + self.B * 4 + w.bs * (w.k_max + 1) * 4 + w.bs * 4
+                 + w.bs * (w.k_max + 1) * 4 + 32 * rows_read)
+        return rows_read * w.V * w.elem + small, rows_read
+
+    def bytes_needed(self):
+        """Bytes of the rows a request needs once its first rejection is
+        known (early exit): target rows up to the accepted length, the draft
+        rows of the slots tested, from the outputs of the last step."""
+        w, n = self.w, self.n
+        acc = self.d_acc.cpu().numpy()
+        sampled = self.temps > 0
+        t_rows = int((np.minimum(acc, n) + 1).sum())
+        d_rows = int(np.minimum(acc + 1, n)[sampled].sum())
+        return (t_rows + d_rows) * w.V * w.elem, t_rows + d_rows
+
+    def free(self):
+        self.sets = None
+        self.d_ws = None
+        self.torch.cuda.empty_cache()
+
+
+def workload_block(gs, steps, warmup, cfg, peak, elapsed=None):
+    """ms per step, launch microseconds, algorithmic bytes and the roofline
+    fraction of one workload (its sampling kernel against the copy peak)."""
+    el, plan_ms, rows_ms = gs.run(steps, warmup, cfg) if elapsed is None else elapsed
+    bytes_alg, rows_read = gs.bytes_alg()
+    verify_us = 1e3 * statistics.median(rows_ms)
+    avg_ms = sum(rows_ms) / len(rows_ms)
+    return {"ms_per_step": el / steps, "verify_us_median": verify_us,
+            "plan_us_median": 1e3 * statistics.median(plan_ms), "bytes_alg_per_launch": bytes_alg,
+            "rows_read": rows_read, "achieved_gbs": bytes_alg / (avg_ms / 1e3) / 1e9,
+            "frac": bytes_alg / (avg_ms / 1e3) / 1e9 / peak,
+            "verified_draft_tokens_per_s": float(gs.n.sum()) * steps / (el / 1e3),
+            "device_err_flag": int(gs.d_err.item())}
+
+
+def detail_workloads(args, sd, dev, stream, peak):
+    """The other workloads, each timed the same way (fewer steps); varlen is
+    the mean over its 20 plan steps; early exit beside the all-rows kernel at
+    adaptive_hc and stress."""
+    out = {}
+    steps, warmup = 100, 5
+    for name in ("stress", "dense_fixed_k", "uniform_hc"):
+        w = S.WORKLOADS[name]
+        gs = GpuStep(w, args.seed, dev, stream)
+        blk = workload_block(gs, steps, warmup, {"blocks": args.blocks, "flags": 0}, peak)
+        if name == "stress":
+            ee = workload_block(gs, steps, warmup, {"blocks": args.blocks,
+                                                    "flags": sd.SD_VERIFY_EARLY_EXIT}, peak)
+            need, rows_need = gs.bytes_needed()
+            blk["early_exit"] = {"ms_per_step": ee["ms_per_step"], "verify_us_median": ee["verify_us_median"],
+                                 "bytes_needed_per_launch": need, "rows_needed": rows_need,
+                                 "speedup_vs_all_rows": blk["verify_us_median"] / ee["verify_us_median"]}
+        blk["config"] = config_of(w)
+        out[name] = blk
+        gs.free()
+    w = S.WORKLOADS["varlen_mixed"]
+    per = []
+    for step in range(20):
+        gs = GpuStep(w, args.seed, dev, stream, step=step)
+        per.append(workload_block(gs, 20, 3, {"blocks": args.blocks, "flags": 0}, peak))
+        gs.free()
+    out["varlen_mixed"] = {
+        "steps": 20, "ms_per_step": statistics.mean(b["ms_per_step"] for b in per),
+        "verify_us_mean": statistics.mean(b["verify_us_median"] for b in per),
+        "bytes_alg_per_launch_mean": statistics.mean(b["bytes_alg_per_launch"] for b in per),
+        "frac_mean": statistics.mean(b["frac"] for b in per),
+        "device_err_flags": sorted({b["device_err_flag"] for b in per}),
+        "config": config_of(w)}
+    return out
+
+
 def run_ours(args, w, rank, world, local):
     import torch
     import speculative_decoding_verification_sd_gb300 as sd
@@ -351,74 +537,10 @@ def run_ours(args, w, rank, world, local):
         dist.init_process_group("nccl", device_id=dev)
     seed = args.seed + 1000 * rank
     stream = torch.cuda.current_stream()
-    bs, k = w.bs, w.k_max
-    dtype = sd.SD_F32 if w.dtype == S.F32 else sd.SD_BF16
-    tdt = torch.float32 if w.dtype == S.F32 else torch.int16
-    rows_cap = bs * (k + 1)
-    elem = w.elem
-
-    def host(a, t):
-        return None if a is None else torch.from_numpy(np.ascontiguousarray(a, t))
-
-    pi = S.plan_inputs(w, seed, 0)
-    d_lens = host(pi["draft_lens"], np.int32).to(dev)
-    d_conf = host(pi["conf"], np.float32).to(dev) if pi["conf"] is not None else None
-    d_cost = host(pi["cost"], np.float32).to(dev) if pi["cost"] is not None else None
-    cost_len = 0 if pi["cost"] is None else len(pi["cost"])
-    d_B = torch.zeros(1, dtype=torch.int32, device=dev)
-    d_mask = torch.zeros((bs, max(k, 1)), dtype=torch.uint8, device=dev)
-    d_nv = torch.zeros(bs, dtype=torch.int32, device=dev)
-    d_cu = torch.zeros(bs + 1, dtype=torch.int32, device=dev)
-    d_err = torch.zeros(1, dtype=torch.int32, device=dev)
-
-    def plan_call():
-        sd.sd_plan(d_conf, None, None, 0, d_lens, bs, k, d_cost, cost_len, w.T, w.mode, d_B, d_mask,
-                   d_nv, d_cu, d_err, None, 0, stream)
-
-    # The plan of this batch fixes the compacted layout the "target forward"
-    # would have produced; build the logits rows in that layout.
-    plan_call()
-    torch.cuda.synchronize()
-    cu = d_cu.cpu().numpy()
-    n = np.diff(cu) - 1
-    t0 = time.perf_counter()
-    vi = S.verify_inputs(w, seed, 0, cu, pi["draft_lens"])
-    gen_s = time.perf_counter() - t0
-    temps = vi["temps"]
-    B = int(cu[-1]) - bs
-    rows_t = int(cu[-1])
-    sets = []
-    for _ in range(2):
-        tgt = torch.empty((rows_cap, w.V), dtype=tdt, device=dev)
-        dft = torch.empty((max(bs * k, 1), w.V), dtype=tdt, device=dev)
-        th = torch.from_numpy(vi["target"].view(np.int16) if w.dtype == S.BF16 else vi["target"])
-        dh = torch.from_numpy(vi["draft"].view(np.int16) if w.dtype == S.BF16 else vi["draft"])
-        tgt[:rows_t].copy_(th)
-        if B > 0:
-            dft[:B].copy_(dh)
-        sets.append((tgt, dft))
-    d_ids = torch.zeros(max(bs * k, 1), dtype=torch.int32, device=dev)
-    if B > 0:
-        d_ids[:B] = torch.from_numpy(vi["draft_ids"]).to(dev)
-    d_u = torch.from_numpy(vi["uniforms"]).to(dev)
-    d_t = torch.from_numpy(temps).to(dev)
-    d_acc = torch.zeros(bs, dtype=torch.int32, device=dev)
-    d_out = torch.zeros((bs, k + 1), dtype=torch.int32, device=dev)
-    ws_bytes = sd.sd_verify_workspace_bytes(bs, k, w.V, dtype)
-    d_ws = sd.verify_workspace(bs, k, w.V, dtype, dev)
     cfg = {"blocks": args.blocks, "flags": sd.SD_VERIFY_EARLY_EXIT if args.early_exit else 0}
-
-    def step(s, ev=None):
-        tgt, dft = sets[s & 1]
-        if ev:
-            ev[0].record(stream)
-        plan_call()
-        if ev:
-            ev[1].record(stream)
-        sd.sd_verify_ex(tgt, dft, dtype, w.V, d_ids, d_u, d_t, d_cu, bs, k, d_acc, d_out, None,
-                        d_err, d_ws, ws_bytes, cfg=cfg, stream=stream)
-        if ev:
-            ev[2].record(stream)
+    gs = GpuStep(w, seed, dev, stream)
+    bs, k = w.bs, w.k_max
+    n = gs.n
 
     def barrier():
         if world > 1:
@@ -427,43 +549,26 @@ def run_ours(args, w, rank, world, local):
         torch.cuda.synchronize()
 
     for s in range(args.warmup):
-        step(s)
+        gs.step(s, cfg)
     barrier()
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
-    t_start = torch.cuda.Event(enable_timing=True)
-    t_end = torch.cuda.Event(enable_timing=True)
     with ClockSampler(local) as clk:
         barrier()
         w0 = time.monotonic()
-        t_start.record(stream)
-        for s in range(args.steps):
-            step(s, evs[s])
-        t_end.record(stream)
-        barrier()
+        elapsed_ms, plan_ms, rows_ms = gs.run(args.steps, 0, cfg, barrier)
         clk.window(w0, time.monotonic())
-    elapsed_ms = t_start.elapsed_time(t_end)
-    plan_ms = [e[0].elapsed_time(e[1]) for e in evs]
-    rows_ms = [e[1].elapsed_time(e[2]) for e in evs]
-    err = int(d_err.item())
-    acc = d_acc.cpu().numpy()
+    err = int(gs.d_err.item())
+    acc = gs.d_acc.cpu().numpy()
 
-    # Work units and algorithmic bytes of one step.
     verified = int(n.sum())
-    sampled = temps > 0
-    rows_read = int((n + 1).sum() + n[sampled].sum())
-    bytes_rows = rows_read * w.V * elem
-    # small inputs and outputs: cu_seqlens, temps, draft ids, uniforms, accepted
-    # lengths and tokens, and the per-row statistics written and read back
-    bytes_small = ((bs + 1) * 4 + bs * 4 + B * 4 + bs * (k + 1) * 4 + bs * 4 + bs * (k + 1) * 4
-                   + 2 * 16 * rows_read)
-    bytes_alg = bytes_rows + bytes_small
+    sampled = gs.temps > 0
+    bytes_alg, rows_read = gs.bytes_alg()
     elapsed_ms, total_verified = reduce_over_ranks(elapsed_ms, verified, dev, world)
     value = whole_job_rate(total_verified, args.steps, elapsed_ms)
     rows_avg_ms = sum(rows_ms) / len(rows_ms)
     achieved = bytes_alg / (rows_avg_ms / 1e3) / 1e9
     peak, peak_kind = hbm_peak()
 
-    # Planner alone: one launch (events) and 1000 launches in a CUDA graph.
+    # Planner alone: 1000 launches in a CUDA graph.
     plan_graph_us = None
     try:
         if args.no_plan_graph:
@@ -472,13 +577,11 @@ def run_ours(args, w, rank, world, local):
         side = torch.cuda.Stream()
         side.wait_stream(stream)
         with torch.cuda.stream(side):
-            plan_call_s = lambda: sd.sd_plan(d_conf, None, None, 0, d_lens, bs, k, d_cost, cost_len,
-                                             w.T, w.mode, d_B, d_mask, d_nv, d_cu, d_err, None, 0, side)
-            plan_call_s()
+            gs.plan(side)
             torch.cuda.synchronize()
             with torch.cuda.graph(g, stream=side):
                 for _ in range(1000):
-                    plan_call_s()
+                    gs.plan(side)
         torch.cuda.synchronize()
         a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         g.replay()
@@ -491,19 +594,35 @@ def run_ours(args, w, rank, world, local):
     except Exception as ex:  # graph capture unsupported -> report the event time only
         print(f"# planner graph timing skipped: {ex}", file=sys.stderr)
 
+    # Early exit beside the all-rows kernel on the same inputs.
+    ee = None
+    if not args.early_exit and not args.no_detail:
+        ee_blk = workload_block(gs, min(args.steps, 200), 5,
+                                {"blocks": args.blocks, "flags": sd.SD_VERIFY_EARLY_EXIT}, peak)
+        need, rows_need = gs.bytes_needed()
+        ee = {"verify_us_median": ee_blk["verify_us_median"], "ms_per_step": ee_blk["ms_per_step"],
+              "bytes_needed_per_launch": need, "rows_needed": rows_need,
+              "speedup_vs_all_rows": (1e3 * statistics.median(rows_ms)) / ee_blk["verify_us_median"]}
+
     # End to end through the C ABI from pinned host buffers.
     e2e = None
     if not args.no_e2e:
-        e2e = run_e2e(args, w, sd, dev, stream, pi, vi, cu, ws_bytes, cfg, rows_cap)
+        e2e = run_e2e(args, w, sd, dev, stream, gs.pi, gs.vi, gs.cu, gs.ws_bytes, cfg, gs.rows_cap)
         if world > 1 and e2e is not None:
             e2e_ms, _ = reduce_over_ranks(e2e["_ms"], 0, dev, world)
             e2e["value"] = whole_job_rate(total_verified, args.steps, e2e_ms)
         if e2e is not None:
             e2e.pop("_ms", None)
 
+    workloads = None
+    if rank == 0 and not args.no_detail and args.workload == "adaptive_hc":
+        gs.free()
+        workloads = detail_workloads(args, sd, dev, stream, peak)
+
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
-        v, sample, _ = oracle_step(w, seed, pi, lambda c: vi, args.cpu_seconds)
+        vi = gs.vi
+        v, sample, _ = oracle_step(w, seed, gs.pi, lambda c: vi, args.cpu_seconds)
         cpu = {"value": v, "unit": "verified draft tokens/s", "cores": 1, "kind": "oracle",
                "sample": sample, "all_cores": all_cores_or_error(w, seed, args.cpu_seconds)}
 
@@ -519,7 +638,7 @@ def run_ours(args, w, rank, world, local):
         "data": "synthetic", "config": config_of(w),
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": profiled_traffic(w.name),
-                     "kernel": "verify_kernel (sd_verify)", "peak_kind": peak_kind,
+                     "kernel": "sampler_kernel (sd_verify)", "peak_kind": peak_kind,
                      "frac_of_nominal_8tbs": achieved / NOMINAL_HBM_GBS,
                      "bytes_per_launch": bytes_alg, "avg_launch_ms": rows_avg_ms},
         "cpu_baseline": cpu,
@@ -527,7 +646,7 @@ def run_ours(args, w, rank, world, local):
         "gpu_launches": 2 * args.steps,
         "clocks": clk.summary(),
         "detail": {
-            "B": B, "verified_draft_tokens_per_step": verified, "target_rows": rows_t,
+            "B": gs.B, "verified_draft_tokens_per_step": verified, "target_rows": gs.rows_t,
             "draft_rows_read": int(n[sampled].sum()), "bytes_alg_per_step": bytes_alg,
             "bytes_per_verified_token": bytes_alg / max(verified, 1),
             "plan_us_event": 1e3 * statistics.median(plan_ms),
@@ -537,8 +656,10 @@ def run_ours(args, w, rank, world, local):
             "emitted_tokens_per_s": (accepted + bs) * args.steps / (elapsed_ms / 1e3),
             "mean_acceptance_length": 1.0 + accepted / bs,
             "per_position_cumulative_acceptance": [round(x, 4) for x in pos],
-            "device_err_flag": err, "input_generation_s": gen_s,
-            "launch": sd.sd_verify_launch_info(w.V, dtype, bs, args.blocks, cfg["flags"]),
+            "device_err_flag": err, "input_generation_s": gs.gen_s,
+            "launch": sd.sd_verify_launch_info(w.V, gs.dtype, bs, args.blocks, cfg["flags"]),
+            "early_exit": ee,
+            "workloads": workloads,
         },
     }
     if rank == 0:

@@ -1292,14 +1292,10 @@ struct Sampler {
     last = __shfl_sync(kFull, last, 0);
     if (last) {
       __threadfence_block();
-      // the finish needs nothing more of the slot: release it first, so the
-      // scheduler can reuse it while this warp finishes the unit
+      // The slot is released only after the finish: a slot freed earlier
+      // lets the scheduler claim rows further ahead of the streaming warps,
+      // which measured slower (rows wait longer before they are decided).
       const uint4 r = (f.kind == kURow && lane < kNW) ? q_rec[slot * kNW + lane] : make_uint4(0u, 0u, 0u, 0u);
-      __syncwarp();
-      if (lane == 0) {
-        __threadfence_block();
-        q_fin[slot] = k;
-      }
       if (f.kind == kURow) {
         row_finish(r, f);
       } else {
@@ -1313,6 +1309,11 @@ struct Sampler {
           if (lane == 0) p.dpc[f.e] = 0;
           draw_finish(f);
         }
+      }
+      __syncwarp();
+      if (lane == 0) {
+        __threadfence_block();
+        q_fin[slot] = k;
       }
     }
   }
