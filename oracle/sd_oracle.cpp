@@ -24,7 +24,7 @@
 //     "추측 디코딩이란" gives its greedy form and "속도, 메모리, 정확도에 주는
 //     영향" (row 정확도) states that it preserves the target distribution).
 //
-// Readings adopted where the pages are silent (each is listed in the design doc):
+// Readings adopted where the pages are silent (labelled O1..O24 below):
 //   O1  acceptance estimate a = sigmoid(confidence logit)
 //   O2  survival = running product in position order, fp64, rounded to fp32
 //       to form the ranking key (the precision the kernel ranks in)
