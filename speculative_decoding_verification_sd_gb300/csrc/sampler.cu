@@ -497,12 +497,6 @@ __device__ __forceinline__ int settled(int s, int n) {
 // ---------------------------------------------------------------------------
 // The kernel.
 
-__device__ __forceinline__ uint64_t policy_evict_normal() {
-  uint64_t pol;
-  asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(pol));
-  return pol;
-}
-
 // One unit of the per-CTA queue.
 struct Unit {
   int kind;
@@ -618,8 +612,11 @@ struct Sampler {
   }
   __device__ uint64_t* bar_of(int g) const { return full + warp * 2 + (g & 1); }
 
-  // Lane 0: chunk c of unit f into buffer g & 1 (vector path only).
-  __device__ void issue(const UInfo& f, int c, int g, uint64_t pol_first, uint64_t pol_normal) const {
+  // Lane 0: chunk c of unit f into buffer g & 1 (vector path only).  Every
+  // row is copied evict-first: the final draws' second reads mostly miss L2
+  // anyway, and the small per-call data (the planner's inputs, the counters)
+  // then stays resident.
+  __device__ void issue(const UInfo& f, int c, int g, uint64_t pol_first) const {
     const int cb = f.kind == kURow ? kChunk : kHalf;
     const int off = sl_begin(warp) + (cbase(f, warp) + c) * cb;
     const uint32_t by = static_cast<uint32_t>(min(cb, sl_end(warp) - off));
@@ -627,7 +624,7 @@ struct Sampler {
     uint64_t* bar = bar_of(g);
     if (f.kind == kURow) {
       mbar_arrive_expect_tx(bar, by);
-      bulk_load(dst, f.src_t + off, by, bar, f.greedy ? pol_first : pol_normal);
+      bulk_load(dst, f.src_t + off, by, bar, pol_first);
     } else {
       mbar_arrive_expect_tx(bar, f.src_d ? 2 * by : by);
       bulk_load(dst, f.src_t + off, by, bar, pol_first);
@@ -1328,8 +1325,7 @@ struct Sampler {
   }
 
   __device__ void stream() const {
-    const uint64_t pol_first = policy_evict_first();    // rows read once, and draws
-    const uint64_t pol_normal = policy_evict_normal();  // sampling rows a draw may read again
+    const uint64_t pol_first = policy_evict_first();
     int ik = 0, ic = 0, gi = 0;  // issue cursor: position, its next chunk; chunks issued
     int ck = 0, cc = 0, gc = 0;  // compute cursor: position, its next chunk; chunks computed
     bool iend = false, fi_ok = false, fc_ok = false;
@@ -1361,7 +1357,7 @@ struct Sampler {
             fi_ok = false;
             continue;
           }
-          if (lane == 0) issue(fi, ic, gi, pol_first, pol_normal);
+          if (lane == 0) issue(fi, ic, gi, pol_first);
           ++ic;
           ++gi;
         }
