@@ -272,8 +272,9 @@ sd_status sd_verify_ex(const void* target_logits, const void* draft_logits, sd_d
  * then runs the sampling kernel on it.  Calls that overlap in time on one
  * device share the scratch and race: issue them on one stream, or order them.
  * Errors: SD_ERR_UNSUPPORTED when sd_verify_workspace_bytes(bs, k_max, V, dt)
- * exceeds SD_NOALLOC_SCRATCH_BYTES (about 1,900 requests at k_max = 7 and
- * V = 129280 bf16), with the reason in sd_last_error_string(); SD_ERR_CUDA
+ * exceeds SD_NOALLOC_SCRATCH_BYTES (every batch sd_verify accepts fits at
+ * V = 129280; at V = 2^20 bf16, about 1,900 requests at k_max = 7), with the
+ * reason in sd_last_error_string(); SD_ERR_CUDA
  * when the lookup or the clear fails; otherwise as sd_verify.
  * ---------------------------------------------------------------------- */
 #define SD_NOALLOC_SCRATCH_BYTES (16u << 20) /* 16 MiB */
@@ -286,7 +287,8 @@ sd_status sd_verify_noalloc(const void* target_logits, const void* draft_logits,
 
 /* Launch shape sd_verify_ex would use for (V, dt, bs) and `req` (NULL =
  * defaults) on the current device: CTAs in chosen->blocks, threads per CTA
- * and ring buffers in *threads and *buffers, dynamic shared memory in
+ * and chunk buffers per CTA (two per streaming warp) in *threads and
+ * *buffers, dynamic shared memory in
  * *smem_bytes (each output pointer may be NULL).  Host-only query. */
 sd_status sd_verify_launch_info(int V, sd_dtype dt, int bs, const sd_launch_cfg* req,
                                 sd_launch_cfg* chosen, int* threads, int* buffers,

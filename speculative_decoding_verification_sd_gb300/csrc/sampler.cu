@@ -414,17 +414,6 @@ __device__ __forceinline__ unsigned long long unit_fast(const DrawCtx& c, const 
   return fixed56(r[0]);
 }
 
-template <int VE>
-__device__ __forceinline__ unsigned long long unit_value(const DrawCtx& c, const float (&ft)[VE],
-                                                         const float (&fd)[VE], const float2* tab) {
-  uint32_t bm;
-  unsigned long long v = unit_fast<VE>(c, ft, fd, bm);
-#pragma unroll
-  for (int e = 0; e < VE; ++e)
-    if ((bm >> e) & 1u) v += elem_precise(c, ft[e], fd[e], tab);
-  return v;
-}
-
 // ---------------------------------------------------------------------------
 // Per-CTA context: the work-list tables built in the prologue.
 

@@ -38,27 +38,6 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t by
                : "memory");
 }
 
-__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(smem_addr(bar)), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-
-// Waits for the phase of `parity`; gives up after `limit` polls (each poll
-// may suspend the thread for a hardware-chosen interval).  Returns false on
-// time-out so the caller can raise SD_DEV_ERR_TIMEOUT and carry on.
-__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, uint32_t limit) {
-  for (uint32_t n = 0; n < limit; ++n)
-    if (mbar_try_wait(bar, parity)) return true;
-  return false;
-}
-
 // 4-byte asynchronous global -> shared copy (cp.async), tracked by the
 // issuing thread's later cp_async_arrive_noinc on an mbarrier.
 __device__ __forceinline__ void cp_async4(void* dst, const void* src) {
@@ -96,16 +75,6 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
       : "memory");
 }
 
-// Same, with the default L2 policy (the data stays in L2 for later reuse).
-__device__ __forceinline__ void bulk_load_nohint(void* dst, const void* src, uint32_t bytes,
-                                                 uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-          smem_addr(dst)),
-      "l"(src), "r"(bytes), "r"(smem_addr(bar))
-      : "memory");
-}
-
 // ---------------------------------------------------------------------------
 // Arithmetic helpers.
 
@@ -116,23 +85,10 @@ __device__ __forceinline__ float exp2_ftz(float x) {
   return y;
 }
 
-// 2^x on the special-function unit, subnormal results kept.
-__device__ __forceinline__ float exp2_full(float x) {
-  float y;
-  asm("ex2.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
-}
-
 // Monotone map of a non-NaN float onto uint32 (larger float -> larger key).
 __device__ __forceinline__ uint32_t ordered_bits(float f) {
   uint32_t u = __float_as_uint(f);
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-}
-
-__device__ __forceinline__ float warp_sum(float v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(kFull, v, o);
-  return v;
 }
 
 __device__ __forceinline__ float warp_max(float v) {
@@ -146,16 +102,6 @@ __device__ __forceinline__ unsigned long long warp_max_u64(unsigned long long v)
   for (int o = 16; o > 0; o >>= 1) {
     unsigned long long w = __shfl_xor_sync(kFull, v, o);
     v = w > v ? w : v;
-  }
-  return v;
-}
-
-// Inclusive prefix sum across the warp, lane order.
-__device__ __forceinline__ float warp_inclusive_scan(float v, int lane) {
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    float t = __shfl_up_sync(kFull, v, o);
-    if (lane >= o) v += t;
   }
   return v;
 }

@@ -47,7 +47,7 @@ constexpr int kSubBytes = kSegBytes / 2;
 constexpr int kMaxRowBytes = 256 * kSegBytes;  // V * elem <= 2 MiB
 constexpr int kSamplerWarps = 12;              // streaming warps per CTA (plus one scheduler warp)
 constexpr int kDrawParts = 1;                  // a final draw's chunks are summed as this many units
-                                               // (more parts measured slower: see the queue note in sampler.cu)
+                                               // (splitting a draw into more parts measured slower)
 
 // Statistics of one logit row, 32 bytes.  M = maximum, 1/Z as a
 // double-float (izh + izl) with Z = sum over the row of
