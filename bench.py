@@ -643,7 +643,7 @@ def run_ours(args, w, rank, world, local):
                      "bytes_per_launch": bytes_alg, "avg_launch_ms": rows_avg_ms},
         "cpu_baseline": cpu,
         "e2e": e2e,
-        "gpu_launches": 2 * args.steps,
+        "gpu_launches": 2 * args.steps,  # sd_plan and sd_verify per step
         "clocks": clk.summary(),
         "detail": {
             "B": gs.B, "verified_draft_tokens_per_step": verified, "target_rows": gs.rows_t,

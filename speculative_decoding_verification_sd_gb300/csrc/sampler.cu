@@ -1440,33 +1440,13 @@ struct Sampler {
     int taken_seen = 0;
   };
 
-  // The next unit for the queue: parts of listed draws, else rows in slot
-  // order; END once every request's outputs are in (or a wait gave up).
+  // The next unit for the queue: rows in slot order, else parts of listed
+  // draws; END once every request's outputs are in (or a wait gave up).
   __device__ Unit claim(Sched& S) const {
     uint64_t idle_end = 0;
     for (;;) {
       if (*stop) return Unit{kUEnd, 0, 0, 0};
-      // parts of listed draws first: a request's last step
-      const int nd = ld_relaxed(p.ctrl + kCtlDraws);
-      if (S.held < 0 && S.taken_seen < nd * kDrawParts) {
-        S.held = atomicAdd(p.ctrl + kCtlDrawTaken, 1);  // a part of a draw
-        S.taken_seen = S.held + 1;
-        if (S.held >= 2 * p.bs * kDrawParts) S.held = -1;  // past the draw list (never listed)
-      }
-      if (S.held >= 0 && S.held / kDrawParts < nd) {
-        const int e = S.held / kDrawParts;
-        int code = ld_acquire(p.dl + e);
-        for (const uint64_t end = now_ns() + p.wait_ns; code == 0 && now_ns() <= end;)
-          code = ld_acquire(p.dl + e);
-        if (code == 0) {
-          halt();
-          return Unit{kUEnd, 0, 0, 0};
-        }
-        const Unit u{kUDraw, e, code, S.held - e * kDrawParts};
-        S.held = -1;
-        return u;
-      }
-      // then rows in slot order
+      // rows in slot order first: every decision, and so every draw, waits on them
       while (!S.rows_done) {
         const int rb = S.rb_next;
         if (rb < 0 || rb >= C.U || (p.flags & kFlagTestStall)) {
@@ -1485,6 +1465,26 @@ struct Sampler {
         }
         const long long row = L.isd ? drow_of(p, L.i, L.j) : trow_of(p, L.i, L.j);
         return Unit{kURow, L.i | (L.j << 12) | (L.isd << 16), static_cast<int>(row), 0};
+      }
+      // then parts of listed draws
+      const int nd = ld_relaxed(p.ctrl + kCtlDraws);
+      if (S.held < 0 && S.taken_seen < nd * kDrawParts) {
+        S.held = atomicAdd(p.ctrl + kCtlDrawTaken, 1);  // a part of a draw
+        S.taken_seen = S.held + 1;
+        if (S.held >= 2 * p.bs * kDrawParts) S.held = -1;  // past the draw list (never listed)
+      }
+      if (S.held >= 0 && S.held / kDrawParts < nd) {
+        const int e = S.held / kDrawParts;
+        int code = ld_acquire(p.dl + e);
+        for (const uint64_t end = now_ns() + p.wait_ns; code == 0 && now_ns() <= end;)
+          code = ld_acquire(p.dl + e);
+        if (code == 0) {
+          halt();
+          return Unit{kUEnd, 0, 0, 0};
+        }
+        const Unit u{kUDraw, e, code, S.held - e * kDrawParts};
+        S.held = -1;
+        return u;
       }
       if (ld_acquire(p.ctrl + kCtlReqDone) >= p.bs) return Unit{kUEnd, 0, 0, 0};
       const uint64_t t = now_ns();
