@@ -16,14 +16,17 @@
 // draw.  Streaming warp w copies its own slice of the unit's row(s) with
 // bulk copies into two buffers of its own (the next chunk lands while the
 // current one is reduced, across unit boundaries) and reduces each chunk to
-// softmax statistics or an argmax.  The last warp to finish a row combines
-// the twelve partials and counts the row into its (request, slot) pair; the
-// row that completes a pair takes the slot's accept decision, and the
-// decision that settles a request lists the request's final draw.  A draw is
-// a unit like a row: every warp sums its slice's inverse-CDF weights in
-// exact 64-bit fixed point, and the last one finds the crossing chunk and
-// walks it.  With SD_VERIFY_EARLY_EXIT the scheduler drops rows of slots
-// after a request's settled first rejection before they are streamed.
+// softmax statistics or an argmax.  A finishing warp takes the units in
+// order once all twelve have counted their part: it combines a row's
+// partials and counts the row into its (request, slot) pair; the row that
+// completes a pair takes the slot's accept decision, and the decision that
+// settles a request lists the request's final draw.  A draw is a unit like a
+// row: every streaming warp sums its slice's inverse-CDF weights in exact
+// 64-bit fixed point, and the finishing warp finds the crossing chunk and
+// walks it.  The finish's global round trips (atomics, statistics loads) so
+// stay off the streaming warps.  With SD_VERIFY_EARLY_EXIT the scheduler
+// drops rows of slots after a request's settled first rejection before they
+// are streamed.
 //
 // Precision.  Row statistics use the hardware base-2 exponent on an argument
 // d * s2 with d = l - m exact and s2 = log2(e)/tau carried in two floats; the
@@ -47,7 +50,8 @@ namespace sdk {
 namespace {
 
 constexpr int kNW = kSamplerWarps;         // streaming warps per CTA
-constexpr int kThreads = (kNW + 1) * 32;   // + the scheduler warp
+constexpr int kFin = kFinishWarps;         // finishing warps per CTA
+constexpr int kThreads = (kNW + 1 + kFin) * 32;  // + the scheduler warp
 constexpr int kQ = 4;                      // positions of the per-CTA unit queue
 constexpr int kChunk = kSegBytes;          // bytes of a row chunk (one bulk copy)
 constexpr int kHalf = kSubBytes;           // bytes per row of a draw chunk
@@ -520,6 +524,7 @@ struct Sampler {
   volatile int* q_seq; // [kQ] position published in each slot
   volatile int* q_fin; // [kQ] position whose unit is complete in each slot
   int* q_cnt;          // [kQ] streaming warps done with the slot's position (grows by kNW a use)
+  volatile int* q_end; // position of the END unit once published (else INT_MAX)
   uint4* q_rec;        // [kQ][kNW] per-warp partial statistics of a row unit
   unsigned char* bufs; // [kNW][2][kChunk]
   unsigned short* heavy;  // [kNW][kHeavyList] heavy elements of a draw chunk
@@ -804,7 +809,7 @@ struct Sampler {
   }
 
   // ---- row unit complete: combine the warps' partials ---------------------
-  // Called by the last streaming warp to finish the unit; writes the row's
+  // Called by the finishing warp once every part is in; writes the row's
   // statistics and counts the row into its pair.
   // r = warp `lane`'s record (lanes < kNW), read before the slot was released.
   __device__ void row_finish(const uint4 r, const UInfo& f) const {
@@ -1251,8 +1256,8 @@ struct Sampler {
     return ok;
   }
 
-  // Warp w's part of position k is done: its record (row units), the count,
-  // and, by the last warp, the unit's finish.
+  // Warp w's part of position k is done: its record (row units) and the
+  // count the finishing warp waits on.
   __device__ void finalize(int k, const UInfo& f, const Part& P) const {
     const int slot = k % kQ;
     if (lane == 0) {
@@ -1269,20 +1274,67 @@ struct Sampler {
       } else {
         __threadfence();  // the chunk sums, read back through L2 by the finishing warp
       }
-    }
-    int last = 0;
-    if (lane == 0) {
       __threadfence_block();
-      last = (atomicAdd(q_cnt + slot, 1) % kNW) == kNW - 1;
+      atomicAdd(q_cnt + slot, 1);
     }
-    last = __shfl_sync(kFull, last, 0);
-    if (last) {
+    __syncwarp();
+  }
+
+  // ---- finishing warps ---------------------------------------------------------
+  // Finishing warp f takes positions f, f + kFin, ... in order: once every
+  // streaming warp has counted its part, it finishes the unit (a row's
+  // statistics and its pair; a draw's threshold and walk) and releases the
+  // slot.  The streaming warps never wait on these global round trips.
+  __device__ void finish_units(int f0) const {
+    for (int k = f0;; k += kFin) {
+      const int slot = k % kQ;
+      // position k published, or END published before it
+      int ok = 1;
+      if (lane == 0 && q_seq[slot] != k) {
+        const uint64_t end = now_ns() + p.wait_ns;
+        for (;;) {
+          if (q_seq[slot] == k) break;
+          if (*q_end < k || *stop) {
+            ok = 0;
+            break;
+          }
+          if (now_ns() > end) {
+            ok = -1;
+            break;
+          }
+          __nanosleep(64);
+        }
+      }
+      ok = __shfl_sync(kFull, ok, 0);
+      if (ok < 0) halt();
+      if (ok <= 0) break;
       __threadfence_block();
-      // The slot is released only after the finish: a slot freed earlier
-      // lets the scheduler claim rows further ahead of the streaming warps,
-      // which measured slower (rows wait longer before they are decided).
-      const uint4 r = (f.kind == kURow && lane < kNW) ? q_rec[slot * kNW + lane] : make_uint4(0u, 0u, 0u, 0u);
+      __syncwarp();
+      const Unit u = q_ent[slot];
+      if (u.kind == kUEnd) break;
+      const UInfo f = info(u);
+      // every streaming warp done with position k
+      if (lane == 0) {
+        const int need = kNW * (k / kQ + 1);
+        volatile int* cnt = q_cnt + slot;
+        const uint64_t end = now_ns() + p.wait_ns;
+        while (*cnt < need) {
+          if (*stop || now_ns() > end) {
+            ok = 0;
+            break;
+          }
+          __nanosleep(32);
+        }
+      }
+      ok = __shfl_sync(kFull, ok, 0);
+      if (!ok) {
+        halt();
+        break;
+      }
+      __threadfence_block();
+      __syncwarp();
       if (f.kind == kURow) {
+        const uint4 r = lane < kNW ? q_rec[slot * kNW + lane] : make_uint4(0u, 0u, 0u, 0u);
         row_finish(r, f);
       } else {
         int parts = 0;
@@ -1517,6 +1569,7 @@ struct Sampler {
       if (!ok) halt();
       const Unit u = ok ? claim(S) : Unit{kUEnd, 0, 0, 0};
       q_ent[slot] = u;
+      if (u.kind == kUEnd) *q_end = k;  // finishing warps waiting on later positions leave
       __threadfence_block();
       q_seq[slot] = k;
       if (u.kind == kUEnd) break;
@@ -1533,7 +1586,7 @@ __global__ void __launch_bounds__(kThreads, 1) sampler_kernel(const __grid_const
   __shared__ Unit s_ent[kQ];
   __shared__ int s_seq[kQ], s_fin[kQ], s_cnt[kQ];
   __shared__ uint4 s_rec[kQ * kNW];
-  __shared__ int s_stop, s_last;
+  __shared__ int s_stop, s_last, s_end;
   __shared__ int s_hist[32], s_base[32];
   __shared__ int s_WS[SD_MAX_K + 3], s_P[SD_MAX_K + 2], s_E[SD_MAX_K + 2];
   __shared__ float2 s_tab[16];
@@ -1546,7 +1599,10 @@ __global__ void __launch_bounds__(kThreads, 1) sampler_kernel(const __grid_const
   // the buffers double as scratch for the request lengths while the tables are built
   int* nscr = reinterpret_cast<int*>(smem);  // [bs] bin of request i
 
-  if (tid == 0) s_stop = 0;
+  if (tid == 0) {
+    s_stop = 0;
+    s_end = INT_MAX;
+  }
   if (tid < 32) s_hist[tid] = 0;
   if (tid < kQ) {
     s_seq[tid] = -1;
@@ -1647,15 +1703,17 @@ __global__ void __launch_bounds__(kThreads, 1) sampler_kernel(const __grid_const
   C.U = s_WS[K1];
   C.tab = s_tab;
 
-  Sampler<T, VEC> S{p, C, s_ent, s_seq, s_fin, s_cnt, s_rec, bufs, s_heavy, s_full, &s_stop, lane, warp,
-                    p.V * static_cast<int>(sizeof(T))};
+  Sampler<T, VEC> S{p, C, s_ent, s_seq, s_fin, s_cnt, &s_end, s_rec, bufs, s_heavy, s_full, &s_stop,
+                    lane, warp, p.V * static_cast<int>(sizeof(T))};
   if (warp < kNW) {
     S.stream();
-  } else {
+  } else if (warp == kNW) {
     if (lane == 0) S.schedule();
     // The CTA barrier below is warp-aligned: the scheduler warp reaches it
     // converged.
     __syncwarp();
+  } else {
+    S.finish_units(warp - kNW - 1);
   }
 
   // ---- the last CTA out resets the call's control words (and, after a

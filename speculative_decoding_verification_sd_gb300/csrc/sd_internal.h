@@ -46,6 +46,7 @@ constexpr int kSegBytes = 8192;
 constexpr int kSubBytes = kSegBytes / 2;
 constexpr int kMaxRowBytes = 256 * kSegBytes;  // V * elem <= 2 MiB
 constexpr int kSamplerWarps = 12;              // streaming warps per CTA (plus one scheduler warp)
+constexpr int kFinishWarps = 1;                // warps that finish the CTA's units (rows, draws)
 constexpr int kDrawParts = 1;                  // a final draw's chunks are summed as this many units
                                                // (splitting a draw into more parts measured slower)
 
