@@ -272,17 +272,18 @@ struct ET<float> {
 
 // Unit q (elements [q*VE, q*VE+VE)) of a region of n elements that starts at
 // `src`: the staged shared-memory copy (vector path, n a multiple of VE), a
-// global row read through L2 (`l2`), or single elements of a global row
-// (element path; positions >= n read as -inf).
+// global row read through the read-only path (`gmem`; the walk's re-reads of
+// one chunk then hit L1), or single elements of a global row (element path;
+// positions >= n read as -inf).
 template <typename T, bool VEC>
-__device__ __forceinline__ void load_unit(const void* src, int q, int n, bool l2,
+__device__ __forceinline__ void load_unit(const void* src, int q, int n, bool gmem,
                                           float (&f)[ET<T>::VE]) {
   using E = ET<T>;
   if constexpr (VEC) {
     const typename E::V* v = static_cast<const typename E::V*>(src) + q;
-    if (l2) {
-      if constexpr (sizeof(T) == 2) E::unpack(__ldcg(reinterpret_cast<const uint4*>(v)), f);
-      else E::unpack(__ldcg(reinterpret_cast<const float4*>(v)), f);
+    if (gmem) {
+      if constexpr (sizeof(T) == 2) E::unpack(__ldg(reinterpret_cast<const uint4*>(v)), f);
+      else E::unpack(__ldg(reinterpret_cast<const float4*>(v)), f);
     } else {
       E::unpack(*v, f);
     }
@@ -293,7 +294,7 @@ __device__ __forceinline__ void load_unit(const void* src, int q, int n, bool l2
       const int k = q * E::VE + e;
       f[e] = k < n ? E::ldg(src, k) : -INFINITY;
     }
-    (void)l2;
+    (void)gmem;
   }
 }
 
@@ -772,27 +773,11 @@ struct Sampler {
     if (lane == 0) p.accepted_len[i] = a;
   }
 
-  // One event of request i (a pair decided or skipped, or the final
-  // token); the last of its n + 2 events resets the request's words for the
-  // next call.  Called by one thread.
-  __device__ static void event1(const SamplerParams& q, int i, int n) {
-    const int old = atom_add_acq_rel(q.ev + i, 1);
-    if (old + 1 == n + 2) {
-      q.st[i] = 0;
-      q.ev[i] = 0;
-    }
-  }
-
-  __device__ static void red_release_add(int* q, int v) {
-    asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(q), "r"(v) : "memory");
-  }
-
-  __device__ void request_done(int i, int n) const {
+  // Request i's outputs are all written: counted for the schedulers' end
+  // test (the outputs themselves are read only after the kernel).
+  __device__ void request_done() const {
     __syncwarp();
-    if (lane == 0) {
-      red_release_add(p.ctrl + kCtlReqDone, 1);
-      event1(p, i, n);
-    }
+    if (lane == 0) atomicAdd(p.ctrl + kCtlReqDone, 1);
   }
 
   __device__ void list_draw(int i, int a, int kind) const {
@@ -886,6 +871,7 @@ struct Sampler {
     const bool has_d = !greedy && j < n;
     const int pid = i * (p.k_max + 1) + j;
     int bits = 0;
+    int tam = -1, tbad = 0, dbad = 0;  // slot j's argmax and bad flags, for settle
     if (!skipped && lane == 0) {
       RowStat t, d;
       *reinterpret_cast<uint4*>(&t) = __ldcg(reinterpret_cast<const uint4*>(tstat(i, j)));
@@ -900,6 +886,9 @@ struct Sampler {
         *(reinterpret_cast<uint4*>(&d) + 1) = __ldcg(reinterpret_cast<const uint4*>(dstat(i, j)) + 1);
       }
       const int bad = t.bad | d.bad;
+      tam = t.amax;
+      tbad = t.bad;
+      dbad = d.bad;
       int x = -1;
       bool x_ok = false;
       if (j < n) {
@@ -945,24 +934,36 @@ struct Sampler {
     bits = __shfl_sync(kFull, bits, 0);
     const int now = settled(old | bits, n);
     const bool settles = bits && settled(old, n) < 0 && now >= 0;
-    if (settles) settle(i, n, now, greedy);
-    if (lane == 0) event1(p, i, n);
+    if (settles) {
+      tam = __shfl_sync(kFull, tam, 0);
+      tbad = __shfl_sync(kFull, tbad, 0);
+      dbad = __shfl_sync(kFull, dbad, 0);
+      settle(i, n, now, greedy, j, tam, tbad | (has_d ? dbad : 0));
+    }
   }
 
   // Request i has its accepted length a: write the outputs, or list its draw.
-  __device__ void settle(int i, int n, int a, bool greedy) const {
-    const uint4 t1 = __ldcg(reinterpret_cast<const uint4*>(tstat(i, a)) + 1);
-    int bad = static_cast<int>(t1.y);
-    if (!greedy && a < n) bad |= static_cast<int>(__ldcg(reinterpret_cast<const uint4*>(dstat(i, a)) + 1).y);
+  // The pair (i, j) that settled it passes its rows' argmax and bad flags,
+  // used when a == j (the usual case) instead of reloading them.
+  __device__ void settle(int i, int n, int a, bool greedy, int j, int jamax, int jbad) const {
+    int bad, amax;
+    if (a == j) {
+      bad = jbad;
+      amax = jamax;
+    } else {
+      const uint4 t1 = __ldcg(reinterpret_cast<const uint4*>(tstat(i, a)) + 1);
+      bad = static_cast<int>(t1.y);
+      if (!greedy && a < n) bad |= static_cast<int>(__ldcg(reinterpret_cast<const uint4*>(dstat(i, a)) + 1).y);
+      amax = static_cast<int>(t1.x);
+    }
     if (greedy) {
-      const int amax = static_cast<int>(t1.x);
       write_prefix(i, a, bad || amax < 0 ? 0 : amax, true);
-      request_done(i, n);
+      request_done();
       return;
     }
     if (bad) {  // flagged already; a well-formed token
       write_prefix(i, a, 0, true);
-      request_done(i, n);
+      request_done();
       return;
     }
     write_prefix(i, a, 0, false);
@@ -1051,20 +1052,34 @@ struct Sampler {
       p.out_tokens[static_cast<size_t>(i) * (p.k_max + 1) + a] = y;
       p.dl[e] = 0;
     }
-    request_done(i, n);
+    request_done();
   }
 
   // Draw unit complete (every warp's chunk sums are in): threshold
   // floor(u * S), the crossing chunk, then the walk of its units and elements.
-  __device__ void draw_finish(const UInfo& f) const {
+  __device__ void draw_finish(const UInfo& f, const DrawCtx& dcx, float u) const {
     const int e = f.e, i = f.i, a = f.a, kind = f.dkind, n = f.n;
     const unsigned long long* rs = p.rs + static_cast<size_t>(e) * kNW * p.ncd;
     const int total = kNW * p.ncd;
     const int spl = (total + 31) / 32;
     const int b0 = min(total, lane * spl), b1 = min(total, b0 + spl);
+    // lane's chunk sums (chunks past a warp's slice weigh 0): held in
+    // registers when they fit, so the crossing search below reloads nothing
+    constexpr int kHeld = 8;
+    const bool held = spl <= kHeld;
+    unsigned long long hv[kHeld];
     unsigned long long ls = 0ull;
-    for (int q = b0; q < b1; ++q)
-      if (q % p.ncd < nchunks(kUDraw, q / p.ncd)) ls += __ldcg(rs + q);
+    if (held) {
+#pragma unroll
+      for (int t = 0; t < kHeld; ++t) {
+        const int q = b0 + t;
+        hv[t] = (q < b1 && q % p.ncd < nchunks(kUDraw, q / p.ncd)) ? __ldcg(rs + q) : 0ull;
+        ls += hv[t];
+      }
+    } else {
+      for (int q = b0; q < b1; ++q)
+        if (q % p.ncd < nchunks(kUDraw, q / p.ncd)) ls += __ldcg(rs + q);
+    }
     unsigned long long inc = ls;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -1072,7 +1087,6 @@ struct Sampler {
       if (lane >= o) inc += t;
     }
     const unsigned long long S = __shfl_sync(kFull, inc, 31);
-    const float u = p.uniforms[static_cast<size_t>(i) * (p.k_max + 1) + p.k_max];
     if (lane == 0 && !(u >= 0.0f && u < 1.0f)) raise_error(p.err, SD_DEV_ERR_UNIFORM);
     if (S == 0ull) {
       if (kind == kDrawResid) {  // no residual mass in fp32: draw from p of the same row
@@ -1095,13 +1109,28 @@ struct Sampler {
     if (lane == L) {
       cq = b1 - 1;
       unsigned long long run = before;
-      for (int q = b0; q < b1; ++q) {
-        const unsigned long long v = q % p.ncd < nchunks(kUDraw, q / p.ncd) ? __ldcg(rs + q) : 0ull;
-        if (run + v > th) {
-          cq = q;
-          break;
+      if (held) {
+        bool found = false;
+#pragma unroll
+        for (int t = 0; t < kHeld; ++t) {
+          if (!found && b0 + t < b1) {
+            if (run + hv[t] > th) {
+              cq = b0 + t;
+              found = true;
+            } else {
+              run += hv[t];
+            }
+          }
         }
-        run += v;
+      } else {
+        for (int q = b0; q < b1; ++q) {
+          const unsigned long long v = q % p.ncd < nchunks(kUDraw, q / p.ncd) ? __ldcg(rs + q) : 0ull;
+          if (run + v > th) {
+            cq = q;
+            break;
+          }
+          run += v;
+        }
       }
       before = run;
     }
@@ -1110,7 +1139,7 @@ struct Sampler {
     const int w = cq / p.ncd, cc = cq % p.ncd;
     const int off = sl_begin(w) + cc * kHalf;
     const int n_el = min(kHalf, sl_end(w) - off) / static_cast<int>(sizeof(T));
-    const int y = walk(draw_ctx(i, a, kind), i, a, off / static_cast<int>(sizeof(T)), n_el, th - before);
+    const int y = walk(dcx, i, a, off / static_cast<int>(sizeof(T)), n_el, th - before);
     finish_token(e, i, n, a, y);
   }
 
@@ -1156,8 +1185,8 @@ struct Sampler {
 #pragma unroll
       for (int t = 0; t < 4; ++t) {
         const int k = kk[t] < 0 ? 0 : kk[t];
-        const float lt = VEC ? E::at(tb, k) : E::ldg(tb, k);
-        const float ld = c.resid ? (VEC ? E::at(db, k) : E::ldg(db, k)) : 0.0f;
+        const float lt = E::ldg(tb, k);
+        const float ld = c.resid ? E::ldg(db, k) : 0.0f;
         const unsigned long long pv = elem_precise(c, lt, ld, C.tab);
 #pragma unroll
         for (int u2 = 0; u2 < kUPL; ++u2) v[u2] += ku[t] == u2 ? pv : 0ull;
@@ -1313,6 +1342,13 @@ struct Sampler {
       const Unit u = q_ent[slot];
       if (u.kind == kUEnd) break;
       const UInfo f = info(u);
+      // a draw's statistics and uniform, loaded while its chunks are summed
+      DrawCtx dcx{};
+      float du = 0.0f;
+      if (f.kind == kUDraw) {
+        dcx = draw_ctx(f.i, f.a, f.dkind);
+        du = p.uniforms[static_cast<size_t>(f.i) * (p.k_max + 1) + p.k_max];
+      }
       // every streaming warp done with position k
       if (lane == 0) {
         const int need = kNW * (k / kQ + 1);
@@ -1336,6 +1372,8 @@ struct Sampler {
       if (f.kind == kURow) {
         const uint4 r = lane < kNW ? q_rec[slot * kNW + lane] : make_uint4(0u, 0u, 0u, 0u);
         row_finish(r, f);
+      } else if constexpr (kDrawParts == 1) {
+        draw_finish(f, dcx, du);  // every chunk sum came from this CTA's warps
       } else {
         int parts = 0;
         if (lane == 0) {
@@ -1345,7 +1383,7 @@ struct Sampler {
         parts = __shfl_sync(kFull, parts, 0);
         if (parts == kDrawParts) {
           if (lane == 0) p.dpc[f.e] = 0;
-          draw_finish(f);
+          draw_finish(f, dcx, du);
         }
       }
       __syncwarp();
@@ -1479,10 +1517,7 @@ struct Sampler {
     const int total = (!greedy && j < n) ? 2 : 1;
     const int add = 1 + (1 << 16);
     const int now = atom_add_acq_rel(p.pc + pid, add) + add;
-    if ((now & 0xFFFF) == total) {
-      p.pc[pid] = 0;
-      event1(p, i, n);
-    }
+    if ((now & 0xFFFF) == total) p.pc[pid] = 0;
   }
 
   struct Sched {
@@ -1726,12 +1761,11 @@ __global__ void __launch_bounds__(kThreads, 1) sampler_kernel(const __grid_const
   __syncthreads();
   if (s_last) {
     __threadfence();
+    for (int i = tid; i < bs; i += kThreads) p.st[i] = 0;  // the requests' decision words
     if (ld_acquire(p.ctrl + kCtlStop)) {
       const int pairs = bs * K1;
       for (int q = tid; q < pairs; q += kThreads) p.pc[q] = 0;
       for (int i = tid; i < bs; i += kThreads) {
-        p.st[i] = 0;
-        p.ev[i] = 0;
         p.accepted_len[i] = 0;
         for (int j = 0; j < K1; ++j)
           p.out_tokens[static_cast<size_t>(i) * K1 + j] = j == 0 ? 0 : -1;
@@ -1813,8 +1847,7 @@ SamplerWs sampler_ws_layout(int bs, int k_max, int V, int elem) {
   L.zero = al(L.rs + 2 * static_cast<size_t>(bs) * kNW * ncd * 8);
   L.pc = L.zero;
   L.st = al(L.pc + rows_t * 4);
-  L.ev = al(L.st + static_cast<size_t>(bs) * 4);
-  L.dl = al(L.ev + static_cast<size_t>(bs) * 4);
+  L.dl = al(L.st + static_cast<size_t>(bs) * 4);
   L.dpc = al(L.dl + 2 * static_cast<size_t>(bs) * 4);
   L.ctrl = al(L.dpc + 2 * static_cast<size_t>(bs) * 4);
   L.total = al(L.ctrl + kCtlWords * 4);

@@ -133,7 +133,6 @@ void verify_bind(VerifyCall* call, void* workspace) {
   p.rs = reinterpret_cast<unsigned long long*>(b + L.rs);
   p.pc = reinterpret_cast<int*>(b + L.pc);
   p.st = reinterpret_cast<int*>(b + L.st);
-  p.ev = reinterpret_cast<int*>(b + L.ev);
   p.dl = reinterpret_cast<int*>(b + L.dl);
   p.dpc = reinterpret_cast<int*>(b + L.dpc);
   p.ctrl = reinterpret_cast<int*>(b + L.ctrl);

@@ -101,7 +101,6 @@ struct SamplerParams {
   int* pc;                    // [bs*(k_max+1)] per pair: rows counted, plus
                               //   skipped rows << 16                           (zero between calls)
   int* st;                    // [bs] slot decisions per request               (zero between calls)
-  int* ev;                    // [bs] pair and final-token events per request  (zero between calls)
   int* dl;                    // [2*bs] listed draws                           (zero between calls)
   int* dpc;                   // [2*bs] parts of each listed draw summed       (zero between calls)
   int* ctrl;                  // [kCtlWords]                                   (zero between calls)
@@ -111,7 +110,7 @@ struct SamplerParams {
 // Workspace layout of the sampling kernel (each part 256-byte aligned); the
 // parts from `zero` on must be zero before a call and are left zero by it.
 struct SamplerWs {
-  size_t rst, rs, zero, pc, st, ev, dl, dpc, ctrl, total;
+  size_t rst, rs, zero, pc, st, dl, dpc, ctrl, total;
 };
 SamplerWs sampler_ws_layout(int bs, int k_max, int V, int elem);
 // Per-warp slice of a row and the chunk counts it gives.
