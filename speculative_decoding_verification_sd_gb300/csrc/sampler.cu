@@ -10,14 +10,14 @@
 //   tau = 0: accept iff x_j == argmax p_j; the correction/bonus is the argmax.
 //
 // Design (GB300).  One persistent CTA per SM: a scheduler warp claims units
-// of work into a small queue in shared memory, and twelve streaming warps
+// of work into a small queue in shared memory, and sixteen streaming warps
 // take every unit together.  A unit is one logit row (claimed in slot order,
 // "waves": slot j's rows of every request before slot j + 1's) or one final
 // draw.  Streaming warp w copies its own slice of the unit's row(s) with
 // bulk copies into two buffers of its own (the next chunk lands while the
 // current one is reduced, across unit boundaries) and reduces each chunk to
 // softmax statistics or an argmax.  A finishing warp takes the units in
-// order once all twelve have counted their part: it combines a row's
+// order once all sixteen have counted their part: it combines a row's
 // partials and counts the row into its (request, slot) pair; the row that
 // completes a pair takes the slot's accept decision, and the decision that
 // settles a request lists the request's final draw.  A draw is a unit like a
@@ -512,6 +512,16 @@ struct UInfo {
   int x;              // row unit of a slot j < n: the slot's draft token (else -1)
 };
 
+// A published unit as the scheduler decoded it: the unit, its exponent
+// scale (sampling rows), a draw's context and uniform.  The scheduler runs
+// ahead of the streaming warps, so their global loads leave the critical path.
+struct QInfo {
+  UInfo f;
+  float s2h, s2l;
+  DrawCtx dc;
+  float du;
+};
+
 template <typename T, bool VEC>
 struct Sampler {
   using E = ET<T>;
@@ -526,6 +536,7 @@ struct Sampler {
   volatile int* q_fin; // [kQ] position whose unit is complete in each slot
   int* q_cnt;          // [kQ] streaming warps done with the slot's position (grows by kNW a use)
   volatile int* q_end; // position of the END unit once published (else INT_MAX)
+  QInfo* q_inf;        // [kQ] the decoded unit of each published position
   uint4* q_rec;        // [kQ][kNW] per-warp partial statistics of a row unit
   unsigned char* bufs; // [kNW][2][kChunk]
   unsigned short* heavy;  // [kNW][kHeavyList] heavy elements of a draw chunk
@@ -1341,14 +1352,9 @@ struct Sampler {
       __syncwarp();
       const Unit u = q_ent[slot];
       if (u.kind == kUEnd) break;
-      const UInfo f = info(u);
-      // a draw's statistics and uniform, loaded while its chunks are summed
-      DrawCtx dcx{};
-      float du = 0.0f;
-      if (f.kind == kUDraw) {
-        dcx = draw_ctx(f.i, f.a, f.dkind);
-        du = p.uniforms[static_cast<size_t>(f.i) * (p.k_max + 1) + p.k_max];
-      }
+      const UInfo f = q_inf[slot].f;
+      const DrawCtx dcx = q_inf[slot].dc;
+      const float du = q_inf[slot].du;
       // every streaming warp done with position k
       if (lane == 0) {
         const int need = kNW * (k / kQ + 1);
@@ -1427,7 +1433,7 @@ struct Sampler {
               iend = true;
               break;
             }
-            fi = info(u);
+            fi = q_inf[ik % kQ].f;
             fi_ok = true;
             ic = 0;
           }
@@ -1449,14 +1455,16 @@ struct Sampler {
         }
         const Unit u = q_ent[ck % kQ];
         if (u.kind == kUEnd) break;
-        fc = info(u);
+        const QInfo& qi = q_inf[ck % kQ];
+        fc = qi.f;
         fc_ok = true;
         cc = 0;
         P = fresh_part();
         if (fc.kind == kURow) {
-          if (!fc.greedy) scale_of(fc.tau, s2h, s2l);
+          s2h = qi.s2h;
+          s2l = qi.s2l;
         } else {
-          dctx = draw_ctx(fc.i, fc.a, fc.dkind);
+          dctx = qi.dc;
         }
       }
       if (cc < ucount(fc, warp)) {
@@ -1603,6 +1611,20 @@ struct Sampler {
       }
       if (!ok) halt();
       const Unit u = ok ? claim(S) : Unit{kUEnd, 0, 0, 0};
+      if (u.kind != kUEnd) {
+        QInfo qi;
+        qi.f = info(u);
+        qi.s2h = qi.s2l = 0.0f;
+        qi.dc = DrawCtx{};
+        qi.du = 0.0f;
+        if (qi.f.kind == kURow) {
+          if (!qi.f.greedy) scale_of(qi.f.tau, qi.s2h, qi.s2l);
+        } else {
+          qi.dc = draw_ctx(qi.f.i, qi.f.a, qi.f.dkind);
+          qi.du = p.uniforms[static_cast<size_t>(qi.f.i) * (p.k_max + 1) + p.k_max];
+        }
+        q_inf[slot] = qi;
+      }
       q_ent[slot] = u;
       if (u.kind == kUEnd) *q_end = k;  // finishing warps waiting on later positions leave
       __threadfence_block();
@@ -1619,6 +1641,7 @@ __global__ void __launch_bounds__(kThreads, 1) sampler_kernel(const __grid_const
   extern __shared__ __align__(128) unsigned char smem[];
   __shared__ uint64_t s_full[kNW * 2];
   __shared__ Unit s_ent[kQ];
+  __shared__ QInfo s_inf[kQ];
   __shared__ int s_seq[kQ], s_fin[kQ], s_cnt[kQ];
   __shared__ uint4 s_rec[kQ * kNW];
   __shared__ int s_stop, s_last, s_end;
@@ -1738,8 +1761,8 @@ __global__ void __launch_bounds__(kThreads, 1) sampler_kernel(const __grid_const
   C.U = s_WS[K1];
   C.tab = s_tab;
 
-  Sampler<T, VEC> S{p, C, s_ent, s_seq, s_fin, s_cnt, &s_end, s_rec, bufs, s_heavy, s_full, &s_stop,
-                    lane, warp, p.V * static_cast<int>(sizeof(T))};
+  Sampler<T, VEC> S{p, C, s_ent, s_seq, s_fin, s_cnt, &s_end, s_inf, s_rec, bufs, s_heavy, s_full,
+                    &s_stop, lane, warp, p.V * static_cast<int>(sizeof(T))};
   if (warp < kNW) {
     S.stream();
   } else if (warp == kNW) {

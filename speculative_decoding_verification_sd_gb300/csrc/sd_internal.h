@@ -42,10 +42,13 @@ cudaError_t launch_plan(const PlanParams& p, cudaStream_t s);
 // warp w takes bytes [w * slice, (w + 1) * slice) of the row, in chunks of
 // kSegBytes (one bulk copy each).  A final draw's row(s) are taken in
 // chunks of kSubBytes per row (a target and a draft chunk share a buffer).
-constexpr int kSegBytes = 8192;
+// kSubBytes is a multiple of 512: a lane's share of a draw chunk is a whole
+// number of 16-byte units.  Sixteen warps, each with two 6 KB buffers,
+// hide more latency than twelve with 8 KB ones (measured).
+constexpr int kSegBytes = 6144;
 constexpr int kSubBytes = kSegBytes / 2;
-constexpr int kMaxRowBytes = 256 * kSegBytes;  // V * elem <= 2 MiB
-constexpr int kSamplerWarps = 12;              // streaming warps per CTA (plus one scheduler warp)
+constexpr int kMaxRowBytes = 2 << 20;          // V * elem <= 2 MiB
+constexpr int kSamplerWarps = 16;              // streaming warps per CTA (plus one scheduler warp)
 constexpr int kFinishWarps = 1;                // warps that finish the CTA's units (rows, draws)
 constexpr int kDrawParts = 1;                  // a final draw's chunks are summed as this many units
                                                // (splitting a draw into more parts measured slower)

@@ -47,7 +47,7 @@ def test_workspace_sizes(lib):
     # at least a 32-byte statistics record per target and draft row, and the
     # per-warp chunk sums of up to two final draws per request
     rows = 256 * 8 + 256 * 7
-    assert sd.sd_verify_workspace_bytes(256, 7, 129280, sd.SD_BF16) >= rows * 32 + 2 * 256 * 12 * 8
+    assert sd.sd_verify_workspace_bytes(256, 7, 129280, sd.SD_BF16) >= rows * 32 + 2 * 256 * 16 * 8
     assert sd.sd_verify_workspace_bytes(256, 7, 129280, sd.SD_F32) > \
         sd.sd_verify_workspace_bytes(256, 7, 129280, sd.SD_BF16)
     assert sd.sd_verify_workspace_bytes(0, 7, 1024, sd.SD_BF16) == 0

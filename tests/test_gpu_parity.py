@@ -65,16 +65,16 @@ def test_small_every_launch_shape(dtype, V, blocks, flags, padded):
 def _ws_zero_offset(bs, k_max, V, elem):
     """Offset of the workspace part that must be zero between calls (the
     sd_verify workspace: a 32-byte statistics record per target and draft
-    row, then the chunk sums of up to two draws per request -- twelve
-    streaming warps, each with ceil(slice / 4 KB) chunks of a row slice of
-    ceil(V * elem / 12) bytes rounded up to 16 -- then the counters; every
+    row, then the chunk sums of up to two draws per request -- sixteen
+    streaming warps, each with ceil(slice / 3 KB) chunks of a row slice of
+    ceil(V * elem / 16) bytes rounded up to 16 -- then the counters; every
     part 256-byte aligned)."""
     al = lambda v: (v + 255) // 256 * 256
     rows_t, rows_d = bs * (k_max + 1), bs * k_max
-    sl = (-(-V * elem // 12) + 15) // 16 * 16
-    ncd = -(-sl // 4096)
+    sl = (-(-V * elem // 16) + 15) // 16 * 16
+    ncd = -(-sl // 3072)
     rs = al((rows_t + rows_d) * 32)
-    return al(rs + 2 * bs * 12 * ncd * 8)
+    return al(rs + 2 * bs * 16 * ncd * 8)
 
 
 def test_workspace_reuse_across_calls():
