@@ -673,7 +673,9 @@ struct Sampler {
   }
 
   // One chunk of a row unit: n_el elements at src (staged copy or global
-  // row), e0 = the chunk's first element in the row.
+  // row), e0 = the chunk's first element in the row.  Lane-private: each
+  // lane folds its own elements into its running partial (no shuffle here);
+  // the warp combines its lanes once per unit (unit_record).
   __device__ void row_chunk(const void* src, int n_el, int e0, const UInfo& f, float s2h, float s2l,
                             Part& P) const {
     const int nu = (n_el + VE - 1) / VE;
@@ -711,63 +713,111 @@ struct Sampler {
         }
         bad |= (vm != vm) | (vm == INFINITY);
       }
-      unsigned long long key = bidx == INT_MAX ? 0ull
+      const unsigned long long key = bidx == INT_MAX ? 0ull
           : (static_cast<unsigned long long>(ordered_bits(best)) << 32) |
                 static_cast<unsigned long long>(0xFFFFFFFFu - static_cast<uint32_t>(e0 + bidx));
-      key = warp_max_u64(key);
       P.key = max(P.key, key);
-      P.bad |= __any_sync(kFull, bad);
+      P.bad |= bad;
       return;
     }
-    float vm = -INFINITY;
-    for (int q = lane; q < nu; q += 32) {
-      if constexpr (VEC) {
-        vm = fmax_nan(vm, E::vmax_nan(static_cast<const typename E::V*>(src)[q]));
-      } else {
-        float fv[VE];
-        load_unit<T, false>(src, q, n_el, false, fv);
+    // four units per step, each with its own dependency chain
+    const int nq = nu > lane ? (nu - lane + 31) / 32 : 0;  // units q = lane + 32 t, t < nq
+    float cm4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+    {
+      int t = 0;
+      for (; t + 4 <= nq; t += 4) {
 #pragma unroll
-        for (int k = 0; k < VE; ++k) vm = fmax_nan(vm, fv[k]);
+        for (int u = 0; u < 4; ++u) cm4[u] = fmax_nan(cm4[u], unit_max(src, lane + 32 * (t + u), n_el));
       }
+      for (; t < nq; ++t) cm4[0] = fmax_nan(cm4[0], unit_max(src, lane + 32 * t, n_el));
     }
-    const float mc = warp_max_nan(vm);
+    const float cm = fmax_nan(fmax_nan(cm4[0], cm4[1]), fmax_nan(cm4[2], cm4[3]));
     if (f.x >= e0 && f.x < e0 + n_el && lane == 0) {
       if constexpr (VEC) P.lx = E::at(src, f.x - e0);
       else P.lx = E::ldg(src, f.x - e0);
     }
-    if (!(mc == mc) || mc == INFINITY) {  // NaN or +inf: the row is bad
+    if (!(cm == cm) || cm == INFINITY) {  // NaN or +inf: the row is bad
       P.bad = 1;
       return;
     }
-    if (mc == -INFINITY) return;  // nothing finite in this chunk
-    float ks = 0.0f, kc = 0.0f;
-    for (int q = lane; q < nu; q += 32) {
-      float fv[VE];
-      load_unit<T, VEC>(src, q, n_el, false, fv);
-      float2 acc = make_float2(0.0f, 0.0f);
+    if (P.bad || cm == -INFINITY) return;  // nothing finite in the lane's part
+    if (cm > P.m) {  // the lane's reference maximum rises: rescale its sum
+      if (P.m != -INFINITY) rescale(P.zh, P.zl, P.m, cm, s2h, s2l);
+      P.m = cm;
+    }
+    const float m = P.m;
+    // the lane's compensated sum, continued, and a second chain beside it
+    float ks = P.zh, kc = P.zl, ks2 = 0.0f, kc2 = 0.0f;
+    int t = 0;
+    for (; t + 4 <= nq; t += 4) {
+      float a[4];
 #pragma unroll
-      for (int k = 0; k < VE; k += 2) {
-        const float2 d = __fadd2_rn(make_float2(fv[k], fv[k + 1]), make_float2(-mc, -mc));
-        const float2 t = __ffma2_rn(d, make_float2(s2h, s2h), __fmul2_rn(d, make_float2(s2l, s2l)));
-        acc = __fadd2_rn(acc, make_float2(exp2_ftz(t.x), exp2_ftz(t.y)));
-      }
-      comp_add(ks, kc, __fadd_rn(acc.x, acc.y));
+      for (int u = 0; u < 4; ++u) a[u] = unit_exp_sum(src, lane + 32 * (t + u), n_el, m, s2h, s2l);
+      comp_add(ks, kc, __fadd_rn(a[0], a[1]));
+      comp_add(ks2, kc2, __fadd_rn(a[2], a[3]));
     }
-    float zh, zl;
-    fast_two_sum(ks, kc, zh, zl);
-    warp_sum_ff(zh, zl);
-    if (P.m == -INFINITY) {
-      P.m = mc;
-      P.zh = zh;
-      P.zl = zl;
-    } else if (mc > P.m) {
-      rescale(P.zh, P.zl, P.m, mc, s2h, s2l);
-      ff_add(P.zh, P.zl, zh, zl, P.zh, P.zl);
-      P.m = mc;
+    for (; t < nq; ++t) comp_add(ks, kc, unit_exp_sum(src, lane + 32 * t, n_el, m, s2h, s2l));
+    fast_two_sum(ks, kc, ks, kc);
+    if (ks2 > 0.0f) {
+      fast_two_sum(ks2, kc2, ks2, kc2);
+      ff_add(ks, kc, ks2, kc2, ks, kc);
+    }
+    P.zh = ks;
+    P.zl = kc;
+  }
+
+  // Maximum (NaN-propagating) of unit q of a chunk.
+  __device__ __forceinline__ float unit_max(const void* src, int q, int n_el) const {
+    if constexpr (VEC) {
+      (void)n_el;
+      return E::vmax_nan(static_cast<const typename E::V*>(src)[q]);
     } else {
-      rescale(zh, zl, mc, P.m, s2h, s2l);
-      ff_add(P.zh, P.zl, zh, zl, P.zh, P.zl);
+      float fv[VE];
+      load_unit<T, false>(src, q, n_el, false, fv);
+      float vm = fv[0];
+#pragma unroll
+      for (int k = 1; k < VE; ++k) vm = fmax_nan(vm, fv[k]);
+      return vm;
     }
+  }
+
+  // fp32 sum of 2^((l - m) s2) over unit q's elements (pairs in fp32x2).
+  __device__ __forceinline__ float unit_exp_sum(const void* src, int q, int n_el, float m, float s2h,
+                                                float s2l) const {
+    float fv[VE];
+    load_unit<T, VEC>(src, q, n_el, false, fv);
+    float2 acc = make_float2(0.0f, 0.0f);
+#pragma unroll
+    for (int k = 0; k < VE; k += 2) {
+      const float2 d = __fadd2_rn(make_float2(fv[k], fv[k + 1]), make_float2(-m, -m));
+      const float2 t = __ffma2_rn(d, make_float2(s2h, s2h), __fmul2_rn(d, make_float2(s2l, s2l)));
+      acc = __fadd2_rn(acc, make_float2(exp2_ftz(t.x), exp2_ftz(t.y)));
+    }
+    return __fadd_rn(acc.x, acc.y);
+  }
+
+  // The warp's record of a row unit from its lanes' partials (warp-wide):
+  // greedy rows the best key and the bad flag; sampling rows the maximum
+  // (NaN when a lane saw NaN or +inf), the double-float sum relative to it,
+  // and the draft token's logit (lane 0).
+  __device__ uint4 unit_record(const UInfo& f, const Part& P, float s2h, float s2l) const {
+    const int bad = __any_sync(kFull, P.bad != 0);
+    if (f.greedy) {
+      const unsigned long long key = warp_max_u64(P.key);
+      return make_uint4(static_cast<uint32_t>(key), static_cast<uint32_t>(key >> 32),
+                        static_cast<uint32_t>(bad), 0u);
+    }
+    const float M = warp_max(P.m);
+    float zh = 0.0f, zl = 0.0f;
+    if (!bad && P.m != -INFINITY) {
+      zh = P.zh;
+      zl = P.zl;
+      fast_two_sum(zh, zl, zh, zl);
+      if (P.m != M) rescale(zh, zl, P.m, M, s2h, s2l);
+    }
+    warp_sum_ff(zh, zl);
+    return make_uint4(__float_as_uint(bad ? NAN : M), __float_as_uint(zh), __float_as_uint(zl),
+                      __float_as_uint(P.lx));
   }
 
   // ---- outputs and per-request bookkeeping --------------------------------
@@ -1298,18 +1348,12 @@ struct Sampler {
 
   // Warp w's part of position k is done: its record (row units) and the
   // count the finishing warp waits on.
-  __device__ void finalize(int k, const UInfo& f, const Part& P) const {
+  __device__ void finalize(int k, const UInfo& f, const Part& P, float s2h, float s2l) const {
     const int slot = k % kQ;
+    uint4 r = make_uint4(0u, 0u, 0u, 0u);
+    if (f.kind == kURow) r = unit_record(f, P, s2h, s2l);
     if (lane == 0) {
       if (f.kind == kURow) {
-        uint4 r;
-        if (f.greedy) {
-          r = make_uint4(static_cast<uint32_t>(P.key), static_cast<uint32_t>(P.key >> 32),
-                         static_cast<uint32_t>(P.bad), 0u);
-        } else {
-          r = make_uint4(__float_as_uint(P.bad ? NAN : P.m), __float_as_uint(P.zh),
-                         __float_as_uint(P.zl), __float_as_uint(P.lx));
-        }
         q_rec[slot * kNW + warp] = r;
       } else {
         __threadfence();  // the chunk sums, read back through L2 by the finishing warp
@@ -1500,7 +1544,7 @@ struct Sampler {
         ++cc;
         continue;
       }
-      finalize(ck, fc, P);
+      finalize(ck, fc, P, s2h, s2l);
       ++ck;
       fc_ok = false;
     }
