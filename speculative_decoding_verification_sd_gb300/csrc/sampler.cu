@@ -428,6 +428,8 @@ struct Cta {
   const int* Pj;     // [nw] sampling requests with n > j
   const int* Ej;     // [nw] sampling requests with n == j
   int nsamp, nw, U;
+  int dshift;         // a final draw is split into 1 << dshift units (the same in every CTA)
+  int dper;           // draw chunks per warp in one part: ceil(ncd >> dshift)
   const float2* tab;  // shared-memory copy of the exponent table
 };
 
@@ -496,7 +498,7 @@ struct Unit {
   int kind;
   int a;  // row: i | j << 12 | draft << 16;  draw: the draw's index e
   int b;  // row: the row's index;  draw: its list entry 1 + (i << 6 | a << 2 | kind)
-  int c;  // draw: which of its kDrawParts parts
+  int c;  // draw: which of its 1 << C.dshift parts
 };
 
 // What a streaming warp needs of a unit.
@@ -562,13 +564,11 @@ struct Sampler {
   // part takes its share of every warp's draw chunks).
   __device__ int cbase(const UInfo& f, int w) const {
     if (f.kind == kURow) return 0;
-    const int per = (p.ncd + kDrawParts - 1) / kDrawParts;
-    return min(f.part * per, nchunks(kUDraw, w));
+    return min(f.part * C.dper, nchunks(kUDraw, w));
   }
   __device__ int ucount(const UInfo& f, int w) const {
     if (f.kind == kURow) return nchunks(kURow, w);
-    const int per = (p.ncd + kDrawParts - 1) / kDrawParts;
-    return min((f.part + 1) * per, nchunks(kUDraw, w)) - cbase(f, w);
+    return min((f.part + 1) * C.dper, nchunks(kUDraw, w)) - cbase(f, w);
   }
 
   __device__ void halt() const {
@@ -1422,19 +1422,20 @@ struct Sampler {
       if (f.kind == kURow) {
         const uint4 r = lane < kNW ? q_rec[slot * kNW + lane] : make_uint4(0u, 0u, 0u, 0u);
         row_finish(r, f);
-      } else if constexpr (kDrawParts == 1) {
-        draw_finish(f, dcx, du);  // every chunk sum came from this CTA's warps
       } else {
-        int parts = 0;
-        if (lane == 0) {
-          __threadfence();
-          parts = atom_add_acq_rel(p.dpc + f.e, 1) + 1;
+        // one part: every chunk sum came from this CTA's warps; two parts:
+        // the second part to finish (in either CTA) walks the draw
+        bool last = true;
+        if (C.dshift) {
+          int parts = 0;
+          if (lane == 0) {
+            __threadfence();
+            parts = atom_add_acq_rel(p.dpc + f.e, 1) + 1;
+            if (parts == 2) p.dpc[f.e] = 0;
+          }
+          last = __shfl_sync(kFull, parts, 0) == 2;
         }
-        parts = __shfl_sync(kFull, parts, 0);
-        if (parts == kDrawParts) {
-          if (lane == 0) p.dpc[f.e] = 0;
-          draw_finish(f, dcx, du);
-        }
+        if (last) draw_finish(f, dcx, du);
       }
       __syncwarp();
       if (lane == 0) {
@@ -1607,13 +1608,13 @@ struct Sampler {
       }
       // then parts of listed draws
       const int nd = ld_relaxed(p.ctrl + kCtlDraws);
-      if (S.held < 0 && S.taken_seen < nd * kDrawParts) {
+      if (S.held < 0 && S.taken_seen < (nd << C.dshift)) {
         S.held = atomicAdd(p.ctrl + kCtlDrawTaken, 1);  // a part of a draw
         S.taken_seen = S.held + 1;
-        if (S.held >= 2 * p.bs * kDrawParts) S.held = -1;  // past the draw list (never listed)
+        if (S.held >= (2 * p.bs << C.dshift)) S.held = -1;  // past the draw list (never listed)
       }
-      if (S.held >= 0 && S.held / kDrawParts < nd) {
-        const int e = S.held / kDrawParts;
+      if (S.held >= 0 && (S.held >> C.dshift) < nd) {
+        const int e = S.held >> C.dshift;
         int code = ld_acquire(p.dl + e);
         for (const uint64_t end = now_ns() + p.wait_ns; code == 0 && now_ns() <= end;)
           code = ld_acquire(p.dl + e);
@@ -1621,7 +1622,7 @@ struct Sampler {
           halt();
           return Unit{kUEnd, 0, 0, 0};
         }
-        const Unit u{kUDraw, e, code, S.held - e * kDrawParts};
+        const Unit u{kUDraw, e, code, S.held & ((1 << C.dshift) - 1)};
         S.held = -1;
         return u;
       }
@@ -1801,6 +1802,13 @@ __global__ void __launch_bounds__(kThreads, 1) sampler_kernel(const __grid_const
   C.Ej = s_E;
   C.nsamp = 0;
   for (int b = 0; b < 16; ++b) C.nsamp += s_hist[b];
+  // Each sampling request ends in one final draw.  With fewer than two per
+  // CTA, the last draws would leave most CTAs idle while a few run two whole
+  // draws: split each draw's chunks over two CTAs (their chunk sums meet in
+  // the workspace, and the second part to finish walks the draw).  With more
+  // draws the split only adds work (measured).
+  C.dshift = (C.nsamp < 2 * static_cast<int>(gridDim.x) && p.ncd >= 2) ? 1 : 0;
+  C.dper = (p.ncd + (1 << C.dshift) - 1) >> C.dshift;
   C.nw = K1;
   C.U = s_WS[K1];
   C.tab = s_tab;

@@ -50,8 +50,6 @@ constexpr int kSubBytes = kSegBytes / 2;
 constexpr int kMaxRowBytes = 2 << 20;          // V * elem <= 2 MiB
 constexpr int kSamplerWarps = 16;              // streaming warps per CTA (plus one scheduler warp)
 constexpr int kFinishWarps = 1;                // warps that finish the CTA's units (rows, draws)
-constexpr int kDrawParts = 1;                  // a final draw's chunks are summed as this many units
-                                               // (splitting a draw into more parts measured slower)
 
 // Statistics of one logit row, 32 bytes.  M = maximum, 1/Z as a
 // double-float (izh + izl) with Z = sum over the row of
