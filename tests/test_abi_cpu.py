@@ -53,6 +53,34 @@ def test_workspace_sizes(lib):
     assert sd.sd_verify_workspace_bytes(0, 7, 1024, sd.SD_BF16) == 0
 
 
+@pytest.mark.parametrize("bs,k_max,V,elem", [(256, 7, 129280, 2), (1024, 7, 129280, 2),
+                                              (64, 3, 256000, 2), (12, 5, 1000, 4),
+                                              (1, 1, 16, 4), (4096, 15, 1 << 20, 2)])
+def test_workspace_layout_exact(lib, bs, k_max, V, elem):
+    """The sampling workspace, part by part, each 256-byte aligned: a 32-byte
+    statistics record per target and draft row; the 2^-56 fixed-point chunk
+    sums of up to two final draws per request (sixteen streaming warps, each
+    with ceil(slice / 3 KB) draw chunks of a slice of ceil(V * elem / 16)
+    bytes rounded up to 16); then the counters that are zero between calls:
+    a pair counter per target row, a decision word per request, the draw
+    list and the split-draw part counters (two per request each), and eight
+    control words.  The GPU tests locate the zero part from this layout."""
+    import speculative_decoding_verification_sd_gb300 as sd
+    al = lambda v: (v + 255) // 256 * 256
+    rows_t, rows_d = bs * (k_max + 1), bs * k_max
+    sl = (-(-V * elem // 16) + 15) // 16 * 16
+    ncd = -(-sl // 3072)
+    rs = al((rows_t + rows_d) * 32)
+    zero = al(rs + 2 * bs * 16 * ncd * 8)
+    st = al(zero + rows_t * 4)
+    dl = al(st + bs * 4)
+    dpc = al(dl + 2 * bs * 4)
+    ctrl = al(dpc + 2 * bs * 4)
+    total = al(ctrl + 8 * 4)
+    dt = sd.SD_BF16 if elem == 2 else sd.SD_F32
+    assert sd.sd_verify_workspace_bytes(bs, k_max, V, dt) == total
+
+
 FAKE = 1 << 20  # a non-null address that is never dereferenced on these paths
 
 
